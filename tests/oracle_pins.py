@@ -1,0 +1,299 @@
+"""Pins of the WKV7 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes an ``OracleLib`` and raises AssertionError when the
+oracle disagrees with a fact that does not come from the oracle itself:
+closed forms of special cases, exact invariants of the recurrence, central
+finite differences and an automatic-differentiation adjoint.  The same pins
+are run against deliberately broken copies of the oracle (see
+``test_oracle_mutants.py``) to show that each plausible mistake trips one.
+
+Notation (the "timemix.cu" page's WKV7 layout): token vectors [B][T][H][N],
+state S[i][j] with i the value index and j the key index.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+N = 64
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _decays(g, shape, lo=0.5, hi=1.0):
+    return g.uniform(lo, hi, size=shape)
+
+
+def _realistic(g, B, T, H):
+    """Inputs shaped like an RWKV-7 time-mix block feeds them (a = -kk, b = kk*gate)."""
+    shp = (B, T, H, N)
+    r, k, v = (g.standard_normal(shp) for _ in range(3))
+    kk = _unit(g.standard_normal(shp))
+    gate = 1.0 / (1.0 + np.exp(-g.standard_normal(shp)))
+    w = np.exp(-0.606531 / (1.0 + np.exp(-g.standard_normal(shp))))
+    return dict(r=r, w=w, k=k, v=v, a=-kk, b=kk * gate)
+
+
+def _close(got, want, rel, what):
+    scale = max(1.0, float(np.abs(want).max()) if want.size else 1.0)
+    err = float(np.abs(got - want).max()) if want.size else 0.0
+    assert err <= rel * scale, f"{what}: max abs err {err:.3e} > {rel:.1e} x {scale:.3e}"
+
+
+# ---------------------------------------------------------------- forward pins
+
+def pin_linear_attention(orc):
+    """w = 1, a = b = 0 reduces to causal linear attention:
+    y_t = sum_{s<=t} v_s (k_s . r_t), and sT = sum_s v_s k_s^T."""
+    g = _rng(1)
+    B, T, H = 2, 13, 3
+    r, k, v = (g.standard_normal((B, T, H, N)) for _ in range(3))
+    one, zero = np.ones_like(r), np.zeros_like(r)
+    y, sT, _ = orc.forward(r, one, k, v, zero, zero, L=4)
+    scores = np.einsum("bthn,bshn->bhts", r, k) * np.tril(np.ones((T, T)))
+    _close(y, np.einsum("bhts,bshn->bthn", scores, v), 1e-12, "linear attention y")
+    _close(sT, np.einsum("bshi,bshj->bhij", v, k), 1e-12, "linear attention sT")
+
+
+def pin_memoryless(orc):
+    """w = 0, a = b = 0: every step forgets the past, y_t = v_t (k_t . r_t)."""
+    g = _rng(2)
+    B, T, H = 1, 7, 2
+    r, k, v = (g.standard_normal((B, T, H, N)) for _ in range(3))
+    s0 = g.standard_normal((B, H, N, N))
+    zero = np.zeros_like(r)
+    y, sT, _ = orc.forward(r, zero, k, v, zero, zero, s0=s0, L=3)
+    _close(y, v * np.sum(k * r, axis=-1, keepdims=True), 1e-12, "memoryless y")
+    _close(sT, np.einsum("bhi,bhj->bhij", v[:, -1], k[:, -1]), 1e-12, "memoryless sT")
+
+
+def pin_decay_only(orc):
+    """a = b = 0, per-key decay w: decayed linear attention with an initial state,
+    y_t[i] = sum_j s0[i][j] prod_{u<=t} w_u[j] r_t[j]
+           + sum_{s<=t} v_s[i] sum_j k_s[j] prod_{s<u<=t} w_u[j] r_t[j]."""
+    g = _rng(3)
+    B, T, H = 1, 9, 2
+    r, k, v = (g.standard_normal((B, T, H, N)) for _ in range(3))
+    w = _decays(g, (B, T, H, N), 0.3, 1.0)
+    s0 = g.standard_normal((B, H, N, N))
+    zero = np.zeros_like(r)
+    y, _, _ = orc.forward(r, w, k, v, zero, zero, s0=s0, L=5)
+    want = np.zeros_like(y)
+    for bi in range(B):
+        for h in range(H):
+            for t in range(T):
+                d0 = np.prod(w[bi, :t + 1, h], axis=0)
+                acc = s0[bi, h] @ (d0 * r[bi, t, h])
+                for s in range(t + 1):
+                    d = np.prod(w[bi, s + 1:t + 1, h], axis=0)
+                    acc = acc + v[bi, s, h] * np.dot(k[bi, s, h] * d, r[bi, t, h])
+                want[bi, t, h] = acc
+    _close(y, want, 1e-12, "decay-only y")
+
+
+def pin_delta_rule_write(orc):
+    """w = 1, a = -kk, b = kk, k = kk (unit): the step is the delta rule
+    S <- S (I - kk kk^T) + v kk^T, after which S kk = v exactly.  Reading with
+    r = kk therefore returns y_t = v_t whatever the earlier state."""
+    g = _rng(4)
+    B, T, H = 2, 6, 2
+    kk = _unit(g.standard_normal((B, T, H, N)))
+    v = g.standard_normal((B, T, H, N))
+    s0 = g.standard_normal((B, H, N, N))
+    y, sT, _ = orc.forward(kk, np.ones_like(kk), kk, v, -kk, kk, s0=s0, L=2)
+    _close(y, v, 1e-12, "delta-rule read-back")
+    _close(np.einsum("bhij,bhj->bhi", sT, kk[:, -1]), v[:, -1], 1e-12, "delta-rule sT kk")
+
+
+def pin_projection_erases(orc):
+    """w = 1, v = 0, a = -kk, b = kk: the transition I - kk kk^T is a projection,
+    so the state forgets direction kk: S_t kk_t = 0 (read with r = kk)."""
+    g = _rng(5)
+    B, T, H = 1, 5, 3
+    kk = _unit(g.standard_normal((B, T, H, N)))
+    s0 = g.standard_normal((B, H, N, N))
+    zero = np.zeros_like(kk)
+    y, _, _ = orc.forward(kk, np.ones_like(kk), g.standard_normal(kk.shape), zero, -kk, kk,
+                          s0=s0, L=2)
+    _close(y, zero, 1e-12, "projection erases kk")
+
+
+def pin_rank1_orientation(orc):
+    """w = 1, v = 0, one step: S1 = S0 (I + a b^T).  For r orthogonal to b the
+    step leaves the read unchanged, y = S0 r; the transposed transition
+    S0 (I + b a^T) would add (S0 b)(a . r)."""
+    g = _rng(6)
+    B, H = 2, 3
+    a = g.standard_normal((B, 1, H, N))
+    b = g.standard_normal((B, 1, H, N))
+    r = g.standard_normal((B, 1, H, N))
+    r = r - b * (np.sum(r * b, -1, keepdims=True) / np.sum(b * b, -1, keepdims=True))
+    s0 = g.standard_normal((B, H, N, N))
+    y, _, _ = orc.forward(r, np.ones_like(r), g.standard_normal(r.shape), np.zeros_like(r),
+                          a, b, s0=s0, L=1)
+    _close(y[:, 0], np.einsum("bhij,bhj->bhi", s0, r[:, 0]), 1e-12, "rank-1 orientation")
+
+
+def pin_empty_sequence(orc):
+    """T = 0: no token, so sT = s0, no checkpoint, ds0 = dsT and no gradients."""
+    g = _rng(7)
+    s0 = g.standard_normal((2, 3, N, N))
+    dsT = g.standard_normal((2, 3, N, N))
+    e = np.zeros((2, 0, 3, N))
+    y, sT, ck = orc.forward(e, e, e, e, e, e, s0=s0, L=4)
+    assert y.shape == (2, 0, 3, N) and ck.shape == (2, 3, 0, N, N)
+    _close(sT, s0, 0.0, "T=0 sT")
+    gr = orc.backward(e, e, e, e, e, e, e, s0=s0, dsT=dsT)
+    _close(gr["ds0"], dsT, 0.0, "T=0 ds0")
+
+
+# --------------------------------------------------------- structural invariants
+
+def pin_checkpoints_are_prefix_states(orc):
+    """ckpt[c] is the state before token c*L, i.e. the final state of the first
+    c*L tokens (ckpt[0] = s0), including a ragged last interval."""
+    g = _rng(8)
+    B, T, H, L = 1, 11, 2, 4
+    x = _realistic(g, B, T, H)
+    s0 = 0.1 * g.standard_normal((B, H, N, N))
+    _, _, ck = orc.forward(**x, s0=s0, L=L)
+    assert ck.shape == (B, H, 3, N, N)
+    for c in range(3):
+        pre = {n: x[n][:, :c * L] for n in x}
+        _, s_c, _ = orc.forward(**pre, s0=s0, L=L)
+        _close(ck[:, :, c], s_c, 0.0, f"checkpoint {c}")
+
+
+def pin_split_sequence(orc):
+    """Running T1 tokens, then T2 tokens from the carried state, equals one
+    T1+T2 call (same operation order, so bit for bit)."""
+    g = _rng(9)
+    B, T, H, T1 = 2, 10, 2, 3
+    x = _realistic(g, B, T, H)
+    s0 = 0.1 * g.standard_normal((B, H, N, N))
+    y, sT, _ = orc.forward(**x, s0=s0, L=4)
+    y1, s1, _ = orc.forward(**{n: x[n][:, :T1] for n in x}, s0=s0, L=4)
+    y2, s2, _ = orc.forward(**{n: x[n][:, T1:] for n in x}, s0=s1, L=4)
+    _close(np.concatenate([y1, y2], axis=1), y, 0.0, "split y")
+    _close(s2, sT, 0.0, "split sT")
+
+
+def pin_decode_is_streaming(orc):
+    """Feeding the tokens one at a time through the decode step (state updated in
+    place, the streaming-inference use) reproduces the sequence call bit for bit."""
+    g = _rng(10)
+    B, T, H = 2, 5, 3
+    x = _realistic(g, B, T, H)
+    s0 = 0.1 * g.standard_normal((B, H, N, N))
+    y, sT, _ = orc.forward(**x, s0=s0, L=2)
+    st = s0.copy()
+    for t in range(T):
+        yt, st = orc.decode_step(*(x[n][:, t] for n in ("r", "w", "k", "v", "a", "b")), st)
+        _close(yt, y[:, t], 0.0, f"decode token {t}")
+    _close(st, sT, 0.0, "decode state")
+
+
+def pin_linear_in_state_and_values(orc):
+    """For fixed r, w, k, a, b the recurrence is linear in (s0, v) jointly:
+    y(s0, v) = y(s0, 0) + y(0, v)."""
+    g = _rng(11)
+    B, T, H = 1, 8, 2
+    x = _realistic(g, B, T, H)
+    s0 = g.standard_normal((B, H, N, N))
+    y, sT, _ = orc.forward(**x, s0=s0, L=3)
+    y_s, sT_s, _ = orc.forward(**{**x, "v": np.zeros_like(x["v"])}, s0=s0, L=3)
+    y_v, sT_v, _ = orc.forward(**x, s0=None, L=3)
+    _close(y, y_s + y_v, 1e-12, "linearity y")
+    _close(sT, sT_s + sT_v, 1e-12, "linearity sT")
+
+
+# ----------------------------------------------------------------- backward pins
+
+def _loss(orc, x, s0, dy, dsT):
+    y, sT, _ = orc.forward(**x, s0=s0, L=4, want_ckpt=False)
+    return float(np.sum(y * dy) + np.sum(sT * dsT))
+
+
+def pin_adjoint_identity(orc):
+    """y and sT are linear in (s0, v), so for any direction (u0, uv):
+    <y(u0, uv), dy> + <sT(u0, uv), dsT> = <u0, ds0> + <uv, dv>."""
+    g = _rng(12)
+    B, T, H = 1, 9, 2
+    x = _realistic(g, B, T, H)
+    dy = g.standard_normal(x["r"].shape)
+    dsT = g.standard_normal((B, H, N, N))
+    gr = orc.backward(**x, dy=dy, s0=g.standard_normal((B, H, N, N)), dsT=dsT)
+    u0 = g.standard_normal((B, H, N, N))
+    uv = g.standard_normal(x["v"].shape)
+    lhs = _loss(orc, {**x, "v": uv}, u0, dy, dsT)
+    rhs = float(np.sum(u0 * gr["ds0"]) + np.sum(uv * gr["dv"]))
+    assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs)), f"adjoint {lhs!r} vs {rhs!r}"
+
+
+def pin_finite_differences(orc):
+    """Central finite differences in float64 on a tiny problem: every gradient
+    (dr, dw, dk, dv, da, db, ds0) at sampled coordinates, relative error < 1e-6
+    (the bar the pages set for f64 gradchecks is 1e-3)."""
+    g = _rng(13)
+    B, T, H = 1, 6, 1
+    x = _realistic(g, B, T, H)
+    s0 = 0.5 * g.standard_normal((B, H, N, N))
+    dy = g.standard_normal(x["r"].shape)
+    dsT = g.standard_normal((B, H, N, N))
+    gr = orc.backward(**x, dy=dy, s0=s0, dsT=dsT)
+    eps = 1e-6
+    for name in ("r", "w", "k", "v", "a", "b", "s0"):
+        base = s0 if name == "s0" else x[name]
+        grad = gr["d" + name]
+        scale = float(np.abs(grad).max())
+        for idx in [tuple(int(g.integers(0, s)) for s in base.shape) for _ in range(10)]:
+            def loss_at(delta):
+                pert = base.copy()
+                pert[idx] += delta
+                if name == "s0":
+                    return _loss(orc, x, pert, dy, dsT)
+                return _loss(orc, {**x, name: pert}, s0, dy, dsT)
+            fd = (loss_at(eps) - loss_at(-eps)) / (2 * eps)
+            err = abs(fd - grad[idx]) / max(abs(grad[idx]), 1e-3 * scale)
+            assert err < 1e-6, f"d{name}{idx}: fd {fd:.9e} vs {grad[idx]:.9e} (rel {err:.2e})"
+
+
+def pin_autograd_adjoint(orc):
+    """The hand-written adjoint equals the one torch's autograd derives (float64)
+    from the recurrence written with the transition matrix P_t = diag(w_t) + a_t b_t^T:
+    S_t = S_{t-1} P_t + v_t k_t^T, y_t = S_t r_t."""
+    import torch
+    g = _rng(14)
+    B, T, H = 1, 7, 2
+    x = _realistic(g, B, T, H)
+    s0 = 0.3 * g.standard_normal((B, H, N, N))
+    dy = g.standard_normal(x["r"].shape)
+    dsT = g.standard_normal((B, H, N, N))
+    gr = orc.backward(**x, dy=dy, s0=s0, dsT=dsT)
+    tx = {n: torch.tensor(x[n], requires_grad=True) for n in x}
+    ts0 = torch.tensor(s0, requires_grad=True)
+    S = ts0
+    ys = []
+    for t in range(T):
+        P = torch.diag_embed(tx["w"][:, t]) + tx["a"][:, t, :, :, None] * tx["b"][:, t, :, None, :]
+        S = S @ P + tx["v"][:, t, :, :, None] * tx["k"][:, t, :, None, :]
+        ys.append((S @ tx["r"][:, t, :, :, None])[..., 0])
+    loss = (torch.stack(ys, 1) * torch.tensor(dy)).sum() + (S * torch.tensor(dsT)).sum()
+    loss.backward()
+    for n in tx:
+        _close(gr["d" + n], tx[n].grad.numpy(), 1e-11, f"autograd d{n}")
+    _close(gr["ds0"], ts0.grad.numpy(), 1e-11, "autograd ds0")
+
+
+ALL_PINS = [
+    pin_linear_attention, pin_memoryless, pin_decay_only, pin_delta_rule_write,
+    pin_projection_erases, pin_rank1_orientation, pin_empty_sequence,
+    pin_checkpoints_are_prefix_states, pin_split_sequence, pin_decode_is_streaming,
+    pin_linear_in_state_and_values, pin_adjoint_identity, pin_finite_differences,
+    pin_autograd_adjoint,
+]

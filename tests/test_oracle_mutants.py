@@ -1,0 +1,57 @@
+"""Plant plausible mistakes in a copy of the oracle's C source and check that
+some pin catches each one (CPU only).  The copies are compiled into a
+temporary directory; the oracle itself is never modified."""
+import os
+
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+# (name, text to replace, replacement, which occurrence (0-based))
+MUTANTS = [
+    ("sa uses b instead of a", "acc += S[i * N + j] * a[o + j];", "acc += S[i * N + j] * b[o + j];", 0),
+    ("decay indexed by value row", "S[i * N + j] = S[i * N + j] * w[o + j]", "S[i * N + j] = S[i * N + j] * w[o + i]", 0),
+    ("rank-1 term sign", "+ sa[i] * b[o + j] + v[o + i]", "- sa[i] * b[o + j] + v[o + i]", 0),
+    ("v k^T transposed", "sa[i] * b[o + j] + v[o + i] * k[o + j];", "sa[i] * b[o + j] + v[o + j] * k[o + i];", 0),
+    ("y reads with k", "acc += S[i * N + j] * r[o + j];", "acc += S[i * N + j] * k[o + j];", 0),
+    ("first checkpoint skipped", "if (ckpt && t % L == 0) {", "if (ckpt && t % L == 0 && t > 0) {", 0),
+    ("s0 ignored", "if (s0) memcpy(S, s0", "if (0) memcpy(S, s0", 0),
+    ("bwd: dr from pre-update state", "acc += Sn[i * N + j] * dy[o + i];", "acc += Sp[i * N + j] * dy[o + i];", 0),
+    ("bwd: carried gradient drops rank-1 term", "G[i * N + j] * w[o + j] + dsa[i] * a[o + j];", "G[i * N + j] * w[o + j];", 0),
+    ("bwd: dw from post-update state", "acc_w += G[i * N + j] * Sp[i * N + j];", "acc_w += G[i * N + j] * Sn[i * N + j];", 0),
+    ("bwd: db uses dsa", "acc_b += G[i * N + j] * sa[i];", "acc_b += G[i * N + j] * dsa[i];", 0),
+    ("bwd: da transposed", "acc_a += Sp[i * N + j] * dsa[i];", "acc_a += Sp[j * N + i] * dsa[i];", 0),
+    ("bwd: dv uses b", "acc_v += G[i * N + j] * k[o + j];", "acc_v += G[i * N + j] * b[o + j];", 0),
+    ("bwd: dsT ignored", "if (dsT) memcpy(G,", "if (0) memcpy(G,", 0),
+    ("bwd: dy r^T transposed", "G[i * N + j] += dy[o + i] * r[o + j];", "G[i * N + j] += dy[o + j] * r[o + i];", 0),
+    ("decode: decay indexed by value row", "S[i * N + j] = S[i * N + j] * w[o + j]", "S[i * N + j] = S[i * N + j] * w[o + i]", 1),
+]
+
+
+def _replace_nth(text, old, new, n):
+    pos = -1
+    for _ in range(n + 1):
+        pos = text.find(old, pos + 1)
+        assert pos >= 0, f"mutation anchor not found: {old!r} (occurrence {n})"
+    return text[:pos] + new + text[pos + len(old):]
+
+
+@pytest.mark.parametrize("mutant", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_some_pin_catches(mutant, tmp_path):
+    name, old, new, nth = mutant
+    src = open(oracle.SOURCE).read()
+    mutated = _replace_nth(src, old, new, nth)
+    assert mutated != src
+    c_path = os.path.join(tmp_path, "mutant.c")
+    with open(c_path, "w") as f:
+        f.write(mutated)
+    so = oracle.compile_c(c_path, os.path.join(tmp_path, "libmutant.so"))
+    orc = oracle.OracleLib(so)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake: {name}"
