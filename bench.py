@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""WKV7 forward+backward throughput on GB300.
+
+One step = wkv7_forward (y, sT, checkpoints every L=16 tokens) + wkv7_backward
+(all six input gradients and ds0) over one batch of the workload
+B=16, T=4096, H=32, N=64 with bf16 r/w/k/v/a/b and fp32 state, outputs and
+gradients (synthetic seeded inputs).  Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the batch (heads are
+independent; no data-path collective): weak scaling, value = all ranks'
+tokens / max-over-ranks time.  ``--impl reference`` times the fp64 CPU
+oracle on this host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from rwkv_linear_attention_wkv7_gb300 import synthetic  # noqa: E402
+
+METRIC = "WKV7 fwd+bwd tokens/sec at B=16,T=4096,H=32,N=64; % HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "bf16_b16_t4096_h32"
+INPUTS = ("r", "w", "k", "v", "a", "b")
+GRADS = ("dr", "dw", "dk", "dv", "da", "db")
+L2_BYTES = 126 * 2**20
+
+
+def esize(spec):
+    return 2 if spec.dtype == "bf16" else 4
+
+
+def algorithmic_bytes(spec):
+    """Bytes a launch must move at minimum (checkpoints excluded: they are an
+    implementation choice).  Forward: 6 inputs + y (+ s0, sT).  Backward:
+    6 inputs + dy + 6 gradients (+ dsT, ds0)."""
+    E = spec.elems
+    st = spec.B * spec.H * spec.N * spec.N * 4
+    fwd = E * (6 * esize(spec) + 4) + st * (2 if spec.s0_std > 0 else 1)
+    bwd = E * (6 * esize(spec) + 4 + 6 * 4) + st * (2 if spec.with_dsT else 1)
+    return fwd, bwd
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the kernels as they are now (source hash recorded with it)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return {}
+    try:
+        with open(p) as f:
+            d = json.loads("".join(l for l in f if not l.startswith("#")))
+    except ValueError:
+        return {}
+    from rwkv_linear_attention_wkv7_gb300 import _build
+    return d.get("kernels", {}) if d.get("source_hash") == _build.source_hash() else {}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.TemporaryFile(mode="w+")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(spec, host_heads, n_heads, threads):
+    """Time the fp64 oracle (fwd+bwd over all T) on n_heads heads; returns
+    (seconds, tokens) where tokens = head-tokens / H."""
+    import oracle
+    heads = list(host_heads.keys())[:n_heads]
+
+    def one(b, h):
+        x = host_heads[(b, h)]
+        oracle.forward(*(x[n] for n in INPUTS), s0=x.get("s0"), L=spec.L)
+        oracle.backward(*(x[n] for n in INPUTS), x["dy"], s0=x.get("s0"), dsT=x.get("dsT"))
+
+    t0 = time.perf_counter()
+    oracle.per_head(one, heads, threads)
+    dt = time.perf_counter() - t0
+    return dt, len(heads) * spec.T / spec.H
+
+
+def host_head_slices(spec, n):
+    """Draw the workload's inputs and keep n heads' slices on the host as float64-ready tensors."""
+    import numpy as np
+    g = np.random.default_rng(1)
+    picks = []
+    while len(picks) < min(n, spec.B * spec.H):
+        bh = (int(g.integers(0, spec.B)), int(g.integers(0, spec.H)))
+        if bh not in picks:
+            picks.append(bh)
+    out = {bh: {} for bh in picks}
+    for name, t in synthetic.stream_inputs(spec):
+        for bh in picks:
+            out[bh][name] = synthetic.head_slice(t, *bh, state=name in ("s0", "dsT"))
+    return out
+
+
+def cpu_baseline(spec, target_s=12.0, host_heads=None):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    if host_heads is None:
+        host_heads = host_head_slices(spec, min(spec.B * spec.H, max(cores * 8, 16)))
+    t1, _ = oracle_sample(spec, host_heads, 1, 1)  # calibrate one head on one core
+    n = max(1, min(len(host_heads), int(target_s * cores / max(t1, 1e-3))))
+    dt, toks = oracle_sample(spec, host_heads, n, cores)
+    return {"value": toks / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {spec.B * spec.H} (b,h) heads, full T={spec.T}, fwd+bwd in fp64; "
+                      f"tokens counted as head-tokens/H; {dt:.1f} s wall"}, dt
+
+
+def run_reference(args, world, rank):
+    spec = synthetic.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    host_heads = host_head_slices(spec, cores)
+    n = min(len(host_heads), cores)
+    for _ in range(args.warmup):
+        oracle_sample(spec, host_heads, 1, 1)
+    times, toks = [], 0.0
+    for _ in range(args.steps):
+        dt, tk = oracle_sample(spec, host_heads, n, cores)
+        times.append(dt)
+        toks = tk
+    value = toks * len(times) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(spec, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {n} (b,h) heads of {spec.B * spec.H}, full T={spec.T}, "
+                                       "fwd+bwd fp64 oracle on all host cores"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(spec, args):
+    return {"workload": spec.name, "B": spec.B, "T": spec.T, "H": spec.H, "N": spec.N,
+            "input_dtype": spec.dtype, "state_dtype": "f32", "ckpt_stride": spec.L,
+            "parallelism": f"replicas x{args.gpus} (independent heads)",
+            "l2": f"inputs larger than L2 ({spec.elems * 6 * esize(spec) / 1e9:.2f} GB of r..b per step), no flush"}
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args, world, rank, local):
+    from rwkv_linear_attention_wkv7_gb300 import build, wkv7
+    build()
+    spec = synthetic.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # inputs: drawn on the host (seeded), moved to HBM before timing
+    host_heads = {}
+    want_cpu = rank == 0 and not args.no_cpu
+    cores = os.cpu_count() or 1
+    n_keep = min(spec.B * spec.H, max(cores * 8, 16)) if want_cpu else 0
+    import numpy as np
+    g = np.random.default_rng(1)
+    keep = []
+    while len(keep) < n_keep:
+        bh = (int(g.integers(0, spec.B)), int(g.integers(0, spec.H)))
+        if bh not in keep:
+            keep.append(bh)
+    host_heads = {bh: {} for bh in keep}
+    d = {}
+    pinned = {}
+    for name, t in synthetic.stream_inputs(spec):
+        for bh in keep:
+            host_heads[bh][name] = None if t is None else synthetic.head_slice(t, *bh, state=name in ("s0", "dsT"))
+        d[name] = None if t is None else t.to(dev)
+        if not args.no_e2e and t is not None and name in INPUTS + ("dy",):
+            pinned[name] = t.pin_memory()
+        del t
+
+    B, T, H, N = spec.B, spec.T, spec.H, spec.N
+    nck = wkv7.ckpt_count(T, spec.L)
+    outs = {"y": torch.empty((B, T, H, N), device=dev), "sT": torch.empty((B, H, N, N), device=dev),
+            "ckpt": torch.empty((B, H, nck, N, N), device=dev)}
+    gouts = {n: torch.empty((B, T, H, N), device=dev) for n in GRADS}
+    gouts["ds0"] = torch.empty((B, H, N, N), device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev_f = []  # per-launch events (forward, backward) on the launching stream
+
+    def step(record=False):
+        if record:
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+        wkv7.forward(*(d[n] for n in INPUTS), s0=d["s0"], L=spec.L, out=outs, stream=stream)
+        if record:
+            e1.record(stream)
+        wkv7.backward(*(d[n] for n in INPUTS), outs["ckpt"], d["dy"], dsT=d["dsT"], L=spec.L, out=gouts,
+                      stream=stream)
+        if record:
+            e2.record(stream)
+            ev_f.append((e0, e1, e2))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_f)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev_f)
+    clocks = clk.summary()
+
+    ms_step = total_ms / args.steps
+    value = world * spec.tokens / (ms_step / 1e3)
+    peak, peak_kind = load_peaks()
+    fwd_bytes, bwd_bytes = algorithmic_bytes(spec)
+    traffic = load_traffic()
+    dom = "backward" if bwd_ms >= fwd_ms else "forward"
+    dom_ms, dom_bytes = (bwd_ms, bwd_bytes) if dom == "backward" else (fwd_ms, fwd_bytes)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    step_gbs = (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs and dy, forward + backward, D2H of y and the six gradients
+    e2e = None
+    if not args.no_e2e:
+        host_out = {n: torch.empty(outs["y"].shape, pin_memory=True) for n in ("y",) + GRADS}
+        h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in pinned)
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n in pinned:
+                d[n].copy_(pinned[n], non_blocking=True)
+            step()
+            host_out["y"].copy_(outs["y"], non_blocking=True)
+            for n in GRADS:
+                host_out[n].copy_(gouts[n], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        n_e2e = max(2, min(args.steps, 5))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a0.elapsed_time(a1), world) / n_e2e
+        e2e = {"value": world * spec.tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    cpu = None
+    if want_cpu:
+        cpu, _ = cpu_baseline(spec, host_heads=host_heads)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(spec, args),
+        "roofline": {"bound": "hbm", "kernel": f"wkv7 {dom}", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic.get(dom), "algorithmic_bytes": dom_bytes, "launch_ms": dom_ms},
+        "hbm_fraction_step": step_gbs / peak,
+        "forward": {"ms": fwd_ms, "tokens_per_s": spec.tokens / (fwd_ms / 1e3),
+                    "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
+        "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,124 @@
+/*
+ * wkv7.h -- C ABI of the GB300 (sm_103a) WKV7 library, libwkv7.so.
+ *
+ * The RWKV-7 WKV7 state recurrence, per batch row b and head h, with a state
+ * S[N][N] (row i = value index, column j = key index) and, for each token t,
+ *
+ *     sa_t    = S_{t-1} a_t                                   (pre-update state)
+ *     S_t     = S_{t-1} diag(w_t) + sa_t b_t^T + v_t k_t^T
+ *     y_t     = S_t r_t                                       (post-update state)
+ *
+ * Sources (web pages, cited by title and section):
+ *   "Foundry/cuda_kernels/timemix.cu" -- file header: WKV7 vectors are
+ *     [B][T][H][N] and the state is [B][H][N][N]; k_composites: the two
+ *     composite vectors handed to the recurrence are a = -kk, b = kk*a_gate;
+ *     tm_fwd_device: one recurrence per (b,h), launched over B*H;
+ *     error convention of the extern "C" entries: integer status, no exit.
+ *   "infotheory/backends/rwkvzip/rwkv7/model.rs" -- Config::validate: the
+ *     head size N is fixed to 64; accumulate_token_step_gradients, WKV kernel
+ *     backward: state orientation, y from the post-update state, sa from the
+ *     pre-update state, the adjoint implemented by wkv7_backward;
+ *     online_train_segment_tbptt: a checkpoint is the state held before a
+ *     replay chunk, and the backward replays each chunk forward from it;
+ *     module header: single-token streaming inference (wkv7_decode_step).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer to memory the caller allocated and
+ *     owns.  The library keeps no pointer after a call returns and allocates
+ *     no device memory.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  Outputs are valid once the stream reaches
+ *     the call.  Gradients are written (=), never accumulated.
+ *   - Outputs must not alias inputs or each other (except the in-place state
+ *     of wkv7_decode_step).
+ *   - r, w, k, v, a, b are fp32 or bf16 (`dtype`); everything else (states,
+ *     checkpoints, y, dy and every gradient) is fp32.  Arithmetic is fp32.
+ *   - Every pointer must be 16-byte aligned.  Tensors are dense row-major in
+ *     the stated layout.
+ *   - Return value: WKV7_OK, or a negative code; arguments are checked on
+ *     the host before anything is launched, so an error code from argument
+ *     checking means nothing ran.  wkv7_last_error() then describes the error
+ *     (per calling thread).  WKV7_ECUDA reports a CUDA launch error.
+ *   - Results are deterministic: the same inputs give bit-identical outputs
+ *     on every run (no atomics, fixed reduction order).
+ */
+#ifndef WKV7_H
+#define WKV7_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { WKV7_F32 = 0, WKV7_BF16 = 1 } wkv7_dtype;
+
+enum {
+    WKV7_OK = 0,
+    WKV7_EINVAL = -1,       /* bad size, NULL required pointer, misaligned pointer */
+    WKV7_ECUDA = -2,        /* a CUDA launch or runtime call failed                 */
+    WKV7_EUNSUPPORTED = -3  /* valid request this build cannot serve (e.g. no GPU)  */
+};
+
+/* The head size every entry point accepts ("model.rs", Config::validate). */
+#define WKV7_HEAD_SIZE 64
+
+/* Number of checkpoints a forward of T tokens writes at stride L: ceil(T/L).
+ * Returns -1 if T < 0 or L < 1. */
+int wkv7_ckpt_count(int T, int L);
+
+/*
+ * Forward over a whole sequence.
+ *   B, T, H   batch rows, tokens, heads; B, H >= 1, T >= 0.  N must be 64.
+ *   dtype     element type of r, w, k, v, a, b.
+ *   r..b      [B][T][H][N] inputs (see the recurrence above).
+ *   s0        [B][H][N][N] initial state, or NULL for zeros.
+ *   y         [B][T][H][N] output, required when T > 0.
+ *   sT        [B][H][N][N] final state, or NULL.
+ *   ckpt      [B][H][ceil(T/L)][N][N], or NULL: ckpt[b][h][c] is the state
+ *             before token c*L (so ckpt[..][0] = s0).
+ *   L         checkpoint stride in tokens, L >= 1 (16 is the tuned value).
+ * T == 0 writes sT = s0 (or zeros) and nothing else.
+ */
+int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype,
+                 const void *r, const void *w, const void *k,
+                 const void *v, const void *a, const void *b,
+                 const float *s0, float *y, float *sT, float *ckpt, int L,
+                 void *stream);
+
+/*
+ * Backward: the exact adjoint of wkv7_forward, run in reverse time from the
+ * checkpoints a forward with the same inputs and the same L wrote.
+ *   r..b      the forward's inputs, same dtype and layout.
+ *   ckpt      [B][H][ceil(T/L)][N][N] from wkv7_forward (required when T > 0).
+ *   dy        [B][T][H][N] gradient of the loss w.r.t. y (required when T > 0).
+ *   dsT       [B][H][N][N] gradient w.r.t. the final state, or NULL for zeros.
+ *   dr..db    [B][T][H][N] gradients w.r.t. r, w, k, v, a, b (all required
+ *             when T > 0).
+ *   ds0       [B][H][N][N] gradient w.r.t. the initial state, or NULL.
+ */
+int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype,
+                  const void *r, const void *w, const void *k,
+                  const void *v, const void *a, const void *b,
+                  const float *ckpt, int L, const float *dy, const float *dsT,
+                  float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                  float *ds0, void *stream);
+
+/*
+ * One token for each of B*H independent heads (streaming inference).
+ *   r..b      [B][H][N] this token's vectors.
+ *   state     [B][H][N][N] fp32, read and overwritten in place.
+ *   y         [B][H][N] output.
+ * Same arithmetic as one step of wkv7_forward.
+ */
+int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype,
+                     const void *r, const void *w, const void *k,
+                     const void *v, const void *a, const void *b,
+                     float *state, float *y, void *stream);
+
+/* Text of the last error on the calling thread ("" if none). */
+const char *wkv7_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WKV7_H */

@@ -1,0 +1,153 @@
+// C ABI of libwkv7: argument checking, error reporting and kernel dispatch.
+// Integer status, no exit and no printing, as the extern "C" entries of the
+// "Foundry/cuda_kernels/timemix.cu" page (timemix_forward_cuda) return -1 on
+// failure instead of aborting.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "wkv7.h"
+#include "wkv7_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptr(const void *p, const char *name, bool required) {
+    if (!p) return required ? fail(WKV7_EINVAL, "%s is NULL", name) : WKV7_OK;
+    if (!aligned16(p)) return fail(WKV7_EINVAL, "%s is not 16-byte aligned", name);
+    return WKV7_OK;
+}
+
+// The kernels are built for sm_103a only; refuse other devices up front.
+int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(WKV7_EUNSUPPORTED, "no CUDA device available");
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(WKV7_EUNSUPPORTED, "cannot query device %d", dev);
+    }
+    if (major != 10 || minor != 3)
+        return fail(WKV7_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+    return WKV7_OK;
+}
+
+int check_dims(int B, int T, int H, int N, int dtype) {
+    if (N != WKV7_HEAD_SIZE) return fail(WKV7_EINVAL, "N must be %d (got %d)", WKV7_HEAD_SIZE, N);
+    if (B < 1 || H < 1) return fail(WKV7_EINVAL, "B and H must be >= 1 (got B=%d, H=%d)", B, H);
+    if (T < 0) return fail(WKV7_EINVAL, "T must be >= 0 (got %d)", T);
+    if (dtype != WKV7_F32 && dtype != WKV7_BF16) return fail(WKV7_EINVAL, "unknown dtype %d", dtype);
+    if ((long long)B * H > 0x7fffffffLL) return fail(WKV7_EINVAL, "B*H too large");
+    return WKV7_OK;
+}
+
+#define TRY(x)                    \
+    do {                          \
+        int rc_ = (x);            \
+        if (rc_ != WKV7_OK) return rc_; \
+    } while (0)
+
+int launch_status(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(WKV7_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return WKV7_OK;
+}
+
+// Copy (or zero) a [B][H][N][N] state when no token is processed.
+int copy_state(const float *src, float *dst, int B, int H, cudaStream_t st) {
+    if (!dst) return WKV7_OK;
+    const size_t bytes = (size_t)B * H * WKV7_HEAD_SIZE * WKV7_HEAD_SIZE * sizeof(float);
+    cudaError_t e = src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(dst, 0, bytes, st);
+    return launch_status(e, "state copy");
+}
+
+}  // namespace
+
+extern "C" {
+
+int wkv7_ckpt_count(int T, int L) {
+    if (T < 0 || L < 1) return -1;
+    return (int)(((long long)T + L - 1) / L);
+}
+
+const char *wkv7_last_error(void) { return g_err; }
+
+int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                 const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
+                 int L, void *stream) {
+    g_err[0] = '\0';
+    TRY(check_dims(B, T, H, N, dtype));
+    if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
+    const bool need = T > 0;
+    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
+    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
+    TRY(check_ptr(s0, "s0", false)); TRY(check_ptr(y, "y", need));
+    TRY(check_ptr(sT, "sT", false)); TRY(check_ptr(ckpt, "ckpt", false));
+    TRY(check_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    if (T == 0) return copy_state(s0, sT, B, H, st);
+
+    wkv7::SeqArgs p{};
+    p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
+    p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt;
+    return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
+}
+
+int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                  const void *v, const void *a, const void *b, const float *ckpt, int L, const float *dy,
+                  const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db, float *ds0,
+                  void *stream) {
+    g_err[0] = '\0';
+    TRY(check_dims(B, T, H, N, dtype));
+    if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
+    const bool need = T > 0;
+    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
+    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
+    TRY(check_ptr(ckpt, "ckpt", need)); TRY(check_ptr(dy, "dy", need)); TRY(check_ptr(dsT, "dsT", false));
+    TRY(check_ptr(dr, "dr", need)); TRY(check_ptr(dw, "dw", need)); TRY(check_ptr(dk, "dk", need));
+    TRY(check_ptr(dv, "dv", need)); TRY(check_ptr(da, "da", need)); TRY(check_ptr(db, "db", need));
+    TRY(check_ptr(ds0, "ds0", false));
+    TRY(check_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    if (T == 0) return copy_state(dsT, ds0, B, H, st);
+
+    wkv7::SeqArgs p{};
+    p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
+    p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.ckpt_in = ckpt; p.dy = dy; p.dsT = dsT;
+    p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0;
+    return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");
+}
+
+int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                     const void *v, const void *a, const void *b, float *state, float *y, void *stream) {
+    g_err[0] = '\0';
+    TRY(check_dims(B, 1, H, N, dtype));
+    TRY(check_ptr(r, "r", true)); TRY(check_ptr(w, "w", true)); TRY(check_ptr(k, "k", true));
+    TRY(check_ptr(v, "v", true)); TRY(check_ptr(a, "a", true)); TRY(check_ptr(b, "b", true));
+    TRY(check_ptr(state, "state", true)); TRY(check_ptr(y, "y", true));
+    TRY(check_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    return launch_status(wkv7::launch_decode_step(B, H, dtype, r, w, k, v, a, b, state, y, st),
+                         "wkv7_decode_step launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+"""Thin Python binding of libwkv7 (the C ABI in include/wkv7.h).
+
+Argument marshalling only: torch supplies device memory and the current CUDA
+stream, every step of the recurrence runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing or the device is not an
+sm_103a GPU, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Tuple
+
+import torch
+
+from . import _build
+
+HEAD_SIZE = 64
+WKV7_F32, WKV7_BF16 = 0, 1
+_CODES = {0: "WKV7_OK", -1: "WKV7_EINVAL", -2: "WKV7_ECUDA", -3: "WKV7_EUNSUPPORTED"}
+_lib = None
+
+
+class WKV7Error(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} -> {_CODES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libwkv7.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libwkv7.so not built at {path}; run rwkv_linear_attention_wkv7_gb300.build()")
+        L = ctypes.CDLL(path)
+        vp, ci, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+        L.wkv7_ckpt_count.argtypes = [ci, ci]
+        L.wkv7_ckpt_count.restype = ci
+        L.wkv7_forward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, fp, ci, vp]
+        L.wkv7_forward.restype = ci
+        L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, ci, fp, fp] + [fp] * 7 + [vp]
+        L.wkv7_backward.restype = ci
+        L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
+        L.wkv7_decode_step.restype = ci
+        L.wkv7_last_error.argtypes = []
+        L.wkv7_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().wkv7_last_error().decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise WKV7Error(fn, rc, last_error())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return WKV7_F32
+    if t.dtype == torch.bfloat16:
+        return WKV7_BF16
+    raise TypeError(f"r, w, k, v, a, b must be float32 or bfloat16 (got {t.dtype})")
+
+
+def _check_inputs(xs):
+    r = xs[0]
+    if r.dim() != 4 or r.shape[-1] != HEAD_SIZE:
+        raise ValueError(f"inputs must be [B][T][H][{HEAD_SIZE}] (got {tuple(r.shape)})")
+    for x in xs:
+        if x.shape != r.shape or x.dtype != r.dtype or x.device != r.device:
+            raise ValueError("r, w, k, v, a, b must share shape, dtype and device")
+        if not x.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    if r.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+
+
+def _f32(t, shape, device, name):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 {tuple(shape)} tensor on {device}")
+    return t
+
+
+def ckpt_count(T: int, L: int) -> int:
+    return lib().wkv7_ckpt_count(T, L)
+
+
+def forward(r, w, k, v, a, b, s0=None, L: int = 16, want_ckpt: bool = True, want_sT: bool = True,
+            out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    """Run the recurrence over [B][T][H][64] inputs.
+
+    Returns (y, sT, ckpt); sT / ckpt are None when not requested.  ``out`` may
+    hold preallocated 'y', 'sT', 'ckpt' tensors.
+    """
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    sshape = (B, H, N, N)
+    out = out or {}
+    y = out.get("y") if out.get("y") is not None else torch.empty((B, T, H, N), device=dev, dtype=torch.float32)
+    sT = (out.get("sT") if out.get("sT") is not None else torch.empty(sshape, device=dev)) if want_sT else None
+    nck = ckpt_count(T, L) if L >= 1 else -1
+    ck = None
+    if want_ckpt and nck >= 0:
+        ck = out.get("ckpt") if out.get("ckpt") is not None else torch.empty((B, H, nck, N, N), device=dev)
+    _f32(y, (B, T, H, N), dev, "y")
+    _f32(s0, sshape, dev, "s0")
+    rc = lib().wkv7_forward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(y), _ptr(sT), _ptr(ck),
+                            L, _stream(stream))
+    _check("wkv7_forward", rc)
+    return y, sT, ck
+
+
+GRAD_NAMES = ("dr", "dw", "dk", "dv", "da", "db")
+
+
+def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool = True,
+             out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Gradients of sum(y*dy) + sum(sT*dsT) w.r.t. r, w, k, v, a, b and s0."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty((B, T, H, N), device=dev) for n in GRAD_NAMES}
+    g["ds0"] = (out.get("ds0") if out.get("ds0") is not None else torch.empty((B, H, N, N), device=dev)) if want_ds0 else None
+    _f32(dy, (B, T, H, N), dev, "dy")
+    _f32(dsT, (B, H, N, N), dev, "dsT")
+    rc = lib().wkv7_backward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), L, _ptr(dy), _ptr(dsT),
+                             *(_ptr(g[n]) for n in GRAD_NAMES), _ptr(g["ds0"]), _stream(stream))
+    _check("wkv7_backward", rc)
+    return g
+
+
+def decode_step(r, w, k, v, a, b, state, y=None, stream=None):
+    """One token for each of B*H heads; vectors [B][H][64], ``state`` updated in place."""
+    if r.dim() != 3 or r.shape[-1] != HEAD_SIZE:
+        raise ValueError(f"decode vectors must be [B][H][{HEAD_SIZE}] (got {tuple(r.shape)})")
+    for x in (r, w, k, v, a, b):
+        if x.shape != r.shape or x.dtype != r.dtype or not x.is_contiguous() or x.device != r.device:
+            raise ValueError("decode vectors must share shape, dtype, device and be contiguous")
+    B, H, N = r.shape
+    _f32(state, (B, H, N, N), r.device, "state")
+    y = y if y is not None else torch.empty((B, H, N), device=r.device)
+    rc = lib().wkv7_decode_step(B, H, N, _dtype_code(r), *map(_ptr, (r, w, k, v, a, b)), _ptr(state), _ptr(y),
+                                _stream(stream))
+    _check("wkv7_decode_step", rc)
+    return y
+
+
+class WKV7Function(torch.autograd.Function):
+    """autograd wrapper: y, sT = wkv7(r, w, k, v, a, b, s0) with checkpoint stride L."""
+
+    @staticmethod
+    def forward(ctx, r, w, k, v, a, b, s0, L):
+        y, sT, ck = forward(r, w, k, v, a, b, s0=s0, L=L)
+        ctx.save_for_backward(r, w, k, v, a, b, ck)
+        ctx.L = L
+        ctx.has_s0 = s0 is not None
+        return y, sT
+
+    @staticmethod
+    def backward(ctx, dy, dsT):
+        r, w, k, v, a, b, ck = ctx.saved_tensors
+        g = backward(r, w, k, v, a, b, ck, dy.contiguous().float(),
+                     None if dsT is None else dsT.contiguous().float(), L=ctx.L, want_ds0=ctx.has_s0)
+        cast = (lambda t: t.to(r.dtype)) if r.dtype != torch.float32 else (lambda t: t)
+        return (*(cast(g[n]) for n in GRAD_NAMES), g["ds0"], None)
+
+
+def wkv7(r, w, k, v, a, b, s0=None, L: int = 16) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Differentiable WKV7: returns (y, sT)."""
+    return WKV7Function.apply(r, w, k, v, a, b, s0, L)

@@ -1,0 +1,136 @@
+"""Helpers for GPU-vs-oracle parity: run both sides on the same seeded inputs
+and compare with the tolerances the library promises.
+
+Forward (y, sT, checkpoints): max |gpu - ref| <= 2e-4 * max |ref| per tensor
+and per (b,h).  Gradients: ||gpu - ref||_F / ||ref||_F <= 1e-3 per tensor
+(the GPU-vs-CPU metric of the "cortiq_engine/fcd_ops.rs" page's
+gemm_dx_gpu_matches_cpu test, with the bar relaxed from 1e-4 to 1e-3 because
+the recurrence chains T dependent fp32 steps instead of one contraction).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from rwkv_linear_attention_wkv7_gb300 import synthetic, wkv7
+
+FWD_TOL = 2e-4
+GRAD_TOL = 1e-3
+INPUTS = ("r", "w", "k", "v", "a", "b")
+GRADS = ("dr", "dw", "dk", "dv", "da", "db")
+STATE_KEYS = ("s0", "dsT", "sT", "ds0", "ckpt")
+
+
+def to_dev(x, dev="cuda"):
+    return None if x is None else x.to(dev).contiguous()
+
+
+def inputs_on_device(spec, heads=None, dev="cuda"):
+    """Draw ``spec``'s inputs, move each to the GPU as soon as it is drawn and
+    keep on the host only the slices of ``heads`` (all heads if None)."""
+    dev_in, host = {}, {}
+    for name, t in synthetic.stream_inputs(spec):
+        if t is None:
+            dev_in[name] = None
+            continue
+        dev_in[name] = t.to(dev).contiguous()
+        if heads is None:
+            host[name] = t
+        else:
+            host[name] = {bh: synthetic.head_slice(t, *bh, state=name in STATE_KEYS) for bh in heads}
+        del t
+    return dev_in, host
+
+
+def run_gpu(d, L=16, backward=True):
+    """Forward (+ backward) through the C ABI on device inputs ``d``; outputs stay on the device."""
+    y, sT, ck = wkv7.forward(*(d[n] for n in INPUTS), s0=d.get("s0"), L=L)
+    out = {"y": y, "sT": sT, "ckpt": ck}
+    if backward:
+        out.update(wkv7.backward(*(d[n] for n in INPUTS), ck, d["dy"], dsT=d.get("dsT"), L=L))
+    torch.cuda.synchronize()
+    return out
+
+
+def _head_input(host, name, b, h):
+    x = host.get(name)
+    if x is None:
+        return None
+    if isinstance(x, dict):
+        return x[(b, h)]
+    return synthetic.head_slice(x, b, h, state=name in STATE_KEYS)
+
+
+def oracle_head(host, b, h, L=16, backward=True):
+    """Oracle results for head (b, h) only, float64 numpy in B=H=1 shapes."""
+    sl = {n: _head_input(host, n, b, h) for n in INPUTS + ("s0", "dy", "dsT")}
+    y, sT, ck = oracle.forward(*(sl[n] for n in INPUTS), s0=sl["s0"], L=L)
+    res = {"y": y, "sT": sT, "ckpt": ck}
+    if backward:
+        res.update(oracle.backward(*(sl[n] for n in INPUTS), sl["dy"], s0=sl["s0"], dsT=sl["dsT"]))
+    return res
+
+
+def gpu_head(out, b, h):
+    """Slice the GPU results to head (b, h) in the oracle's B=H=1 shapes (host float64)."""
+    res = {}
+    for k, v in out.items():
+        if v is None:
+            continue
+        if k in STATE_KEYS:
+            res[k] = v[b:b + 1, h:h + 1].double().cpu().numpy()
+        else:
+            res[k] = v[b:b + 1, :, h:h + 1].double().cpu().numpy()
+    return res
+
+
+def max_rel(got, ref):
+    den = float(np.abs(ref).max()) if ref.size else 0.0
+    num = float(np.abs(got - ref).max()) if ref.size else 0.0
+    return num / den if den > 0 else num
+
+
+def fro_rel(got, ref):
+    den = float(np.linalg.norm(ref))
+    num = float(np.linalg.norm(got - ref))
+    return num / den if den > 0 else num
+
+
+def compare(gpu, ref, backward=True, what=""):
+    """Assert the tolerances; return the measured errors."""
+    errs = {}
+    for k in ("y", "sT", "ckpt"):
+        if ref.get(k) is not None and k in gpu:
+            errs[k] = max_rel(gpu[k], ref[k])
+            assert errs[k] <= FWD_TOL, f"{what} {k}: max err {errs[k]:.3e} x max|ref| > {FWD_TOL}"
+    if backward:
+        for k in GRADS + ("ds0",):
+            if k in gpu:
+                errs[k] = fro_rel(gpu[k], ref[k])
+                assert errs[k] <= GRAD_TOL, f"{what} {k}: rel Frobenius {errs[k]:.3e} > {GRAD_TOL}"
+    return errs
+
+
+def check_heads(host, out, heads, L=16, backward=True, threads=None):
+    """Oracle the given heads in parallel and compare each with the GPU result."""
+    refs = oracle.per_head(lambda b, h: oracle_head(host, b, h, L=L, backward=backward), heads, threads)
+    worst = {}
+    for (b, h), ref in zip(heads, refs):
+        e = compare(gpu_head(out, b, h), ref, backward=backward, what=f"head (b={b}, h={h})")
+        for k, v in e.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    return worst
+
+
+def all_heads(B, H):
+    return [(b, h) for b in range(B) for h in range(H)]
+
+
+def sample_heads(B, H, n=6, seed=0):
+    """Corners, the middle, and seeded random heads."""
+    g = np.random.default_rng(seed)
+    heads = {(0, 0), (B - 1, H - 1), (B // 2, H // 2)}
+    while len(heads) < min(n, B * H):
+        heads.add((int(g.integers(0, B)), int(g.integers(0, H))))
+    return sorted(heads)

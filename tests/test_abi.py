@@ -1,0 +1,96 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/wkv7.h
+declares, and rejects bad arguments on the host before anything is launched
+(no GPU needed: none of these calls reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from rwkv_linear_attention_wkv7_gb300 import build, wkv7
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+EINVAL, EUNSUPPORTED = -1, -3
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(wkv7_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return wkv7.lib()
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_ckpt_count(lib):
+    assert lib.wkv7_ckpt_count(0, 16) == 0
+    assert lib.wkv7_ckpt_count(17, 16) == 2
+    assert lib.wkv7_ckpt_count(4096, 16) == 256
+    assert lib.wkv7_ckpt_count(-1, 16) == -1
+    assert lib.wkv7_ckpt_count(5, 0) == -1
+
+
+def _fwd(lib, B=1, T=4, H=1, N=64, dt=0, ptr=None, y=None, L=16, s0=None):
+    p = ctypes.c_void_p(4096) if ptr is None else ptr
+    y = p if y is None else y
+    return lib.wkv7_forward(B, T, H, N, dt, p, p, p, p, p, p, s0, y, None, None, L, None)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    assert _fwd(lib, N=63) == EINVAL and "N must be 64" in wkv7.last_error()
+    assert _fwd(lib, B=0) == EINVAL
+    assert _fwd(lib, T=-1) == EINVAL
+    assert _fwd(lib, dt=7) == EINVAL
+    assert _fwd(lib, L=0) == EINVAL
+    assert _fwd(lib, ptr=ctypes.c_void_p(4100)) == EINVAL and "aligned" in wkv7.last_error()
+    assert lib.wkv7_forward(1, 4, 1, 64, 0, None, *([ctypes.c_void_p(4096)] * 5), None,
+                            ctypes.c_void_p(4096), None, None, 16, None) == EINVAL
+    assert "r is NULL" in wkv7.last_error()
+    assert _fwd(lib, s0=ctypes.c_void_p(4104)) == EINVAL
+
+
+def test_backward_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    args = [1, 4, 1, 64, 0] + [p] * 6 + [p, 16, p, None] + [p] * 6 + [None, None]
+    bad = list(args)
+    bad[11] = None  # ckpt missing
+    assert lib.wkv7_backward(*bad) == EINVAL and "ckpt" in wkv7.last_error()
+    bad = list(args)
+    bad[12] = 0  # L
+    assert lib.wkv7_backward(*bad) == EINVAL
+    bad = list(args)
+    bad[17] = ctypes.c_void_p(4098)  # dv misaligned
+    assert lib.wkv7_backward(*bad) == EINVAL
+
+
+def test_decode_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    assert lib.wkv7_decode_step(1, 1, 32, 0, *([p] * 6), p, p, None) == EINVAL
+    assert lib.wkv7_decode_step(1, 1, 64, 0, *([p] * 6), None, p, None) == EINVAL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_no_gpu_is_reported_not_faked(lib):
+    """Without a usable sm_103a device the library refuses; it has no CPU path."""
+    assert _fwd(lib) == EUNSUPPORTED
+    assert "device" in wkv7.last_error()

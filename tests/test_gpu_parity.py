@@ -1,0 +1,133 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on
+the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rwkv_linear_attention_wkv7_gb300 import synthetic, wkv7
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny_b1_t64_h4", "stream_b1_t512_h48", "mid_b8_t1024_h12"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from rwkv_linear_attention_wkv7_gb300 import build
+    build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workloads_all_heads(name):
+    """Every head of the small workloads: forward (y, sT, checkpoints) and all gradients."""
+    spec = synthetic.WORKLOADS[name]
+    d, host = parity.inputs_on_device(spec)
+    out = parity.run_gpu(d, L=spec.L)
+    worst = parity.check_heads(host, out, parity.all_heads(spec.B, spec.H), L=spec.L)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+def _custom(B, T, H, dtype="f32", s0_std=0.1, dsT=True, seed=3, w_shift=0.0):
+    return synthetic.WorkloadSpec("custom", B, T, H, dtype=dtype, s0_std=s0_std, with_dsT=dsT, seed=seed,
+                                  w_shift=w_shift)
+
+
+@pytest.mark.parametrize("T,L", [(1, 16), (15, 16), (17, 16), (37, 5), (37, 1), (100, 64), (130, 16), (45, 200)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_lengths_and_strides(T, L, dtype):
+    """Ragged sequence lengths (partial staging chunks, partial checkpoint
+    intervals, partial backward windows) with an initial state and dsT."""
+    spec = _custom(2, T, 3, dtype=dtype)
+    d, host = parity.inputs_on_device(spec)
+    out = parity.run_gpu(d, L=L)
+    assert out["ckpt"].shape[2] == (T + L - 1) // L
+    parity.check_heads(host, out, parity.all_heads(2, 3), L=L)
+
+
+def test_empty_sequence():
+    """T = 0: the forward copies s0 to sT, the backward copies dsT to ds0."""
+    B, H, N = 2, 3, 64
+    s0 = torch.randn(B, H, N, N, device="cuda")
+    dsT = torch.randn(B, H, N, N, device="cuda")
+    e = torch.empty(B, 0, H, N, device="cuda")
+    y, sT, ck = wkv7.forward(e, e, e, e, e, e, s0=s0, L=16)
+    assert y.shape == (B, 0, H, N) and ck.shape == (B, H, 0, N, N)
+    assert torch.equal(sT, s0)
+    g = wkv7.backward(e, e, e, e, e, e, ck, torch.empty(B, 0, H, N, device="cuda"), dsT=dsT, L=16)
+    assert torch.equal(g["ds0"], dsT)
+    _, sT0, _ = wkv7.forward(e, e, e, e, e, e, s0=None, L=16)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(sT0) == 0
+
+
+def test_bitwise_reproducible():
+    """Two runs on the same inputs give bit-identical y, sT, checkpoints and gradients."""
+    d, _ = parity.inputs_on_device(_custom(2, 200, 4, dtype="bf16"))
+    o1 = parity.run_gpu(d)
+    o2 = parity.run_gpu(d)
+    for k in o1:
+        if o1[k] is not None:
+            assert torch.equal(o1[k], o2[k]), k
+
+
+def test_decode_step_from_nonzero_state():
+    """One decode token from the state a T=512 forward (nonzero s0) ends in --
+    the streaming-inference case -- against the oracle's decode step."""
+    spec = synthetic.WORKLOADS["stream_b1_t512_h48"]
+    d, _ = parity.inputs_on_device(spec)
+    out = parity.run_gpu(d, backward=False)
+    tok = synthetic.make_inputs(synthetic.WorkloadSpec("token", 1, 1, spec.H, seed=12))
+    vec = {n: tok[n][:, 0].contiguous() for n in parity.INPUTS}
+    host_state = out["sT"].cpu()
+    state = out["sT"].clone()
+    y = wkv7.decode_step(*(vec[n].cuda() for n in parity.INPUTS), state)
+    torch.cuda.synchronize()
+    ry, rs = oracle.decode_step(*(vec[n] for n in parity.INPUTS), host_state)
+    assert parity.max_rel(y.cpu().double().numpy(), ry) <= parity.FWD_TOL
+    assert parity.max_rel(state.cpu().double().numpy(), rs) <= parity.FWD_TOL
+
+
+def test_decode_chain_matches_forward():
+    """Feeding tokens one by one through the decode step reproduces the
+    sequence forward (bf16 inputs)."""
+    spec = _custom(2, 24, 5, dtype="bf16")
+    d, _ = parity.inputs_on_device(spec)
+    out = parity.run_gpu(d, backward=False)
+    state = d["s0"].clone()
+    ys = [wkv7.decode_step(*(d[n][:, t].contiguous() for n in parity.INPUTS), state) for t in range(spec.T)]
+    y = torch.stack(ys, 1)
+    torch.cuda.synchronize()
+    assert parity.max_rel(y.double().cpu().numpy(), out["y"].double().cpu().numpy()) <= 1e-6
+    assert parity.max_rel(state.double().cpu().numpy(), out["sT"].double().cpu().numpy()) <= 1e-6
+
+
+def test_autograd_function():
+    """The torch.autograd wrapper routes gradients from the library."""
+    spec = _custom(1, 33, 2)
+    d, host = parity.inputs_on_device(spec)
+    xs = [d[n].clone().requires_grad_(True) for n in parity.INPUTS]
+    s0 = d["s0"].clone().requires_grad_(True)
+    y, sT = wkv7.wkv7(*xs, s0=s0, L=16)
+    ((y * d["dy"]).sum() + (sT * d["dsT"]).sum()).backward()
+    ref = parity.oracle_head(host, 0, 1, L=16)
+    for n, x in zip(parity.GRADS, xs):
+        assert parity.fro_rel(x.grad[:, :, 1:2].double().cpu().numpy(), ref[n]) <= parity.GRAD_TOL, n
+    assert parity.fro_rel(s0.grad[:, 1:2].double().cpu().numpy(), ref["ds0"]) <= parity.GRAD_TOL
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["bf16_b16_t4096_h32", "long_b64_t4096_h40"])
+def test_full_size_sampled_heads(name):
+    """The full-size workloads, run in the launch configuration the bench
+    times, checked on sampled heads the oracle recomputes over all T."""
+    spec = synthetic.WORKLOADS[name]
+    heads = parity.sample_heads(spec.B, spec.H, n=6)
+    d, host = parity.inputs_on_device(spec, heads=heads)
+    out = parity.run_gpu(d, L=spec.L)
+    for k in ("y", "sT") + parity.GRADS + ("ds0",):
+        assert bool(torch.isfinite(out[k]).all()), k
+    worst = parity.check_heads(host, out, heads, L=spec.L)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
