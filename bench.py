@@ -22,7 +22,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -254,7 +253,7 @@ def run_ours(args, world, rank, local):
     host_heads = {}
     want_cpu = rank == 0 and not args.no_cpu
     cores = os.cpu_count() or 1
-    n_keep = min(spec.B * spec.H, max(cores * 8, 16)) if want_cpu else 0
+    n_keep = min(spec.B * spec.H, max(cores * 32, 16)) if want_cpu else 0
     import numpy as np
     g = np.random.default_rng(1)
     keep = []
@@ -380,8 +379,8 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")

@@ -106,6 +106,7 @@ int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt;
+    if (wkv7::forward_chunk_supported(p)) return launch_status(wkv7::launch_forward_chunk(p, st), "wkv7_forward launch");
     return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
 }
 

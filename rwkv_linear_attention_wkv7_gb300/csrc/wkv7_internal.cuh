@@ -23,6 +23,8 @@ struct SeqArgs {
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_forward_plain(const SeqArgs &a, cudaStream_t s);
+bool forward_chunk_supported(const SeqArgs &a);
+cudaError_t launch_forward_chunk(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_backward_plain(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_decode_step(int B, int H, int dtype, const void *r, const void *w,
                                const void *k, const void *v, const void *a, const void *b,

@@ -1,0 +1,88 @@
+// Warp-level tensor-core helpers for the chunked WKV7 kernels: bf16 m16n8k16
+// MMA with fp32 accumulation, and the three-product split ("bf16x3") that
+// recovers about 17 bits of operand precision: x = hi + lo with hi = bf16(x),
+// lo = bf16(x - hi); a*b ~ hi_a*hi_b + hi_a*lo_b + lo_a*hi_b.
+//
+// Fragment layouts (PTX ISA, mma.m16n8k16 with .bf16): lane l, g = l/4,
+// q = l%4.  A (16x16, row major): a0 = A[g][2q..2q+1], a1 = A[g+8][2q..],
+// a2 = A[g][2q+8..], a3 = A[g+8][2q+8..].  B (16x8): b0 = B[2q..2q+1][g],
+// b1 = B[2q+8..2q+9][g].  C (16x8, fp32): c0,c1 = C[g][2q..2q+1],
+// c2,c3 = C[g+8][2q..2q+1].  The lower half of each 32-bit register holds the
+// element with the smaller k index.
+#pragma once
+#include <stdint.h>
+
+namespace wkv7 {
+
+struct Frag2 {  // one 32-bit bf16x2 register as hi and lo parts
+    uint32_t hi, lo;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float x0, float x1) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+    return r;
+}
+
+// Split (x0, x1) into bf16x2 hi and lo registers.
+__device__ __forceinline__ Frag2 split2(float x0, float x1) {
+    Frag2 f;
+    f.hi = pack_bf16x2(x0, x1);
+    const float h0 = __uint_as_float(f.hi << 16);
+    const float h1 = __uint_as_float(f.hi & 0xffff0000u);
+    f.lo = pack_bf16x2(x0 - h0, x1 - h1);
+    return f;
+}
+
+__device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], const uint32_t b[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// A operand (16x16) split into hi and lo fragments.
+struct AFrag {
+    uint32_t hi[4], lo[4];
+};
+// B operand (16x8) split into hi and lo fragments.
+struct BFrag {
+    uint32_t hi[2], lo[2];
+};
+
+// c += A*B with split operands: small cross terms first, then hi*hi.
+__device__ __forceinline__ void mma3(float c[4], const AFrag &a, const BFrag &b) {
+    mma_bf16(c, a.lo, b.hi);
+    mma_bf16(c, a.hi, b.lo);
+    mma_bf16(c, a.hi, b.hi);
+}
+
+// A fragment from four fp32 pairs: (r0: row g, k 2q..), (r1: row g+8, k 2q..),
+// (r2: row g, k 2q+8..), (r3: row g+8, k 2q+8..).
+__device__ __forceinline__ AFrag make_a(float2 r0, float2 r1, float2 r2, float2 r3) {
+    AFrag f;
+    Frag2 t;
+    t = split2(r0.x, r0.y); f.hi[0] = t.hi; f.lo[0] = t.lo;
+    t = split2(r1.x, r1.y); f.hi[1] = t.hi; f.lo[1] = t.lo;
+    t = split2(r2.x, r2.y); f.hi[2] = t.hi; f.lo[2] = t.lo;
+    t = split2(r3.x, r3.y); f.hi[3] = t.hi; f.lo[3] = t.lo;
+    return f;
+}
+__device__ __forceinline__ BFrag make_b(float2 k0, float2 k8) {
+    BFrag f;
+    Frag2 t;
+    t = split2(k0.x, k0.y); f.hi[0] = t.hi; f.lo[0] = t.lo;
+    t = split2(k8.x, k8.y); f.hi[1] = t.hi; f.lo[1] = t.lo;
+    return f;
+}
+
+// A fragment for k-tile kt from a 16-row x 64-column fp32 accumulator slab
+// held as 8 n-tiles of C fragments (c[nt][0..3]): the C layout of n-tiles
+// 2kt and 2kt+1 is exactly the A layout of k-tile kt.
+__device__ __forceinline__ AFrag a_from_acc(const float c[][4], int kt) {
+    return make_a(make_float2(c[2 * kt][0], c[2 * kt][1]), make_float2(c[2 * kt][2], c[2 * kt][3]),
+                  make_float2(c[2 * kt + 1][0], c[2 * kt + 1][1]), make_float2(c[2 * kt + 1][2], c[2 * kt + 1][3]));
+}
+
+}  // namespace wkv7

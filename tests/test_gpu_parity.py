@@ -131,3 +131,32 @@ def test_full_size_sampled_heads(name):
         assert bool(torch.isfinite(out[k]).all()), k
     worst = parity.check_heads(host, out, heads, L=spec.L)
     print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_extreme_decay_chunks(dtype):
+    """Chunks whose cumulative decay underflows (w = 0 for a token, or a run of
+    tiny w) next to ordinary chunks: the forward takes the exact per-token
+    path there and must still match the oracle."""
+    spec = _custom(2, 80, 3, dtype=dtype)
+    d, host = parity.inputs_on_device(spec)
+    for x in (d, host):
+        w = x["w"].clone()
+        w[0, 20, 0, :] = 0.0               # hard reset of head 0 in chunk 1
+        w[1, 33:47, 1, :7] = 1e-3          # long run of tiny decay in chunk 2 of head (1,1)
+        w[0, 70, 2, 5] = 0.0               # a single zero column in the last chunk
+        x["w"] = w.to(x["w"].device) if x is d else w
+    out = parity.run_gpu(d, L=16)
+    parity.check_heads(host, out, parity.all_heads(2, 3), L=16)
+
+
+def test_forward_paths_agree():
+    """Checkpoint strides that are multiples of 16 run the chunked tensor-core
+    forward; others run the per-token kernel.  Both give the same y and sT."""
+    spec = _custom(2, 100, 4, dtype="bf16")
+    d, _ = parity.inputs_on_device(spec)
+    y1, s1, _ = wkv7.forward(*(d[n] for n in parity.INPUTS), s0=d["s0"], L=16)
+    y2, s2, _ = wkv7.forward(*(d[n] for n in parity.INPUTS), s0=d["s0"], L=7)
+    torch.cuda.synchronize()
+    assert parity.max_rel(y1.double().cpu().numpy(), y2.double().cpu().numpy()) <= parity.FWD_TOL
+    assert parity.max_rel(s1.double().cpu().numpy(), s2.double().cpu().numpy()) <= parity.FWD_TOL
