@@ -134,6 +134,7 @@ int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.ckpt_in = ckpt; p.dy = dy; p.dsT = dsT;
     p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0;
+    if (wkv7::backward_chunk_supported(p)) return launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward launch");
     return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");
 }
 

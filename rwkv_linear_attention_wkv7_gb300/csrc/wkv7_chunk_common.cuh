@@ -1,0 +1,169 @@
+// Shared pieces of the chunked WKV7 kernels (forward and backward): chunk
+// staging, the per-chunk decay-scaled vectors, the 32x32 Gram of the scaled
+// vectors and the inverse W = (I - M_b)^{-1}.
+//
+// Notation (one (b,h), one chunk of C = 16 tokens, local index t = 0..15):
+//   d_t  = w_0 o ... o w_t          cumulative decay per key column
+//   a^_t = a_t o d_{t-1}            r^_t = r_t o d_t
+//   b~_t = b_t / d_t                k~_t = k_t / d_t
+//   Gram rows (b~_s, k~_s), columns (a^_t, r^_t):
+//     M_b[s][t] = b~_s.a^_t  (s<t)   M_k[s][t] = k~_s.a^_t  (s<t)
+//     Q_b[s][t] = b~_s.r^_t  (s<=t)  Q_k[s][t] = k~_s.r^_t  (s<=t)
+// The unrolled recurrence of a chunk is
+//   S_t = (S_0 + sum_{s<=t} sa_s b~_s^T + v_s k~_s^T) diag(d_t),
+//   sa_t = S_0 a^_t + sum_{s<t} sa_s M_b[s][t] + v_s M_k[s][t].
+#pragma once
+#include "wkv7_internal.cuh"
+#include "wkv7_mma.cuh"
+
+namespace wkv7 {
+namespace chunk {
+
+constexpr int C = 16;          // tokens per chunk
+constexpr int SP = 72;         // row stride (floats) of [token][64] and [row][64] arrays
+constexpr int GS = 33;         // row stride of 32x32 Grams
+constexpr int WS = 17;         // row stride of W
+constexpr float kTiny = 1e-20f;  // smallest cumulative decay the factorised form accepts
+enum { VR = 0, VW = 1, VK = 2, VV = 3, VA = 4, VB = 5 };
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
+
+template <typename E>
+__device__ __forceinline__ float ld_raw(const E *raw, int vec, int t, int j);
+template <>
+__device__ __forceinline__ float ld_raw<float>(const float *raw, int vec, int t, int j) {
+    return raw[(vec * C + t) * 64 + j];
+}
+template <>
+__device__ __forceinline__ float ld_raw<__nv_bfloat16>(const __nv_bfloat16 *raw, int vec, int t, int j) {
+    return __bfloat162float(raw[(vec * C + t) * 64 + j]);
+}
+
+template <typename E>
+__host__ __device__ constexpr size_t raw_bytes() { return (size_t)6 * C * 64 * sizeof(E); }
+
+// cp.async copies of NV [C][64] token blocks (tokens [t0, t0 + C) of each
+// source, `base` = element offset of (b, t0, h, 0)) into dst[v][C][64];
+// tokens at or beyond `nvalid` are zero-filled.
+template <typename E, int NV, int NTHR>
+__device__ __forceinline__ void stage(E *dst, const E *const (&src)[NV], size_t base, size_t tstride, int nvalid) {
+    constexpr int P = 16 / sizeof(E);
+    constexpr int per_tok = 64 / P;
+    constexpr int per_vec = C * per_tok;
+#pragma unroll
+    for (int vv = 0; vv < NV; ++vv) {
+        for (int e = threadIdx.x; e < per_vec; e += NTHR) {
+            const int u = e / per_tok, n = (e % per_tok) * P;
+            const bool ok = u < nvalid;
+            const E *g = ok ? src[vv] + base + (size_t)u * tstride + n : src[vv];
+            cp_async16(dst + (vv * C + u) * 64 + n, g, ok ? 16 : 0);
+        }
+    }
+}
+
+// Padded fp32 [rows][64] copy (row stride SP) of a dense [rows][64] block.
+template <int NTHR>
+__device__ __forceinline__ void stage_rows(float *dst, const float *src, size_t src_stride, int rows, int nvalid) {
+    for (int e = threadIdx.x; e < rows * 16; e += NTHR) {
+        const int u = e >> 4, n = (e & 15) * 4;
+        const bool ok = u < nvalid;
+        cp_async16(dst + u * SP + n, ok ? src + (size_t)u * src_stride + n : src, ok ? 16 : 0);
+    }
+}
+
+__device__ __forceinline__ float2 f2(const float *a, int row, int col) {
+    return *reinterpret_cast<const float2 *>(a + row * SP + col);
+}
+
+// d_t per key column (threads 0..63); padding tokens (t >= nv) decay by 1.
+// Returns true (on the calling thread) when the chunk's decay underflows.
+template <typename E>
+__device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
+    bool tiny = false;
+    if (threadIdx.x < 64) {
+        const int j = threadIdx.x;
+        float dc = 1.f;
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+            const float wv = t < nv ? ld_raw(raw, VW, t, j) : 1.f;
+            dc = __fmul_rn(dc, wv);
+            dd[t * SP + j] = dc;
+        }
+        tiny = !(dc >= kTiny);
+    }
+    return tiny;
+}
+
+// a^, r^, b~, k~ (token-major, row stride SP).
+template <typename E, int NTHR>
+__device__ __forceinline__ void prep_scaled(const E *raw, const float *dd, float *ah, float *rh, float *bt, float *kt) {
+    for (int e = threadIdx.x; e < C * 64; e += NTHR) {
+        const int t = e >> 6, j = e & 63;
+        const float d = dd[t * SP + j];
+        const float dp = t ? dd[(t - 1) * SP + j] : 1.f;
+        const float inv = __frcp_rn(d);
+        ah[t * SP + j] = ld_raw(raw, VA, t, j) * dp;
+        rh[t * SP + j] = ld_raw(raw, VR, t, j) * d;
+        bt[t * SP + j] = ld_raw(raw, VB, t, j) * inv;
+        kt[t * SP + j] = ld_raw(raw, VK, t, j) * inv;
+    }
+}
+
+// Gram [b~; k~] [a^; r^]^T (32 x 32, contraction over the 64 key columns) on
+// four warps (warp -> one 16-row m-tile and two 8-column n-tiles), written to
+// G[32][GS].  Warps >= 4 do nothing.
+__device__ __forceinline__ void prep_gram(const float *ah, const float *rh, const float *bt, const float *kt,
+                                          float *G) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp >= 4) return;
+    const int g = lane >> 2, q = lane & 3;
+    const int mt = warp >> 1;
+    const float *As = mt ? kt : bt;
+    float acc[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const AFrag af = make_a(f2(As, g, 16 * kk + 2 * q), f2(As, g + 8, 16 * kk + 2 * q),
+                                f2(As, g, 16 * kk + 2 * q + 8), f2(As, g + 8, 16 * kk + 2 * q + 8));
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int nt = 2 * (warp & 1) + u;
+            const float *Bs = nt < 2 ? ah : rh;
+            const int tt = 8 * (nt & 1) + g;
+            mma3(acc[u], af, make_b(f2(Bs, tt, 16 * kk + 2 * q), f2(Bs, tt, 16 * kk + 2 * q + 8)));
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int col = 8 * (2 * (warp & 1) + u) + 2 * q, row = 16 * mt + g;
+        G[row * GS + col] = acc[u][0];
+        G[row * GS + col + 1] = acc[u][1];
+        G[(row + 8) * GS + col] = acc[u][2];
+        G[(row + 8) * GS + col + 1] = acc[u][3];
+    }
+}
+
+// W = (I - M_b)^{-1} (unit upper triangular) by back substitution: lanes
+// 0..15 of warp 0 each build one column.
+__device__ __forceinline__ void prep_inverse(const float *G, float *Wm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp != 0 || lane >= C) return;
+    const int t = lane;
+    float wc[C];
+#pragma unroll
+    for (int s = C - 1; s >= 0; --s) {
+        float acc = (s == t) ? 1.f : 0.f;
+#pragma unroll
+        for (int u = s + 1; u < C; ++u) acc = __fmaf_rn(G[s * GS + u], wc[u], acc);
+        wc[s] = acc;
+    }
+#pragma unroll
+    for (int s = 0; s < C; ++s) Wm[s * WS + t] = wc[s];
+}
+
+}  // namespace chunk
+}  // namespace wkv7
