@@ -208,7 +208,7 @@ def cpu_baseline(spec, target_s=12.0, host_heads=None):
 
 
 def run_reference(args, world, rank):
-    spec = synthetic.WORKLOADS[args.workload]
+    spec = workload_of(args)
     if rank != 0:
         return
     cores = os.cpu_count() or 1
@@ -242,10 +242,18 @@ def config_of(spec, args):
 
 # ------------------------------------------------------------------ GPU leg
 
+def workload_of(args):
+    spec = synthetic.WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        spec = dataclasses.replace(spec, B=args.batch, name=f"{spec.name}@B={args.batch}")
+    return spec
+
+
 def run_ours(args, world, rank, local):
     from rwkv_linear_attention_wkv7_gb300 import build, wkv7
     build()
-    spec = synthetic.WORKLOADS[args.workload]
+    spec = workload_of(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
@@ -383,6 +391,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B of the workload (smaller profiling cases of the same kernels)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
