@@ -76,15 +76,25 @@ __device__ __forceinline__ void stage_rows(float *dst, const float *src, size_t 
     }
 }
 
+// Hardware approximate reciprocal (rcp.approx, about 1 ulp); used for 1/d_t,
+// whose rounding is far below the split-bf16 product error.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float2 f2(const float *a, int row, int col) {
     return *reinterpret_cast<const float2 *>(a + row * SP + col);
 }
 
 // d_t per key column (threads 0..63); padding tokens (t >= nv) decay by 1.
-// Returns true (on the calling thread) when the chunk's decay underflows.
+// Returns true (on the calling thread) when some d_t of its column leaves
+// [1e-20, 1e20] (or is not finite): the factorised form then cannot divide
+// by d_t and the chunk takes the exact per-token path.
 template <typename E>
 __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
-    bool tiny = false;
+    bool bad = false;
     if (threadIdx.x < 64) {
         const int j = threadIdx.x;
         float dc = 1.f;
@@ -93,10 +103,10 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
             const float wv = t < nv ? ld_raw(raw, VW, t, j) : 1.f;
             dc = __fmul_rn(dc, wv);
             dd[t * SP + j] = dc;
+            bad |= !(dc >= kTiny && dc <= 1.f / kTiny);
         }
-        tiny = !(dc >= kTiny);
     }
-    return tiny;
+    return bad;
 }
 
 // a^, r^, b~, k~ (token-major, row stride SP).
