@@ -166,9 +166,11 @@ __device__ __forceinline__ void prep_inverse(const float *G, float *Wm) {
     float wc[C];
 #pragma unroll
     for (int s = C - 1; s >= 0; --s) {
+        // sum the terms of the rows found longest ago first, so that only one
+        // FMA depends on the row computed just before (wc[s + 1])
         float acc = (s == t) ? 1.f : 0.f;
 #pragma unroll
-        for (int u = s + 1; u < C; ++u) acc = __fmaf_rn(G[s * GS + u], wc[u], acc);
+        for (int u = C - 1; u > s; --u) acc = __fmaf_rn(G[s * GS + u], wc[u], acc);
         wc[s] = acc;
     }
 #pragma unroll
