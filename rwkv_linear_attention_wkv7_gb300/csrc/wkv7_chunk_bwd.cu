@@ -245,6 +245,21 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     auto r_hat = [&](int t, int j) { return ld_raw(raw, VR, t, j) * dd[t * SP + j]; };
     auto b_til = [&](int t, int j) { return ld_raw(raw, VB, t, j) * rcp_approx(dd[t * SP + j]); };
     auto k_til = [&](int t, int j) { return ld_raw(raw, VK, t, j) * rcp_approx(dd[t * SP + j]); };
+    // pairs (j, j + 1), j even: one load each for the input and the decay
+    auto d2 = [&](int t, int j) { return *reinterpret_cast<const float2 *>(dd + t * SP + j); };
+    auto a_hat2 = [&](int t, int j) {
+        const float2 x = ld_raw2(raw, VA, t, j);
+        const float2 d = t ? d2(t - 1, j) : make_float2(1.f, 1.f);
+        return make_float2(x.x * d.x, x.y * d.y);
+    };
+    auto r_hat2 = [&](int t, int j) {
+        const float2 x = ld_raw2(raw, VR, t, j), d = d2(t, j);
+        return make_float2(x.x * d.x, x.y * d.y);
+    };
+    auto bk_til2 = [&](int vec, int t, int j) {
+        const float2 x = ld_raw2(raw, vec, t, j), d = d2(t, j);
+        return make_float2(x.x * rcp_approx(d.x), x.y * rcp_approx(d.y));
+    };
 
     float Gh[8][4];  // dL/dS at the current chunk end, rows rA/rB, columns 8nt+2q+{0,1}
 #pragma unroll
@@ -300,27 +315,15 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const int j0 = 16 * kk + 2 * q;
-                float x[8];
-                if (mt == 0) {
-                    x[0] = b_til(g, j0); x[1] = b_til(g, j0 + 1); x[2] = b_til(g + 8, j0); x[3] = b_til(g + 8, j0 + 1);
-                    x[4] = b_til(g, j0 + 8); x[5] = b_til(g, j0 + 9); x[6] = b_til(g + 8, j0 + 8); x[7] = b_til(g + 8, j0 + 9);
-                } else {
-                    x[0] = k_til(g, j0); x[1] = k_til(g, j0 + 1); x[2] = k_til(g + 8, j0); x[3] = k_til(g + 8, j0 + 1);
-                    x[4] = k_til(g, j0 + 8); x[5] = k_til(g, j0 + 9); x[6] = k_til(g + 8, j0 + 8); x[7] = k_til(g + 8, j0 + 9);
-                }
-                const AFrag af = make_a(make_float2(x[0], x[1]), make_float2(x[2], x[3]), make_float2(x[4], x[5]),
-                                        make_float2(x[6], x[7]));
+                const int av = mt ? VK : VB;
+                const AFrag af = make_a(bk_til2(av, g, j0), bk_til2(av, g + 8, j0), bk_til2(av, g, j0 + 8),
+                                        bk_til2(av, g + 8, j0 + 8));
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int nt = 2 * (warp & 1) + u;
                     const int tt = 8 * (nt & 1) + g;
-                    float y0, y1, y8, y9;
-                    if (nt < 2) {
-                        y0 = a_hat(tt, j0); y1 = a_hat(tt, j0 + 1); y8 = a_hat(tt, j0 + 8); y9 = a_hat(tt, j0 + 9);
-                    } else {
-                        y0 = r_hat(tt, j0); y1 = r_hat(tt, j0 + 1); y8 = r_hat(tt, j0 + 8); y9 = r_hat(tt, j0 + 9);
-                    }
-                    mma3(acc[u], af, make_b(make_float2(y0, y1), make_float2(y8, y9)));
+                    const BFrag bf = nt < 2 ? make_b(a_hat2(tt, j0), a_hat2(tt, j0 + 8)) : make_b(r_hat2(tt, j0), r_hat2(tt, j0 + 8));
+                    mma3(acc[u], af, bf);
                 }
             }
 #pragma unroll
@@ -553,8 +556,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 const float2 a = f2(s_, t, i0), b = f2(s_, t, i0 + 8);
                 x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;
             } else if (nt < 2) {
-                x0 = ld_raw(raw, VV, t, i0); x1 = ld_raw(raw, VV, t, i0 + 1);
-                x8 = ld_raw(raw, VV, t, i0 + 8); x9 = ld_raw(raw, VV, t, i0 + 9);
+                const float2 a = ld_raw2(raw, VV, t, i0), b = ld_raw2(raw, VV, t, i0 + 8);
+                x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;
             } else {
                 const float2 a = f2(SAt, t, i0), b = f2(SAt, t, i0 + 8);
                 x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;

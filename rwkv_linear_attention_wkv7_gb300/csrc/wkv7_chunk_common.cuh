@@ -23,6 +23,7 @@ constexpr int C = 16;          // tokens per chunk
 constexpr int SP = 72;         // row stride (floats) of [token][64] and [row][64] arrays
 constexpr int GS = 33;         // row stride of 32x32 Grams
 constexpr int WS = 17;         // row stride of W
+constexpr int RS = 72;         // row stride (elements) of the staged raw inputs: rows start 4 banks apart
 constexpr float kTiny = 1e-20f;  // smallest cumulative decay the factorised form accepts
 enum { VR = 0, VW = 1, VK = 2, VV = 3, VA = 4, VB = 5 };
 
@@ -37,15 +38,28 @@ template <typename E>
 __device__ __forceinline__ float ld_raw(const E *raw, int vec, int t, int j);
 template <>
 __device__ __forceinline__ float ld_raw<float>(const float *raw, int vec, int t, int j) {
-    return raw[(vec * C + t) * 64 + j];
+    return raw[(vec * C + t) * RS + j];
 }
 template <>
 __device__ __forceinline__ float ld_raw<__nv_bfloat16>(const __nv_bfloat16 *raw, int vec, int t, int j) {
-    return __bfloat162float(raw[(vec * C + t) * 64 + j]);
+    return __bfloat162float(raw[(vec * C + t) * RS + j]);
+}
+
+// Elements j and j + 1 (j even) of a staged row as one 32/64-bit load.
+template <typename E>
+__device__ __forceinline__ float2 ld_raw2(const E *raw, int vec, int t, int j);
+template <>
+__device__ __forceinline__ float2 ld_raw2<float>(const float *raw, int vec, int t, int j) {
+    return *reinterpret_cast<const float2 *>(raw + (vec * C + t) * RS + j);
+}
+template <>
+__device__ __forceinline__ float2 ld_raw2<__nv_bfloat16>(const __nv_bfloat16 *raw, int vec, int t, int j) {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(raw + (vec * C + t) * RS + j);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 template <typename E>
-__host__ __device__ constexpr size_t raw_bytes() { return (size_t)6 * C * 64 * sizeof(E); }
+__host__ __device__ constexpr size_t raw_bytes() { return (size_t)6 * C * RS * sizeof(E); }
 
 // cp.async copies of NV [C][64] token blocks (tokens [t0, t0 + C) of each
 // source, `base` = element offset of (b, t0, h, 0)) into dst[v][C][64];
@@ -61,7 +75,7 @@ __device__ __forceinline__ void stage(E *dst, const E *const (&src)[NV], size_t 
             const int u = e / per_tok, n = (e % per_tok) * P;
             const bool ok = u < nvalid;
             const E *g = ok ? src[vv] + base + (size_t)u * tstride + n : src[vv];
-            cp_async16(dst + (vv * C + u) * 64 + n, g, ok ? 16 : 0);
+            cp_async16(dst + (vv * C + u) * RS + n, g, ok ? 16 : 0);
         }
     }
 }
