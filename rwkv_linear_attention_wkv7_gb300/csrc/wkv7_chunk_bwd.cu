@@ -31,29 +31,8 @@ namespace {
 using namespace chunk;
 
 constexpr int NT = 128;
-constexpr int QS = 36;   // QM [C][QS]: M_k' in columns 16..31
 constexpr unsigned kFull = 0xffffffffu;
 
-// Float offsets of the shared-memory carve-up (after the raw input block).
-constexpr int O_DY = 0;                   // dy       [C][SP]
-constexpr int O_S0 = O_DY + C * SP;       // S_0      [64][SP]
-constexpr int O_GD = O_S0 + 64 * SP;      // G d_C    [64][SP]  (exact path: S_{t-1})
-constexpr int O_DD = O_GD + 64 * SP;      // d        [C][SP]
-constexpr int O_G = O_DD + C * SP;        // Gram, then Gam [32][GS]
-constexpr int O_W = O_G + C * SP;         // W [C][WS]
-constexpr int O_QM = O_W + C * WS;        // M_k' in columns 16..31 [C][QS]
-constexpr int O_SAT = O_QM + C * QS;      // SA (token-major) [C][SP]
-constexpr int O_DST = O_SAT + C * SP;     // DSA (token-major) [C][SP]; dw start scratch
-constexpr int O_X = O_DST + C * SP;       // u32 x 4096: G1/G2 operands, then [DY|DSA], [V|SA]; exact-path scratch
-constexpr int O_B5 = O_X + 4096;          // u32 x 2048: B of G_prev's product
-constexpr int O_GM = O_B5 + 2048;         // u32 x 2048: masked Gam blocks
-constexpr int kFloats = O_GM + 2048;
-static_assert(32 * GS <= C * SP, "Gam must fit its slot");
-static_assert(5 * 4 * 64 <= 4096, "exact-path scratch must fit region X");
-static_assert(O_X % 4 == 0 && O_B5 % 4 == 0 && O_GM % 4 == 0, "16-byte fragment buffers");
-
-template <typename E>
-__host__ __device__ constexpr size_t bwd_smem_bytes() { return raw_bytes<E>() + (size_t)kFloats * sizeof(float); }
 
 __device__ __forceinline__ float quad_sum(float x) {
     x += __shfl_xor_sync(kFull, x, 1);
@@ -194,44 +173,74 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
     }
 }
 
+// Shared-memory carve-up (byte offsets after the raw input block).  HL16 /
+// HL32 / HL64 = split operand matrices (bf16 hi then lo) of 16 / 32 / 64 rows
+// with row stride MS.
+constexpr int HL16 = 2 * 16 * MS * 2, HL32 = 2 * HL16, HL64 = 2 * HL32;
+constexpr int B_DYF = 0;                       // dy fp32 [C][SP]        (chunk start .. conversion)
+constexpr int B_DD = B_DYF + C * SP * 4;       // d fp32 [C][SP]
+constexpr int B_G = B_DD + C * SP * 4;         // Gram, then Gam, fp32 [32][GS] (slot C*SP floats)
+constexpr int B_W = B_G + C * SP * 4;          // W fp32 [C][WS]
+constexpr int B_SX = B_W + 1104;               // S_0: fp32 [64][SP] staging, then HL64; then G d_C (HL64)
+constexpr int B_BT = B_SX + HL64;              // b~, k~, a^, r^ (HL16 each) [t][j]; exact path: S_{t-1} fp32
+constexpr int B_KT = B_BT + HL16;
+constexpr int B_AH = B_KT + HL16;
+constexpr int B_RH = B_AH + HL16;
+constexpr int B_VV = B_RH + HL16;              // v [t][i]
+constexpr int B_DYH = B_VV + HL16;             // dy [t][i]
+constexpr int B_SAH = B_DYH + HL16;            // SA [t][i]
+constexpr int B_DSH = B_SAH + HL16;            // DSA [t][i]
+constexpr int B_Y = B_DSH + HL16;              // A' [t][j] (HL16), M_k' [s][t] (HL16), [K'; B'] (HL32), [Q'; W Q_b] (HL32)
+constexpr int B_AP = B_Y, B_MK = B_Y + HL16, B_KB = B_Y + 2 * HL16, B_QQ = B_KB + HL32;
+constexpr int B_M3 = B_Y, B_M4 = B_Y + HL32;   // masked Gam blocks [k][n] (HL32 each), after G1/G2
+constexpr int kBytes = B_QQ + HL32;
+static_assert(B_SX % 16 == 0 && B_BT % 16 == 0 && B_Y % 16 == 0, "16-byte aligned operand matrices");
+static_assert(32 * GS <= C * SP && C * WS * 4 <= 1104, "small fp32 blocks fit");
+static_assert(64 * SP * 4 == HL64, "S_0 staging and its split share one slot");
+static_assert(4 * HL16 >= 64 * SP * 4, "exact-path S_{t-1} fits the four scaled blocks");
+static_assert(5 * 4 * 64 * 4 <= 2 * HL32, "exact-path scratch fits region Y");
 
-__device__ __forceinline__ uint4 pack_b(float x0, float x1, float x8, float x9) {
-    const Frag2 a = split2(x0, x1), b = split2(x8, x9);
-    return make_uint4(a.hi, b.hi, a.lo, b.lo);
+template <typename E>
+__host__ __device__ constexpr size_t bwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
+
+__device__ __forceinline__ HL hl(const unsigned char *base, int off, int rows) {
+    const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
+    return HL{p, p + rows * MS};
 }
-__device__ __forceinline__ BFrag ld_b(const uint32_t *buf, int idx) {
-    const uint4 u = reinterpret_cast<const uint4 *>(buf)[idx];
-    BFrag f;
-    f.hi[0] = u.x; f.hi[1] = u.y; f.lo[0] = u.z; f.lo[1] = u.w;
-    return f;
+__device__ __forceinline__ __nv_bfloat16 *hi_of(unsigned char *base, int off) {
+    return reinterpret_cast<__nv_bfloat16 *>(base + off);
 }
-// A fragment (16 rows x 16 k) assembled from the B fragments of the two
-// n-tiles that hold those rows (same element pairs, other register order).
-__device__ __forceinline__ AFrag a_from_b(const uint32_t *buf, int idx_rows0_7, int idx_rows8_15) {
-    const uint4 u = reinterpret_cast<const uint4 *>(buf)[idx_rows0_7];
-    const uint4 v = reinterpret_cast<const uint4 *>(buf)[idx_rows8_15];
-    AFrag f;
-    f.hi[0] = u.x; f.hi[1] = v.x; f.hi[2] = u.y; f.hi[3] = v.y;
-    f.lo[0] = u.z; f.lo[1] = v.z; f.lo[2] = u.w; f.lo[3] = v.w;
-    return f;
+__device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off, int rows) {
+    return reinterpret_cast<__nv_bfloat16 *>(base + off) + rows * MS;
 }
-__device__ __forceinline__ void st_b_half(uint32_t *buf, int idx, int half, const Frag2 &f) {
-    buf[idx * 4 + half] = f.hi;
-    buf[idx * 4 + 2 + half] = f.lo;
+// split x into (hi, lo) and store both at element (row, col) of a split matrix
+__device__ __forceinline__ void st_hl1(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row, int col, float x) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi[row * MS + col] = h;
+    lo[row * MS + col] = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+// fp32 values of an A fragment's 8 elements (hi + lo), in C-tile order:
+// v[0..1] = (row g, k 2q..2q+1), v[2..3] = (row g+8, ..), v[4..5] = (row g, k 2q+8..), v[6..7] = (row g+8, ..)
+__device__ __forceinline__ void a_values(const AFrag &f, float v[8]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        v[2 * r] = __uint_as_float(f.hi[r] << 16) + __uint_as_float(f.lo[r] << 16);
+        v[2 * r + 1] = __uint_as_float(f.hi[r] & 0xffff0000u) + __uint_as_float(f.lo[r] & 0xffff0000u);
+    }
 }
 
 template <typename E>
 __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
     E *raw = reinterpret_cast<E *>(smem);
-    float *F = reinterpret_cast<float *>(smem + raw_bytes<E>());
-    float *dys = F + O_DY, *S0s = F + O_S0, *Gds = F + O_GD, *dd = F + O_DD, *Gm = F + O_G, *Wm = F + O_W;
-    float *QM = F + O_QM, *SAt = F + O_SAT, *DSt = F + O_DST;
-    uint32_t *X = reinterpret_cast<uint32_t *>(F + O_X);
-    uint32_t *B1 = X, *B1V = X + 1024, *B2 = X + 1280, *B2D = X + 3328;  // per-chunk operands
-    uint32_t *DYDS = X, *VSA = X + 2048;                                  // after G1/G2
-    uint32_t *B5 = reinterpret_cast<uint32_t *>(F + O_B5);
-    uint32_t *GM3 = reinterpret_cast<uint32_t *>(F + O_GM), *GM4 = GM3 + 1024;
+    unsigned char *Bs = smem + raw_bytes<E>();
+    float *dyf = reinterpret_cast<float *>(Bs + B_DYF), *dd = reinterpret_cast<float *>(Bs + B_DD);
+    float *Gm = reinterpret_cast<float *>(Bs + B_G), *Wm = reinterpret_cast<float *>(Bs + B_W);
+    float *S0f = reinterpret_cast<float *>(Bs + B_SX);
+    const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, B_BT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, B_AH, 16),
+             RH = hl(Bs, B_RH, 16), VM = hl(Bs, B_VV, 16), DYH = hl(Bs, B_DYH, 16), SAH = hl(Bs, B_SAH, 16),
+             DSH = hl(Bs, B_DSH, 16), AP = hl(Bs, B_AP, 16), MK = hl(Bs, B_MK, 16), KB = hl(Bs, B_KB, 32),
+             QQ = hl(Bs, B_QQ, 32), M3 = hl(Bs, B_M3, 32), M4 = hl(Bs, B_M4, 32);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -240,26 +249,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     const size_t base0 = ((size_t)bi * p.T * p.H + h) * 64;
     const size_t sbase = (size_t)bh * 64 * 64;
     const int rA = warp * 16 + g, rB = rA + 8;  // value rows (row-owned products) / key rows (G3, G4)
-
-    auto a_hat = [&](int t, int j) { return ld_raw(raw, VA, t, j) * (t ? dd[(t - 1) * SP + j] : 1.f); };
-    auto r_hat = [&](int t, int j) { return ld_raw(raw, VR, t, j) * dd[t * SP + j]; };
-    auto b_til = [&](int t, int j) { return ld_raw(raw, VB, t, j) * rcp_approx(dd[t * SP + j]); };
-    auto k_til = [&](int t, int j) { return ld_raw(raw, VK, t, j) * rcp_approx(dd[t * SP + j]); };
-    // pairs (j, j + 1), j even: one load each for the input and the decay
-    auto d2 = [&](int t, int j) { return *reinterpret_cast<const float2 *>(dd + t * SP + j); };
-    auto a_hat2 = [&](int t, int j) {
-        const float2 x = ld_raw2(raw, VA, t, j);
-        const float2 d = t ? d2(t - 1, j) : make_float2(1.f, 1.f);
-        return make_float2(x.x * d.x, x.y * d.y);
-    };
-    auto r_hat2 = [&](int t, int j) {
-        const float2 x = ld_raw2(raw, VR, t, j), d = d2(t, j);
-        return make_float2(x.x * d.x, x.y * d.y);
-    };
-    auto bk_til2 = [&](int vec, int t, int j) {
-        const float2 x = ld_raw2(raw, vec, t, j), d = d2(t, j);
-        return make_float2(x.x * rcp_approx(d.x), x.y * rcp_approx(d.y));
-    };
 
     float Gh[8][4];  // dL/dS at the current chunk end, rows rA/rB, columns 8nt+2q+{0,1}
 #pragma unroll
@@ -277,13 +266,15 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     const E *const src[6] = {static_cast<const E *>(p.r), static_cast<const E *>(p.w), static_cast<const E *>(p.k),
                              static_cast<const E *>(p.v), static_cast<const E *>(p.a), static_cast<const E *>(p.b)};
     const int nchunks = (p.T + C - 1) / C;
-    {
-        const int c = nchunks - 1, t0 = c * C, nv = min(C, p.T - t0);
+    auto stage_in = [&](int c) {  // inputs and dy of chunk c
+        const int t0 = c * C, nv = min(C, p.T - t0);
         stage<E, 6, NT>(raw, src, base0 + (size_t)t0 * tstride, tstride, nv);
-        stage_rows<NT>(dys, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
-        stage_rows<NT>(S0s, p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64, 64, 64, 64);
-        cp_async_commit();
-    }
+        stage_rows<NT>(dyf, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
+    };
+    auto stage_s0 = [&](int c) { stage_rows<NT>(S0f, p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64, 64, 64, 64); };
+    stage_in(nchunks - 1);
+    stage_s0(nchunks - 1);
+    cp_async_commit();
 
     for (int c = nchunks - 1; c >= 0; --c) {
         const int t0 = c * C;
@@ -294,37 +285,65 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (exact) {
-            bwd_chunk_exact<E>(raw, dys, S0s, Gds, reinterpret_cast<float *>(X), Gh, nv, p, base0, tstride, t0,
-                               carryA, carryB);
+            bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
+                               Gh, nv, p, base0, tstride, t0, carryA, carryB);
             __syncthreads();
             if (c > 0) {
-                stage<E, 6, NT>(raw, src, base0 + (size_t)(t0 - C) * tstride, tstride, C);
-                stage_rows<NT>(dys, p.dy + base0 + (size_t)(t0 - C) * tstride, tstride, C, C);
-                stage_rows<NT>(S0s, p.ckpt_in + ((size_t)bh * p.nck + c - 1) * 64 * 64, 64, 64, 64);
+                stage_in(c - 1);
+                stage_s0(c - 1);
             }
             cp_async_commit();
             continue;
         }
         const float *dC = dd + (C - 1) * SP;
 
+        // ================= split every operand matrix once
+        {   // S_0 in place: fp32 staging -> hi/lo
+            float2 sv[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int e = tid + NT * m, row = e >> 5, col = (e & 31) * 2;
+                sv[m] = *reinterpret_cast<const float2 *>(S0f + row * SP + col);
+            }
+            __syncthreads();
+            __nv_bfloat16 *sh = hi_of(Bs, B_SX), *sl = lo_of(Bs, B_SX, 64);
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int e = tid + NT * m, row = e >> 5, col = (e & 31) * 2;
+                st_hl(sh, sl, row, col, sv[m].x, sv[m].y);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {  // decay-scaled vectors, v and dy: [t][j] pairs
+            const int e = tid + NT * m, t = e >> 5, j = (e & 31) * 2;
+            const float2 d = *reinterpret_cast<const float2 *>(dd + t * SP + j);
+            const float2 dp = t ? *reinterpret_cast<const float2 *>(dd + (t - 1) * SP + j) : make_float2(1.f, 1.f);
+            const float i0 = rcp_approx(d.x), i1 = rcp_approx(d.y);
+            float2 x;
+            x = ld_raw2(raw, VB, t, j); st_hl(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, x.x * i0, x.y * i1);
+            x = ld_raw2(raw, VK, t, j); st_hl(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, x.x * i0, x.y * i1);
+            x = ld_raw2(raw, VA, t, j); st_hl(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, x.x * dp.x, x.y * dp.y);
+            x = ld_raw2(raw, VR, t, j); st_hl(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, x.x * d.x, x.y * d.y);
+            x = ld_raw2(raw, VV, t, j); st_hl(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, j, x.x, x.y);
+            x = *reinterpret_cast<const float2 *>(dyf + t * SP + j);
+            st_hl(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, x.x, x.y);
+        }
+        __syncthreads();
+        // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
+        if (c > 0) stage_in(c - 1);
+        cp_async_commit();
+
         // ================= per-chunk operands (no state involved)
-        // Gram [B~; K~] [A^; R^]^T on the fly: warp -> m-tile (b~ | k~), two n-tiles (a^ | r^)
-        {
+        {   // Gram [B~; K~] [A^; R^]^T: warp -> m-tile (b~ | k~), n-tile pair (a^ | r^)
             const int mt = warp >> 1;
             float acc[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const int j0 = 16 * kk + 2 * q;
-                const int av = mt ? VK : VB;
-                const AFrag af = make_a(bk_til2(av, g, j0), bk_til2(av, g + 8, j0), bk_til2(av, g, j0 + 8),
-                                        bk_til2(av, g + 8, j0 + 8));
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int nt = 2 * (warp & 1) + u;
-                    const int tt = 8 * (nt & 1) + g;
-                    const BFrag bf = nt < 2 ? make_b(a_hat2(tt, j0), a_hat2(tt, j0 + 8)) : make_b(r_hat2(tt, j0), r_hat2(tt, j0 + 8));
-                    mma3(acc[u], af, bf);
-                }
+                const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
+                BFrag b0, b1;
+                ldb2((warp & 1) ? RH : AH, 0, 16 * kk, lane, b0, b1);
+                mma3(acc[0], af, b0);
+                mma3(acc[1], af, b1);
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -335,46 +354,28 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 Gm[(row + 8) * GS + col + 1] = acc[u][3];
             }
         }
-        // B fragments of G_prev's product [DY | DSA] [R^ | A^]^T: B[k = token][n = key column]
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int f = tid + NT * m;  // 512 fragments: kt = f >> 8 (0: r^, 1: a^), nt = (f >> 5) & 7
-            const int kt = f >> 8, nt = (f >> 5) & 7, ln = f & 31, gg = ln >> 2, qq = ln & 3, j = 8 * nt + gg;
-            float x[4];
-            const int s4[4] = {2 * qq, 2 * qq + 1, 2 * qq + 8, 2 * qq + 9};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = kt ? a_hat(s4[e], j) : r_hat(s4[e], j);
-            reinterpret_cast<uint4 *>(B5)[f] = pack_b(x[0], x[1], x[2], x[3]);
-        }
-        // G diag(d_C) for Gd^T (rows = value index)
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int j0 = 8 * nt + 2 * q;
-            const float2 dc = *reinterpret_cast<const float2 *>(dC + j0);
-            *reinterpret_cast<float2 *>(Gds + rA * SP + j0) = make_float2(Gh[nt][0] * dc.x, Gh[nt][1] * dc.y);
-            *reinterpret_cast<float2 *>(Gds + rB * SP + j0) = make_float2(Gh[nt][2] * dc.x, Gh[nt][3] * dc.y);
-        }
         __syncthreads();
         prep_inverse(Gm, Wm);
         __syncthreads();
-
-        // W^T as an A operand: wt[t][s] = W[s][t]
-        const AFrag wt = make_a(make_float2(Wm[(2 * q) * WS + g], Wm[(2 * q + 1) * WS + g]),
-                                make_float2(Wm[(2 * q) * WS + g + 8], Wm[(2 * q + 1) * WS + g + 8]),
-                                make_float2(Wm[(2 * q + 8) * WS + g], Wm[(2 * q + 9) * WS + g]),
-                                make_float2(Wm[(2 * q + 8) * WS + g + 8], Wm[(2 * q + 9) * WS + g + 8]));
-        // A' = W^T-weighted A^ (M = token, N = key; warp w owns keys 16w..16w+15) -> B of G1
+        {   // A' = W^T-weighted A^ (M = token, N = key; warp w owns keys 16w..16w+15)
+            const AFrag wt = make_a(make_float2(Wm[(2 * q) * WS + g], Wm[(2 * q + 1) * WS + g]),
+                                    make_float2(Wm[(2 * q) * WS + g + 8], Wm[(2 * q + 1) * WS + g + 8]),
+                                    make_float2(Wm[(2 * q + 8) * WS + g], Wm[(2 * q + 9) * WS + g]),
+                                    make_float2(Wm[(2 * q + 8) * WS + g + 8], Wm[(2 * q + 9) * WS + g + 8]));
+            BFrag b0, b1;
+            ldb2_t(AH, 16 * warp, 0, lane, b0, b1);
+            float ca[2][4] = {};
+            mma3(ca[0], wt, b0);
+            mma3(ca[1], wt, b1);
+            __nv_bfloat16 *ah = hi_of(Bs, B_AP), *al = lo_of(Bs, B_AP, 16);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int jn = 16 * warp + 8 * u + g;
-            float ca[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3(ca, wt, make_b(make_float2(a_hat(2 * q, jn), a_hat(2 * q + 1, jn)),
-                                make_float2(a_hat(2 * q + 8, jn), a_hat(2 * q + 9, jn))));
-            // G1 B layout: [kt = warp][nt = token half][lane], register half u
-            st_b_half(B1, (warp * 2 + 0) * 32 + lane, u, split2(ca[0], ca[1]));
-            st_b_half(B1, (warp * 2 + 1) * 32 + lane, u, split2(ca[2], ca[3]));
+            for (int u = 0; u < 2; ++u) {
+                const int jc = 16 * warp + 8 * u + 2 * q;
+                st_hl(ah, al, g, jc, ca[u][0], ca[u][1]);
+                st_hl(ah, al, g + 8, jc, ca[u][2], ca[u][3]);
+            }
         }
-        if (warp == 0) {  // M_k' = M_k W, Q' = Q_k + M_k' Q_b, Q_b' = W Q_b (all 16 x 16)
+        if (warp == 0) {  // M_k' = M_k W, Q' = Q_k + M_k' Q_b, W Q_b (all 16 x 16)
             auto mk = [&](int s, int u) { return u > s ? Gm[(16 + s) * GS + u] : 0.f; };
             auto qbv = [&](int u, int t) { return u <= t ? Gm[u * GS + 16 + t] : 0.f; };
             auto qkv = [&](int s, int t) { return s <= t ? Gm[(16 + s) * GS + 16 + t] : 0.f; };
@@ -404,114 +405,113 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 mma3(cq[nt], amp, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
                                          make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
             }
-            // DY-side B of G2: B[k = s][n] = Q'[n][s] (n < 16), (W Q_b)[n - 16][s]; C rows of Q' / W Q_b are n
+            __nv_bfloat16 *mh = hi_of(Bs, B_MK), *ml = lo_of(Bs, B_MK, 16);
+            __nv_bfloat16 *qh = hi_of(Bs, B_QQ), *ql = lo_of(Bs, B_QQ, 32);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {  // column half nt of the C tile = register half of the B fragment
-                st_b_half(B2D, 0 * 32 + lane, nt, split2(cq[nt][0], cq[nt][1]));
-                st_b_half(B2D, 1 * 32 + lane, nt, split2(cq[nt][2], cq[nt][3]));
-                st_b_half(B2D, 2 * 32 + lane, nt, split2(cb[nt][0], cb[nt][1]));
-                st_b_half(B2D, 3 * 32 + lane, nt, split2(cb[nt][2], cb[nt][3]));
+            for (int nt = 0; nt < 2; ++nt) {
                 const int tc = 8 * nt + 2 * q;
-                QM[g * QS + 16 + tc] = cm[nt][0]; QM[g * QS + 16 + tc + 1] = cm[nt][1];
-                QM[(g + 8) * QS + 16 + tc] = cm[nt][2]; QM[(g + 8) * QS + 16 + tc + 1] = cm[nt][3];
-            }
-            __syncwarp();
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {  // V-side B of G1: B[k = s][n = t] = M_k'[s][t]
-                const int n = 16 + 8 * nt + g;
-                reinterpret_cast<uint4 *>(B1V)[nt * 32 + lane] =
-                    pack_b(QM[(2 * q) * QS + n], QM[(2 * q + 1) * QS + n], QM[(2 * q + 8) * QS + n], QM[(2 * q + 9) * QS + n]);
+                st_hl(mh, ml, g, tc, cm[nt][0], cm[nt][1]);       // M_k'[s][t]
+                st_hl(mh, ml, g + 8, tc, cm[nt][2], cm[nt][3]);
+                st_hl(qh, ql, g, tc, cq[nt][0], cq[nt][1]);       // Q'[t][s]
+                st_hl(qh, ql, g + 8, tc, cq[nt][2], cq[nt][3]);
+                st_hl(qh, ql, 16 + g, tc, cb[nt][0], cb[nt][1]);  // (W Q_b)[t][s]
+                st_hl(qh, ql, 24 + g, tc, cb[nt][2], cb[nt][3]);
             }
         }
         __syncthreads();
-        // K' = d_C o (K~ + M_k' B~) and B' = d_C o (W B~)  (M = token, N = key) -> B of G2
-        {
-            auto mkp = [&](int t, int s) { return QM[t * QS + 16 + s]; };
-            const AFrag amk = make_a(make_float2(mkp(g, 2 * q), mkp(g, 2 * q + 1)), make_float2(mkp(g + 8, 2 * q), mkp(g + 8, 2 * q + 1)),
-                                     make_float2(mkp(g, 2 * q + 8), mkp(g, 2 * q + 9)),
-                                     make_float2(mkp(g + 8, 2 * q + 8), mkp(g + 8, 2 * q + 9)));
+        {   // K' = d_C o (K~ + M_k' B~), B' = d_C o (W B~) (M = token, N = key; warp w owns keys 16w..)
+            const AFrag amk = lda(MK, 0, 0, lane);
             const AFrag awn = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
                                      make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
                                      make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
                                      make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+            BFrag b0, b1;
+            ldb2_t(BT, 16 * warp, 0, lane, b0, b1);
+            __nv_bfloat16 *kh = hi_of(Bs, B_KB), *kl = lo_of(Bs, B_KB, 32);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int jn = 16 * warp + 8 * u + g, jc = 16 * warp + 8 * u + 2 * q;
-                const BFrag bb = make_b(make_float2(b_til(2 * q, jn), b_til(2 * q + 1, jn)),
-                                        make_float2(b_til(2 * q + 8, jn), b_til(2 * q + 9, jn)));
-                float ck[4] = {k_til(g, jc), k_til(g, jc + 1), k_til(g + 8, jc), k_til(g + 8, jc + 1)};
+                const int jc = 16 * warp + 8 * u + 2 * q;
+                const float2 k0 = ld_hl(KT.hi, KT.lo, g, jc), k8 = ld_hl(KT.hi, KT.lo, g + 8, jc);
+                float ck[4] = {k0.x, k0.y, k8.x, k8.y};
                 float cb2[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3(ck, amk, bb);
-                mma3(cb2, awn, bb);
+                mma3(ck, amk, u ? b1 : b0);
+                mma3(cb2, awn, u ? b1 : b0);
                 const float2 dc = *reinterpret_cast<const float2 *>(dC + jc);
-                ck[0] *= dc.x; ck[1] *= dc.y; ck[2] *= dc.x; ck[3] *= dc.y;
-                cb2[0] *= dc.x; cb2[1] *= dc.y; cb2[2] *= dc.x; cb2[3] *= dc.y;
-                // G2 B layout: [kt = warp][nt: 0,1 = K' token halves, 2,3 = B'][lane], register half u
-                st_b_half(B2, (warp * 4 + 0) * 32 + lane, u, split2(ck[0], ck[1]));
-                st_b_half(B2, (warp * 4 + 1) * 32 + lane, u, split2(ck[2], ck[3]));
-                st_b_half(B2, (warp * 4 + 2) * 32 + lane, u, split2(cb2[0], cb2[1]));
-                st_b_half(B2, (warp * 4 + 3) * 32 + lane, u, split2(cb2[2], cb2[3]));
+                st_hl(kh, kl, g, jc, ck[0] * dc.x, ck[1] * dc.y);
+                st_hl(kh, kl, g + 8, jc, ck[2] * dc.x, ck[3] * dc.y);
+                st_hl(kh, kl, 16 + g, jc, cb2[0] * dc.x, cb2[1] * dc.y);
+                st_hl(kh, kl, 24 + g, jc, cb2[2] * dc.x, cb2[3] * dc.y);
             }
         }
         __syncthreads();
 
         // ================= state-dependent products
-        const AFrag vA = make_a(make_float2(ld_raw(raw, VV, 2 * q, rA), ld_raw(raw, VV, 2 * q + 1, rA)),
-                                make_float2(ld_raw(raw, VV, 2 * q, rB), ld_raw(raw, VV, 2 * q + 1, rB)),
-                                make_float2(ld_raw(raw, VV, 2 * q + 8, rA), ld_raw(raw, VV, 2 * q + 9, rA)),
-                                make_float2(ld_raw(raw, VV, 2 * q + 8, rB), ld_raw(raw, VV, 2 * q + 9, rB)));
-        const AFrag dyA = make_a(make_float2(dys[(2 * q) * SP + rA], dys[(2 * q + 1) * SP + rA]),
-                                 make_float2(dys[(2 * q) * SP + rB], dys[(2 * q + 1) * SP + rB]),
-                                 make_float2(dys[(2 * q + 8) * SP + rA], dys[(2 * q + 9) * SP + rA]),
-                                 make_float2(dys[(2 * q + 8) * SP + rB], dys[(2 * q + 9) * SP + rB]));
         // G1: SA = S_0 A' + V M_k'  (rows = value index)
         float sa[2][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const AFrag sf = make_a(f2(S0s, rA, 16 * kk + 2 * q), f2(S0s, rB, 16 * kk + 2 * q),
-                                    f2(S0s, rA, 16 * kk + 2 * q + 8), f2(S0s, rB, 16 * kk + 2 * q + 8));
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) mma3(sa[nt], sf, ld_b(B1, (kk * 2 + nt) * 32 + lane));
+            const AFrag sf = lda(SX, 16 * warp, 16 * kk, lane);
+            BFrag b0, b1;
+            ldb2(AP, 0, 16 * kk, lane, b0, b1);
+            mma3(sa[0], sf, b0);
+            mma3(sa[1], sf, b1);
         }
+        const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
+        {
+            BFrag b0, b1;
+            ldb2_t(MK, 0, 0, lane, b0, b1);
+            mma3(sa[0], vA, b0);
+            mma3(sa[1], vA, b1);
+        }
+        {
+            __nv_bfloat16 *shh = hi_of(Bs, B_SAH), *shl = lo_of(Bs, B_SAH, 16);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) mma3(sa[nt], vA, ld_b(B1V, nt * 32 + lane));
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int t = 8 * nt + 2 * q;
-            SAt[t * SP + rA] = sa[nt][0];
-            SAt[(t + 1) * SP + rA] = sa[nt][1];
-            SAt[t * SP + rB] = sa[nt][2];
-            SAt[(t + 1) * SP + rB] = sa[nt][3];
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = 8 * nt + 2 * q;
+                st_hl1(shh, shl, t, rA, sa[nt][0]); st_hl1(shh, shl, t + 1, rA, sa[nt][1]);
+                st_hl1(shh, shl, t, rB, sa[nt][2]); st_hl1(shh, shl, t + 1, rB, sa[nt][3]);
+            }
         }
 
         // the dw running sum starts at diag(dsT^T sT): sT from the last chunk's start state
         if (last && p.dsT) {
             const AFrag saA = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
                                      make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
+            float part[8][2];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int j0 = 8 * nt + 2 * q;
-                const float2 x = f2(S0s, rA, j0), z = f2(S0s, rB, j0);
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + j0);
-                float ST[4] = {x.x * dc.x, x.y * dc.y, z.x * dc.x, z.y * dc.y};
-                const int jn = 8 * nt + g;
-                const float dcn = dC[jn];
-                const BFrag bb = make_b(make_float2(b_til(2 * q, jn) * dcn, b_til(2 * q + 1, jn) * dcn),
-                                        make_float2(b_til(2 * q + 8, jn) * dcn, b_til(2 * q + 9, jn) * dcn));
-                const BFrag kb = make_b(make_float2(k_til(2 * q, jn) * dcn, k_til(2 * q + 1, jn) * dcn),
-                                        make_float2(k_til(2 * q + 8, jn) * dcn, k_til(2 * q + 9, jn) * dcn));
-                mma3(ST, saA, bb);
-                mma3(ST, vA, kb);
+            for (int half = 0; half < 2; ++half) {
+                BFrag bb0, bb1, kb0, kb1;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float s = rows_sum(__fmaf_rn(Gh[nt][e], ST[e], __fmul_rn(Gh[nt][2 + e], ST[2 + e])));
-                    if (g == 0) DSt[warp * 64 + j0 + e] = s;
+                for (int pp = 0; pp < 2; ++pp) {  // n-tile pairs 4*half + 2*pp
+                    const int n0 = 32 * half + 16 * pp;
+                    ldb2_t(BT, n0, 0, lane, bb0, bb1);
+                    ldb2_t(KT, n0, 0, lane, kb0, kb1);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int nt = 4 * half + 2 * pp + u, j0 = 8 * nt + 2 * q;
+                        const float2 x = ld_hl(SX.hi, SX.lo, rA, j0), z = ld_hl(SX.hi, SX.lo, rB, j0);
+                        float ST[4] = {x.x, x.y, z.x, z.y};
+                        mma3(ST, saA, u ? bb1 : bb0);
+                        mma3(ST, vA, u ? kb1 : kb0);
+                        const float2 dc = *reinterpret_cast<const float2 *>(dC + j0);
+                        ST[0] *= dc.x; ST[1] *= dc.y; ST[2] *= dc.x; ST[3] *= dc.y;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            part[nt][e] = rows_sum(__fmaf_rn(Gh[nt][e], ST[e], __fmul_rn(Gh[nt][2 + e], ST[2 + e])));
+                    }
+                }
+            }
+            // the Gram slot is idle between W and Gam: 4 x 64 floats of per-warp column sums
+            if (g == 0) {
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+                    Gm[warp * 64 + 8 * nt + 2 * q] = part[nt][0];
+                    Gm[warp * 64 + 8 * nt + 2 * q + 1] = part[nt][1];
                 }
             }
             __syncthreads();
-            carryA = DSt[rA] + DSt[64 + rA] + DSt[128 + rA] + DSt[192 + rA];
-            carryB = DSt[rB] + DSt[64 + rB] + DSt[128 + rB] + DSt[192 + rB];
-            __syncthreads();
+            carryA = Gm[rA] + Gm[64 + rA] + Gm[128 + rA] + Gm[192 + rA];
+            carryB = Gm[rB] + Gm[64 + rB] + Gm[128 + rB] + Gm[192 + rB];
         }
 
         // G2: [DV | DSA] = G [K' | B'] + DY [Q'^T | (W Q_b)^T]
@@ -519,66 +519,49 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const AFrag gf = a_from_acc(Gh, kk);
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma3(dvs[nt], gf, ld_b(B2, (kk * 4 + nt) * 32 + lane));
+            BFrag b0, b1, b2, b3;
+            ldb2(KB, 0, 16 * kk, lane, b0, b1);
+            ldb2(KB, 16, 16 * kk, lane, b2, b3);
+            mma3(dvs[0], gf, b0); mma3(dvs[1], gf, b1); mma3(dvs[2], gf, b2); mma3(dvs[3], gf, b3);
         }
+        const AFrag dyA = lda_t(DYH, 16 * warp, 0, lane);
+        {
+            BFrag b0, b1, b2, b3;
+            ldb2(QQ, 0, 0, lane, b0, b1);
+            ldb2(QQ, 16, 0, lane, b2, b3);
+            mma3(dvs[0], dyA, b0); mma3(dvs[1], dyA, b1); mma3(dvs[2], dyA, b2); mma3(dvs[3], dyA, b3);
+        }
+        {
+            __nv_bfloat16 *dhh = hi_of(Bs, B_DSH), *dhl = lo_of(Bs, B_DSH, 16);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma3(dvs[nt], dyA, ld_b(B2D, nt * 32 + lane));
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int t = 8 * nt + 2 * q;
-            if (t < nv) {
-                p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dvs[nt][0];
-                p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dvs[nt][2];
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = 8 * nt + 2 * q;
+                if (t < nv) {
+                    p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dvs[nt][0];
+                    p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dvs[nt][2];
+                }
+                if (t + 1 < nv) {
+                    p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rA] = dvs[nt][1];
+                    p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rB] = dvs[nt][3];
+                }
+                st_hl1(dhh, dhl, t, rA, dvs[nt + 2][0]); st_hl1(dhh, dhl, t + 1, rA, dvs[nt + 2][1]);
+                st_hl1(dhh, dhl, t, rB, dvs[nt + 2][2]); st_hl1(dhh, dhl, t + 1, rB, dvs[nt + 2][3]);
             }
-            if (t + 1 < nv) {
-                p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rA] = dvs[nt][1];
-                p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rB] = dvs[nt][3];
-            }
-            DSt[t * SP + rA] = dvs[nt + 2][0];
-            DSt[(t + 1) * SP + rA] = dvs[nt + 2][1];
-            DSt[t * SP + rB] = dvs[nt + 2][2];
-            DSt[(t + 1) * SP + rB] = dvs[nt + 2][3];
         }
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
 
-        // [DY | DSA] and [V | SA] as B operands over the value rows: B[k = i][n = token]
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int f = tid + NT * m;  // 1024 fragments: which = f >> 9, kt = (f >> 7) & 3, nt = (f >> 5) & 3
-            const int which = f >> 9, kt = (f >> 7) & 3, nt = (f >> 5) & 3, ln = f & 31, gg = ln >> 2, qq = ln & 3;
-            const int t = 8 * (nt & 1) + gg, i0 = 16 * kt + 2 * qq;
-            float x0, x1, x8, x9;
-            if (which == 0) {
-                const float *s_ = nt < 2 ? dys : DSt;
-                const float2 a = f2(s_, t, i0), b = f2(s_, t, i0 + 8);
-                x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;
-            } else if (nt < 2) {
-                const float2 a = ld_raw2(raw, VV, t, i0), b = ld_raw2(raw, VV, t, i0 + 8);
-                x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;
-            } else {
-                const float2 a = f2(SAt, t, i0), b = f2(SAt, t, i0 + 8);
-                x0 = a.x; x1 = a.y; x8 = b.x; x9 = b.y;
-            }
-            reinterpret_cast<uint4 *>(which ? VSA : DYDS)[(kt * 4 + nt) * 32 + ln] = pack_b(x0, x1, x8, x9);
-        }
-        __syncthreads();
-
-        // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA rows | V rows), two n-tiles
-        {
+        {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA)
             const int mt = warp >> 1;
             float acc[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const int nb = mt ? 0 : 2;  // VSA n-tiles holding V (0,1) or SA (2,3)
-                const AFrag af = a_from_b(VSA, (kk * 4 + nb) * 32 + lane, (kk * 4 + nb + 1) * 32 + lane);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int nt = 2 * (warp & 1) + u;
-                    mma3(acc[u], af, ld_b(DYDS, (kk * 4 + nt) * 32 + lane));
-                }
+                const AFrag af = lda(mt ? VM : SAH, 0, 16 * kk, lane);
+                BFrag b0, b1;
+                ldb2((warp & 1) ? DSH : DYH, 0, 16 * kk, lane, b0, b1);
+                mma3(acc[0], af, b0);
+                mma3(acc[1], af, b1);
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -590,28 +573,26 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
         }
         __syncthreads();
-        // masked Gam blocks as B fragments: GM3 pairs (b~_s | k~_s) with (dy_t | dsa_t),
-        // GM4 pairs (r^_s | a^_s) with (v_t | sa_t)
+        {   // masked Gam blocks [k][n]: M3 pairs (b~_s | k~_s) with (dy_t | dsa_t); M4 pairs (r^_s | a^_s) with (v_t | sa_t)
+            __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
+            __nv_bfloat16 *h4 = hi_of(Bs, B_M4), *l4 = lo_of(Bs, B_M4, 32);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int f = tid + NT * m;  // 512: which = f >> 8, kt = (f >> 7) & 1, nt = (f >> 5) & 3
-            const int which = f >> 8, kt = (f >> 7) & 1, nt = (f >> 5) & 3, ln = f & 31, gg = ln >> 2, qq = ln & 3;
-            const int n = 8 * nt + gg, t = n & 15;
-            const int s4[4] = {2 * qq, 2 * qq + 1, 2 * qq + 8, 2 * qq + 9};
-            float x[4];
+            for (int m = 0; m < 4; ++m) {
+                const int e = tid + NT * m, k = e >> 4, n = (e & 15) * 2;  // 512 pairs (k, n..n+1)
+                const int s = k & 15, kt = k >> 4;
+                float x3v[2], x4v[2];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int s = s4[e];
-                if (which == 0) {
-                    const bool keep = nt >= 2 ? (s < t) : (s <= t);
-                    x[e] = keep ? Gm[(16 * kt + s) * GS + n] : 0.f;
-                } else {
-                    const int grow = nt < 2 ? 16 + t : t;
-                    const bool keep = kt ? (s > t) : (s >= t);
-                    x[e] = keep ? Gm[grow * GS + 16 * kt + s] : 0.f;
+                for (int z = 0; z < 2; ++z) {
+                    const int nn = n + z, t = nn & 15;
+                    const bool keep3 = nn >= 16 ? (s < t) : (s <= t);
+                    x3v[z] = keep3 ? Gm[k * GS + nn] : 0.f;
+                    const int grow = nn < 16 ? 16 + t : t;
+                    const bool keep4 = kt ? (s > t) : (s >= t);
+                    x4v[z] = keep4 ? Gm[grow * GS + 16 * kt + s] : 0.f;
                 }
+                st_hl(h3, l3, k, n, x3v[0], x3v[1]);
+                st_hl(h4, l4, k, n, x4v[0], x4v[1]);
             }
-            reinterpret_cast<uint4 *>(which ? GM4 : GM3)[(kt * 4 + nt) * 32 + ln] = pack_b(x[0], x[1], x[2], x[3]);
         }
         __syncthreads();
 
@@ -619,80 +600,75 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         float x3[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const int i0 = 16 * kk + 2 * q;
-            const AFrag sT = make_a(make_float2(S0s[i0 * SP + rA], S0s[(i0 + 1) * SP + rA]),
-                                    make_float2(S0s[i0 * SP + rB], S0s[(i0 + 1) * SP + rB]),
-                                    make_float2(S0s[(i0 + 8) * SP + rA], S0s[(i0 + 9) * SP + rA]),
-                                    make_float2(S0s[(i0 + 8) * SP + rB], S0s[(i0 + 9) * SP + rB]));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma3(x3[nt], sT, ld_b(DYDS, (kk * 4 + nt) * 32 + lane));
+            const AFrag sT = lda_t(SX, 16 * warp, 16 * kk, lane);
+            BFrag b0, b1, b2, b3;
+            ldb2(DYH, 0, 16 * kk, lane, b0, b1);
+            ldb2(DSH, 0, 16 * kk, lane, b2, b3);
+            mma3(x3[0], sT, b0); mma3(x3[1], sT, b1); mma3(x3[2], sT, b2); mma3(x3[3], sT, b3);
         }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {  // [B~ | K~] (rows j, k = token)
-            float x[8];
-            const int s4[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
+        for (int kk = 0; kk < 2; ++kk) {
+            const AFrag af = lda_t(kk ? KT : BT, 16 * warp, 0, lane);
+            BFrag b0, b1, b2, b3;
+            ldb2_t(M3, 0, 16 * kk, lane, b0, b1);
+            ldb2_t(M3, 16, 16 * kk, lane, b2, b3);
+            mma3(x3[0], af, b0); mma3(x3[1], af, b1); mma3(x3[2], af, b2); mma3(x3[3], af, b3);
+        }
+        __syncthreads();  // S_0 no longer read: its slot takes G d_C (split)
+        {
+            __nv_bfloat16 *gh = hi_of(Bs, B_SX), *gl = lo_of(Bs, B_SX, 64);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[2 * e] = kk ? k_til(s4[e], rA) : b_til(s4[e], rA);
-                x[2 * e + 1] = kk ? k_til(s4[e], rB) : b_til(s4[e], rB);
+            for (int nt = 0; nt < 8; ++nt) {
+                const int j0 = 8 * nt + 2 * q;
+                const float2 dc = *reinterpret_cast<const float2 *>(dC + j0);
+                st_hl(gh, gl, rA, j0, Gh[nt][0] * dc.x, Gh[nt][1] * dc.y);
+                st_hl(gh, gl, rB, j0, Gh[nt][2] * dc.x, Gh[nt][3] * dc.y);
             }
-            const AFrag af = make_a(make_float2(x[0], x[2]), make_float2(x[1], x[3]), make_float2(x[4], x[6]),
-                                    make_float2(x[5], x[7]));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma3(x3[nt], af, ld_b(GM3, (kk * 4 + nt) * 32 + lane));
         }
-        __syncthreads();  // S_0 and dy no longer read: fetch the previous chunk's
-        if (c > 0) {
-            stage_rows<NT>(dys, p.dy + base0 + (size_t)(t0 - C) * tstride, tstride, C, C);
-            stage_rows<NT>(S0s, p.ckpt_in + ((size_t)bh * p.nck + c - 1) * 64 * 64, 64, 64, 64);
-        }
-        cp_async_commit();
+        __syncthreads();
 
         // G4: [DK | DB] (rows = key index)
         float x4[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const int i0 = 16 * kk + 2 * q;
-            const AFrag gT = make_a(make_float2(Gds[i0 * SP + rA], Gds[(i0 + 1) * SP + rA]),
-                                    make_float2(Gds[i0 * SP + rB], Gds[(i0 + 1) * SP + rB]),
-                                    make_float2(Gds[(i0 + 8) * SP + rA], Gds[(i0 + 9) * SP + rA]),
-                                    make_float2(Gds[(i0 + 8) * SP + rB], Gds[(i0 + 9) * SP + rB]));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma3(x4[nt], gT, ld_b(VSA, (kk * 4 + nt) * 32 + lane));
+            const AFrag gT = lda_t(SX, 16 * warp, 16 * kk, lane);
+            BFrag b0, b1, b2, b3;
+            ldb2(VM, 0, 16 * kk, lane, b0, b1);
+            ldb2(SAH, 0, 16 * kk, lane, b2, b3);
+            mma3(x4[0], gT, b0); mma3(x4[1], gT, b1); mma3(x4[2], gT, b2); mma3(x4[3], gT, b3);
         }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {  // [R^ | A^] (rows j, k = token)
-            float x[8];
-            const int s4[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                x[2 * e] = kk ? a_hat(s4[e], rA) : r_hat(s4[e], rA);
-                x[2 * e + 1] = kk ? a_hat(s4[e], rB) : r_hat(s4[e], rB);
-            }
-            const AFrag af = make_a(make_float2(x[0], x[2]), make_float2(x[1], x[3]), make_float2(x[4], x[6]),
-                                    make_float2(x[5], x[7]));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma3(x4[nt], af, ld_b(GM4, (kk * 4 + nt) * 32 + lane));
+        for (int kk = 0; kk < 2; ++kk) {
+            const AFrag af = lda_t(kk ? AH : RH, 16 * warp, 0, lane);
+            BFrag b0, b1, b2, b3;
+            ldb2_t(M4, 0, 16 * kk, lane, b0, b1);
+            ldb2_t(M4, 16, 16 * kk, lane, b2, b3);
+            mma3(x4[0], af, b0); mma3(x4[1], af, b1); mma3(x4[2], af, b2); mma3(x4[3], af, b3);
         }
 
-        // outputs of the key-indexed gradients and the dw running sum
+        // ================= key-indexed gradients and the dw running sum
         {
+            // r^, a^, b~, k~ at this lane's (token, key) positions, in accumulator order
+            float rv[8], av[8], bv[8], kv[8];
+            a_values(lda_t(RH, 16 * warp, 0, lane), rv);
+            a_values(lda_t(AH, 16 * warp, 0, lane), av);
+            a_values(lda_t(BT, 16 * warp, 0, lane), bv);
+            a_values(lda_t(KT, 16 * warp, 0, lane), kv);
             float zz[2][4], ee[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
+                    const int vi = 4 * nt + m;  // value index in a_values order
                     const int row = m < 2 ? rA : rB;
                     const int t = 8 * nt + 2 * q + (m & 1);
                     const float d = dd[t * SP + row];
                     const float dp = t ? dd[(t - 1) * SP + row] : 1.f;
                     const float inv = rcp_approx(d);
                     const float xr = x3[nt][m], xa = x3[nt + 2][m], xk = x4[nt][m], xb = x4[nt + 2][m];
-                    const float rv = ld_raw(raw, VR, t, row), av = ld_raw(raw, VA, t, row);
-                    const float bv = ld_raw(raw, VB, t, row), kv = ld_raw(raw, VK, t, row);
                     // r o dr = r^ o X3_r, a o da = a^ o X3_a, b o db = b~ o X4_b, k o dk = k~ o X4_k
-                    ee[nt][m] = av * dp * xa;
-                    zz[nt][m] = rv * d * xr + ee[nt][m] - bv * inv * xb - kv * inv * xk;
+                    ee[nt][m] = av[vi] * xa;
+                    zz[nt][m] = rv[vi] * xr + ee[nt][m] - bv[vi] * xb - kv[vi] * xk;
                     if (t < nv) {
                         const size_t o = base0 + (size_t)(t0 + t) * tstride + row;
                         p.dr[o] = d * xr;
@@ -735,18 +711,25 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 if (hr) carryB = total; else carryA = total;
             }
         }
-        __syncthreads();  // raw no longer read
-        if (c > 0) stage<E, 6, NT>(raw, src, base0 + (size_t)(t0 - C) * tstride, tstride, C);
-        cp_async_commit();
 
         // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index)
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
-            Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
-            mma3(Gh[nt], dyA, ld_b(B5, (0 * 8 + nt) * 32 + lane));
-            mma3(Gh[nt], dsA, ld_b(B5, (1 * 8 + nt) * 32 + lane));
+        for (int pp = 0; pp < 4; ++pp) {
+            BFrag r0, r1, a0, a1;
+            ldb2_t(RH, 16 * pp, 0, lane, r0, r1);
+            ldb2_t(AH, 16 * pp, 0, lane, a0, a1);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int nt = 2 * pp + u;
+                const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
+                Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
+                mma3(Gh[nt], dyA, u ? r1 : r0);
+                mma3(Gh[nt], dsA, u ? a1 : a0);
+            }
         }
+        __syncthreads();  // G d_C (S_0 slot) no longer read: fetch the previous chunk's start state
+        if (c > 0) stage_s0(c - 1);
+        cp_async_commit();
     }
     cp_async_wait_all();
     if (p.ds0) {

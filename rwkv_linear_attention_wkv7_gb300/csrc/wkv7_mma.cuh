@@ -11,6 +11,7 @@
 // element with the smaller k index.
 #pragma once
 #include <stdint.h>
+#include <cuda_bf16.h>
 
 namespace wkv7 {
 
@@ -83,6 +84,78 @@ __device__ __forceinline__ BFrag make_b(float2 k0, float2 k8) {
 __device__ __forceinline__ AFrag a_from_acc(const float c[][4], int kt) {
     return make_a(make_float2(c[2 * kt][0], c[2 * kt][1]), make_float2(c[2 * kt][2], c[2 * kt][3]),
                   make_float2(c[2 * kt + 1][0], c[2 * kt + 1][1]), make_float2(c[2 * kt + 1][2], c[2 * kt + 1][3]));
+}
+
+}  // namespace wkv7
+
+namespace wkv7 {
+
+// ---- bf16 hi/lo operand matrices in shared memory, loaded with ldmatrix.
+// A matrix is stored twice (hi and lo parts), row-major, row stride MS
+// elements (144 bytes: the eight rows of an 8x8 ldmatrix tile start in
+// distinct bank groups).
+constexpr int MS = 72;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void *p) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], const void *p) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+struct HL {  // a split operand matrix: hi and lo parts, same layout
+    const __nv_bfloat16 *hi, *lo;
+};
+
+// A fragment, A[m][k] = M[m0 + m][k0 + k] (M stored [m][k]).
+__device__ __forceinline__ AFrag lda(const HL &M, int m0, int k0, int lane) {
+    const int off = (m0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + k0 + 8 * (lane >> 4);
+    AFrag f;
+    ldsm_x4(f.hi, M.hi + off);
+    ldsm_x4(f.lo, M.lo + off);
+    return f;
+}
+// A fragment, A[m][k] = M[k0 + k][m0 + m] (M stored [k][m]).
+__device__ __forceinline__ AFrag lda_t(const HL &M, int m0, int k0, int lane) {
+    const int off = (k0 + (lane & 7) + 8 * (lane >> 4)) * MS + m0 + 8 * ((lane >> 3) & 1);
+    AFrag f;
+    ldsm_x4_t(f.hi, M.hi + off);
+    ldsm_x4_t(f.lo, M.lo + off);
+    return f;
+}
+// B fragments of two n-tiles (n0..n0+7, n0+8..n0+15), B[k][n] = M[n][k] (M stored [n][k]).
+__device__ __forceinline__ void ldb2(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
+    const int off = (n0 + (lane & 7) + 8 * (lane >> 4)) * MS + k0 + 8 * ((lane >> 3) & 1);
+    uint32_t h[4], l[4];
+    ldsm_x4(h, M.hi + off);
+    ldsm_x4(l, M.lo + off);
+    b0.hi[0] = h[0]; b0.hi[1] = h[1]; b1.hi[0] = h[2]; b1.hi[1] = h[3];
+    b0.lo[0] = l[0]; b0.lo[1] = l[1]; b1.lo[0] = l[2]; b1.lo[1] = l[3];
+}
+// B fragments of two n-tiles, B[k][n] = M[k][n] (M stored [k][n]).
+__device__ __forceinline__ void ldb2_t(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
+    const int off = (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + n0 + 8 * (lane >> 4);
+    uint32_t h[4], l[4];
+    ldsm_x4_t(h, M.hi + off);
+    ldsm_x4_t(l, M.lo + off);
+    b0.hi[0] = h[0]; b0.hi[1] = h[1]; b1.hi[0] = h[2]; b1.hi[1] = h[3];
+    b0.lo[0] = l[0]; b0.lo[1] = l[1]; b1.lo[0] = l[2]; b1.lo[1] = l[3];
+}
+// Store the split of (x0, x1) at M[row][col], M[row][col + 1] (col even).
+__device__ __forceinline__ void st_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row, int col, float x0, float x1) {
+    const Frag2 f = split2(x0, x1);
+    *reinterpret_cast<uint32_t *>(hi + row * MS + col) = f.hi;
+    *reinterpret_cast<uint32_t *>(lo + row * MS + col) = f.lo;
+}
+__device__ __forceinline__ float2 ld_hl(const __nv_bfloat16 *hi, const __nv_bfloat16 *lo, int row, int col) {
+    const uint32_t h = *reinterpret_cast<const uint32_t *>(hi + row * MS + col);
+    const uint32_t l = *reinterpret_cast<const uint32_t *>(lo + row * MS + col);
+    return make_float2(__uint_as_float(h << 16) + __uint_as_float(l << 16),
+                       __uint_as_float(h & 0xffff0000u) + __uint_as_float(l & 0xffff0000u));
 }
 
 }  // namespace wkv7
