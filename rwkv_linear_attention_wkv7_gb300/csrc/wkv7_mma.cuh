@@ -35,8 +35,10 @@ __device__ __forceinline__ Frag2 split2(float x0, float x1) {
     return f;
 }
 
+// Pure register operation: not volatile, so the compiler may interleave
+// independent accumulators (the three products of one split MMA are serial).
 __device__ __forceinline__ void mma_bf16(float c[4], const uint32_t a[4], const uint32_t b[2]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
