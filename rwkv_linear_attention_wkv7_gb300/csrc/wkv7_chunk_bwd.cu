@@ -271,7 +271,20 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         stage<E, 6, NT>(raw, src, base0 + (size_t)t0 * tstride, tstride, nv);
         stage_rows<NT>(dyf, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
     };
-    auto stage_s0 = [&](int c) { stage_rows<NT>(S0f, p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64, 64, 64, 64); };
+    // The next chunk's start state is fetched (fp32) while G4, the outputs and
+    // G5 still run, into three slots that are idle by then: rows 0..15 -> the
+    // dy split, 16..31 -> the DSA split, 32..63 -> the first masked-Gam block.
+    auto s0_row = [&](int row) -> float * {
+        const int off = row < 16 ? B_DYH + row * SP * 4 : row < 32 ? B_DSH + (row - 16) * SP * 4 : B_M3 + (row - 32) * SP * 4;
+        return reinterpret_cast<float *>(Bs + off);
+    };
+    auto stage_s0 = [&](int c) {
+        const float *src0 = p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64;
+        for (int e = threadIdx.x; e < 64 * 16; e += NT) {
+            const int u = e >> 4, n = (e & 15) * 4;
+            cp_async16(s0_row(u) + n, src0 + u * 64 + n, 16);
+        }
+    };
     stage_in(nchunks - 1);
     stage_s0(nchunks - 1);
     cp_async_commit();
@@ -285,6 +298,11 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (exact) {
+            for (int e = tid; e < 64 * 16; e += NT) {  // contiguous fp32 start state for the per-token path
+                const int u = e >> 4, n = (e & 15) * 4;
+                *reinterpret_cast<float4 *>(S0f + u * SP + n) = *reinterpret_cast<const float4 *>(s0_row(u) + n);
+            }
+            __syncthreads();
             bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
             __syncthreads();
@@ -303,7 +321,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int e = tid + NT * m, row = e >> 5, col = (e & 31) * 2;
-                sv[m] = *reinterpret_cast<const float2 *>(S0f + row * SP + col);
+                sv[m] = *reinterpret_cast<const float2 *>(s0_row(row) + col);
             }
             __syncthreads();
             __nv_bfloat16 *sh = hi_of(Bs, B_SX), *sl = lo_of(Bs, B_SX, 64);
@@ -614,7 +632,10 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             ldb2_t(M3, 16, 16 * kk, lane, b2, b3);
             mma3(x3[0], af, b0); mma3(x3[1], af, b1); mma3(x3[2], af, b2); mma3(x3[3], af, b3);
         }
-        __syncthreads();  // S_0 no longer read: its slot takes G d_C (split)
+        __syncthreads();  // S_0, dy, DSA and the first masked block no longer read
+        if (c > 0) stage_s0(c - 1);
+        cp_async_commit();
+        // the S_0 slot takes G d_C (split)
         {
             __nv_bfloat16 *gh = hi_of(Bs, B_SX), *gl = lo_of(Bs, B_SX, 64);
 #pragma unroll
@@ -727,9 +748,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 mma3(Gh[nt], dsA, u ? a1 : a0);
             }
         }
-        __syncthreads();  // G d_C (S_0 slot) no longer read: fetch the previous chunk's start state
-        if (c > 0) stage_s0(c - 1);
-        cp_async_commit();
+        __syncthreads();
     }
     cp_async_wait_all();
     if (p.ds0) {
