@@ -229,6 +229,30 @@ __device__ __forceinline__ void a_values(const AFrag &f, float v[8]) {
     }
 }
 
+// A' = W^T-weighted a^ for NS 16-key slabs starting at slab0 (M = token,
+// N = key), the slabs' MMAs issued together; written split to the A' slot.
+template <int NS>
+__device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned char *Bs, int slab0, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    float ca[NS][2][4] = {};
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        BFrag b0, b1;
+        ldb2_t(AH, 16 * (slab0 + s), 0, lane, b0, b1);
+        mma3(ca[s][0], wt, b0);
+        mma3(ca[s][1], wt, b1);
+    }
+    __nv_bfloat16 *ah = hi_of(Bs, B_AP), *al = lo_of(Bs, B_AP, 16);
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
+            st_hl(ah, al, g, jc, ca[s][u][0], ca[s][u][1]);
+            st_hl(ah, al, g + 8, jc, ca[s][u][2], ca[s][u][3]);
+        }
+}
+
 template <typename E>
 __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -317,34 +341,32 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 
         // ================= split every operand matrix once
         {   // S_0 in place: fp32 staging -> hi/lo
-            float2 sv[16];
+            float4 sv[8];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int e = tid + NT * m, row = e >> 5, col = (e & 31) * 2;
-                sv[m] = *reinterpret_cast<const float2 *>(s0_row(row) + col);
+            for (int m = 0; m < 8; ++m) {
+                const int e = tid + NT * m, row = e >> 4, col = (e & 15) * 4;
+                sv[m] = *reinterpret_cast<const float4 *>(s0_row(row) + col);
             }
             __syncthreads();
             __nv_bfloat16 *sh = hi_of(Bs, B_SX), *sl = lo_of(Bs, B_SX, 64);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int e = tid + NT * m, row = e >> 5, col = (e & 31) * 2;
-                st_hl(sh, sl, row, col, sv[m].x, sv[m].y);
+            for (int m = 0; m < 8; ++m) {
+                const int e = tid + NT * m, row = e >> 4, col = (e & 15) * 4;
+                st_hl4(sh, sl, row, col, sv[m]);
             }
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {  // decay-scaled vectors, v and dy: [t][j] pairs
-            const int e = tid + NT * m, t = e >> 5, j = (e & 31) * 2;
-            const float2 d = *reinterpret_cast<const float2 *>(dd + t * SP + j);
-            const float2 dp = t ? *reinterpret_cast<const float2 *>(dd + (t - 1) * SP + j) : make_float2(1.f, 1.f);
-            const float i0 = rcp_approx(d.x), i1 = rcp_approx(d.y);
-            float2 x;
-            x = ld_raw2(raw, VB, t, j); st_hl(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, x.x * i0, x.y * i1);
-            x = ld_raw2(raw, VK, t, j); st_hl(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, x.x * i0, x.y * i1);
-            x = ld_raw2(raw, VA, t, j); st_hl(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, x.x * dp.x, x.y * dp.y);
-            x = ld_raw2(raw, VR, t, j); st_hl(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, x.x * d.x, x.y * d.y);
-            x = ld_raw2(raw, VV, t, j); st_hl(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, j, x.x, x.y);
-            x = *reinterpret_cast<const float2 *>(dyf + t * SP + j);
-            st_hl(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, x.x, x.y);
+        for (int m = 0; m < 2; ++m) {  // decay-scaled vectors, v and dy: [t][j] quads
+            const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
+            const float4 d = *reinterpret_cast<const float4 *>(dd + t * SP + j);
+            const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * SP + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+            const float4 id = rcp4(d);
+            st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(ld_raw4(raw, VB, t, j), id));
+            st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
+            st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
+            st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
+            st_hl4(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, j, ld_raw4(raw, VV, t, j));
+            st_hl4(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
         }
         __syncthreads();
         // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
@@ -375,43 +397,47 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         __syncthreads();
         prep_inverse(Gm, Wm);
         __syncthreads();
-        {   // A' = W^T-weighted A^ (M = token, N = key; warp w owns keys 16w..16w+15)
+        // A' = W^T-weighted A^ (M = token, N = key): warp 0 keys 0..31, warps 2 and 3
+        // keys 16w..16w+15 (warp 3 also W Q_b); warp 1 builds M_k' and then Q'
+        auto qbv = [&](int u, int t) { return u <= t ? Gm[u * GS + 16 + t] : 0.f; };
+        if (warp != 1) {
             const AFrag wt = make_a(make_float2(Wm[(2 * q) * WS + g], Wm[(2 * q + 1) * WS + g]),
                                     make_float2(Wm[(2 * q) * WS + g + 8], Wm[(2 * q + 1) * WS + g + 8]),
                                     make_float2(Wm[(2 * q + 8) * WS + g], Wm[(2 * q + 9) * WS + g]),
                                     make_float2(Wm[(2 * q + 8) * WS + g + 8], Wm[(2 * q + 9) * WS + g + 8]));
-            BFrag b0, b1;
-            ldb2_t(AH, 16 * warp, 0, lane, b0, b1);
-            float ca[2][4] = {};
-            mma3(ca[0], wt, b0);
-            mma3(ca[1], wt, b1);
-            __nv_bfloat16 *ah = hi_of(Bs, B_AP), *al = lo_of(Bs, B_AP, 16);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int jc = 16 * warp + 8 * u + 2 * q;
-                st_hl(ah, al, g, jc, ca[u][0], ca[u][1]);
-                st_hl(ah, al, g + 8, jc, ca[u][2], ca[u][3]);
-            }
+            if (warp == 0)
+                build_ap<2>(wt, AH, Bs, 0, lane);
+            else
+                build_ap<1>(wt, AH, Bs, warp, lane);
         }
-        if (warp == 0) {  // M_k' = M_k W, Q' = Q_k + M_k' Q_b, W Q_b (all 16 x 16)
-            auto mk = [&](int s, int u) { return u > s ? Gm[(16 + s) * GS + u] : 0.f; };
-            auto qbv = [&](int u, int t) { return u <= t ? Gm[u * GS + 16 + t] : 0.f; };
-            auto qkv = [&](int s, int t) { return s <= t ? Gm[(16 + s) * GS + 16 + t] : 0.f; };
-            const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
-                                    make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
-                                    make_float2(mk(g + 8, 2 * q + 8), mk(g + 8, 2 * q + 9)));
+        if (warp == 3) {  // W Q_b -> rows 16..31 of the [Q'; W Q_b] block
             const AFrag wa = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
                                     make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
                                     make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
                                     make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
-            float cm[2][4] = {}, cb[2][4] = {};
+            __nv_bfloat16 *qh = hi_of(Bs, B_QQ), *ql = lo_of(Bs, B_QQ, 32);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tc = 8 * nt + 2 * q, t = 8 * nt + g;
+                float cb[4] = {0.f, 0.f, 0.f, 0.f};
+                mma3(cb, wa, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
+                                    make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
+                st_hl(qh, ql, 16 + g, tc, cb[0], cb[1]);  // (W Q_b)[t][s]
+                st_hl(qh, ql, 24 + g, tc, cb[2], cb[3]);
+            }
+        }
+        if (warp == 1) {  // M_k' = M_k W, then Q' = Q_k + M_k' Q_b (16 x 16)
+            auto mk = [&](int s, int u) { return u > s ? Gm[(16 + s) * GS + u] : 0.f; };
+            auto qkv = [&](int s, int t) { return s <= t ? Gm[(16 + s) * GS + 16 + t] : 0.f; };
+            const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
+                                    make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
+                                    make_float2(mk(g + 8, 2 * q + 8), mk(g + 8, 2 * q + 9)));
+            float cm[2][4] = {};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int t = 8 * nt + g;
                 mma3(cm[nt], am, make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
                                         make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t])));
-                mma3(cb[nt], wa, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
-                                        make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
             }
             const AFrag amp = make_a(make_float2(cm[0][0], cm[0][1]), make_float2(cm[0][2], cm[0][3]),
                                      make_float2(cm[1][0], cm[1][1]), make_float2(cm[1][2], cm[1][3]));
@@ -428,12 +454,10 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int tc = 8 * nt + 2 * q;
-                st_hl(mh, ml, g, tc, cm[nt][0], cm[nt][1]);       // M_k'[s][t]
+                st_hl(mh, ml, g, tc, cm[nt][0], cm[nt][1]);  // M_k'[s][t]
                 st_hl(mh, ml, g + 8, tc, cm[nt][2], cm[nt][3]);
-                st_hl(qh, ql, g, tc, cq[nt][0], cq[nt][1]);       // Q'[t][s]
+                st_hl(qh, ql, g, tc, cq[nt][0], cq[nt][1]);  // Q'[t][s]
                 st_hl(qh, ql, g + 8, tc, cq[nt][2], cq[nt][3]);
-                st_hl(qh, ql, 16 + g, tc, cb[nt][0], cb[nt][1]);  // (W Q_b)[t][s]
-                st_hl(qh, ql, 24 + g, tc, cb[nt][2], cb[nt][3]);
             }
         }
         __syncthreads();

@@ -58,6 +58,20 @@ __device__ __forceinline__ float2 ld_raw2<__nv_bfloat16>(const __nv_bfloat16 *ra
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
+// Elements j .. j + 3 (j % 4 == 0) of a staged row as one 64/128-bit load.
+template <typename E>
+__device__ __forceinline__ float4 ld_raw4(const E *raw, int vec, int t, int j);
+template <>
+__device__ __forceinline__ float4 ld_raw4<float>(const float *raw, int vec, int t, int j) {
+    return *reinterpret_cast<const float4 *>(raw + (vec * C + t) * RS + j);
+}
+template <>
+__device__ __forceinline__ float4 ld_raw4<__nv_bfloat16>(const __nv_bfloat16 *raw, int vec, int t, int j) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(raw + (vec * C + t) * RS + j);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+}
+
 template <typename E>
 __host__ __device__ constexpr size_t raw_bytes() { return (size_t)6 * C * RS * sizeof(E); }
 
@@ -98,6 +112,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+__device__ __forceinline__ float4 rcp4(float4 a) {
+    return make_float4(rcp_approx(a.x), rcp_approx(a.y), rcp_approx(a.z), rcp_approx(a.w));
+}
+
 __device__ __forceinline__ float2 f2(const float *a, int row, int col) {
     return *reinterpret_cast<const float2 *>(a + row * SP + col);
 }
@@ -111,11 +130,14 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
     bool bad = false;
     if (threadIdx.x < 64) {
         const int j = threadIdx.x;
+        // all loads first: the product chain then runs at FMUL latency
+        float wv[C];
+#pragma unroll
+        for (int t = 0; t < C; ++t) wv[t] = t < nv ? ld_raw(raw, VW, t, j) : 1.f;
         float dc = 1.f;
 #pragma unroll
         for (int t = 0; t < C; ++t) {
-            const float wv = t < nv ? ld_raw(raw, VW, t, j) : 1.f;
-            dc = __fmul_rn(dc, wv);
+            dc = __fmul_rn(dc, wv[t]);
             dd[t * SP + j] = dc;
             bad |= !(dc >= kTiny && dc <= 1.f / kTiny);
         }

@@ -62,6 +62,54 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + 16 * MS;
 }
 
+// A' = W^T-weighted a^ and R' = r^ + Q_b^T A' for NS 16-key slabs starting at
+// slab0 (M = token, N = key); the slabs' MMAs are issued together.  R' takes
+// the a^ slot of its slab, which only this warp reads.
+template <int NS>
+__device__ __forceinline__ void build_ap_rp(const AFrag &wt, const AFrag &qbt, const HL &AH, const HL &AP, const HL &RH,
+                                            unsigned char *Bs, int slab0, int lane) {
+    const int g = lane >> 2, q = lane & 3;
+    BFrag b[NS][2];
+    float ca[NS][2][4] = {};
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        ldb2_t(AH, 16 * (slab0 + s), 0, lane, b[s][0], b[s][1]);
+        mma3(ca[s][0], wt, b[s][0]);
+        mma3(ca[s][1], wt, b[s][1]);
+    }
+    __nv_bfloat16 *aph = hi_of(Bs, B_AP), *apl = lo_of(Bs, B_AP);
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
+            st_hl(aph, apl, g, jc, ca[s][u][0], ca[s][u][1]);
+            st_hl(aph, apl, g + 8, jc, ca[s][u][2], ca[s][u][3]);
+        }
+    __syncwarp();
+    __nv_bfloat16 *rph = hi_of(Bs, B_AH), *rpl = lo_of(Bs, B_AH);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) ldb2_t(AP, 16 * (slab0 + s), 0, lane, b[s][0], b[s][1]);
+    float cr[NS][2][4];
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
+            const float2 r0 = ld_hl(RH.hi, RH.lo, g, jc), r8 = ld_hl(RH.hi, RH.lo, g + 8, jc);
+            cr[s][u][0] = r0.x; cr[s][u][1] = r0.y; cr[s][u][2] = r8.x; cr[s][u][3] = r8.y;
+            mma3(cr[s][u], qbt, b[s][u]);
+        }
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
+            st_hl(rph, rpl, g, jc, cr[s][u][0], cr[s][u][1]);
+            st_hl(rph, rpl, g + 8, jc, cr[s][u][2], cr[s][u][3]);
+        }
+}
+
 template <typename E>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -105,30 +153,34 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
         cp_async_wait_all();
         __syncthreads();
 
-        if (p.ckpt && t0 % p.L == 0) {  // state before token t0
-            float *dst = p.ckpt + ((size_t)bh * p.nck + t0 / p.L) * 64 * 64;
+        // checkpoint of the state before token t0; written once the previous
+        // chunk's state update has long completed (after the Gram), not at
+        // the chunk start where it would wait on those MMAs
+        auto write_ckpt = [&]() {
+            if (p.ckpt && t0 % p.L == 0) {
+                float *dst = p.ckpt + ((size_t)bh * p.nck + t0 / p.L) * 64 * 64;
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                *reinterpret_cast<float2 *>(dst + rA * 64 + 8 * nt + 2 * q) = make_float2(S[nt][0], S[nt][1]);
-                *reinterpret_cast<float2 *>(dst + rB * 64 + 8 * nt + 2 * q) = make_float2(S[nt][2], S[nt][3]);
+                for (int nt = 0; nt < 8; ++nt) {
+                    *reinterpret_cast<float2 *>(dst + rA * 64 + 8 * nt + 2 * q) = make_float2(S[nt][0], S[nt][1]);
+                    *reinterpret_cast<float2 *>(dst + rB * 64 + 8 * nt + 2 * q) = make_float2(S[nt][2], S[nt][3]);
+                }
             }
-        }
+        };
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (!exact) {
-            // ---- split the decay-scaled vectors and v once: [t][j] pairs
+            // ---- split the decay-scaled vectors and v once: [t][j] quads
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int e = tid + NT * m, t = e >> 5, j = (e & 31) * 2;
-                const float2 d = *reinterpret_cast<const float2 *>(dd + t * SP + j);
-                const float2 dp = t ? *reinterpret_cast<const float2 *>(dd + (t - 1) * SP + j) : make_float2(1.f, 1.f);
-                const float i0 = rcp_approx(d.x), i1 = rcp_approx(d.y);
-                float2 x;
-                x = ld_raw2(raw, VB, t, j); st_hl(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, x.x * i0, x.y * i1);
-                x = ld_raw2(raw, VK, t, j); st_hl(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, x.x * i0, x.y * i1);
-                x = ld_raw2(raw, VA, t, j); st_hl(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, x.x * dp.x, x.y * dp.y);
-                x = ld_raw2(raw, VR, t, j); st_hl(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, x.x * d.x, x.y * d.y);
-                x = ld_raw2(raw, VV, t, j); st_hl(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, x.x, x.y);
+            for (int m = 0; m < 2; ++m) {
+                const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
+                const float4 d = *reinterpret_cast<const float4 *>(dd + t * SP + j);
+                const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * SP + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float4 id = rcp4(d);
+                st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, mul4(ld_raw4(raw, VB, t, j), id));
+                st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
+                st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
+                st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
+                st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
             }
             __syncthreads();
             // raw is no longer read in this chunk: fetch the next one now
@@ -155,11 +207,12 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     G[(row + 8) * GS + col + 1] = acc[u][3];
                 }
             }
+            write_ckpt();
             __syncthreads();
             prep_inverse(G, Wm);
             __syncthreads();
 
-            {   // A' = W^T-weighted A^ and R' = R^ + Q_b^T A'  (M = token, N = key; warp w owns keys 16w..16w+15)
+            if (warp != 1) {  // A' = W^T-weighted A^ and R' = R^ + Q_b^T A' (warp 0: keys 0..31, warps 2, 3: 16w..16w+15)
                 const AFrag wt = make_a(make_float2(Wm[(2 * q) * WS + g], Wm[(2 * q + 1) * WS + g]),
                                         make_float2(Wm[(2 * q) * WS + g + 8], Wm[(2 * q + 1) * WS + g + 8]),
                                         make_float2(Wm[(2 * q + 8) * WS + g], Wm[(2 * q + 9) * WS + g]),
@@ -169,32 +222,12 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                                          make_float2(qb(2 * q, g + 8), qb(2 * q + 1, g + 8)),
                                          make_float2(qb(2 * q + 8, g), qb(2 * q + 9, g)),
                                          make_float2(qb(2 * q + 8, g + 8), qb(2 * q + 9, g + 8)));
-                BFrag b0, b1;
-                ldb2_t(AH, 16 * warp, 0, lane, b0, b1);
-                float ca[2][4] = {};
-                mma3(ca[0], wt, b0);
-                mma3(ca[1], wt, b1);
-                __nv_bfloat16 *aph = hi_of(Bs, B_AP), *apl = lo_of(Bs, B_AP);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int jc = 16 * warp + 8 * u + 2 * q;
-                    st_hl(aph, apl, g, jc, ca[u][0], ca[u][1]);
-                    st_hl(aph, apl, g + 8, jc, ca[u][2], ca[u][3]);
-                }
-                __syncwarp();
-                ldb2_t(AP, 16 * warp, 0, lane, b0, b1);
-                __nv_bfloat16 *rph = hi_of(Bs, B_AH), *rpl = lo_of(Bs, B_AH);  // a^ slab of this warp is consumed
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int jc = 16 * warp + 8 * u + 2 * q;
-                    const float2 r0 = ld_hl(RH.hi, RH.lo, g, jc), r8 = ld_hl(RH.hi, RH.lo, g + 8, jc);
-                    float cr[4] = {r0.x, r0.y, r8.x, r8.y};
-                    mma3(cr, qbt, u ? b1 : b0);
-                    st_hl(rph, rpl, g, jc, cr[0], cr[1]);
-                    st_hl(rph, rpl, g + 8, jc, cr[2], cr[3]);
-                }
+                if (warp == 0)
+                    build_ap_rp<2>(wt, qbt, AH, AP, RH, Bs, 0, lane);
+                else
+                    build_ap_rp<1>(wt, qbt, AH, AP, RH, Bs, warp, lane);
             }
-            if (warp == 0) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b (16 x 16) -> [s][Q' | M_k']
+            if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b (16 x 16) -> [s][Q' | M_k']
                 auto mk = [&](int s, int u) { return u > s ? G[(16 + s) * GS + u] : 0.f; };
                 const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
                                         make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
@@ -270,6 +303,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
             }
         } else {
             // exact per-token recurrence for a chunk whose decay leaves the factorisable range
+            write_ckpt();
             for (int t = 0; t < nv; ++t) {
                 float sa0 = 0.f, sa1 = 0.f;
 #pragma unroll

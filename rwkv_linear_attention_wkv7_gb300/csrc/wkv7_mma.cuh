@@ -153,6 +153,12 @@ __device__ __forceinline__ void st_hl(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int 
     *reinterpret_cast<uint32_t *>(hi + row * MS + col) = f.hi;
     *reinterpret_cast<uint32_t *>(lo + row * MS + col) = f.lo;
 }
+// Store the split of four consecutive values at M[row][col..col + 3] (col % 4 == 0).
+__device__ __forceinline__ void st_hl4(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row, int col, float4 x) {
+    const Frag2 f0 = split2(x.x, x.y), f1 = split2(x.z, x.w);
+    *reinterpret_cast<uint2 *>(hi + row * MS + col) = make_uint2(f0.hi, f1.hi);
+    *reinterpret_cast<uint2 *>(lo + row * MS + col) = make_uint2(f0.lo, f1.lo);
+}
 __device__ __forceinline__ float2 ld_hl(const __nv_bfloat16 *hi, const __nv_bfloat16 *lo, int row, int col) {
     const uint32_t h = *reinterpret_cast<const uint32_t *>(hi + row * MS + col);
     const uint32_t l = *reinterpret_cast<const uint32_t *>(lo + row * MS + col);
