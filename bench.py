@@ -236,6 +236,7 @@ def run_reference(args, world, rank):
 def config_of(spec, args):
     return {"workload": spec.name, "B": spec.B, "T": spec.T, "H": spec.H, "N": spec.N,
             "input_dtype": spec.dtype, "state_dtype": "f32", "ckpt_stride": spec.L,
+            "factor_cache": spec.L == 16,
             "parallelism": f"replicas x{args.gpus} (independent heads)",
             "l2": f"inputs larger than L2 ({spec.elems * 6 * esize(spec) / 1e9:.2f} GB of r..b per step), no flush"}
 
@@ -282,8 +283,11 @@ def run_ours(args, world, rank, local):
 
     B, T, H, N = spec.B, spec.T, spec.H, spec.N
     nck = wkv7.ckpt_count(T, spec.L)
+    use_fac = spec.L == 16
     outs = {"y": torch.empty((B, T, H, N), device=dev), "sT": torch.empty((B, H, N, N), device=dev),
             "ckpt": torch.empty((B, H, nck, N, N), device=dev)}
+    if use_fac:  # the forward's per-chunk factor cache, reused by the backward
+        outs["factors"] = torch.empty((B, H, wkv7.factor_floats(T)), device=dev)
     gouts = {n: torch.empty((B, T, H, N), device=dev) for n in GRADS}
     gouts["ds0"] = torch.empty((B, H, N, N), device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -294,11 +298,11 @@ def run_ours(args, world, rank, local):
         if record:
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
-        wkv7.forward(*(d[n] for n in INPUTS), s0=d["s0"], L=spec.L, out=outs, stream=stream)
+        wkv7.forward(*(d[n] for n in INPUTS), s0=d["s0"], L=spec.L, want_factors=use_fac, out=outs, stream=stream)
         if record:
             e1.record(stream)
-        wkv7.backward(*(d[n] for n in INPUTS), outs["ckpt"], d["dy"], dsT=d["dsT"], L=spec.L, out=gouts,
-                      stream=stream)
+        wkv7.backward(*(d[n] for n in INPUTS), outs["ckpt"], d["dy"], dsT=d["dsT"], L=spec.L,
+                      factors=outs.get("factors"), out=gouts, stream=stream)
         if record:
             e2.record(stream)
             ev_f.append((e0, e1, e2))

@@ -65,6 +65,10 @@ enum {
  * Returns -1 if T < 0 or L < 1. */
 int wkv7_ckpt_count(int T, int L);
 
+/* Length, in floats, of one (b, h) row of the per-chunk factor cache a
+ * forward of T tokens writes: 2048 * ceil(T/16).  Returns -1 if T < 0. */
+long long wkv7_factor_floats(int T);
+
 /*
  * Forward over a whole sequence.
  *   B, T, H   batch rows, tokens, heads; B, H >= 1, T >= 0.  N must be 64.
@@ -75,20 +79,28 @@ int wkv7_ckpt_count(int T, int L);
  *   sT        [B][H][N][N] final state, or NULL.
  *   ckpt      [B][H][ceil(T/L)][N][N], or NULL: ckpt[b][h][c] is the state
  *             before token c*L (so ckpt[..][0] = s0).
+ *   factors   [B][H][wkv7_factor_floats(T)], or NULL: a cache of per-chunk
+ *             quantities of the chunked form (the inverse W, M_k W, Q', W Q_b
+ *             and SA of every 16-token chunk) for wkv7_backward to reuse
+ *             instead of recomputing them.  Its layout is internal to this
+ *             library; only wkv7_backward reads it.  Needs L == 16.
  *   L         checkpoint stride in tokens, L >= 1 (16 is the tuned value).
  * T == 0 writes sT = s0 (or zeros) and nothing else.
  */
 int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype,
                  const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b,
-                 const float *s0, float *y, float *sT, float *ckpt, int L,
-                 void *stream);
+                 const float *s0, float *y, float *sT, float *ckpt,
+                 float *factors, int L, void *stream);
 
 /*
  * Backward: the exact adjoint of wkv7_forward, run in reverse time from the
  * checkpoints a forward with the same inputs and the same L wrote.
  *   r..b      the forward's inputs, same dtype and layout.
  *   ckpt      [B][H][ceil(T/L)][N][N] from wkv7_forward (required when T > 0).
+ *   factors   the factor cache of that same forward call, or NULL (then the
+ *             backward recomputes those quantities).  Needs L == 16.  The
+ *             results are the same either way up to fp32 rounding order.
  *   dy        [B][T][H][N] gradient of the loss w.r.t. y (required when T > 0).
  *   dsT       [B][H][N][N] gradient w.r.t. the final state, or NULL for zeros.
  *   dr..db    [B][T][H][N] gradients w.r.t. r, w, k, v, a, b (all required
@@ -98,7 +110,8 @@ int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype,
 int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype,
                   const void *r, const void *w, const void *k,
                   const void *v, const void *a, const void *b,
-                  const float *ckpt, int L, const float *dy, const float *dsT,
+                  const float *ckpt, const float *factors, int L,
+                  const float *dy, const float *dsT,
                   float *dr, float *dw, float *dk, float *dv, float *da, float *db,
                   float *ds0, void *stream);
 

@@ -84,19 +84,26 @@ int wkv7_ckpt_count(int T, int L) {
     return (int)(((long long)T + L - 1) / L);
 }
 
+long long wkv7_factor_floats(int T) {
+    if (T < 0) return -1;
+    return (((long long)T + 15) / 16) * wkv7::fac::kWords;
+}
+
 const char *wkv7_last_error(void) { return g_err; }
 
 int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
-                 int L, void *stream) {
+                 float *factors, int L, void *stream) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
+    if (factors && L != 16) return fail(WKV7_EINVAL, "factors need L == 16 (got %d)", L);
     const bool need = T > 0;
     TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
     TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
     TRY(check_ptr(s0, "s0", false)); TRY(check_ptr(y, "y", need));
     TRY(check_ptr(sT, "sT", false)); TRY(check_ptr(ckpt, "ckpt", false));
+    TRY(check_ptr(factors, "factors", false));
     TRY(check_device());
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();
@@ -105,22 +112,24 @@ int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
     wkv7::SeqArgs p{};
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
-    p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt;
+    p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt; p.fac = factors;
     if (wkv7::forward_chunk_supported(p)) return launch_status(wkv7::launch_forward_chunk(p, st), "wkv7_forward launch");
     return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
 }
 
 int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
-                  const void *v, const void *a, const void *b, const float *ckpt, int L, const float *dy,
-                  const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db, float *ds0,
-                  void *stream) {
+                  const void *v, const void *a, const void *b, const float *ckpt, const float *factors, int L,
+                  const float *dy, const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                  float *ds0, void *stream) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
+    if (factors && L != 16) return fail(WKV7_EINVAL, "factors need L == 16 (got %d)", L);
     const bool need = T > 0;
     TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
     TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
-    TRY(check_ptr(ckpt, "ckpt", need)); TRY(check_ptr(dy, "dy", need)); TRY(check_ptr(dsT, "dsT", false));
+    TRY(check_ptr(ckpt, "ckpt", need)); TRY(check_ptr(factors, "factors", false));
+    TRY(check_ptr(dy, "dy", need)); TRY(check_ptr(dsT, "dsT", false));
     TRY(check_ptr(dr, "dr", need)); TRY(check_ptr(dw, "dw", need)); TRY(check_ptr(dk, "dk", need));
     TRY(check_ptr(dv, "dv", need)); TRY(check_ptr(da, "da", need)); TRY(check_ptr(db, "db", need));
     TRY(check_ptr(ds0, "ds0", false));
@@ -132,7 +141,7 @@ int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     wkv7::SeqArgs p{};
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
-    p.ckpt_in = ckpt; p.dy = dy; p.dsT = dsT;
+    p.ckpt_in = ckpt; p.fac_in = factors; p.dy = dy; p.dsT = dsT;
     p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0;
     if (wkv7::backward_chunk_supported(p)) return launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward launch");
     return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");

@@ -253,7 +253,10 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
         }
 }
 
-template <typename E>
+// kFac: the per-chunk factors (W, M_k', Q', W Q_b, SA) come from the
+// forward's factor cache, prefetched into the [Q'; W Q_b] slot, instead of
+// being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
+template <typename E, bool kFac>
 __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
     E *raw = reinterpret_cast<E *>(smem);
@@ -309,8 +312,17 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             cp_async16(s0_row(u) + n, src0 + u * 64 + n, 16);
         }
     };
+    const float *FC = reinterpret_cast<const float *>(Bs + B_QQ);  // factor block of the current chunk
+    auto stage_fac = [&](int c) {
+        if constexpr (kFac) {
+            const float *src0 = p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords;
+            for (int e = threadIdx.x; e < fac::kWords / 4; e += NT)
+                cp_async16(Bs + B_QQ + e * 16, src0 + e * 4, 16);
+        }
+    };
     stage_in(nchunks - 1);
     stage_s0(nchunks - 1);
+    stage_fac(nchunks - 1);
     cp_async_commit();
 
     for (int c = nchunks - 1; c >= 0; --c) {
@@ -333,6 +345,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             if (c > 0) {
                 stage_in(c - 1);
                 stage_s0(c - 1);
+                stage_fac(c - 1);
             }
             cp_async_commit();
             continue;
@@ -374,6 +387,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         cp_async_commit();
 
         // ================= per-chunk operands (no state involved)
+        if constexpr (!kFac) {
         {   // Gram [B~; K~] [A^; R^]^T: warp -> m-tile (b~ | k~), n-tile pair (a^ | r^)
             const int mt = warp >> 1;
             float acc[2][4] = {};
@@ -461,12 +475,19 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
         }
         __syncthreads();
+        }
         {   // K' = d_C o (K~ + M_k' B~), B' = d_C o (W B~) (M = token, N = key; warp w owns keys 16w..)
-            const AFrag amk = lda(MK, 0, 0, lane);
-            const AFrag awn = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
-                                     make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
-                                     make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
-                                     make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+            AFrag amk, awn;
+            if constexpr (kFac) {
+                amk = ld_afrag(FC + fac::kMkA, lane);
+                awn = ld_afrag(FC + fac::kWA, lane);
+            } else {
+                amk = lda(MK, 0, 0, lane);
+                awn = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
+                             make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
+                             make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
+                             make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+            }
             BFrag b0, b1;
             ldb2_t(BT, 16 * warp, 0, lane, b0, b1);
             __nv_bfloat16 *kh = hi_of(Bs, B_KB), *kl = lo_of(Bs, B_KB, 32);
@@ -490,16 +511,21 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         // ================= state-dependent products
         // G1: SA = S_0 A' + V M_k'  (rows = value index)
         float sa[2][4] = {};
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const AFrag sf = lda(SX, 16 * warp, 16 * kk, lane);
-            BFrag b0, b1;
-            ldb2(AP, 0, 16 * kk, lane, b0, b1);
-            mma3(sa[0], sf, b0);
-            mma3(sa[1], sf, b1);
-        }
         const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
-        {
+        if constexpr (kFac) {  // SA from the forward
+            const float4 *f = reinterpret_cast<const float4 *>(FC + fac::kSA) + (warp * 32 + lane) * 2;
+            const float4 s0v = f[0], s1v = f[1];
+            sa[0][0] = s0v.x; sa[0][1] = s0v.y; sa[0][2] = s0v.z; sa[0][3] = s0v.w;
+            sa[1][0] = s1v.x; sa[1][1] = s1v.y; sa[1][2] = s1v.z; sa[1][3] = s1v.w;
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const AFrag sf = lda(SX, 16 * warp, 16 * kk, lane);
+                BFrag b0, b1;
+                ldb2(AP, 0, 16 * kk, lane, b0, b1);
+                mma3(sa[0], sf, b0);
+                mma3(sa[1], sf, b1);
+            }
             BFrag b0, b1;
             ldb2_t(MK, 0, 0, lane, b0, b1);
             mma3(sa[0], vA, b0);
@@ -569,8 +595,13 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         const AFrag dyA = lda_t(DYH, 16 * warp, 0, lane);
         {
             BFrag b0, b1, b2, b3;
-            ldb2(QQ, 0, 0, lane, b0, b1);
-            ldb2(QQ, 16, 0, lane, b2, b3);
+            if constexpr (kFac) {
+                ld_bfrags(FC + fac::kQB, lane, b0, b1);
+                ld_bfrags(FC + fac::kWQbB, lane, b2, b3);
+            } else {
+                ldb2(QQ, 0, 0, lane, b0, b1);
+                ldb2(QQ, 16, 0, lane, b2, b3);
+            }
             mma3(dvs[0], dyA, b0); mma3(dvs[1], dyA, b1); mma3(dvs[2], dyA, b2); mma3(dvs[3], dyA, b3);
         }
         {
@@ -593,6 +624,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
+        if (c > 0) stage_fac(c - 1);  // this chunk's factors are consumed
+        cp_async_commit();
 
         {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA)
             const int mt = warp >> 1;
@@ -784,12 +817,12 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     }
 }
 
-template <typename E>
+template <typename E, bool kFac>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
-    cudaError_t e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E><<<p.B * p.H, NT, sm, st>>>(p);
+    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -798,7 +831,8 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 bool backward_chunk_supported(const SeqArgs &p) { return p.L == C; }
 
 cudaError_t launch_backward_chunk(const SeqArgs &p, cudaStream_t st) {
-    return p.dtype == 1 ? launch_t<__nv_bfloat16>(p, st) : launch_t<float>(p, st);
+    if (p.fac_in) return p.dtype == 1 ? launch_t<__nv_bfloat16, true>(p, st) : launch_t<float, true>(p, st);
+    return p.dtype == 1 ? launch_t<__nv_bfloat16, false>(p, st) : launch_t<float, false>(p, st);
 }
 
 }  // namespace wkv7

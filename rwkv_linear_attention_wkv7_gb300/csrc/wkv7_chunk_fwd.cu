@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
             }
         };
 
+        float *const fc = p.fac ? p.fac + ((size_t)bh * nchunks + c) * fac::kWords : nullptr;
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (!exact) {
             // ---- split the decay-scaled vectors and v once: [t][j] quads
@@ -226,6 +227,21 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     build_ap_rp<2>(wt, qbt, AH, AP, RH, Bs, 0, lane);
                 else
                     build_ap_rp<1>(wt, qbt, AH, AP, RH, Bs, warp, lane);
+                if (fc && warp == 3) {  // factor cache: W (A operand of W B~) and W Q_b
+                    const AFrag wa = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
+                                            make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
+                                            make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
+                                            make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+                    float cb[2][4] = {};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int t = 8 * nt + g;
+                        mma3(cb[nt], wa, make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)),
+                                                make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t))));
+                    }
+                    st_afrag(fc + fac::kWA, wa, lane);
+                    st_bfrags_acc(fc + fac::kWQbB, cb, lane);
+                }
             }
             if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b (16 x 16) -> [s][Q' | M_k']
                 auto mk = [&](int s, int u) { return u > s ? G[(16 + s) * GS + u] : 0.f; };
@@ -244,16 +260,21 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 auto qbv = [&](int u, int t) { return u <= t ? G[u * GS + 16 + t] : 0.f; };
                 auto qkv = [&](int s, int t) { return s <= t ? G[(16 + s) * GS + 16 + t] : 0.f; };
                 __nv_bfloat16 *qh = hi_of(Bs, B_QM), *ql = lo_of(Bs, B_QM);
+                float cq[2][4];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const int tc = 8 * nt + 2 * q, t = 8 * nt + g;
-                    float cq[4] = {qkv(g, tc), qkv(g, tc + 1), qkv(g + 8, tc), qkv(g + 8, tc + 1)};
-                    mma3(cq, amp, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
-                                         make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
-                    st_hl(qh, ql, g, tc, cq[0], cq[1]);
-                    st_hl(qh, ql, g + 8, tc, cq[2], cq[3]);
+                    cq[nt][0] = qkv(g, tc); cq[nt][1] = qkv(g, tc + 1); cq[nt][2] = qkv(g + 8, tc); cq[nt][3] = qkv(g + 8, tc + 1);
+                    mma3(cq[nt], amp, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
+                                             make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
+                    st_hl(qh, ql, g, tc, cq[nt][0], cq[nt][1]);
+                    st_hl(qh, ql, g + 8, tc, cq[nt][2], cq[nt][3]);
                     st_hl(qh, ql, g, 16 + tc, cm[nt][0], cm[nt][1]);
                     st_hl(qh, ql, g + 8, 16 + tc, cm[nt][2], cm[nt][3]);
+                }
+                if (fc) {  // factor cache: M_k' (A operand of K') and Q' (B operand of the DY Q'^T product)
+                    st_afrag(fc + fac::kMkA, amp, lane);
+                    st_bfrags_acc(fc + fac::kQB, cq, lane);
                 }
             }
             __syncthreads();
@@ -274,6 +295,11 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 ldb2_t(QM, 0, 0, lane, b0, b1);
                 ldb2_t(QM, 16, 0, lane, b2, b3);
                 mma3(ya[0], vA, b0); mma3(ya[1], vA, b1); mma3(ya[2], vA, b2); mma3(ya[3], vA, b3);
+            }
+            if (fc) {  // factor cache: SA of this warp's value rows
+                float4 *d = reinterpret_cast<float4 *>(fc + fac::kSA) + (warp * 32 + lane) * 2;
+                d[0] = make_float4(ya[2][0], ya[2][1], ya[2][2], ya[2][3]);
+                d[1] = make_float4(ya[3][0], ya[3][1], ya[3][2], ya[3][3]);
             }
             // ---- S_C = (S_0 + SA B~^T + V K~^T) diag(d_C)
             const AFrag saf = make_a(make_float2(ya[2][0], ya[2][1]), make_float2(ya[2][2], ya[2][3]),

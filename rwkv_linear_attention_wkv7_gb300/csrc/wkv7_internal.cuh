@@ -16,10 +16,25 @@ struct SeqArgs {
     const void *r, *w, *k, *v, *a, *b;
     const float *s0;
     float *y, *sT, *ckpt;
+    float *fac;  // per-chunk factor cache written by the forward (L == 16), or NULL
     // backward only
     const float *dy, *dsT, *ckpt_in;
+    const float *fac_in;  // factor cache from the forward, or NULL (recomputed)
     float *dr, *dw, *dk, *dv, *da, *db, *ds0;
 };
+
+// Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the
+// register-fragment order of the backward's warps (lane-major), so that both
+// sides move it with 16-byte accesses.  Split operands are stored as bf16x2
+// (hi, lo) pairs of mma.m16n8k16 fragments.
+namespace fac {
+constexpr int kWA = 0;      // W as an A fragment: lane * 8 + {hi[0..3], lo[0..3]}
+constexpr int kMkA = 256;   // M_k' (= M_k W) as an A fragment, same packing
+constexpr int kQB = 512;    // Q' as the B fragments of the two 8-column n-tiles: lane * 8 + {b0.hi, b0.lo, b1.hi, b1.lo}
+constexpr int kWQbB = 768;  // W Q_b, same packing
+constexpr int kSA = 1024;   // SA fp32, (warp * 32 + lane) * 8 + n-tile * 4 + accumulator element
+constexpr int kWords = 2048;
+}  // namespace fac
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_forward_plain(const SeqArgs &a, cudaStream_t s);

@@ -166,4 +166,37 @@ __device__ __forceinline__ float2 ld_hl(const __nv_bfloat16 *hi, const __nv_bflo
                        __uint_as_float(h & 0xffff0000u) + __uint_as_float(l & 0xffff0000u));
 }
 
+// ---- fragments to and from global memory, lane-major, 32 bytes per lane.
+// A fragment: {hi[0..3]}, {lo[0..3]}.
+__device__ __forceinline__ void st_afrag(float *dst, const AFrag &f, int lane) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst) + lane * 2;
+    d[0] = make_uint4(f.hi[0], f.hi[1], f.hi[2], f.hi[3]);
+    d[1] = make_uint4(f.lo[0], f.lo[1], f.lo[2], f.lo[3]);
+}
+__device__ __forceinline__ AFrag ld_afrag(const float *src, int lane) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(src) + lane * 2;
+    const uint4 h = s[0], l = s[1];
+    AFrag f;
+    f.hi[0] = h.x; f.hi[1] = h.y; f.hi[2] = h.z; f.hi[3] = h.w;
+    f.lo[0] = l.x; f.lo[1] = l.y; f.lo[2] = l.z; f.lo[3] = l.w;
+    return f;
+}
+// The B fragments of the two 8-column n-tiles of X (16 x 16, B[k][n] = X[n][k])
+// from X's two accumulator tiles c[kt] (rows = n, columns = 8kt + ...): the
+// accumulator layout of X is the B layout of its transpose.  Stored as
+// {b0.hi, b0.lo}, {b1.hi, b1.lo}.
+__device__ __forceinline__ void st_bfrags_acc(float *dst, const float c[2][4], int lane) {
+    const Frag2 a = split2(c[0][0], c[0][1]), b = split2(c[1][0], c[1][1]);
+    const Frag2 e = split2(c[0][2], c[0][3]), f = split2(c[1][2], c[1][3]);
+    uint4 *d = reinterpret_cast<uint4 *>(dst) + lane * 2;
+    d[0] = make_uint4(a.hi, b.hi, a.lo, b.lo);
+    d[1] = make_uint4(e.hi, f.hi, e.lo, f.lo);
+}
+__device__ __forceinline__ void ld_bfrags(const float *src, int lane, BFrag &b0, BFrag &b1) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(src) + lane * 2;
+    const uint4 x = s[0], y = s[1];
+    b0.hi[0] = x.x; b0.hi[1] = x.y; b0.lo[0] = x.z; b0.lo[1] = x.w;
+    b1.hi[0] = y.x; b1.hi[1] = y.y; b1.lo[0] = y.z; b1.lo[1] = y.w;
+}
+
 }  // namespace wkv7

@@ -42,9 +42,11 @@ def lib() -> ctypes.CDLL:
         vp, ci, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
         L.wkv7_ckpt_count.argtypes = [ci, ci]
         L.wkv7_ckpt_count.restype = ci
-        L.wkv7_forward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, fp, ci, vp]
+        L.wkv7_factor_floats.argtypes = [ci]
+        L.wkv7_factor_floats.restype = ctypes.c_longlong
+        L.wkv7_forward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, fp, fp, ci, vp]
         L.wkv7_forward.restype = ci
-        L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, ci, fp, fp] + [fp] * 7 + [vp]
+        L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci, fp, fp] + [fp] * 7 + [vp]
         L.wkv7_backward.restype = ci
         L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
         L.wkv7_decode_step.restype = ci
@@ -105,12 +107,19 @@ def ckpt_count(T: int, L: int) -> int:
     return lib().wkv7_ckpt_count(T, L)
 
 
+def factor_floats(T: int) -> int:
+    """Floats per (b, h) of the forward's per-chunk factor cache."""
+    return lib().wkv7_factor_floats(T)
+
+
 def forward(r, w, k, v, a, b, s0=None, L: int = 16, want_ckpt: bool = True, want_sT: bool = True,
-            out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+            want_factors: bool = False, out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
     """Run the recurrence over [B][T][H][64] inputs.
 
-    Returns (y, sT, ckpt); sT / ckpt are None when not requested.  ``out`` may
-    hold preallocated 'y', 'sT', 'ckpt' tensors.
+    Returns (y, sT, ckpt), or (y, sT, ckpt, factors) with ``want_factors``
+    (the per-chunk factor cache for ``backward``; needs L == 16); sT / ckpt
+    are None when not requested.  ``out`` may hold preallocated 'y', 'sT',
+    'ckpt', 'factors' tensors.
     """
     xs = (r, w, k, v, a, b)
     _check_inputs(xs)
@@ -124,20 +133,28 @@ def forward(r, w, k, v, a, b, s0=None, L: int = 16, want_ckpt: bool = True, want
     ck = None
     if want_ckpt and nck >= 0:
         ck = out.get("ckpt") if out.get("ckpt") is not None else torch.empty((B, H, nck, N, N), device=dev)
+    fac = None
+    if want_factors:
+        nf = factor_floats(T)
+        fac = out.get("factors") if out.get("factors") is not None else torch.empty((B, H, max(nf, 0)), device=dev)
+        _f32(fac, (B, H, nf), dev, "factors")
     _f32(y, (B, T, H, N), dev, "y")
     _f32(s0, sshape, dev, "s0")
     rc = lib().wkv7_forward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(y), _ptr(sT), _ptr(ck),
-                            L, _stream(stream))
+                            _ptr(fac), L, _stream(stream))
     _check("wkv7_forward", rc)
-    return y, sT, ck
+    return (y, sT, ck, fac) if want_factors else (y, sT, ck)
 
 
 GRAD_NAMES = ("dr", "dw", "dk", "dv", "da", "db")
 
 
-def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool = True,
+def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool = True, factors=None,
              out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
-    """Gradients of sum(y*dy) + sum(sT*dsT) w.r.t. r, w, k, v, a, b and s0."""
+    """Gradients of sum(y*dy) + sum(sT*dsT) w.r.t. r, w, k, v, a, b and s0.
+
+    ``factors`` is the cache of the forward call that wrote ``ckpt`` (or None
+    to recompute those per-chunk quantities)."""
     xs = (r, w, k, v, a, b)
     _check_inputs(xs)
     B, T, H, N = r.shape
@@ -147,7 +164,10 @@ def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool =
     g["ds0"] = (out.get("ds0") if out.get("ds0") is not None else torch.empty((B, H, N, N), device=dev)) if want_ds0 else None
     _f32(dy, (B, T, H, N), dev, "dy")
     _f32(dsT, (B, H, N, N), dev, "dsT")
-    rc = lib().wkv7_backward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), L, _ptr(dy), _ptr(dsT),
+    if factors is not None:
+        _f32(factors, (B, H, factor_floats(T)), dev, "factors")
+    rc = lib().wkv7_backward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), _ptr(factors), L,
+                             _ptr(dy), _ptr(dsT),
                              *(_ptr(g[n]) for n in GRAD_NAMES), _ptr(g["ds0"]), _stream(stream))
     _check("wkv7_backward", rc)
     return g
@@ -174,17 +194,18 @@ class WKV7Function(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, r, w, k, v, a, b, s0, L):
-        y, sT, ck = forward(r, w, k, v, a, b, s0=s0, L=L)
-        ctx.save_for_backward(r, w, k, v, a, b, ck)
+        y, sT, ck, fac = forward(r, w, k, v, a, b, s0=s0, L=L, want_factors=True) if L == 16 else (
+            *forward(r, w, k, v, a, b, s0=s0, L=L), None)
+        ctx.save_for_backward(r, w, k, v, a, b, ck, fac)
         ctx.L = L
         ctx.has_s0 = s0 is not None
         return y, sT
 
     @staticmethod
     def backward(ctx, dy, dsT):
-        r, w, k, v, a, b, ck = ctx.saved_tensors
+        r, w, k, v, a, b, ck, fac = ctx.saved_tensors
         g = backward(r, w, k, v, a, b, ck, dy.contiguous().float(),
-                     None if dsT is None else dsT.contiguous().float(), L=ctx.L, want_ds0=ctx.has_s0)
+                     None if dsT is None else dsT.contiguous().float(), L=ctx.L, want_ds0=ctx.has_s0, factors=fac)
         cast = (lambda t: t.to(r.dtype)) if r.dtype != torch.float32 else (lambda t: t)
         return (*(cast(g[n]) for n in GRAD_NAMES), g["ds0"], None)
 

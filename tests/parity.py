@@ -43,12 +43,18 @@ def inputs_on_device(spec, heads=None, dev="cuda"):
     return dev_in, host
 
 
-def run_gpu(d, L=16, backward=True):
-    """Forward (+ backward) through the C ABI on device inputs ``d``; outputs stay on the device."""
-    y, sT, ck = wkv7.forward(*(d[n] for n in INPUTS), s0=d.get("s0"), L=L)
+def run_gpu(d, L=16, backward=True, factors=None):
+    """Forward (+ backward) through the C ABI on device inputs ``d``; outputs stay on the device.
+
+    ``factors``: pass the forward's per-chunk factor cache to the backward
+    (the training path); default: whenever L == 16, the stride it needs."""
+    use_fac = (L == 16) if factors is None else factors
+    res = wkv7.forward(*(d[n] for n in INPUTS), s0=d.get("s0"), L=L, want_factors=use_fac)
+    y, sT, ck = res[:3]
+    fac = res[3] if use_fac else None
     out = {"y": y, "sT": sT, "ckpt": ck}
     if backward:
-        out.update(wkv7.backward(*(d[n] for n in INPUTS), ck, d["dy"], dsT=d.get("dsT"), L=L))
+        out.update(wkv7.backward(*(d[n] for n in INPUTS), ck, d["dy"], dsT=d.get("dsT"), L=L, factors=fac))
     torch.cuda.synchronize()
     return out
 

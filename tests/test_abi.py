@@ -33,7 +33,8 @@ def lib():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_last_error"):
+    for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
+                     "wkv7_last_error"):
         assert required in names
 
 
@@ -50,10 +51,18 @@ def test_ckpt_count(lib):
     assert lib.wkv7_ckpt_count(5, 0) == -1
 
 
-def _fwd(lib, B=1, T=4, H=1, N=64, dt=0, ptr=None, y=None, L=16, s0=None):
+def test_factor_floats(lib):
+    assert lib.wkv7_factor_floats(0) == 0
+    assert lib.wkv7_factor_floats(1) == 2048
+    assert lib.wkv7_factor_floats(17) == 2 * 2048
+    assert lib.wkv7_factor_floats(4096) == 256 * 2048
+    assert lib.wkv7_factor_floats(-1) == -1
+
+
+def _fwd(lib, B=1, T=4, H=1, N=64, dt=0, ptr=None, y=None, L=16, s0=None, fac=None):
     p = ctypes.c_void_p(4096) if ptr is None else ptr
     y = p if y is None else y
-    return lib.wkv7_forward(B, T, H, N, dt, p, p, p, p, p, p, s0, y, None, None, L, None)
+    return lib.wkv7_forward(B, T, H, N, dt, p, p, p, p, p, p, s0, y, None, None, fac, L, None)
 
 
 def test_forward_rejects_bad_arguments(lib):
@@ -64,23 +73,28 @@ def test_forward_rejects_bad_arguments(lib):
     assert _fwd(lib, L=0) == EINVAL
     assert _fwd(lib, ptr=ctypes.c_void_p(4100)) == EINVAL and "aligned" in wkv7.last_error()
     assert lib.wkv7_forward(1, 4, 1, 64, 0, None, *([ctypes.c_void_p(4096)] * 5), None,
-                            ctypes.c_void_p(4096), None, None, 16, None) == EINVAL
+                            ctypes.c_void_p(4096), None, None, None, 16, None) == EINVAL
     assert "r is NULL" in wkv7.last_error()
     assert _fwd(lib, s0=ctypes.c_void_p(4104)) == EINVAL
+    assert _fwd(lib, fac=ctypes.c_void_p(4096), L=32) == EINVAL and "L == 16" in wkv7.last_error()
+    assert _fwd(lib, fac=ctypes.c_void_p(4104)) == EINVAL and "factors" in wkv7.last_error()
 
 
 def test_backward_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(4096)
-    args = [1, 4, 1, 64, 0] + [p] * 6 + [p, 16, p, None] + [p] * 6 + [None, None]
+    args = [1, 4, 1, 64, 0] + [p] * 6 + [p, None, 16, p, None] + [p] * 6 + [None, None]
     bad = list(args)
     bad[11] = None  # ckpt missing
     assert lib.wkv7_backward(*bad) == EINVAL and "ckpt" in wkv7.last_error()
     bad = list(args)
-    bad[12] = 0  # L
+    bad[13] = 0  # L
     assert lib.wkv7_backward(*bad) == EINVAL
     bad = list(args)
-    bad[17] = ctypes.c_void_p(4098)  # dv misaligned
+    bad[18] = ctypes.c_void_p(4098)  # dk misaligned
     assert lib.wkv7_backward(*bad) == EINVAL
+    bad = list(args)
+    bad[12], bad[13] = p, 8  # factors with a stride other than 16
+    assert lib.wkv7_backward(*bad) == EINVAL and "L == 16" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

@@ -47,16 +47,34 @@ def test_ragged_lengths_and_strides(T, L, dtype):
     parity.check_heads(host, out, parity.all_heads(2, 3), L=L)
 
 
+@pytest.mark.parametrize("T", [15, 130, 512])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_with_and_without_factor_cache(T, dtype):
+    """The backward that reuses the forward's per-chunk factors and the one
+    that recomputes them both match the oracle, and agree with each other to
+    fp32 rounding."""
+    spec = _custom(2, T, 3, dtype=dtype)
+    d, host = parity.inputs_on_device(spec)
+    with_fac = parity.run_gpu(d, L=16, factors=True)
+    without = parity.run_gpu(d, L=16, factors=False)
+    heads = parity.all_heads(2, 3)
+    parity.check_heads(host, with_fac, heads, L=16)
+    parity.check_heads(host, without, heads, L=16)
+    for k in parity.GRADS + ("ds0",):
+        a, b = with_fac[k].double(), without[k].double()
+        assert float((a - b).norm() / b.norm().clamp_min(1e-30)) <= 1e-5, k
+
+
 def test_empty_sequence():
     """T = 0: the forward copies s0 to sT, the backward copies dsT to ds0."""
     B, H, N = 2, 3, 64
     s0 = torch.randn(B, H, N, N, device="cuda")
     dsT = torch.randn(B, H, N, N, device="cuda")
     e = torch.empty(B, 0, H, N, device="cuda")
-    y, sT, ck = wkv7.forward(e, e, e, e, e, e, s0=s0, L=16)
-    assert y.shape == (B, 0, H, N) and ck.shape == (B, H, 0, N, N)
+    y, sT, ck, fac = wkv7.forward(e, e, e, e, e, e, s0=s0, L=16, want_factors=True)
+    assert y.shape == (B, 0, H, N) and ck.shape == (B, H, 0, N, N) and fac.shape == (B, H, 0)
     assert torch.equal(sT, s0)
-    g = wkv7.backward(e, e, e, e, e, e, ck, torch.empty(B, 0, H, N, device="cuda"), dsT=dsT, L=16)
+    g = wkv7.backward(e, e, e, e, e, e, ck, torch.empty(B, 0, H, N, device="cuda"), dsT=dsT, L=16, factors=fac)
     assert torch.equal(g["ds0"], dsT)
     _, sT0, _ = wkv7.forward(e, e, e, e, e, e, s0=None, L=16)
     torch.cuda.synchronize()
