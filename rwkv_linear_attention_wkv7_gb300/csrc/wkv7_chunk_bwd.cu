@@ -369,8 +369,12 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // decay-scaled vectors, v and dy: [t][j] quads
-            const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
+        for (int m = 0; m < 2; ++m) {  // decay-scaled vectors: [t][j] quads
+            // with the factor cache, warp w converts its own 16-key slab (all
+            // tokens), which is all its K'/B' products read: no block barrier
+            // between the split and K'/B'
+            const int e = kFac ? lane + 32 * m : tid + NT * m;
+            const int t = kFac ? e >> 2 : e >> 4, j = kFac ? 16 * warp + (e & 3) * 4 : (e & 15) * 4;
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * SP + j);
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * SP + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
@@ -378,13 +382,21 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
             st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
             st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // v and dy: [t][i] quads
+            const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
             st_hl4(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, j, ld_raw4(raw, VV, t, j));
             st_hl4(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
         }
-        __syncthreads();
-        // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
-        if (c > 0) stage_in(c - 1);
-        cp_async_commit();
+        if constexpr (kFac) {
+            __syncwarp();
+        } else {
+            __syncthreads();
+            // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
+            if (c > 0) stage_in(c - 1);
+            cp_async_commit();
+        }
 
         // ================= per-chunk operands (no state involved)
         if constexpr (!kFac) {
@@ -507,6 +519,10 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
         }
         __syncthreads();
+        if constexpr (kFac) {  // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
+            if (c > 0) stage_in(c - 1);
+            cp_async_commit();
+        }
 
         // ================= state-dependent products
         // G1: SA = S_0 A' + V M_k'  (rows = value index)
@@ -627,7 +643,11 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         if (c > 0) stage_fac(c - 1);  // this chunk's factors are consumed
         cp_async_commit();
 
-        {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA)
+        {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA),
+            // written straight into its two masked split blocks:
+            //   M3[k][n] = Gam[k][n] where (n < 16 ? s <= t : s < t)           (s = k % 16, t = n % 16)
+            //   M4[k][n] = Gam[n < 16 ? 16 + t : t][k] where (k < 16 ? s >= t : s > t)
+            // M3 pairs (b~_s | k~_s) with (dy_t | dsa_t); M4 pairs (r^_s | a^_s) with (v_t | sa_t)
             const int mt = warp >> 1;
             float acc[2][4] = {};
 #pragma unroll
@@ -638,36 +658,26 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 mma3(acc[0], af, b0);
                 mma3(acc[1], af, b1);
             }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int col = 8 * (2 * (warp & 1) + u) + 2 * q, row = 16 * mt + g;
-                Gm[row * GS + col] = acc[u][0];
-                Gm[row * GS + col + 1] = acc[u][1];
-                Gm[(row + 8) * GS + col] = acc[u][2];
-                Gm[(row + 8) * GS + col + 1] = acc[u][3];
-            }
-        }
-        __syncthreads();
-        {   // masked Gam blocks [k][n]: M3 pairs (b~_s | k~_s) with (dy_t | dsa_t); M4 pairs (r^_s | a^_s) with (v_t | sa_t)
             __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
             __nv_bfloat16 *h4 = hi_of(Bs, B_M4), *l4 = lo_of(Bs, B_M4, 32);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int e = tid + NT * m, k = e >> 4, n = (e & 15) * 2;  // 512 pairs (k, n..n+1)
-                const int s = k & 15, kt = k >> 4;
-                float x3v[2], x4v[2];
+            for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int z = 0; z < 2; ++z) {
-                    const int nn = n + z, t = nn & 15;
-                    const bool keep3 = nn >= 16 ? (s < t) : (s <= t);
-                    x3v[z] = keep3 ? Gm[k * GS + nn] : 0.f;
-                    const int grow = nn < 16 ? 16 + t : t;
-                    const bool keep4 = kt ? (s > t) : (s >= t);
-                    x4v[z] = keep4 ? Gm[grow * GS + 16 * kt + s] : 0.f;
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int R = 16 * mt + g + 8 * hr;              // Gam row
+                    const int Cc = 16 * (warp & 1) + 8 * u + 2 * q;  // Gam column (even)
+                    const int s3 = R & 15, t4 = R & 15, nn = R >= 16 ? t4 : 16 + t4;
+                    float x3v[2];
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        const int n = Cc + z, t = n & 15;
+                        const float x = acc[u][2 * hr + z];
+                        x3v[z] = (n >= 16 ? s3 < t : s3 <= t) ? x : 0.f;
+                        // M4 row n (its s = t), column nn from the Gam row
+                        st_hl1(h4, l4, n, nn, ((n >= 16) ? (t > t4) : (t >= t4)) ? x : 0.f);
+                    }
+                    st_hl(h3, l3, R, Cc, x3v[0], x3v[1]);
                 }
-                st_hl(h3, l3, k, n, x3v[0], x3v[1]);
-                st_hl(h4, l4, k, n, x4v[0], x4v[1]);
-            }
         }
         __syncthreads();
 
@@ -724,6 +734,22 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             mma3(x4[0], af, b0); mma3(x4[1], af, b1); mma3(x4[2], af, b2); mma3(x4[3], af, b3);
         }
 
+        // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index); issued
+        // before the output code so that its MMAs run under the scalar work
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            BFrag r0, r1, a0, a1;
+            ldb2_t(RH, 16 * pp, 0, lane, r0, r1);
+            ldb2_t(AH, 16 * pp, 0, lane, a0, a1);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int nt = 2 * pp + u;
+                const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
+                Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
+                mma3(Gh[nt], dyA, u ? r1 : r0);
+                mma3(Gh[nt], dsA, u ? a1 : a0);
+            }
+        }
         // ================= key-indexed gradients and the dw running sum
         {
             // r^, a^, b~, k~ at this lane's (token, key) positions, in accumulator order
@@ -790,21 +816,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
         }
 
-        // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index)
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-            BFrag r0, r1, a0, a1;
-            ldb2_t(RH, 16 * pp, 0, lane, r0, r1);
-            ldb2_t(AH, 16 * pp, 0, lane, a0, a1);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int nt = 2 * pp + u;
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
-                Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
-                mma3(Gh[nt], dyA, u ? r1 : r0);
-                mma3(Gh[nt], dsA, u ? a1 : a0);
-            }
-        }
         __syncthreads();
     }
     cp_async_wait_all();
