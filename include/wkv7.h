@@ -127,6 +127,49 @@ int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype,
                      const void *v, const void *a, const void *b,
                      float *state, float *y, void *stream);
 
+/* Largest B*H*ceil(T/16) that wkv7_forward_backward_noalloc accepts. */
+#define WKV7_NOALLOC_MAX_CHUNK_HEADS 4096
+
+/*
+ * Forward followed by backward in one call that allocates no memory at all.
+ * This entry point is a library convenience; the method's description has
+ * no counterpart to it.
+ *
+ * It is for callers that cannot call cudaMalloc or hand out temporary device
+ * buffers: code that runs under a host framework with a fixed, pre-planned
+ * memory pool, inside a real-time loop where allocation is forbidden, or from
+ * a language binding with no CUDA allocator of its own.  wkv7_forward +
+ * wkv7_backward with a factor cache need a caller-owned workspace (the cache,
+ * wkv7_factor_floats(T) floats per (b, h)); here that workspace is a
+ * fixed-size array inside the library instead.
+ *
+ * The call runs exactly the tuned path: wkv7_forward with checkpoint stride
+ * 16 writing the factor cache into the library's array, then wkv7_backward
+ * reading it.  The caller passes every input and output:
+ *   r..b, s0, dy, dsT, y, sT, dr..db, ds0   as in wkv7_forward / wkv7_backward
+ *   ckpt      [B][H][ceil(T/16)][N][N] checkpoints (stride 16), required when
+ *             T > 0; written by the forward half, read by the backward half.
+ * Limits and sharing:
+ *   - B*H*ceil(T/16) must not exceed WKV7_NOALLOC_MAX_CHUNK_HEADS (the array
+ *     is 4096 * 8 KiB = 32 MiB); larger requests return WKV7_EINVAL with a
+ *     message naming the limit.
+ *   - Every GPU that loads this library holds that 32 MiB until the process
+ *     exits.
+ *   - All calls on a device share the one array.  Each call writes every
+ *     entry it later reads, so nothing needs clearing, but two calls whose
+ *     work overlaps on the GPU (different streams, no ordering between them)
+ *     race on it and give wrong results.
+ *   - The first call on a device looks up the array's device address once
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ */
+int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
+                                  const void *r, const void *w, const void *k,
+                                  const void *v, const void *a, const void *b,
+                                  const float *s0, const float *dy, const float *dsT,
+                                  float *y, float *sT, float *ckpt,
+                                  float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                                  float *ds0, void *stream);
+
 /* Text of the last error on the calling thread ("" if none). */
 const char *wkv7_last_error(void);
 

@@ -77,6 +77,10 @@ int copy_state(const float *src, float *dst, int B, int H, cudaStream_t st) {
 
 }  // namespace
 
+namespace wkv7 {
+int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
+}  // namespace wkv7
+
 extern "C" {
 
 int wkv7_ckpt_count(int T, int L) {

@@ -36,6 +36,9 @@ constexpr int kSA = 1024;   // SA fp32, (warp * 32 + lane) * 8 + n-tile * 4 + ac
 constexpr int kWords = 2048;
 }  // namespace fac
 
+// Record an error for wkv7_last_error() and return `code` (C ABI layer).
+int set_error(int code, const char *msg);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_forward_plain(const SeqArgs &a, cudaStream_t s);
 bool forward_chunk_supported(const SeqArgs &a);
