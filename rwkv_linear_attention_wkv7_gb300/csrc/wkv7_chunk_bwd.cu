@@ -214,11 +214,6 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off, in
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + rows * MS;
 }
 // split x into (hi, lo) and store both at element (row, col) of a split matrix
-__device__ __forceinline__ void st_hl1(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row, int col, float x) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi[row * MS + col] = h;
-    lo[row * MS + col] = __float2bfloat16_rn(x - __bfloat162float(h));
-}
 // fp32 values of an A fragment's 8 elements (hi + lo), in C-tile order:
 // v[0..1] = (row g, k 2q..2q+1), v[2..3] = (row g+8, ..), v[4..5] = (row g, k 2q+8..), v[6..7] = (row g+8, ..)
 __device__ __forceinline__ void a_values(const AFrag &f, float v[8]) {
@@ -350,7 +345,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             cp_async_commit();
             continue;
         }
-        const float *dC = dd + (C - 1) * SP;
+        const float *dC = dd + (C - 1) * DS;
 
         // ================= split every operand matrix once
         {   // S_0 in place: fp32 staging -> hi/lo
@@ -375,8 +370,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             // between the split and K'/B'
             const int e = kFac ? lane + 32 * m : tid + NT * m;
             const int t = kFac ? e >> 2 : e >> 4, j = kFac ? 16 * warp + (e & 3) * 4 : (e & 15) * 4;
-            const float4 d = *reinterpret_cast<const float4 *>(dd + t * SP + j);
-            const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * SP + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+            const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
+            const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
             st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(ld_raw4(raw, VB, t, j), id));
             st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
@@ -408,8 +403,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
                 BFrag b0, b1;
                 ldb2((warp & 1) ? RH : AH, 0, 16 * kk, lane, b0, b1);
-                mma3(acc[0], af, b0);
-                mma3(acc[1], af, b1);
+                const BFrag bq[2] = {b0, b1};
+                mma3n<2>(acc, af, bq);
             }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -529,10 +524,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         float sa[2][4] = {};
         const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
         if constexpr (kFac) {  // SA from the forward
-            const float4 *f = reinterpret_cast<const float4 *>(FC + fac::kSA) + (warp * 32 + lane) * 2;
-            const float4 s0v = f[0], s1v = f[1];
-            sa[0][0] = s0v.x; sa[0][1] = s0v.y; sa[0][2] = s0v.z; sa[0][3] = s0v.w;
-            sa[1][0] = s1v.x; sa[1][1] = s1v.y; sa[1][2] = s1v.z; sa[1][3] = s1v.w;
+            ld_acc2(FC + fac::kSA + 256 * warp, sa[0], sa[1], lane);
         } else {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -549,12 +541,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         }
         {
             __nv_bfloat16 *shh = hi_of(Bs, B_SAH), *shl = lo_of(Bs, B_SAH, 16);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t = 8 * nt + 2 * q;
-                st_hl1(shh, shl, t, rA, sa[nt][0]); st_hl1(shh, shl, t + 1, rA, sa[nt][1]);
-                st_hl1(shh, shl, t, rB, sa[nt][2]); st_hl1(shh, shl, t + 1, rB, sa[nt][3]);
-            }
+            st_acc_t16(shh, shl, 0, 16 * warp, sa, lane);  // SA[i][t] -> SAH[t][i]
         }
 
         // the dw running sum starts at diag(dsT^T sT): sT from the last chunk's start state
@@ -606,7 +593,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2(KB, 0, 16 * kk, lane, b0, b1);
             ldb2(KB, 16, 16 * kk, lane, b2, b3);
-            mma3(dvs[0], gf, b0); mma3(dvs[1], gf, b1); mma3(dvs[2], gf, b2); mma3(dvs[3], gf, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(dvs, gf, bq); }
         }
         const AFrag dyA = lda_t(DYH, 16 * warp, 0, lane);
         {
@@ -618,7 +605,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 ldb2(QQ, 0, 0, lane, b0, b1);
                 ldb2(QQ, 16, 0, lane, b2, b3);
             }
-            mma3(dvs[0], dyA, b0); mma3(dvs[1], dyA, b1); mma3(dvs[2], dyA, b2); mma3(dvs[3], dyA, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(dvs, dyA, bq); }
         }
         {
             __nv_bfloat16 *dhh = hi_of(Bs, B_DSH), *dhl = lo_of(Bs, B_DSH, 16);
@@ -633,9 +620,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                     p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rA] = dvs[nt][1];
                     p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rB] = dvs[nt][3];
                 }
-                st_hl1(dhh, dhl, t, rA, dvs[nt + 2][0]); st_hl1(dhh, dhl, t + 1, rA, dvs[nt + 2][1]);
-                st_hl1(dhh, dhl, t, rB, dvs[nt + 2][2]); st_hl1(dhh, dhl, t + 1, rB, dvs[nt + 2][3]);
             }
+            st_acc_t16(dhh, dhl, 0, 16 * warp, dvs + 2, lane);  // DSA[i][t] -> DSH[t][i]
         }
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
@@ -655,29 +641,31 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 const AFrag af = lda(mt ? VM : SAH, 0, 16 * kk, lane);
                 BFrag b0, b1;
                 ldb2((warp & 1) ? DSH : DYH, 0, 16 * kk, lane, b0, b1);
-                mma3(acc[0], af, b0);
-                mma3(acc[1], af, b1);
+                const BFrag bq[2] = {b0, b1};
+                mma3n<2>(acc, af, bq);
             }
             __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
             __nv_bfloat16 *h4 = hi_of(Bs, B_M4), *l4 = lo_of(Bs, B_M4, 32);
+            float m4[2][4];
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int R = 16 * mt + g + 8 * hr;              // Gam row
                     const int Cc = 16 * (warp & 1) + 8 * u + 2 * q;  // Gam column (even)
-                    const int s3 = R & 15, t4 = R & 15, nn = R >= 16 ? t4 : 16 + t4;
+                    const int s3 = R & 15;
                     float x3v[2];
 #pragma unroll
                     for (int z = 0; z < 2; ++z) {
                         const int n = Cc + z, t = n & 15;
                         const float x = acc[u][2 * hr + z];
                         x3v[z] = (n >= 16 ? s3 < t : s3 <= t) ? x : 0.f;
-                        // M4 row n (its s = t), column nn from the Gam row
-                        st_hl1(h4, l4, n, nn, ((n >= 16) ? (t > t4) : (t >= t4)) ? x : 0.f);
+                        m4[u][2 * hr + z] = ((n >= 16) ? (t > s3) : (t >= s3)) ? x : 0.f;
                     }
                     st_hl(h3, l3, R, Cc, x3v[0], x3v[1]);
                 }
+            // M4[n][nn] with n = the Gam column, nn = the Gam row with its halves swapped
+            st_acc_t16(h4, l4, 16 * (warp & 1), mt ? 0 : 16, m4, lane);
         }
         __syncthreads();
 
@@ -689,7 +677,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2(DYH, 0, 16 * kk, lane, b0, b1);
             ldb2(DSH, 0, 16 * kk, lane, b2, b3);
-            mma3(x3[0], sT, b0); mma3(x3[1], sT, b1); mma3(x3[2], sT, b2); mma3(x3[3], sT, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, sT, bq); }
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
@@ -697,7 +685,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2_t(M3, 0, 16 * kk, lane, b0, b1);
             ldb2_t(M3, 16, 16 * kk, lane, b2, b3);
-            mma3(x3[0], af, b0); mma3(x3[1], af, b1); mma3(x3[2], af, b2); mma3(x3[3], af, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, af, bq); }
         }
         __syncthreads();  // S_0, dy, DSA and the first masked block no longer read
         if (c > 0) stage_s0(c - 1);
@@ -723,7 +711,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2(VM, 0, 16 * kk, lane, b0, b1);
             ldb2(SAH, 0, 16 * kk, lane, b2, b3);
-            mma3(x4[0], gT, b0); mma3(x4[1], gT, b1); mma3(x4[2], gT, b2); mma3(x4[3], gT, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x4, gT, bq); }
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
@@ -731,24 +719,24 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2_t(M4, 0, 16 * kk, lane, b0, b1);
             ldb2_t(M4, 16, 16 * kk, lane, b2, b3);
-            mma3(x4[0], af, b0); mma3(x4[1], af, b1); mma3(x4[2], af, b2); mma3(x4[3], af, b3);
+            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x4, af, bq); }
         }
 
         // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index); issued
         // before the output code so that its MMAs run under the scalar work
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
-            BFrag r0, r1, a0, a1;
-            ldb2_t(RH, 16 * pp, 0, lane, r0, r1);
-            ldb2_t(AH, 16 * pp, 0, lane, a0, a1);
+            BFrag rr[2], aa[2];
+            ldb2_t(RH, 16 * pp, 0, lane, rr[0], rr[1]);
+            ldb2_t(AH, 16 * pp, 0, lane, aa[0], aa[1]);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int nt = 2 * pp + u;
                 const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
                 Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
-                mma3(Gh[nt], dyA, u ? r1 : r0);
-                mma3(Gh[nt], dsA, u ? a1 : a0);
             }
+            mma3n<2>(Gh + 2 * pp, dyA, rr);
+            mma3n<2>(Gh + 2 * pp, dsA, aa);
         }
         // ================= key-indexed gradients and the dw running sum
         {
@@ -766,8 +754,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                     const int vi = 4 * nt + m;  // value index in a_values order
                     const int row = m < 2 ? rA : rB;
                     const int t = 8 * nt + 2 * q + (m & 1);
-                    const float d = dd[t * SP + row];
-                    const float dp = t ? dd[(t - 1) * SP + row] : 1.f;
+                    const float d = dd[t * DS + row];
+                    const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
                     const float inv = rcp_approx(d);
                     const float xr = x3[nt][m], xa = x3[nt + 2][m], xk = x4[nt][m], xb = x4[nt + 2][m];
                     // r o dr = r^ o X3_r, a o da = a^ o X3_a, b o db = b~ o X4_b, k o dk = k~ o X4_k
@@ -806,8 +794,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 for (int m = 0; m < 4; ++m) {
                     const int t = tv[m];
                     if (t < nv) {
-                        const float d = dd[t * SP + row];
-                        const float dp = t ? dd[(t - 1) * SP + row] : 1.f;
+                        const float d = dd[t * DS + row];
+                        const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
                         p.dw[base0 + (size_t)(t0 + t) * tstride + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
                     }
                 }

@@ -21,6 +21,8 @@ namespace chunk {
 
 constexpr int C = 16;          // tokens per chunk
 constexpr int SP = 72;         // row stride (floats) of [token][64] and [row][64] arrays
+constexpr int DS = 68;         // row stride (floats) of the cumulative decays d[t][j]: reads at
+                               // tokens 2q, 2q + 1 and 8 consecutive columns hit 32 distinct banks
 constexpr int GS = 33;         // row stride of 32x32 Grams
 constexpr int WS = 17;         // row stride of W
 constexpr int RS = 72;         // row stride (elements) of the staged raw inputs: rows start 4 banks apart
@@ -138,7 +140,7 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
 #pragma unroll
         for (int t = 0; t < C; ++t) {
             dc = __fmul_rn(dc, wv[t]);
-            dd[t * SP + j] = dc;
+            dd[t * DS + j] = dc;
             bad |= !(dc >= kTiny && dc <= 1.f / kTiny);
         }
     }
@@ -150,8 +152,8 @@ template <typename E, int NTHR>
 __device__ __forceinline__ void prep_scaled(const E *raw, const float *dd, float *ah, float *rh, float *bt, float *kt) {
     for (int e = threadIdx.x; e < C * 64; e += NTHR) {
         const int t = e >> 6, j = e & 63;
-        const float d = dd[t * SP + j];
-        const float dp = t ? dd[(t - 1) * SP + j] : 1.f;
+        const float d = dd[t * DS + j];
+        const float dp = t ? dd[(t - 1) * DS + j] : 1.f;
         const float inv = __frcp_rn(d);
         ah[t * SP + j] = ld_raw(raw, VA, t, j) * dp;
         rh[t * SP + j] = ld_raw(raw, VR, t, j) * d;

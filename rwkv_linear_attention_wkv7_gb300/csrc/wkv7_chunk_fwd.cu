@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
-                const float4 d = *reinterpret_cast<const float4 *>(dd + t * SP + j);
-                const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * SP + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+                const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
+                const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
                 const float4 id = rcp4(d);
                 st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, mul4(ld_raw4(raw, VB, t, j), id));
                 st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
@@ -196,8 +196,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
                     BFrag b0, b1;
                     ldb2((warp & 1) ? RH : AH, 0, 16 * kk, lane, b0, b1);
-                    mma3(acc[0], af, b0);
-                    mma3(acc[1], af, b1);
+                    const BFrag bq[2] = {b0, b1};
+                    mma3n<2>(acc, af, bq);
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -287,20 +287,16 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 BFrag b0, b1, b2, b3;
                 ldb2(RP, 0, 16 * kk, lane, b0, b1);
                 ldb2(AP, 0, 16 * kk, lane, b2, b3);
-                mma3(ya[0], sf, b0); mma3(ya[1], sf, b1); mma3(ya[2], sf, b2); mma3(ya[3], sf, b3);
+                { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(ya, sf, bq); }
             }
             const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
             {
                 BFrag b0, b1, b2, b3;
                 ldb2_t(QM, 0, 0, lane, b0, b1);
                 ldb2_t(QM, 16, 0, lane, b2, b3);
-                mma3(ya[0], vA, b0); mma3(ya[1], vA, b1); mma3(ya[2], vA, b2); mma3(ya[3], vA, b3);
+                { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(ya, vA, bq); }
             }
-            if (fc) {  // factor cache: SA of this warp's value rows
-                float4 *d = reinterpret_cast<float4 *>(fc + fac::kSA) + (warp * 32 + lane) * 2;
-                d[0] = make_float4(ya[2][0], ya[2][1], ya[2][2], ya[2][3]);
-                d[1] = make_float4(ya[3][0], ya[3][1], ya[3][2], ya[3][3]);
-            }
+            if (fc) st_acc2(fc + fac::kSA + 256 * warp, ya[2], ya[3], lane);  // factor cache: SA of this warp's rows
             // ---- S_C = (S_0 + SA B~^T + V K~^T) diag(d_C)
             const AFrag saf = make_a(make_float2(ya[2][0], ya[2][1]), make_float2(ya[2][2], ya[2][3]),
                                      make_float2(ya[3][0], ya[3][1]), make_float2(ya[3][2], ya[3][3]));
@@ -309,12 +305,13 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 BFrag bb0, bb1, kb0, kb1;
                 ldb2_t(BT, 16 * pp, 0, lane, bb0, bb1);
                 ldb2_t(KT, 16 * pp, 0, lane, kb0, kb1);
+                const BFrag bq[2] = {bb0, bb1}, kq[2] = {kb0, kb1};
+                mma3n<2>(S + 2 * pp, saf, bq);
+                mma3n<2>(S + 2 * pp, vA, kq);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int nt = 2 * pp + u;
-                    mma3(S[nt], saf, u ? bb1 : bb0);
-                    mma3(S[nt], vA, u ? kb1 : kb0);
-                    const float2 dc = *reinterpret_cast<const float2 *>(dd + (C - 1) * SP + 8 * nt + 2 * q);
+                    const float2 dc = *reinterpret_cast<const float2 *>(dd + (C - 1) * DS + 8 * nt + 2 * q);
                     S[nt][0] *= dc.x; S[nt][1] *= dc.y; S[nt][2] *= dc.x; S[nt][3] *= dc.y;
                 }
             }

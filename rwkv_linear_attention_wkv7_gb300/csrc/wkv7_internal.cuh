@@ -24,15 +24,16 @@ struct SeqArgs {
 };
 
 // Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the
-// register-fragment order of the backward's warps (lane-major), so that both
-// sides move it with 16-byte accesses.  Split operands are stored as bf16x2
-// (hi, lo) pairs of mma.m16n8k16 fragments.
+// register-fragment order of the backward's warps, so that both sides move it
+// with 16-byte accesses over contiguous lanes.  Split operands are stored as
+// bf16x2 (hi, lo) pairs of mma.m16n8k16 fragments; each 32-byte lane record
+// is two 16-byte halves 512 bytes apart (half h of lane l at word 128 h + 4 l).
 namespace fac {
-constexpr int kWA = 0;      // W as an A fragment: lane * 8 + {hi[0..3], lo[0..3]}
+constexpr int kWA = 0;      // W as an A fragment: halves {hi[0..3]}, {lo[0..3]}
 constexpr int kMkA = 256;   // M_k' (= M_k W) as an A fragment, same packing
-constexpr int kQB = 512;    // Q' as the B fragments of the two 8-column n-tiles: lane * 8 + {b0.hi, b0.lo, b1.hi, b1.lo}
+constexpr int kQB = 512;    // Q' as the B fragments of the two 8-column n-tiles: halves {b0.hi, b0.lo}, {b1.hi, b1.lo}
 constexpr int kWQbB = 768;  // W Q_b, same packing
-constexpr int kSA = 1024;   // SA fp32, (warp * 32 + lane) * 8 + n-tile * 4 + accumulator element
+constexpr int kSA = 1024;   // SA fp32, 256 words per warp: halves = its two token tiles (4 accumulator values each)
 constexpr int kWords = 2048;
 }  // namespace fac
 

@@ -166,16 +166,18 @@ __device__ __forceinline__ float2 ld_hl(const __nv_bfloat16 *hi, const __nv_bflo
                        __uint_as_float(h & 0xffff0000u) + __uint_as_float(l & 0xffff0000u));
 }
 
-// ---- fragments to and from global memory, lane-major, 32 bytes per lane.
+// ---- fragments to and from memory, 32 bytes per lane stored as two 16-byte
+// halves 512 bytes apart (half h of lane l at uint4 index 32 h + l), so that
+// every warp-wide 16-byte access covers 512 contiguous bytes.
 // A fragment: {hi[0..3]}, {lo[0..3]}.
 __device__ __forceinline__ void st_afrag(float *dst, const AFrag &f, int lane) {
-    uint4 *d = reinterpret_cast<uint4 *>(dst) + lane * 2;
-    d[0] = make_uint4(f.hi[0], f.hi[1], f.hi[2], f.hi[3]);
-    d[1] = make_uint4(f.lo[0], f.lo[1], f.lo[2], f.lo[3]);
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[lane] = make_uint4(f.hi[0], f.hi[1], f.hi[2], f.hi[3]);
+    d[32 + lane] = make_uint4(f.lo[0], f.lo[1], f.lo[2], f.lo[3]);
 }
 __device__ __forceinline__ AFrag ld_afrag(const float *src, int lane) {
-    const uint4 *s = reinterpret_cast<const uint4 *>(src) + lane * 2;
-    const uint4 h = s[0], l = s[1];
+    const uint4 *s = reinterpret_cast<const uint4 *>(src);
+    const uint4 h = s[lane], l = s[32 + lane];
     AFrag f;
     f.hi[0] = h.x; f.hi[1] = h.y; f.hi[2] = h.z; f.hi[3] = h.w;
     f.lo[0] = l.x; f.lo[1] = l.y; f.lo[2] = l.z; f.lo[3] = l.w;
@@ -188,15 +190,62 @@ __device__ __forceinline__ AFrag ld_afrag(const float *src, int lane) {
 __device__ __forceinline__ void st_bfrags_acc(float *dst, const float c[2][4], int lane) {
     const Frag2 a = split2(c[0][0], c[0][1]), b = split2(c[1][0], c[1][1]);
     const Frag2 e = split2(c[0][2], c[0][3]), f = split2(c[1][2], c[1][3]);
-    uint4 *d = reinterpret_cast<uint4 *>(dst) + lane * 2;
-    d[0] = make_uint4(a.hi, b.hi, a.lo, b.lo);
-    d[1] = make_uint4(e.hi, f.hi, e.lo, f.lo);
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[lane] = make_uint4(a.hi, b.hi, a.lo, b.lo);
+    d[32 + lane] = make_uint4(e.hi, f.hi, e.lo, f.lo);
 }
 __device__ __forceinline__ void ld_bfrags(const float *src, int lane, BFrag &b0, BFrag &b1) {
-    const uint4 *s = reinterpret_cast<const uint4 *>(src) + lane * 2;
-    const uint4 x = s[0], y = s[1];
+    const uint4 *s = reinterpret_cast<const uint4 *>(src);
+    const uint4 x = s[lane], y = s[32 + lane];
     b0.hi[0] = x.x; b0.hi[1] = x.y; b0.lo[0] = x.z; b0.lo[1] = x.w;
     b1.hi[0] = y.x; b1.hi[1] = y.y; b1.lo[0] = y.z; b1.lo[1] = y.w;
+}
+// Two fp32 accumulator tiles (8 values per lane) of one warp, same halves.
+__device__ __forceinline__ void st_acc2(float *dst, const float c0[4], const float c1[4], int lane) {
+    float4 *d = reinterpret_cast<float4 *>(dst);
+    d[lane] = make_float4(c0[0], c0[1], c0[2], c0[3]);
+    d[32 + lane] = make_float4(c1[0], c1[1], c1[2], c1[3]);
+}
+__device__ __forceinline__ void ld_acc2(const float *src, float c0[4], float c1[4], int lane) {
+    const float4 *s = reinterpret_cast<const float4 *>(src);
+    const float4 x = s[lane], y = s[32 + lane];
+    c0[0] = x.x; c0[1] = x.y; c0[2] = x.z; c0[3] = x.w;
+    c1[0] = y.x; c1[1] = y.y; c1[2] = y.z; c1[3] = y.w;
+}
+
+// c[n] += A B[n] for NB accumulators, the three split products of each
+// interleaved across the accumulators so that no two consecutive MMAs
+// depend on each other.
+template <int NB>
+__device__ __forceinline__ void mma3n(float (*c)[4], const AFrag &a, const BFrag *b) {
+#pragma unroll
+    for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.lo, b[n].hi);
+#pragma unroll
+    for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.hi, b[n].lo);
+#pragma unroll
+    for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.hi, b[n].hi);
+}
+
+// ---- transposed stores of accumulator blocks with stmatrix (.trans): the
+// 16 x 16 fp32 block held as two n-tiles c[0], c[1] (rows g, g + 8; columns
+// 8u + 2q, +1) is split and written as M[row0 + n][col0 + m] = block[m][n]
+// into a hi/lo matrix pair with row stride MS.  Lane l gives the address of
+// row l % 8 of 8x8 tile l / 8 (tiles: rows 0-7 / 8-15 of the block times
+// columns 0-7 / 8-15, in the order of the fragment registers).
+__device__ __forceinline__ void stsm_x4_t(void *p, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
+__device__ __forceinline__ void st_acc_t16(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row0, int col0, const float c[2][4],
+                                           int lane) {
+    const Frag2 f0 = split2(c[0][0], c[0][1]), f1 = split2(c[0][2], c[0][3]);
+    const Frag2 f2 = split2(c[1][0], c[1][1]), f3 = split2(c[1][2], c[1][3]);
+    const int k = lane >> 3, r = lane & 7;
+    const int off = (row0 + 8 * (k >> 1) + r) * MS + col0 + 8 * (k & 1);
+    stsm_x4_t(hi + off, f0.hi, f1.hi, f2.hi, f3.hi);
+    stsm_x4_t(lo + off, f0.lo, f1.lo, f2.lo, f3.lo);
 }
 
 }  // namespace wkv7
