@@ -498,20 +498,24 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1;
             ldb2_t(BT, 16 * warp, 0, lane, b0, b1);
             __nv_bfloat16 *kh = hi_of(Bs, B_KB), *kl = lo_of(Bs, B_KB, 32);
+            float ck[2][4], cb2[2][4] = {};
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int jc = 16 * warp + 8 * u + 2 * q;
                 const float2 k0 = ld_hl(KT.hi, KT.lo, g, jc), k8 = ld_hl(KT.hi, KT.lo, g + 8, jc);
-                float ck[4] = {k0.x, k0.y, k8.x, k8.y};
-                float cb2[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3(ck, amk, u ? b1 : b0);
-                mma3(cb2, awn, u ? b1 : b0);
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + jc);
-                st_hl(kh, kl, g, jc, ck[0] * dc.x, ck[1] * dc.y);
-                st_hl(kh, kl, g + 8, jc, ck[2] * dc.x, ck[3] * dc.y);
-                st_hl(kh, kl, 16 + g, jc, cb2[0] * dc.x, cb2[1] * dc.y);
-                st_hl(kh, kl, 24 + g, jc, cb2[2] * dc.x, cb2[3] * dc.y);
+                ck[u][0] = k0.x; ck[u][1] = k0.y; ck[u][2] = k8.x; ck[u][3] = k8.y;
             }
+            const BFrag bq[2] = {b0, b1};
+            mma3n<2>(ck, amk, bq);
+            mma3n<2>(cb2, awn, bq);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float2 dc = *reinterpret_cast<const float2 *>(dC + 16 * warp + 8 * u + 2 * q);
+                ck[u][0] *= dc.x; ck[u][1] *= dc.y; ck[u][2] *= dc.x; ck[u][3] *= dc.y;
+                cb2[u][0] *= dc.x; cb2[u][1] *= dc.y; cb2[u][2] *= dc.x; cb2[u][3] *= dc.y;
+            }
+            st_acc16(kh, kl, 0, 16 * warp, ck, lane);   // K' rows (tokens)
+            st_acc16(kh, kl, 16, 16 * warp, cb2, lane); // B' rows
         }
         __syncthreads();
         if constexpr (kFac) {  // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
@@ -646,7 +650,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             }
             __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
             __nv_bfloat16 *h4 = hi_of(Bs, B_M4), *l4 = lo_of(Bs, B_M4, 32);
-            float m4[2][4];
+            float m3[2][4], m4[2][4];
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -654,16 +658,15 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                     const int R = 16 * mt + g + 8 * hr;              // Gam row
                     const int Cc = 16 * (warp & 1) + 8 * u + 2 * q;  // Gam column (even)
                     const int s3 = R & 15;
-                    float x3v[2];
 #pragma unroll
                     for (int z = 0; z < 2; ++z) {
                         const int n = Cc + z, t = n & 15;
                         const float x = acc[u][2 * hr + z];
-                        x3v[z] = (n >= 16 ? s3 < t : s3 <= t) ? x : 0.f;
+                        m3[u][2 * hr + z] = (n >= 16 ? s3 < t : s3 <= t) ? x : 0.f;
                         m4[u][2 * hr + z] = ((n >= 16) ? (t > s3) : (t >= s3)) ? x : 0.f;
                     }
-                    st_hl(h3, l3, R, Cc, x3v[0], x3v[1]);
                 }
+            st_acc16(h3, l3, 16 * mt, 16 * (warp & 1), m3, lane);
             // M4[n][nn] with n = the Gam column, nn = the Gam row with its halves swapped
             st_acc_t16(h4, l4, 16 * (warp & 1), mt ? 0 : 16, m4, lane);
         }
@@ -694,11 +697,16 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         {
             __nv_bfloat16 *gh = hi_of(Bs, B_SX), *gl = lo_of(Bs, B_SX, 64);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int j0 = 8 * nt + 2 * q;
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + j0);
-                st_hl(gh, gl, rA, j0, Gh[nt][0] * dc.x, Gh[nt][1] * dc.y);
-                st_hl(gh, gl, rB, j0, Gh[nt][2] * dc.x, Gh[nt][3] * dc.y);
+            for (int pp = 0; pp < 4; ++pp) {
+                float gd[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int nt = 2 * pp + u;
+                    const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
+                    gd[u][0] = Gh[nt][0] * dc.x; gd[u][1] = Gh[nt][1] * dc.y;
+                    gd[u][2] = Gh[nt][2] * dc.x; gd[u][3] = Gh[nt][3] * dc.y;
+                }
+                st_acc16(gh, gl, 16 * warp, 16 * pp, gd, lane);
             }
         }
         __syncthreads();

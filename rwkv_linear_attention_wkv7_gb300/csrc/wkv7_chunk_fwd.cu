@@ -79,13 +79,7 @@ __device__ __forceinline__ void build_ap_rp(const AFrag &wt, const AFrag &qbt, c
     }
     __nv_bfloat16 *aph = hi_of(Bs, B_AP), *apl = lo_of(Bs, B_AP);
 #pragma unroll
-    for (int s = 0; s < NS; ++s)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
-            st_hl(aph, apl, g, jc, ca[s][u][0], ca[s][u][1]);
-            st_hl(aph, apl, g + 8, jc, ca[s][u][2], ca[s][u][3]);
-        }
+    for (int s = 0; s < NS; ++s) st_acc16(aph, apl, 0, 16 * (slab0 + s), ca[s], lane);
     __syncwarp();
     __nv_bfloat16 *rph = hi_of(Bs, B_AH), *rpl = lo_of(Bs, B_AH);
 #pragma unroll
@@ -101,13 +95,7 @@ __device__ __forceinline__ void build_ap_rp(const AFrag &wt, const AFrag &qbt, c
             mma3(cr[s][u], qbt, b[s][u]);
         }
 #pragma unroll
-    for (int s = 0; s < NS; ++s)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
-            st_hl(rph, rpl, g, jc, cr[s][u][0], cr[s][u][1]);
-            st_hl(rph, rpl, g + 8, jc, cr[s][u][2], cr[s][u][3]);
-        }
+    for (int s = 0; s < NS; ++s) st_acc16(rph, rpl, 0, 16 * (slab0 + s), cr[s], lane);
 }
 
 template <typename E>
@@ -267,11 +255,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     cq[nt][0] = qkv(g, tc); cq[nt][1] = qkv(g, tc + 1); cq[nt][2] = qkv(g + 8, tc); cq[nt][3] = qkv(g + 8, tc + 1);
                     mma3(cq[nt], amp, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
                                              make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
-                    st_hl(qh, ql, g, tc, cq[nt][0], cq[nt][1]);
-                    st_hl(qh, ql, g + 8, tc, cq[nt][2], cq[nt][3]);
-                    st_hl(qh, ql, g, 16 + tc, cm[nt][0], cm[nt][1]);
-                    st_hl(qh, ql, g + 8, 16 + tc, cm[nt][2], cm[nt][3]);
                 }
+                st_acc16(qh, ql, 0, 0, cq, lane);   // Q'[s][t]
+                st_acc16(qh, ql, 0, 16, cm, lane);  // M_k'[s][t]
                 if (fc) {  // factor cache: M_k' (A operand of K') and Q' (B operand of the DY Q'^T product)
                     st_afrag(fc + fac::kMkA, amp, lane);
                     st_bfrags_acc(fc + fac::kQB, cq, lane);

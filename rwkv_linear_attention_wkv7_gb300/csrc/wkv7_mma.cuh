@@ -248,4 +248,21 @@ __device__ __forceinline__ void st_acc_t16(__nv_bfloat16 *hi, __nv_bfloat16 *lo,
     stsm_x4_t(lo + off, f0.lo, f1.lo, f2.lo, f3.lo);
 }
 
+// Same block stored untransposed: M[row0 + m][col0 + n] = block[m][n].
+__device__ __forceinline__ void stsm_x4(void *p, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(r0), "r"(r1), "r"(r2),
+                 "r"(r3)
+                 : "memory");
+}
+__device__ __forceinline__ void st_acc16(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row0, int col0, const float c[2][4],
+                                         int lane) {
+    const Frag2 f0 = split2(c[0][0], c[0][1]), f1 = split2(c[0][2], c[0][3]);
+    const Frag2 f2 = split2(c[1][0], c[1][1]), f3 = split2(c[1][2], c[1][3]);
+    const int k = lane >> 3, r = lane & 7;
+    const int off = (row0 + 8 * (k & 1) + r) * MS + col0 + 8 * (k >> 1);
+    stsm_x4(hi + off, f0.hi, f1.hi, f2.hi, f3.hi);
+    stsm_x4(lo + off, f0.lo, f1.lo, f2.lo, f3.lo);
+}
+
 }  // namespace wkv7
