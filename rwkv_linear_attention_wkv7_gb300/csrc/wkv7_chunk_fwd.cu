@@ -6,14 +6,15 @@
 // wkv7_chunk_common.cuh the chunk's sa_t solve a unit triangular 16x16 system
 // and every state-dependent quantity is a dense contraction with the
 // chunk-start state S_0:
-//     SA  = S_0 A' + V M_k'              (A' = A^ W,  M_k' = M_k W,  W = (I - M_b)^{-1})
-//     Y   = S_0 R' + V Q'                (R' = R^ + A' Q_b,  Q' = Q_k + M_k' Q_b)
+//     SA  = S_0 A' + V M_k' = U W        U = S_0 A^ + V M_k,  W = (I - M_b)^{-1}
+//     Y   = S_0 R' + V Q'   = Z + SA Q_b  Z = S_0 R^ + V Q_k
 //     S_C = S_0 diag(d_C) + SA Bbar^T + V Kbar^T      (Bbar = B~ diag(d_C), Kbar = K~ diag(d_C))
-// and, since the column scaling commutes, S_C = (S_0 + SA B~^T + V K~^T) diag(d_C).
-// Everything that does not involve S_0 (the Gram, W, A', R', M_k', Q') is
-// built once per chunk, on tensor cores where it is a contraction, and every
-// matrix operand is split into bf16 hi + lo once, into row-major shared
-// matrices that ldmatrix (.trans where the use is transposed) turns into MMA
+// (A' = A^ W, M_k' = M_k W, R' = R^ + A' Q_b, Q' = Q_k + M_k' Q_b) and, since
+// the column scaling commutes, S_C = (S_0 + SA B~^T + V K~^T) diag(d_C).  The
+// large products U and Z need only the Gram, so they run while one warp
+// solves for W; SA and Y then take two 16 x 16 products.  Every matrix
+// operand is split into bf16 hi + lo once, into row-major shared matrices
+// that ldmatrix (.trans where the use is transposed) turns into MMA
 // fragments.  The state
 // products run on mma.sync bf16 with split operands (three products) and
 // fp32 accumulation; the state lives in registers as MMA accumulators: warp w
@@ -34,19 +35,18 @@ constexpr int YS = 68;  // row stride (floats) of the y staging block
 // Shared-memory carve-up (byte offsets after the raw input block).  HL16 = a
 // split operand matrix (bf16 hi then lo) of 16 rows, row stride MS.
 constexpr int HL16 = 2 * 16 * MS * 2;
-constexpr int B_DD = 0;                              // d fp32 [C][SP]
-constexpr int B_G = B_DD + C * SP * 4;               // Gram fp32 [32][GS]; later y staging [C][YS]
-constexpr int G_SLOT = (32 * GS > C * YS ? 32 * GS : C * YS) * 4;
+constexpr int B_DD = 0;                              // d fp32 [C][DS]
+constexpr int B_G = B_DD + C * SP * 4;               // Gram fp32 [32][GS]
+constexpr int G_SLOT = 32 * GS * 4;
 constexpr int B_BT = B_G + ((G_SLOT + 15) / 16) * 16;  // b~ [t][j]
 constexpr int B_KT = B_BT + HL16;                    // k~ [t][j]
-constexpr int B_AH = B_KT + HL16;                    // a^ [t][j], then R' [t][j]
+constexpr int B_AH = B_KT + HL16;                    // a^ [t][j]
 constexpr int B_RH = B_AH + HL16;                    // r^ [t][j]
 constexpr int B_VM = B_RH + HL16;                    // v [t][i]
-constexpr int B_AP = B_VM + HL16;                    // A' [t][j]
-constexpr int B_QM = B_AP + HL16;                    // [s][0..15] = Q', [s][16..31] = M_k'
-constexpr int B_W = B_QM + HL16;                     // W fp32 [C][WS]
+constexpr int B_Y = B_VM + HL16;                     // y staging fp32 [C][YS]
+constexpr int B_W = B_Y + C * YS * 4;                // W fp32 [C][WS]
 constexpr int kBytes = B_W + C * WS * 4;
-static_assert(B_BT % 16 == 0, "16-byte aligned operand matrices");
+static_assert(B_BT % 16 == 0 && B_Y % 16 == 0 && B_W % 16 == 0, "16-byte aligned blocks");
 
 template <typename E>
 __host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
@@ -62,52 +62,14 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + 16 * MS;
 }
 
-// A' = W^T-weighted a^ and R' = r^ + Q_b^T A' for NS 16-key slabs starting at
-// slab0 (M = token, N = key); the slabs' MMAs are issued together.  R' takes
-// the a^ slot of its slab, which only this warp reads.
-template <int NS>
-__device__ __forceinline__ void build_ap_rp(const AFrag &wt, const AFrag &qbt, const HL &AH, const HL &AP, const HL &RH,
-                                            unsigned char *Bs, int slab0, int lane) {
-    const int g = lane >> 2, q = lane & 3;
-    BFrag b[NS][2];
-    float ca[NS][2][4] = {};
-#pragma unroll
-    for (int s = 0; s < NS; ++s) {
-        ldb2_t(AH, 16 * (slab0 + s), 0, lane, b[s][0], b[s][1]);
-        mma3(ca[s][0], wt, b[s][0]);
-        mma3(ca[s][1], wt, b[s][1]);
-    }
-    __nv_bfloat16 *aph = hi_of(Bs, B_AP), *apl = lo_of(Bs, B_AP);
-#pragma unroll
-    for (int s = 0; s < NS; ++s) st_acc16(aph, apl, 0, 16 * (slab0 + s), ca[s], lane);
-    __syncwarp();
-    __nv_bfloat16 *rph = hi_of(Bs, B_AH), *rpl = lo_of(Bs, B_AH);
-#pragma unroll
-    for (int s = 0; s < NS; ++s) ldb2_t(AP, 16 * (slab0 + s), 0, lane, b[s][0], b[s][1]);
-    float cr[NS][2][4];
-#pragma unroll
-    for (int s = 0; s < NS; ++s)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int jc = 16 * (slab0 + s) + 8 * u + 2 * q;
-            const float2 r0 = ld_hl(RH.hi, RH.lo, g, jc), r8 = ld_hl(RH.hi, RH.lo, g + 8, jc);
-            cr[s][u][0] = r0.x; cr[s][u][1] = r0.y; cr[s][u][2] = r8.x; cr[s][u][3] = r8.y;
-            mma3(cr[s][u], qbt, b[s][u]);
-        }
-#pragma unroll
-    for (int s = 0; s < NS; ++s) st_acc16(rph, rpl, 0, 16 * (slab0 + s), cr[s], lane);
-}
-
 template <typename E>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
     E *raw = reinterpret_cast<E *>(smem);
     unsigned char *Bs = smem + raw_bytes<E>();
     float *dd = reinterpret_cast<float *>(Bs + B_DD), *G = reinterpret_cast<float *>(Bs + B_G);
-    float *ys = G, *Wm = reinterpret_cast<float *>(Bs + B_W);
-    const HL BT = hl(Bs, B_BT), KT = hl(Bs, B_KT), AH = hl(Bs, B_AH), RH = hl(Bs, B_RH), VM = hl(Bs, B_VM),
-             AP = hl(Bs, B_AP), QM = hl(Bs, B_QM);
-    const HL RP = AH;  // R' takes the slot of a^ once A' is built
+    float *ys = reinterpret_cast<float *>(Bs + B_Y), *Wm = reinterpret_cast<float *>(Bs + B_W);
+    const HL BT = hl(Bs, B_BT), KT = hl(Bs, B_KT), AH = hl(Bs, B_AH), RH = hl(Bs, B_RH), VM = hl(Bs, B_VM);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -198,24 +160,86 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
             }
             write_ckpt();
             __syncthreads();
-            prep_inverse(G, Wm);
-            __syncthreads();
 
-            if (warp != 1) {  // A' = W^T-weighted A^ and R' = R^ + Q_b^T A' (warp 0: keys 0..31, warps 2, 3: 16w..16w+15)
-                const AFrag wt = make_a(make_float2(Wm[(2 * q) * WS + g], Wm[(2 * q + 1) * WS + g]),
-                                        make_float2(Wm[(2 * q) * WS + g + 8], Wm[(2 * q + 1) * WS + g + 8]),
-                                        make_float2(Wm[(2 * q + 8) * WS + g], Wm[(2 * q + 9) * WS + g]),
-                                        make_float2(Wm[(2 * q + 8) * WS + g + 8], Wm[(2 * q + 9) * WS + g + 8]));
-                auto qb = [&](int s, int t) { return s <= t ? G[s * GS + 16 + t] : 0.f; };  // Q_b[s][t]
-                const AFrag qbt = make_a(make_float2(qb(2 * q, g), qb(2 * q + 1, g)),
-                                         make_float2(qb(2 * q, g + 8), qb(2 * q + 1, g + 8)),
-                                         make_float2(qb(2 * q + 8, g), qb(2 * q + 9, g)),
-                                         make_float2(qb(2 * q + 8, g + 8), qb(2 * q + 9, g + 8)));
-                if (warp == 0)
-                    build_ap_rp<2>(wt, qbt, AH, AP, RH, Bs, 0, lane);
-                else
-                    build_ap_rp<1>(wt, qbt, AH, AP, RH, Bs, warp, lane);
-                if (fc && warp == 3) {  // factor cache: W (A operand of W B~) and W Q_b
+            // W on warp 0 while every warp forms [Z | U] = S_0 [R^ | A^] + V [Q_k | M_k]
+            // (warp 0 follows with its own rows once W is done)
+            prep_inverse(G, Wm);
+            auto mk = [&](int s, int t) { return s < t ? G[(16 + s) * GS + t] : 0.f; };        // M_k[s][t]
+            auto qk = [&](int s, int t) { return s <= t ? G[(16 + s) * GS + 16 + t] : 0.f; };  // Q_k[s][t]
+            auto qb = [&](int s, int t) { return s <= t ? G[s * GS + 16 + t] : 0.f; };         // Q_b[s][t]
+            float ya[4][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const AFrag sf = a_from_acc(S, kk);
+                BFrag bq[4];
+                ldb2(RH, 0, 16 * kk, lane, bq[0], bq[1]);
+                ldb2(AH, 0, 16 * kk, lane, bq[2], bq[3]);
+                mma3n<4>(ya, sf, bq);
+            }
+            const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
+            {
+                BFrag bq[4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = 8 * u + g;
+                    bq[u] = make_b(make_float2(qk(2 * q, t), qk(2 * q + 1, t)), make_float2(qk(2 * q + 8, t), qk(2 * q + 9, t)));
+                    bq[2 + u] = make_b(make_float2(mk(2 * q, t), mk(2 * q + 1, t)), make_float2(mk(2 * q + 8, t), mk(2 * q + 9, t)));
+                }
+                mma3n<4>(ya, vA, bq);
+            }
+            __syncthreads();  // W
+
+            // ---- SA = U W and Y = Z + SA Q_b (16 x 16 per warp)
+            float sa[2][4] = {};
+            {
+                const AFrag ua = make_a(make_float2(ya[2][0], ya[2][1]), make_float2(ya[2][2], ya[2][3]),
+                                        make_float2(ya[3][0], ya[3][1]), make_float2(ya[3][2], ya[3][3]));
+                BFrag bw[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = 8 * u + g;
+                    bw[u] = make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
+                                   make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t]));
+                }
+                mma3n<2>(sa, ua, bw);
+            }
+            const AFrag saf = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
+                                     make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
+            {
+                BFrag bq[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = 8 * u + g;
+                    bq[u] = make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)), make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t)));
+                }
+                mma3n<2>(ya, saf, bq);  // Y (tiles 0, 1 of ya)
+            }
+            if (fc) {  // factor cache for the backward
+                st_acc2(fc + fac::kSA + 256 * warp, sa[0], sa[1], lane);
+                if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b
+                    const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
+                                            make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
+                                            make_float2(mk(g + 8, 2 * q + 8), mk(g + 8, 2 * q + 9)));
+                    float cm[2][4] = {};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int t = 8 * nt + g;
+                        mma3(cm[nt], am, make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
+                                                make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t])));
+                    }
+                    const AFrag amp = make_a(make_float2(cm[0][0], cm[0][1]), make_float2(cm[0][2], cm[0][3]),
+                                             make_float2(cm[1][0], cm[1][1]), make_float2(cm[1][2], cm[1][3]));
+                    float cq[2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int tc = 8 * nt + 2 * q, t = 8 * nt + g;
+                        cq[nt][0] = qk(g, tc); cq[nt][1] = qk(g, tc + 1); cq[nt][2] = qk(g + 8, tc); cq[nt][3] = qk(g + 8, tc + 1);
+                        mma3(cq[nt], amp, make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)),
+                                                 make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t))));
+                    }
+                    st_afrag(fc + fac::kMkA, amp, lane);
+                    st_bfrags_acc(fc + fac::kQB, cq, lane);
+                } else if (warp == 3) {  // W (A operand of W B~) and W Q_b
                     const AFrag wa = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
                                             make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
                                             make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
@@ -231,61 +255,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     st_bfrags_acc(fc + fac::kWQbB, cb, lane);
                 }
             }
-            if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b (16 x 16) -> [s][Q' | M_k']
-                auto mk = [&](int s, int u) { return u > s ? G[(16 + s) * GS + u] : 0.f; };
-                const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
-                                        make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
-                                        make_float2(mk(g + 8, 2 * q + 8), mk(g + 8, 2 * q + 9)));
-                float cm[2][4] = {};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int t = 8 * nt + g;
-                    mma3(cm[nt], am, make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
-                                            make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t])));
-                }
-                const AFrag amp = make_a(make_float2(cm[0][0], cm[0][1]), make_float2(cm[0][2], cm[0][3]),
-                                         make_float2(cm[1][0], cm[1][1]), make_float2(cm[1][2], cm[1][3]));
-                auto qbv = [&](int u, int t) { return u <= t ? G[u * GS + 16 + t] : 0.f; };
-                auto qkv = [&](int s, int t) { return s <= t ? G[(16 + s) * GS + 16 + t] : 0.f; };
-                __nv_bfloat16 *qh = hi_of(Bs, B_QM), *ql = lo_of(Bs, B_QM);
-                float cq[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int tc = 8 * nt + 2 * q, t = 8 * nt + g;
-                    cq[nt][0] = qkv(g, tc); cq[nt][1] = qkv(g, tc + 1); cq[nt][2] = qkv(g + 8, tc); cq[nt][3] = qkv(g + 8, tc + 1);
-                    mma3(cq[nt], amp, make_b(make_float2(qbv(2 * q, t), qbv(2 * q + 1, t)),
-                                             make_float2(qbv(2 * q + 8, t), qbv(2 * q + 9, t))));
-                }
-                st_acc16(qh, ql, 0, 0, cq, lane);   // Q'[s][t]
-                st_acc16(qh, ql, 0, 16, cm, lane);  // M_k'[s][t]
-                if (fc) {  // factor cache: M_k' (A operand of K') and Q' (B operand of the DY Q'^T product)
-                    st_afrag(fc + fac::kMkA, amp, lane);
-                    st_bfrags_acc(fc + fac::kQB, cq, lane);
-                }
-            }
-            __syncthreads();
-
-            // ---- [Y | SA] = S_0 [R' | A'] + V [Q' | M_k']
-            float ya[4][4] = {};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const AFrag sf = a_from_acc(S, kk);
-                BFrag b0, b1, b2, b3;
-                ldb2(RP, 0, 16 * kk, lane, b0, b1);
-                ldb2(AP, 0, 16 * kk, lane, b2, b3);
-                { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(ya, sf, bq); }
-            }
-            const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
-            {
-                BFrag b0, b1, b2, b3;
-                ldb2_t(QM, 0, 0, lane, b0, b1);
-                ldb2_t(QM, 16, 0, lane, b2, b3);
-                { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(ya, vA, bq); }
-            }
-            if (fc) st_acc2(fc + fac::kSA + 256 * warp, ya[2], ya[3], lane);  // factor cache: SA of this warp's rows
             // ---- S_C = (S_0 + SA B~^T + V K~^T) diag(d_C)
-            const AFrag saf = make_a(make_float2(ya[2][0], ya[2][1]), make_float2(ya[2][2], ya[2][3]),
-                                     make_float2(ya[3][0], ya[3][1]), make_float2(ya[3][2], ya[3][3]));
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
                 BFrag bb0, bb1, kb0, kb1;
@@ -301,7 +271,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     S[nt][0] *= dc.x; S[nt][1] *= dc.y; S[nt][2] *= dc.x; S[nt][3] *= dc.y;
                 }
             }
-            // y of the chunk -> staging [t][row] (the Gram slot is free now)
+            // y of the chunk -> staging [t][row]
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int t = 8 * nt + 2 * q;
