@@ -24,6 +24,8 @@
 // a reverse running sum whose value past the last token is diag(dsT^T sT).
 // Chunks whose decay underflows take an exact per-token path that replays
 // the chunk from its checkpoint.
+#include <type_traits>
+
 #include "wkv7_chunk_common.cuh"
 
 namespace wkv7 {
@@ -253,6 +255,8 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
 template <typename E, bool kFac>
 __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
+    // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
+    constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     extern __shared__ __align__(16) unsigned char smem[];
     E *raw = reinterpret_cast<E *>(smem);
     unsigned char *Bs = smem + raw_bytes<E>();
@@ -719,7 +723,11 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             BFrag b0, b1, b2, b3;
             ldb2(VM, 0, 16 * kk, lane, b0, b1);
             ldb2(SAH, 0, 16 * kk, lane, b2, b3);
-            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x4, gT, bq); }
+            {
+                const BFrag bv[2] = {b0, b1}, bs[2] = {b2, b3};
+                mma3n<2, true, kVLo>(x4, gT, bv);
+                mma3n<2>(x4 + 2, gT, bs);
+            }
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {

@@ -215,5 +215,32 @@ __device__ __forceinline__ void prep_inverse(const float *G, float *Wm) {
     for (int s = 0; s < C; ++s) Wm[s * WS + t] = wc[s];
 }
 
+// W = (I - M_b)^{-1} as above, M_b read from a row-major copy with row
+// stride MBS floats (16-byte aligned rows): each row comes in with broadcast
+// 16-byte loads issued ahead of the product chain.
+constexpr int MBS = 20;
+__device__ __forceinline__ void prep_inverse_v(const float *Mb, float *Wm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp != 0 || lane >= C) return;
+    const int t = lane;
+    float wc[C];
+#pragma unroll
+    for (int s = C - 1; s >= 0; --s) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(Mb + s * MBS);
+        float m[C];
+#pragma unroll
+        for (int k = (s + 1) >> 2; k < 4; ++k) {
+            const float4 x = r4[k];
+            m[4 * k] = x.x; m[4 * k + 1] = x.y; m[4 * k + 2] = x.z; m[4 * k + 3] = x.w;
+        }
+        float acc = (s == t) ? 1.f : 0.f;
+#pragma unroll
+        for (int u = C - 1; u > s; --u) acc = __fmaf_rn(m[u], wc[u], acc);
+        wc[s] = acc;
+    }
+#pragma unroll
+    for (int s = 0; s < C; ++s) Wm[s * WS + t] = wc[s];
+}
+
 }  // namespace chunk
 }  // namespace wkv7

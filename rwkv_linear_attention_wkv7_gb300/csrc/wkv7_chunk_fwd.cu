@@ -23,6 +23,8 @@
 //
 // A chunk whose cumulative decay leaves [1e-20, 1e20] (e.g. w = 0) cannot use
 // 1/d_t; it takes the exact per-token recurrence on the same register layout.
+#include <type_traits>
+
 #include "wkv7_chunk_common.cuh"
 
 namespace wkv7 {
@@ -45,8 +47,9 @@ constexpr int B_RH = B_AH + HL16;                    // r^ [t][j]
 constexpr int B_VM = B_RH + HL16;                    // v [t][i]
 constexpr int B_Y = B_VM + HL16;                     // y staging fp32 [C][YS]
 constexpr int B_W = B_Y + C * YS * 4;                // W fp32 [C][WS]
-constexpr int kBytes = B_W + C * WS * 4;
-static_assert(B_BT % 16 == 0 && B_Y % 16 == 0 && B_W % 16 == 0, "16-byte aligned blocks");
+constexpr int B_MB = B_W + ((C * WS * 4 + 15) / 16) * 16;  // M_b fp32 [C][MBS] (for the inverse)
+constexpr int kBytes = B_MB + C * MBS * 4;
+static_assert(B_BT % 16 == 0 && B_Y % 16 == 0 && B_W % 16 == 0 && B_MB % 16 == 0, "16-byte aligned blocks");
 
 template <typename E>
 __host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
@@ -65,10 +68,13 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
 template <typename E>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
     extern __shared__ __align__(16) unsigned char smem[];
+    // bf16 inputs: v is exact in bf16, so products with v as the A operand skip its (zero) lo part
+    constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     E *raw = reinterpret_cast<E *>(smem);
     unsigned char *Bs = smem + raw_bytes<E>();
     float *dd = reinterpret_cast<float *>(Bs + B_DD), *G = reinterpret_cast<float *>(Bs + B_G);
     float *ys = reinterpret_cast<float *>(Bs + B_Y), *Wm = reinterpret_cast<float *>(Bs + B_W);
+    float *Mb = reinterpret_cast<float *>(Bs + B_MB);
     const HL BT = hl(Bs, B_BT), KT = hl(Bs, B_KT), AH = hl(Bs, B_AH), RH = hl(Bs, B_RH), VM = hl(Bs, B_VM);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -104,8 +110,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
         __syncthreads();
 
         // checkpoint of the state before token t0; written once the previous
-        // chunk's state update has long completed (after the Gram), not at
-        // the chunk start where it would wait on those MMAs
+        // chunk's state update has long completed, not at the chunk start where
+        // it would wait on those MMAs
         auto write_ckpt = [&]() {
             if (p.ckpt && t0 % p.L == 0) {
                 float *dst = p.ckpt + ((size_t)bh * p.nck + t0 / p.L) * 64 * 64;
@@ -156,14 +162,17 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     G[row * GS + col + 1] = acc[u][1];
                     G[(row + 8) * GS + col] = acc[u][2];
                     G[(row + 8) * GS + col + 1] = acc[u][3];
+                    if (warp == 0) {  // b~ . a^ tile = M_b (and its unused lower part)
+                        *reinterpret_cast<float2 *>(Mb + row * MBS + col) = make_float2(acc[u][0], acc[u][1]);
+                        *reinterpret_cast<float2 *>(Mb + (row + 8) * MBS + col) = make_float2(acc[u][2], acc[u][3]);
+                    }
                 }
             }
-            write_ckpt();
             __syncthreads();
 
             // W on warp 0 while every warp forms [Z | U] = S_0 [R^ | A^] + V [Q_k | M_k]
             // (warp 0 follows with its own rows once W is done)
-            prep_inverse(G, Wm);
+            prep_inverse_v(Mb, Wm);
             auto mk = [&](int s, int t) { return s < t ? G[(16 + s) * GS + t] : 0.f; };        // M_k[s][t]
             auto qk = [&](int s, int t) { return s <= t ? G[(16 + s) * GS + 16 + t] : 0.f; };  // Q_k[s][t]
             auto qb = [&](int s, int t) { return s <= t ? G[s * GS + 16 + t] : 0.f; };         // Q_b[s][t]
@@ -185,8 +194,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                     bq[u] = make_b(make_float2(qk(2 * q, t), qk(2 * q + 1, t)), make_float2(qk(2 * q + 8, t), qk(2 * q + 9, t)));
                     bq[2 + u] = make_b(make_float2(mk(2 * q, t), mk(2 * q + 1, t)), make_float2(mk(2 * q + 8, t), mk(2 * q + 9, t)));
                 }
-                mma3n<4>(ya, vA, bq);
+                mma3n<4, kVLo>(ya, vA, bq);
             }
+            write_ckpt();
             __syncthreads();  // W
 
             // ---- SA = U W and Y = Z + SA Q_b (16 x 16 per warp)
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 ldb2_t(KT, 16 * pp, 0, lane, kb0, kb1);
                 const BFrag bq[2] = {bb0, bb1}, kq[2] = {kb0, kb1};
                 mma3n<2>(S + 2 * pp, saf, bq);
-                mma3n<2>(S + 2 * pp, vA, kq);
+                mma3n<2, kVLo>(S + 2 * pp, vA, kq);
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int nt = 2 * pp + u;

@@ -216,12 +216,18 @@ __device__ __forceinline__ void ld_acc2(const float *src, float c0[4], float c1[
 // c[n] += A B[n] for NB accumulators, the three split products of each
 // interleaved across the accumulators so that no two consecutive MMAs
 // depend on each other.
-template <int NB>
+// kALo / kBLo = false drops the product of an operand whose lo part is
+// identically zero (an input that is exact in bf16): it would add exact zeros.
+template <int NB, bool kALo = true, bool kBLo = true>
 __device__ __forceinline__ void mma3n(float (*c)[4], const AFrag &a, const BFrag *b) {
+    if constexpr (kALo) {
 #pragma unroll
-    for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.lo, b[n].hi);
+        for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.lo, b[n].hi);
+    }
+    if constexpr (kBLo) {
 #pragma unroll
-    for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.hi, b[n].lo);
+        for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.hi, b[n].lo);
+    }
 #pragma unroll
     for (int n = 0; n < NB; ++n) mma_bf16(c[n], a.hi, b[n].hi);
 }
