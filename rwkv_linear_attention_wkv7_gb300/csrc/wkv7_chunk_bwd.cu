@@ -297,17 +297,18 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         stage<E, 6, NT>(raw, src, base0 + (size_t)t0 * tstride, tstride, nv);
         stage_rows<NT>(dyf, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
     };
-    // The next chunk's start state is fetched (fp32) while G4, the outputs and
-    // G5 still run, into three slots that are idle by then: rows 0..15 -> the
-    // dy split, 16..31 -> the DSA split, 32..63 -> the first masked-Gam block.
+    // The next chunk's start state is fetched (fp32) while this chunk's last
+    // products still run, into three slots idle by then: rows 0..15 -> the dy
+    // split and 16..31 -> the DSA split (once Gam and G3's S_0 part are done),
+    // 32..63 -> the first masked-Gam block (once G3 is done).
     auto s0_row = [&](int row) -> float * {
         const int off = row < 16 ? B_DYH + row * SP * 4 : row < 32 ? B_DSH + (row - 16) * SP * 4 : B_M3 + (row - 32) * SP * 4;
         return reinterpret_cast<float *>(Bs + off);
     };
-    auto stage_s0 = [&](int c) {
+    auto stage_s0 = [&](int c, int r0, int r1) {  // rows r0 .. r1 - 1
         const float *src0 = p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64;
-        for (int e = threadIdx.x; e < 64 * 16; e += NT) {
-            const int u = e >> 4, n = (e & 15) * 4;
+        for (int e = threadIdx.x; e < (r1 - r0) * 16; e += NT) {
+            const int u = r0 + (e >> 4), n = (e & 15) * 4;
             cp_async16(s0_row(u) + n, src0 + u * 64 + n, 16);
         }
     };
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         }
     };
     stage_in(nchunks - 1);
-    stage_s0(nchunks - 1);
+    stage_s0(nchunks - 1, 0, 64);
     stage_fac(nchunks - 1);
     cp_async_commit();
 
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             __syncthreads();
             if (c > 0) {
                 stage_in(c - 1);
-                stage_s0(c - 1);
+                stage_s0(c - 1, 0, 64);
                 stage_fac(c - 1);
             }
             cp_async_commit();
@@ -674,9 +675,9 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             // M4[n][nn] with n = the Gam column, nn = the Gam row with its halves swapped
             st_acc_t16(h4, l4, 16 * (warp & 1), mt ? 0 : 16, m4, lane);
         }
-        __syncthreads();
 
-        // G3: [DR | DA] (rows = key index j = rA / rB)
+        // G3: [DR | DA] (rows = key index j = rA / rB).  Its S_0 part needs only
+        // DY, DSA and S_0, so it is issued beside Gam, before the barrier.
         float x3[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -686,6 +687,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             ldb2(DSH, 0, 16 * kk, lane, b2, b3);
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, sT, bq); }
         }
+        __syncthreads();  // masked Gam blocks visible; S_0, dy and DSA no longer read
+        if (c > 0) stage_s0(c - 1, 0, 32);  // next start state, rows 0..31 (dy and DSA slots)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
             const AFrag af = lda_t(kk ? KT : BT, 16 * warp, 0, lane);
@@ -694,9 +697,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             ldb2_t(M3, 16, 16 * kk, lane, b2, b3);
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, af, bq); }
         }
-        __syncthreads();  // S_0, dy, DSA and the first masked block no longer read
-        if (c > 0) stage_s0(c - 1);
-        cp_async_commit();
         // the S_0 slot takes G d_C (split)
         {
             __nv_bfloat16 *gh = hi_of(Bs, B_SX), *gl = lo_of(Bs, B_SX, 64);
@@ -713,7 +713,9 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 st_acc16(gh, gl, 16 * warp, 16 * pp, gd, lane);
             }
         }
-        __syncthreads();
+        __syncthreads();  // G d_C visible; the first masked block no longer read
+        if (c > 0) stage_s0(c - 1, 32, 64);  // rows 32..63 (first masked block's slot)
+        cp_async_commit();
 
         // G4: [DK | DB] (rows = key index)
         float x4[4][4] = {};
