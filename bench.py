@@ -320,6 +320,7 @@ def run_ours(args, world, rank, local):
             step(record=True)
         t_end.record(stream)
         torch.cuda.synchronize()
+    wkv7.async_status()  # raises if a kernel's bounded wait on its bulk copies ran out
     barrier(world)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_f)

@@ -170,6 +170,18 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
                                   float *dr, float *dw, float *dk, float *dv, float *da, float *db,
                                   float *ds0, void *stream);
 
+/*
+ * Status of the kernels' asynchronous copies on the current device.  The
+ * kernels stage their inputs with bulk copies whose completion they wait for
+ * a bounded time; a wait that runs out (which no correct run should see) sets
+ * a per-device flag instead of hanging the GPU.  This call waits for the
+ * device to finish its work, returns WKV7_ECUDA (and clears the flag) if any
+ * launch since the last check set it, WKV7_OK otherwise.  The library looks
+ * up the flag's device address on its first forward, backward or status call
+ * on each device.
+ */
+int wkv7_async_status(void);
+
 /* Text of the last error on the calling thread ("" if none). */
 const char *wkv7_last_error(void);
 

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "wkv7.h"
 #include "wkv7_internal.cuh"
@@ -77,8 +78,35 @@ int copy_state(const float *src, float *dst, int B, int H, cudaStream_t st) {
 
 }  // namespace
 
+// Set by a kernel whose bounded wait on its bulk copies ran out (see
+// wkv7_async_status); one flag per device.
+static __device__ unsigned g_async_err;
+static std::mutex g_flag_mu;
+static unsigned *g_flag_ptr[64] = {};
+
 namespace wkv7 {
 int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
+unsigned *async_error_flag() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        fail(WKV7_ECUDA, "cannot identify the current device");
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_flag_mu);
+    if (!g_flag_ptr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_async_err);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            fail(WKV7_ECUDA, "device error flag lookup failed: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        g_flag_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_flag_ptr[dev];
+}
 }  // namespace wkv7
 
 extern "C" {
@@ -94,6 +122,23 @@ long long wkv7_factor_floats(int T) {
 }
 
 const char *wkv7_last_error(void) { return g_err; }
+
+int wkv7_async_status(void) {
+    g_err[0] = '\0';
+    TRY(check_device());
+    unsigned *flag = wkv7::async_error_flag();
+    if (!flag) return WKV7_ECUDA;
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpy(&v, flag, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return launch_status(e, "wkv7_async_status");
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(flag, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return launch_status(e, "wkv7_async_status");
+        return fail(WKV7_ECUDA, "a kernel's bounded wait on its bulk copies ran out; the results of that call are invalid");
+    }
+    return WKV7_OK;
+}
 
 int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
@@ -117,6 +162,7 @@ int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt; p.fac = factors;
+    if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (wkv7::forward_chunk_supported(p)) return launch_status(wkv7::launch_forward_chunk(p, st), "wkv7_forward launch");
     return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
 }
@@ -147,6 +193,7 @@ int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.ckpt_in = ckpt; p.fac_in = factors; p.dy = dy; p.dsT = dsT;
     p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0;
+    if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (wkv7::backward_chunk_supported(p)) return launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward launch");
     return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");
 }

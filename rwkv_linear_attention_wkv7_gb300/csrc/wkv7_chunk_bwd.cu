@@ -292,45 +292,58 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     const E *const src[6] = {static_cast<const E *>(p.r), static_cast<const E *>(p.w), static_cast<const E *>(p.k),
                              static_cast<const E *>(p.v), static_cast<const E *>(p.a), static_cast<const E *>(p.b)};
     const int nchunks = (p.T + C - 1) / C;
+    // A chunk's inputs and dy arrive by cp.async (rows of 128 / 256 bytes);
+    // its start state and factor block (contiguous 4-8 KB blocks) by bulk
+    // copies on the TMA engine, completed on one mbarrier whose phase k holds
+    // the chunk processed k-th (nchunks - 1 - c).  Thread 0 announces the
+    // bytes right after the previous phase completed and arrives once the last
+    // block is issued.
+    __shared__ __align__(8) uint64_t bar;
+    if (tid == 0) mbar_init(&bar, 1);
+    __syncthreads();
+    bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
+    constexpr unsigned kChunkBytes = 64 * 64 * 4 + (kFac ? fac::kWords * 4 : 0);
     auto stage_in = [&](int c) {  // inputs and dy of chunk c
         const int t0 = c * C, nv = min(C, p.T - t0);
         stage<E, 6, NT>(raw, src, base0 + (size_t)t0 * tstride, tstride, nv);
         stage_rows<NT>(dyf, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
+        cp_async_commit();
     };
-    // The next chunk's start state is fetched (fp32) while this chunk's last
-    // products still run, into three slots idle by then: rows 0..15 -> the dy
-    // split and 16..31 -> the DSA split (once Gam and G3's S_0 part are done),
-    // 32..63 -> the first masked-Gam block (once G3 is done).
+    // The next chunk's start state (fp32, dense 256-byte rows) is fetched
+    // while this chunk's last products still run, into three slots idle by
+    // then: rows 0..15 -> the dy split and 16..31 -> the DSA split (once Gam
+    // and G3's S_0 part are done), 32..63 -> the first masked-Gam block (once
+    // G3 is done).
     auto s0_row = [&](int row) -> float * {
-        const int off = row < 16 ? B_DYH + row * SP * 4 : row < 32 ? B_DSH + (row - 16) * SP * 4 : B_M3 + (row - 32) * SP * 4;
+        const int off = row < 16 ? B_DYH + row * 256 : row < 32 ? B_DSH + (row - 16) * 256 : B_M3 + (row - 32) * 256;
         return reinterpret_cast<float *>(Bs + off);
     };
-    auto stage_s0 = [&](int c, int r0, int r1) {  // rows r0 .. r1 - 1
+    auto stage_s0 = [&](int c, int r0, int r1) {  // rows r0 .. r1 - 1: whole slots
         const float *src0 = p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64;
-        for (int e = threadIdx.x; e < (r1 - r0) * 16; e += NT) {
-            const int u = r0 + (e >> 4), n = (e & 15) * 4;
-            cp_async16(s0_row(u) + n, src0 + u * 64 + n, 16);
-        }
+        if (tid == 0 && r0 <= 0 && r1 >= 16) bulk_g2s(s0_row(0), src0, 16 * 256, &bar);
+        if (tid == 1 && r0 <= 16 && r1 >= 32) bulk_g2s(s0_row(16), src0 + 16 * 64, 16 * 256, &bar);
+        if (tid == 2 && r0 <= 32 && r1 >= 64) bulk_g2s(s0_row(32), src0 + 32 * 64, 32 * 256, &bar);
     };
     const float *FC = reinterpret_cast<const float *>(Bs + B_QQ);  // factor block of the current chunk
     auto stage_fac = [&](int c) {
         if constexpr (kFac) {
-            const float *src0 = p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords;
-            for (int e = threadIdx.x; e < fac::kWords / 4; e += NT)
-                cp_async16(Bs + B_QQ + e * 16, src0 + e * 4, 16);
+            if (tid == 3) bulk_g2s(Bs + B_QQ, p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords, fac::kWords * 4, &bar);
         }
     };
+    if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     stage_in(nchunks - 1);
     stage_s0(nchunks - 1, 0, 64);
     stage_fac(nchunks - 1);
-    cp_async_commit();
+    if (tid == 0) mbar_arrive(&bar);
 
     for (int c = nchunks - 1; c >= 0; --c) {
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
         cp_async_wait_all();
+        lost |= !mbar_wait(&bar, (nchunks - 1 - c) & 1, p.err);
         __syncthreads();
+        if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (exact) {
@@ -341,13 +354,14 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             __syncthreads();
             bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
+            fence_proxy_async();  // the per-token path wrote into slots the copies refill
             __syncthreads();
             if (c > 0) {
                 stage_in(c - 1);
                 stage_s0(c - 1, 0, 64);
                 stage_fac(c - 1);
+                if (tid == 0) mbar_arrive(&bar);
             }
-            cp_async_commit();
             continue;
         }
         const float *dC = dd + (C - 1) * DS;
@@ -395,7 +409,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             __syncthreads();
             // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
             if (c > 0) stage_in(c - 1);
-            cp_async_commit();
         }
 
         // ================= per-chunk operands (no state involved)
@@ -525,7 +538,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         __syncthreads();
         if constexpr (kFac) {  // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
             if (c > 0) stage_in(c - 1);
-            cp_async_commit();
         }
 
         // ================= state-dependent products
@@ -636,7 +648,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
         if (c > 0) stage_fac(c - 1);  // this chunk's factors are consumed
-        cp_async_commit();
 
         {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA),
             // written straight into its two masked split blocks:
@@ -687,7 +698,8 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
             ldb2(DSH, 0, 16 * kk, lane, b2, b3);
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, sT, bq); }
         }
-        __syncthreads();  // masked Gam blocks visible; S_0, dy and DSA no longer read
+        fence_proxy_async();  // the dy and DSA slots were written by ordinary stores
+        __syncthreads();      // masked Gam blocks visible; S_0, dy and DSA no longer read
         if (c > 0) stage_s0(c - 1, 0, 32);  // next start state, rows 0..31 (dy and DSA slots)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
@@ -713,9 +725,12 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
                 st_acc16(gh, gl, 16 * warp, 16 * pp, gd, lane);
             }
         }
-        __syncthreads();  // G d_C visible; the first masked block no longer read
-        if (c > 0) stage_s0(c - 1, 32, 64);  // rows 32..63 (first masked block's slot)
-        cp_async_commit();
+        fence_proxy_async();  // the first masked block was written by ordinary stores
+        __syncthreads();      // G d_C visible; the first masked block no longer read
+        if (c > 0) {
+            stage_s0(c - 1, 32, 64);  // rows 32..63 (first masked block's slot)
+            if (tid == 0) mbar_arrive(&bar);
+        }
 
         // G4: [DK | DB] (rows = key index)
         float x4[4][4] = {};
@@ -824,7 +839,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 
         __syncthreads();
     }
-    cp_async_wait_all();
+    if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
     if (p.ds0) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {

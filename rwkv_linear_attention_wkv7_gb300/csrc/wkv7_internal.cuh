@@ -21,6 +21,7 @@ struct SeqArgs {
     const float *dy, *dsT, *ckpt_in;
     const float *fac_in;  // factor cache from the forward, or NULL (recomputed)
     float *dr, *dw, *dk, *dv, *da, *db, *ds0;
+    unsigned *err;  // device flag a kernel sets when a bounded wait on its copies times out
 };
 
 // Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the
@@ -39,6 +40,9 @@ constexpr int kWords = 2048;
 
 // Record an error for wkv7_last_error() and return `code` (C ABI layer).
 int set_error(int code, const char *msg);
+// Device address of the current device's asynchronous-error flag (looked up
+// once per device), or NULL with the error recorded.
+unsigned *async_error_flag();
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_forward_plain(const SeqArgs &a, cudaStream_t s);

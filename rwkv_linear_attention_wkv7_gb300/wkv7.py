@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.wkv7_backward.restype = ci
         L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
         L.wkv7_decode_step.restype = ci
+        L.wkv7_async_status.argtypes = []
+        L.wkv7_async_status.restype = ci
         L.wkv7_last_error.argtypes = []
         L.wkv7_last_error.restype = ctypes.c_char_p
         _lib = L
@@ -101,6 +103,12 @@ def _f32(t, shape, device, name):
     if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous float32 {tuple(shape)} tensor on {device}")
     return t
+
+
+def async_status() -> None:
+    """Raise if a kernel's bounded wait on its bulk copies ran out since the
+    last check (waits for the device to finish its work)."""
+    _check("wkv7_async_status", lib().wkv7_async_status())
 
 
 def ckpt_count(T: int, L: int) -> int:

@@ -56,6 +56,7 @@ def run_gpu(d, L=16, backward=True, factors=None):
     if backward:
         out.update(wkv7.backward(*(d[n] for n in INPUTS), ck, d["dy"], dsT=d.get("dsT"), L=L, factors=fac))
     torch.cuda.synchronize()
+    wkv7.async_status()  # no bounded wait on the kernels' bulk copies ran out
     return out
 
 

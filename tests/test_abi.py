@@ -34,7 +34,7 @@ def lib():
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
-                     "wkv7_last_error"):
+                     "wkv7_async_status", "wkv7_last_error"):
         assert required in names
 
 
@@ -107,4 +107,5 @@ def test_decode_rejects_bad_arguments(lib):
 def test_no_gpu_is_reported_not_faked(lib):
     """Without a usable sm_103a device the library refuses; it has no CPU path."""
     assert _fwd(lib) == EUNSUPPORTED
+    assert lib.wkv7_async_status() == EUNSUPPORTED
     assert "device" in wkv7.last_error()
