@@ -254,10 +254,10 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // forward's factor cache, prefetched into the [Q'; W Q_b] slot, instead of
 // being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
 template <typename E, bool kFac>
-__global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
+__global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
     // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     E *raw = reinterpret_cast<E *>(smem);
     unsigned char *Bs = smem + raw_bytes<E>();
     float *dyf = reinterpret_cast<float *>(Bs + B_DYF), *dd = reinterpret_cast<float *>(Bs + B_DD);
@@ -289,25 +289,23 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
     }
     float carryA = 0.f, carryB = 0.f;  // dw running sum for key columns rA / rB
 
-    const E *const src[6] = {static_cast<const E *>(p.r), static_cast<const E *>(p.w), static_cast<const E *>(p.k),
-                             static_cast<const E *>(p.v), static_cast<const E *>(p.a), static_cast<const E *>(p.b)};
     const int nchunks = (p.T + C - 1) / C;
-    // A chunk's inputs and dy arrive by cp.async (rows of 128 / 256 bytes);
-    // its start state and factor block (contiguous 4-8 KB blocks) by bulk
-    // copies on the TMA engine, completed on one mbarrier whose phase k holds
-    // the chunk processed k-th (nchunks - 1 - c).  Thread 0 announces the
-    // bytes right after the previous phase completed and arrives once the last
-    // block is issued.
+    // A chunk's inputs and dy (tensor copies), start state and factor block
+    // (bulk copies) arrive on the TMA engine, completed on one mbarrier whose
+    // phase k holds the chunk processed k-th (nchunks - 1 - c).  Thread 0
+    // announces the bytes right after the previous phase completed and
+    // arrives once the last block is issued.
     __shared__ __align__(8) uint64_t bar;
     if (tid == 0) mbar_init(&bar, 1);
     __syncthreads();
     bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
-    constexpr unsigned kChunkBytes = 64 * 64 * 4 + (kFac ? fac::kWords * 4 : 0);
-    auto stage_in = [&](int c) {  // inputs and dy of chunk c
-        const int t0 = c * C, nv = min(C, p.T - t0);
-        stage<E, 6, NT>(raw, src, base0 + (size_t)t0 * tstride, tstride, nv);
-        stage_rows<NT>(dyf, p.dy + base0 + (size_t)t0 * tstride, tstride, C, nv);
-        cp_async_commit();
+    constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + 64 * 64 * 4 + (kFac ? fac::kWords * 4 : 0));
+    auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each
+        if (tid == 0) {
+#pragma unroll
+            for (int v = 0; v < 6; ++v) tma_rows(raw + v * C * RS, &maps.m[v], h, c * C, bi, &bar);
+            tma_rows(dyf, &maps.m[6], h, c * C, bi, &bar);
+        }
     };
     // The next chunk's start state (fp32, dense 256-byte rows) is fetched
     // while this chunk's last products still run, into three slots idle by
@@ -340,7 +338,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
-        cp_async_wait_all();
         lost |= !mbar_wait(&bar, (nchunks - 1 - c) & 1, p.err);
         __syncthreads();
         if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
@@ -852,9 +849,12 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p) {
 template <typename E, bool kFac>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
-    cudaError_t e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    InputMaps maps;
+    cudaError_t e = encode_input_maps(&maps, p, p.dy);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p);
+    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p, maps);
     return cudaGetLastError();
 }
 

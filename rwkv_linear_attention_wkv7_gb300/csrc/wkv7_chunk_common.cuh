@@ -13,6 +13,8 @@
 //   S_t = (S_0 + sum_{s<=t} sa_s b~_s^T + v_s k~_s^T) diag(d_t),
 //   sa_t = S_0 a^_t + sum_{s<t} sa_s M_b[s][t] + v_s M_k[s][t].
 #pragma once
+#include <cuda.h>
+
 #include "wkv7_internal.cuh"
 #include "wkv7_mma.cuh"
 
@@ -76,6 +78,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
                  "l"(src), "r"(bytes), "r"(smem_addr(bar))
                  : "memory");
 }
+// Tensor copies of a chunk's input rows: 4-D maps over [B][T][H][64] (r, w,
+// k, v, a, b and, for the backward, dy), box RS x 1 x C x 1, so that one copy
+// fills a padded [C][RS] staging block; the columns past 64 and the tokens
+// past T are out of range and arrive as zeros.
+struct InputMaps {
+    CUtensorMap m[7];
+};
+__device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int h, int t0, int b, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];\n" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(h), "r"(t0), "r"(b), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared accesses before later
 // async-proxy (bulk copy) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -120,6 +137,50 @@ __device__ __forceinline__ float4 ld_raw4<__nv_bfloat16>(const __nv_bfloat16 *ra
 
 template <typename E>
 __host__ __device__ constexpr size_t raw_bytes() { return (size_t)6 * C * RS * sizeof(E); }
+
+// Host: the driver's tensor-map encoder, looked up through the runtime so
+// that the library does not link against the driver library itself.
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+inline EncodeTiledFn encode_tiled_fn() {
+    static const EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Host: encode the row map of one [B][T][H][64] tensor (element size esize).
+inline cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int esize, int B, int T, int H) {
+    const EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {64ull * esize, 64ull * esize * H, 64ull * esize * H * T};
+    const cuuint32_t box[4] = {RS, 1, C, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = encode(
+        m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base),
+        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+// Host: maps of the six inputs, and of dy when given.
+inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const float *dy) {
+    const int es = p.dtype == 1 ? 2 : 4;
+    const void *src[6] = {p.r, p.w, p.k, p.v, p.a, p.b};
+    for (int i = 0; i < 6; ++i) {
+        const cudaError_t e = encode_rows_map(&maps->m[i], src[i], es, p.B, p.T, p.H);
+        if (e != cudaSuccess) return e;
+    }
+    return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
+}
 
 // cp.async copies of NV [C][64] token blocks (tokens [t0, t0 + C) of each
 // source, `base` = element offset of (b, t0, h, 0)) into dst[v][C][64];

@@ -66,8 +66,8 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
 }
 
 template <typename E>
-__global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
-    extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
+    extern __shared__ __align__(128) unsigned char smem[];
     // bf16 inputs: v is exact in bf16, so products with v as the A operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     E *raw = reinterpret_cast<E *>(smem);
@@ -97,17 +97,30 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
         }
     }
 
-    const E *const src[6] = {static_cast<const E *>(p.r), static_cast<const E *>(p.w), static_cast<const E *>(p.k),
-                             static_cast<const E *>(p.v), static_cast<const E *>(p.a), static_cast<const E *>(p.b)};
     const int nchunks = (p.T + C - 1) / C;
-    stage<E, 6, NT>(raw, src, base0, tstride, min(C, p.T));
-    cp_async_commit();
+    // chunk inputs arrive by tensor copies (one per input) on the TMA engine;
+    // phase c of the mbarrier is chunk c
+    __shared__ __align__(8) uint64_t bar;
+    if (tid == 0) mbar_init(&bar, 1);
+    __syncthreads();
+    bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
+    constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>();
+    auto prefetch = [&](int c) {  // chunk c's copies; thread 0 announced its bytes
+        if (tid == 0) {
+#pragma unroll
+            for (int v = 0; v < 6; ++v) tma_rows(raw + v * C * RS, &maps.m[v], h, c * C, bi, &bar);
+            mbar_arrive(&bar);
+        }
+    };
+    if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
+    prefetch(0);
 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
-        cp_async_wait_all();
+        lost |= !mbar_wait(&bar, c & 1, p.err);
         __syncthreads();
+        if (tid == 0 && c + 1 < nchunks) mbar_expect_tx(&bar, kChunkBytes);
 
         // checkpoint of the state before token t0; written once the previous
         // chunk's state update has long completed, not at the chunk start where
@@ -141,8 +154,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
             }
             __syncthreads();
             // raw is no longer read in this chunk: fetch the next one now
-            if (c + 1 < nchunks) stage<E, 6, NT>(raw, src, base0 + (size_t)(t0 + C) * tstride, tstride, min(C, p.T - t0 - C));
-            cp_async_commit();
+            if (c + 1 < nchunks) prefetch(c + 1);
 
             {   // Gram [B~; K~] [A^; R^]^T: warp -> m-tile (b~ | k~), n-tile pair (a^ | r^)
                 const int mt = warp >> 1;
@@ -331,8 +343,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 }
             }
             __syncthreads();
-            if (c + 1 < nchunks) stage<E, 6, NT>(raw, src, base0 + (size_t)(t0 + C) * tstride, tstride, min(C, p.T - t0 - C));
-            cp_async_commit();
+            if (c + 1 < nchunks) prefetch(c + 1);
         }
         __syncthreads();
         for (int e = tid; e < nv * 16; e += NT) {
@@ -341,7 +352,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
                 *reinterpret_cast<const float4 *>(ys + t * YS + n);
         }
     }
-    cp_async_wait_all();
+    if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
     if (p.sT) {
         float *dst = p.sT + sbase;
 #pragma unroll
@@ -355,9 +366,12 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p) {
 template <typename E>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = fwd_smem_bytes<E>();
-    cudaError_t e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    InputMaps maps;
+    cudaError_t e = encode_input_maps(&maps, p, nullptr);
     if (e != cudaSuccess) return e;
-    wkv7_fwd_chunk_kernel<E><<<p.B * p.H, NT, sm, st>>>(p);
+    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    wkv7_fwd_chunk_kernel<E><<<p.B * p.H, NT, sm, st>>>(p, maps);
     return cudaGetLastError();
 }
 
