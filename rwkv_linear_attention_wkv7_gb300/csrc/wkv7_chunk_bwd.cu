@@ -646,20 +646,28 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
         __syncthreads();
         if (c > 0) stage_fac(c - 1);  // this chunk's factors are consumed
 
+        // G3: [DR | DA] (rows = key index j = rA / rB)
+        float x3[4][4] = {};
         {   // Gam = [SA | V]^T [DY | DSA] (32 x 32): warp -> m-tile (SA | V), n-tile pair (DY | DSA),
             // written straight into its two masked split blocks:
             //   M3[k][n] = Gam[k][n] where (n < 16 ? s <= t : s < t)           (s = k % 16, t = n % 16)
             //   M4[k][n] = Gam[n < 16 ? 16 + t : t][k] where (k < 16 ? s >= t : s > t)
             // M3 pairs (b~_s | k~_s) with (dy_t | dsa_t); M4 pairs (r^_s | a^_s) with (v_t | sa_t)
+            // G3's S_0 part, S_0^T [DY | DSA], needs only DY, DSA and S_0: it shares
+            // this loop (and its DY / DSA fragments) with Gam.
             const int mt = warp >> 1;
             float acc[2][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+                BFrag bq[4];
+                ldb2(DYH, 0, 16 * kk, lane, bq[0], bq[1]);
+                ldb2(DSH, 0, 16 * kk, lane, bq[2], bq[3]);
                 const AFrag af = lda(mt ? VM : SAH, 0, 16 * kk, lane);
-                BFrag b0, b1;
-                ldb2((warp & 1) ? DSH : DYH, 0, 16 * kk, lane, b0, b1);
-                const BFrag bq[2] = {b0, b1};
-                mma3n<2>(acc, af, bq);
+                const bool ds = warp & 1;
+                const BFrag gq[2] = {ds ? bq[2] : bq[0], ds ? bq[3] : bq[1]};
+                mma3n<2>(acc, af, gq);
+                const AFrag sT = lda_t(SX, 16 * warp, 16 * kk, lane);
+                mma3n<4>(x3, sT, bq);
             }
             __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
             __nv_bfloat16 *h4 = hi_of(Bs, B_M4), *l4 = lo_of(Bs, B_M4, 32);
@@ -684,27 +692,17 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
             st_acc_t16(h4, l4, 16 * (warp & 1), mt ? 0 : 16, m4, lane);
         }
 
-        // G3: [DR | DA] (rows = key index j = rA / rB).  Its S_0 part needs only
-        // DY, DSA and S_0, so it is issued beside Gam, before the barrier.
-        float x3[4][4] = {};
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const AFrag sT = lda_t(SX, 16 * warp, 16 * kk, lane);
-            BFrag b0, b1, b2, b3;
-            ldb2(DYH, 0, 16 * kk, lane, b0, b1);
-            ldb2(DSH, 0, 16 * kk, lane, b2, b3);
-            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, sT, bq); }
-        }
         fence_proxy_async();  // the dy and DSA slots were written by ordinary stores
         __syncthreads();      // masked Gam blocks visible; S_0, dy and DSA no longer read
         if (c > 0) stage_s0(c - 1, 0, 32);  // next start state, rows 0..31 (dy and DSA slots)
+        // b~ and k~ of this warp's key rows as A operands, kept for the outputs
+        const AFrag btA = lda_t(BT, 16 * warp, 0, lane), ktA = lda_t(KT, 16 * warp, 0, lane);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-            const AFrag af = lda_t(kk ? KT : BT, 16 * warp, 0, lane);
-            BFrag b0, b1, b2, b3;
-            ldb2_t(M3, 0, 16 * kk, lane, b0, b1);
-            ldb2_t(M3, 16, 16 * kk, lane, b2, b3);
-            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x3, af, bq); }
+            BFrag bq[4];
+            ldb2_t(M3, 0, 16 * kk, lane, bq[0], bq[1]);
+            ldb2_t(M3, 16, 16 * kk, lane, bq[2], bq[3]);
+            mma3n<4>(x3, kk ? ktA : btA, bq);
         }
         // the S_0 slot takes G d_C (split)
         {
@@ -743,13 +741,13 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
                 mma3n<2>(x4 + 2, gT, bs);
             }
         }
+        const AFrag rhA = lda_t(RH, 16 * warp, 0, lane), ahA = lda_t(AH, 16 * warp, 0, lane);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-            const AFrag af = lda_t(kk ? AH : RH, 16 * warp, 0, lane);
-            BFrag b0, b1, b2, b3;
-            ldb2_t(M4, 0, 16 * kk, lane, b0, b1);
-            ldb2_t(M4, 16, 16 * kk, lane, b2, b3);
-            { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(x4, af, bq); }
+            BFrag bq[4];
+            ldb2_t(M4, 0, 16 * kk, lane, bq[0], bq[1]);
+            ldb2_t(M4, 16, 16 * kk, lane, bq[2], bq[3]);
+            mma3n<4>(x4, kk ? ahA : rhA, bq);
         }
 
         // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index); issued
@@ -772,10 +770,10 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
         {
             // r^, a^, b~, k~ at this lane's (token, key) positions, in accumulator order
             float rv[8], av[8], bv[8], kv[8];
-            a_values(lda_t(RH, 16 * warp, 0, lane), rv);
-            a_values(lda_t(AH, 16 * warp, 0, lane), av);
-            a_values(lda_t(BT, 16 * warp, 0, lane), bv);
-            a_values(lda_t(KT, 16 * warp, 0, lane), kv);
+            a_values(rhA, rv);
+            a_values(ahA, av);
+            a_values(btA, bv);
+            a_values(ktA, kv);
             float zz[2][4], ee[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
