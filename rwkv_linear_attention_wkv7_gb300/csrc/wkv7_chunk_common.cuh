@@ -1,6 +1,6 @@
-// Shared pieces of the chunked WKV7 kernels (forward and backward): chunk
-// staging, the per-chunk decay-scaled vectors, the 32x32 Gram of the scaled
-// vectors and the inverse W = (I - M_b)^{-1}.
+// Shared pieces of the chunked WKV7 kernels (forward and backward): TMA
+// staging of a chunk on an mbarrier, the cumulative decays of a chunk and the
+// inverse W = (I - M_b)^{-1}.
 //
 // Notation (one (b,h), one chunk of C = 16 tokens, local index t = 0..15):
 //   d_t  = w_0 o ... o w_t          cumulative decay per key column
@@ -30,13 +30,6 @@ constexpr int WS = 17;         // row stride of W
 constexpr int RS = 72;         // row stride (elements) of the staged raw inputs: rows start 4 banks apart
 constexpr float kTiny = 1e-20f;  // smallest cumulative decay the factorised form accepts
 enum { VR = 0, VW = 1, VK = 2, VV = 3, VA = 4, VB = 5 };
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
-    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::); }
 
 // ---- bulk copies on the TMA engine (global -> shared), completed through
 // an mbarrier's transaction count.
@@ -108,19 +101,6 @@ __device__ __forceinline__ float ld_raw<__nv_bfloat16>(const __nv_bfloat16 *raw,
     return __bfloat162float(raw[(vec * C + t) * RS + j]);
 }
 
-// Elements j and j + 1 (j even) of a staged row as one 32/64-bit load.
-template <typename E>
-__device__ __forceinline__ float2 ld_raw2(const E *raw, int vec, int t, int j);
-template <>
-__device__ __forceinline__ float2 ld_raw2<float>(const float *raw, int vec, int t, int j) {
-    return *reinterpret_cast<const float2 *>(raw + (vec * C + t) * RS + j);
-}
-template <>
-__device__ __forceinline__ float2 ld_raw2<__nv_bfloat16>(const __nv_bfloat16 *raw, int vec, int t, int j) {
-    const uint32_t u = *reinterpret_cast<const uint32_t *>(raw + (vec * C + t) * RS + j);
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
-
 // Elements j .. j + 3 (j % 4 == 0) of a staged row as one 64/128-bit load.
 template <typename E>
 __device__ __forceinline__ float4 ld_raw4(const E *raw, int vec, int t, int j);
@@ -182,35 +162,6 @@ inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const fl
     return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
 }
 
-// cp.async copies of NV [C][64] token blocks (tokens [t0, t0 + C) of each
-// source, `base` = element offset of (b, t0, h, 0)) into dst[v][C][64];
-// tokens at or beyond `nvalid` are zero-filled.
-template <typename E, int NV, int NTHR>
-__device__ __forceinline__ void stage(E *dst, const E *const (&src)[NV], size_t base, size_t tstride, int nvalid) {
-    constexpr int P = 16 / sizeof(E);
-    constexpr int per_tok = 64 / P;
-    constexpr int per_vec = C * per_tok;
-#pragma unroll
-    for (int vv = 0; vv < NV; ++vv) {
-        for (int e = threadIdx.x; e < per_vec; e += NTHR) {
-            const int u = e / per_tok, n = (e % per_tok) * P;
-            const bool ok = u < nvalid;
-            const E *g = ok ? src[vv] + base + (size_t)u * tstride + n : src[vv];
-            cp_async16(dst + (vv * C + u) * RS + n, g, ok ? 16 : 0);
-        }
-    }
-}
-
-// Padded fp32 [rows][64] copy (row stride SP) of a dense [rows][64] block.
-template <int NTHR>
-__device__ __forceinline__ void stage_rows(float *dst, const float *src, size_t src_stride, int rows, int nvalid) {
-    for (int e = threadIdx.x; e < rows * 16; e += NTHR) {
-        const int u = e >> 4, n = (e & 15) * 4;
-        const bool ok = u < nvalid;
-        cp_async16(dst + u * SP + n, ok ? src + (size_t)u * src_stride + n : src, ok ? 16 : 0);
-    }
-}
-
 // Hardware approximate reciprocal (rcp.approx, about 1 ulp); used for 1/d_t,
 // whose rounding is far below the split-bf16 product error.
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -222,10 +173,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
 __device__ __forceinline__ float4 rcp4(float4 a) {
     return make_float4(rcp_approx(a.x), rcp_approx(a.y), rcp_approx(a.z), rcp_approx(a.w));
-}
-
-__device__ __forceinline__ float2 f2(const float *a, int row, int col) {
-    return *reinterpret_cast<const float2 *>(a + row * SP + col);
 }
 
 // d_t per key column (threads 0..63); padding tokens (t >= nv) decay by 1.
@@ -250,54 +197,6 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
         }
     }
     return bad;
-}
-
-// a^, r^, b~, k~ (token-major, row stride SP).
-template <typename E, int NTHR>
-__device__ __forceinline__ void prep_scaled(const E *raw, const float *dd, float *ah, float *rh, float *bt, float *kt) {
-    for (int e = threadIdx.x; e < C * 64; e += NTHR) {
-        const int t = e >> 6, j = e & 63;
-        const float d = dd[t * DS + j];
-        const float dp = t ? dd[(t - 1) * DS + j] : 1.f;
-        const float inv = __frcp_rn(d);
-        ah[t * SP + j] = ld_raw(raw, VA, t, j) * dp;
-        rh[t * SP + j] = ld_raw(raw, VR, t, j) * d;
-        bt[t * SP + j] = ld_raw(raw, VB, t, j) * inv;
-        kt[t * SP + j] = ld_raw(raw, VK, t, j) * inv;
-    }
-}
-
-// Gram [b~; k~] [a^; r^]^T (32 x 32, contraction over the 64 key columns) on
-// four warps (warp -> one 16-row m-tile and two 8-column n-tiles), written to
-// G[32][GS].  Warps >= 4 do nothing.
-__device__ __forceinline__ void prep_gram(const float *ah, const float *rh, const float *bt, const float *kt,
-                                          float *G) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (warp >= 4) return;
-    const int g = lane >> 2, q = lane & 3;
-    const int mt = warp >> 1;
-    const float *As = mt ? kt : bt;
-    float acc[2][4] = {};
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const AFrag af = make_a(f2(As, g, 16 * kk + 2 * q), f2(As, g + 8, 16 * kk + 2 * q),
-                                f2(As, g, 16 * kk + 2 * q + 8), f2(As, g + 8, 16 * kk + 2 * q + 8));
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int nt = 2 * (warp & 1) + u;
-            const float *Bs = nt < 2 ? ah : rh;
-            const int tt = 8 * (nt & 1) + g;
-            mma3(acc[u], af, make_b(f2(Bs, tt, 16 * kk + 2 * q), f2(Bs, tt, 16 * kk + 2 * q + 8)));
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int col = 8 * (2 * (warp & 1) + u) + 2 * q, row = 16 * mt + g;
-        G[row * GS + col] = acc[u][0];
-        G[row * GS + col + 1] = acc[u][1];
-        G[(row + 8) * GS + col] = acc[u][2];
-        G[(row + 8) * GS + col + 1] = acc[u][3];
-    }
 }
 
 // W = (I - M_b)^{-1} (unit upper triangular) by back substitution: lanes
