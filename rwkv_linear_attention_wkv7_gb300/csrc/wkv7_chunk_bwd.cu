@@ -183,7 +183,7 @@ constexpr int B_DYF = 0;                       // dy fp32 [C][SP]        (chunk 
 constexpr int B_DD = B_DYF + C * SP * 4;       // d fp32 [C][SP]
 constexpr int B_G = B_DD + C * SP * 4;         // Gram, then Gam, fp32 [32][GS] (slot C*SP floats)
 constexpr int B_W = B_G + C * SP * 4;          // W fp32 [C][WS]
-constexpr int B_SX = B_W + 1104;               // S_0: fp32 [64][SP] staging, then HL64; then G d_C (HL64)
+constexpr int B_SX = B_W + 1280;               // S_0 split (HL64), then G d_C (HL64), then gradient staging
 constexpr int B_BT = B_SX + HL64;              // b~, k~, a^, r^ (HL16 each) [t][j]; exact path: S_{t-1} fp32
 constexpr int B_KT = B_BT + HL16;
 constexpr int B_AH = B_KT + HL16;
@@ -197,7 +197,9 @@ constexpr int B_AP = B_Y, B_MK = B_Y + HL16, B_KB = B_Y + 2 * HL16, B_QQ = B_KB 
 constexpr int B_M3 = B_Y, B_M4 = B_Y + HL32;   // masked Gam blocks [k][n] (HL32 each), after G1/G2
 constexpr int kBytes = B_QQ + HL32;
 static_assert(B_SX % 16 == 0 && B_BT % 16 == 0 && B_Y % 16 == 0, "16-byte aligned operand matrices");
-static_assert(32 * GS <= C * SP && C * WS * 4 <= 1104, "small fp32 blocks fit");
+static_assert(32 * GS <= C * SP && C * WS * 4 <= 1280, "small fp32 blocks fit");
+static_assert(B_SX % 128 == 0 && B_VV % 128 == 0 && B_SAH % 128 == 0 && C * OS * 4 <= HL16,
+              "gradient staging blocks: 128-byte aligned, one per 4.5 KiB slot");
 static_assert(64 * SP * 4 == HL64, "S_0 staging and its split share one slot");
 static_assert(4 * HL16 >= 64 * SP * 4, "exact-path S_{t-1} fits the four scaled blocks");
 static_assert(5 * 4 * 64 * 4 <= 2 * HL32, "exact-path scratch fits region Y");
@@ -254,7 +256,8 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // forward's factor cache, prefetched into the [Q'; W Q_b] slot, instead of
 // being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
 template <typename E, bool kFac>
-__global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
+__global__ void __launch_bounds__(NT, 2)
+    wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
     // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -339,6 +342,7 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
         lost |= !mbar_wait(&bar, (nchunks - 1 - c) & 1, p.err);
+        if (tid == 0) bulk_wait_read();  // the last chunk's gradient stores have read their staging
         __syncthreads();
         if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
 
@@ -627,18 +631,6 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
         }
         {
             __nv_bfloat16 *dhh = hi_of(Bs, B_DSH), *dhl = lo_of(Bs, B_DSH, 16);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t = 8 * nt + 2 * q;
-                if (t < nv) {
-                    p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dvs[nt][0];
-                    p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dvs[nt][2];
-                }
-                if (t + 1 < nv) {
-                    p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rA] = dvs[nt][1];
-                    p.dv[base0 + (size_t)(t0 + t + 1) * tstride + rB] = dvs[nt][3];
-                }
-            }
             st_acc_t16(dhh, dhl, 0, 16 * warp, dvs + 2, lane);  // DSA[i][t] -> DSH[t][i]
         }
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
@@ -766,7 +758,20 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
             mma3n<2>(Gh + 2 * pp, dyA, rr);
             mma3n<2>(Gh + 2 * pp, dsA, aa);
         }
-        // ================= key-indexed gradients and the dw running sum
+        // ================= gradients: staged as [t][key] tiles (stride OS) in the
+        // S_0 / G d_C quarters and the v and SA slots, then one tensor store each
+        __syncthreads();  // G4 and G5 no longer read those slots
+        float *const gdr = reinterpret_cast<float *>(Bs + B_SX), *const gdw = gdr + 1152, *const gdk = gdr + 2 * 1152;
+        float *const gdv = gdr + 3 * 1152, *const gda = reinterpret_cast<float *>(Bs + B_VV);
+        float *const gdb = reinterpret_cast<float *>(Bs + B_SAH);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {  // dv (rows of G2 = value index)
+            const int t = 8 * nt + 2 * q;
+            gdv[t * OS + rA] = dvs[nt][0];
+            gdv[(t + 1) * OS + rA] = dvs[nt][1];
+            gdv[t * OS + rB] = dvs[nt][2];
+            gdv[(t + 1) * OS + rB] = dvs[nt][3];
+        }
         {
             // r^, a^, b~, k~ at this lane's (token, key) positions, in accumulator order
             float rv[8], av[8], bv[8], kv[8];
@@ -789,13 +794,10 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
                     // r o dr = r^ o X3_r, a o da = a^ o X3_a, b o db = b~ o X4_b, k o dk = k~ o X4_k
                     ee[nt][m] = av[vi] * xa;
                     zz[nt][m] = rv[vi] * xr + ee[nt][m] - bv[vi] * xb - kv[vi] * xk;
-                    if (t < nv) {
-                        const size_t o = base0 + (size_t)(t0 + t) * tstride + row;
-                        p.dr[o] = d * xr;
-                        p.da[o] = dp * xa;
-                        p.dk[o] = inv * xk;
-                        p.db[o] = inv * xb;
-                    }
+                    gdr[t * OS + row] = d * xr;
+                    gda[t * OS + row] = dp * xa;
+                    gdk[t * OS + row] = inv * xk;
+                    gdb[t * OS + row] = inv * xb;
                 }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
@@ -821,19 +823,25 @@ __global__ void __launch_bounds__(NT, 2) wkv7_bwd_chunk_kernel(SeqArgs p, const 
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int t = tv[m];
-                    if (t < nv) {
-                        const float d = dd[t * DS + row];
-                        const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
-                        p.dw[base0 + (size_t)(t0 + t) * tstride + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
-                    }
+                    const float d = dd[t * DS + row];
+                    const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
+                    gdw[t * OS + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
                 }
                 const float total = __shfl_sync(kFull, S0v, 0, 4);
                 if (hr) carryB = total; else carryA = total;
             }
         }
 
+        fence_proxy_async();  // the staged tiles are read by the tensor stores
         __syncthreads();
+        if (tid == 0) {
+            const float *const tiles[6] = {gdr, gdw, gdk, gdv, gda, gdb};
+#pragma unroll
+            for (int o = 0; o < 6; ++o) tma_store_rows(&omaps.m[o], tiles[o], h, t0, bi);
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();
     if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
     if (p.ds0) {
 #pragma unroll
@@ -848,11 +856,13 @@ template <typename E, bool kFac>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
     InputMaps maps;
+    OutputMaps omaps;
     cudaError_t e = encode_input_maps(&maps, p, p.dy);
+    if (e == cudaSuccess) e = encode_output_maps(&omaps, p);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p, maps);
+    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
     return cudaGetLastError();
 }
 

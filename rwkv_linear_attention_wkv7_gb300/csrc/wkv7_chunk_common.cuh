@@ -86,6 +86,26 @@ __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int 
         : "memory");
 }
 
+// Tensor stores of a chunk's gradient tiles: maps over [B][T][H][64] fp32 with
+// box OS x 1 x C x 1 read from padded [C][OS] staging blocks (OS = 68 keeps
+// the accumulator-layout writes into them free of bank conflicts); the
+// columns past 64 and the tokens past T are out of range and not written.
+constexpr int OS = 68;
+struct OutputMaps {
+    CUtensorMap m[6];
+};
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap *map, const void *src, int h, int t0, int b) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(0), "r"(h), "r"(t0), "r"(b)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// The shared sources of this thread's committed bulk stores may be reused.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// This thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy shared accesses before later
 // async-proxy (bulk copy) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -137,13 +157,14 @@ inline EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// Host: encode the row map of one [B][T][H][64] tensor (element size esize).
-inline cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int esize, int B, int T, int H) {
+// Host: encode the row map of one [B][T][H][64] tensor (element size esize),
+// box width `box0` elements (RS for the input staging, OS for gradient tiles).
+inline cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int esize, int B, int T, int H, int box0 = RS) {
     const EncodeTiledFn encode = encode_tiled_fn();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[4] = {64, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t strides[3] = {64ull * esize, 64ull * esize * H, 64ull * esize * H * T};
-    const cuuint32_t box[4] = {RS, 1, C, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)box0, 1, C, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUresult r = encode(
         m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base),
@@ -160,6 +181,15 @@ inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const fl
         if (e != cudaSuccess) return e;
     }
     return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
+}
+// Host: maps of the six gradients dr, dw, dk, dv, da, db (fp32).
+inline cudaError_t encode_output_maps(OutputMaps *maps, const SeqArgs &p) {
+    float *const dst[6] = {p.dr, p.dw, p.dk, p.dv, p.da, p.db};
+    for (int i = 0; i < 6; ++i) {
+        const cudaError_t e = encode_rows_map(&maps->m[i], dst[i], 4, p.B, p.T, p.H, OS);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Hardware approximate reciprocal (rcp.approx, about 1 ulp); used for 1/d_t,
