@@ -49,7 +49,8 @@ constexpr int B_Y = B_VM + HL16;                     // y staging fp32 [C][YS]
 constexpr int B_W = B_Y + C * YS * 4;                // W fp32 [C][WS]
 constexpr int B_MB = B_W + ((C * WS * 4 + 15) / 16) * 16;  // M_b fp32 [C][MBS] (for the inverse)
 constexpr int kBytes = B_MB + C * MBS * 4;
-static_assert(B_BT % 16 == 0 && B_Y % 16 == 0 && B_W % 16 == 0 && B_MB % 16 == 0, "16-byte aligned blocks");
+static_assert(B_BT % 16 == 0 && B_Y % 128 == 0 && B_W % 16 == 0 && B_MB % 16 == 0 && YS == OS,
+              "aligned blocks; the y staging block is a tensor-store source");
 
 template <typename E>
 __host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 mma3n<4, kVLo>(ya, vA, bq);
             }
             write_ckpt();
+            if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();  // W
 
             // ---- SA = U W and Y = Z + SA Q_b (16 x 16 per warp)
@@ -305,6 +307,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         } else {
             // exact per-token recurrence for a chunk whose decay leaves the factorisable range
             write_ckpt();
+            if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
+            __syncthreads();
             for (int t = 0; t < nv; ++t) {
                 float sa0 = 0.f, sa1 = 0.f;
 #pragma unroll
@@ -345,13 +349,14 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             __syncthreads();
             if (c + 1 < nchunks) prefetch(c + 1);
         }
+        fence_proxy_async();  // the staged y tile is read by a tensor store
         __syncthreads();
-        for (int e = tid; e < nv * 16; e += NT) {
-            const int t = e >> 4, n = (e & 15) * 4;
-            *reinterpret_cast<float4 *>(p.y + base0 + (size_t)(t0 + t) * tstride + n) =
-                *reinterpret_cast<const float4 *>(ys + t * YS + n);
+        if (tid == 0) {  // y of the chunk: one tensor store (tokens past T are not written)
+            tma_store_rows(&maps.m[6], ys, h, t0, bi);
+            bulk_commit();
         }
     }
+    if (tid == 0) bulk_wait_all();
     if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
     if (p.sT) {
         float *dst = p.sT + sbase;
@@ -366,8 +371,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
 template <typename E>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = fwd_smem_bytes<E>();
-    InputMaps maps;
+    InputMaps maps;  // six inputs, and y (box OS) in the last slot
     cudaError_t e = encode_input_maps(&maps, p, nullptr);
+    if (e == cudaSuccess) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
