@@ -76,7 +76,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
 // fills a padded [C][RS] staging block; the columns past 64 and the tokens
 // past T are out of range and arrive as zeros.
 struct InputMaps {
-    CUtensorMap m[7];
+    CUtensorMap m[8];  // r, w, k, v, a, b; then dy (backward) or y; then the checkpoints (forward)
 };
 __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int h, int t0, int b, uint64_t *bar) {
     asm volatile(
@@ -98,6 +98,13 @@ __device__ __forceinline__ void tma_store_rows(const CUtensorMap *map, const voi
     asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(smem_addr(src)), "r"(0), "r"(h), "r"(t0), "r"(b)
+                 : "memory");
+}
+// 2-D tensor store: box at (column 0, row `row`).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int row) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(0), "r"(row)
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
@@ -181,6 +188,20 @@ inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const fl
         if (e != cudaSuccess) return e;
     }
     return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
+}
+// Host: map of the checkpoints as rows of 64 fp32 (nrows = B*H*ceil(T/L)*64),
+// box OS x 8 (eight state rows of one warp from a padded staging block).
+inline cudaError_t encode_ckpt_map(CUtensorMap *m, const float *ckpt, long long nrows) {
+    const EncodeTiledFn encode = encode_tiled_fn();
+    if (!encode) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {64, (cuuint64_t)nrows};
+    const cuuint64_t strides[1] = {64ull * 4};
+    const cuuint32_t box[2] = {OS, 8};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ckpt), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 // Host: maps of the six gradients dr, dw, dk, dv, da, db (fp32).
 inline cudaError_t encode_output_maps(OutputMaps *maps, const SeqArgs &p) {

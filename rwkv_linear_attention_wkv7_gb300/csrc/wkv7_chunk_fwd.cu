@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
         lost |= !mbar_wait(&bar, c & 1, p.err);
+        if (lane == 0) bulk_wait_read();  // this warp's checkpoint stores have left the a^ / r^ slots
         __syncthreads();
         if (tid == 0 && c + 1 < nchunks) mbar_expect_tx(&bar, kChunkBytes);
 
@@ -209,9 +210,29 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 }
                 mma3n<4, kVLo>(ya, vA, bq);
             }
-            write_ckpt();
             if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();  // W
+
+            // Checkpoint of S_0 (before P2 updates S): each warp stages its 16 rows,
+            // 8 at a time, in its quarter of the a^ / r^ slots (free once every warp's
+            // U/Z is done) and writes them with 2-D tensor stores; the second half
+            // waits for the first to have left the staging block.
+            const bool ck = p.ckpt && t0 % p.L == 0;
+            float *const ckst = reinterpret_cast<float *>(Bs + (warp < 2 ? B_AH : B_RH)) + (warp & 1) * 8 * OS;
+            const int ckrow = (bh * p.nck + t0 / p.L) * 64 + 16 * warp;
+            auto stage_ck = [&](int half) {
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+                    *reinterpret_cast<float2 *>(ckst + g * OS + 8 * nt + 2 * q) =
+                        make_float2(S[nt][2 * half], S[nt][2 * half + 1]);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&maps.m[7], ckst, ckrow + 8 * half);
+                    bulk_commit();
+                }
+            };
+            if (ck) stage_ck(0);
 
             // ---- SA = U W and Y = Z + SA Q_b (16 x 16 per warp)
             float sa[2][4] = {};
@@ -278,6 +299,11 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                     st_afrag(fc + fac::kWA, wa, lane);
                     st_bfrags_acc(fc + fac::kWQbB, cb, lane);
                 }
+            }
+            if (ck) {
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                stage_ck(1);
             }
             // ---- S_C = (S_0 + SA B~^T + V K~^T) diag(d_C)
 #pragma unroll
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
     if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
     if (p.sT) {
         float *dst = p.sT + sbase;
@@ -374,6 +400,7 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     InputMaps maps;  // six inputs, and y (box OS) in the last slot
     cudaError_t e = encode_input_maps(&maps, p, nullptr);
     if (e == cudaSuccess) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
+    if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
