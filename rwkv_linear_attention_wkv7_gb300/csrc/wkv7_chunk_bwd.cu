@@ -342,12 +342,13 @@ __global__ void __launch_bounds__(NT, 2)
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
         lost |= !mbar_wait(&bar, (nchunks - 1 - c) & 1, p.err);
-        if (tid == 0) bulk_wait_read();  // the last chunk's gradient stores have read their staging
         __syncthreads();
         if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (exact) {
+            if (tid == 0) bulk_wait_read();  // the last chunk's gradient stores have read their staging
+            __syncthreads();
             for (int e = tid; e < 64 * 16; e += NT) {  // contiguous fp32 start state for the per-token path
                 const int u = e >> 4, n = (e & 15) * 4;
                 *reinterpret_cast<float4 *>(S0f + u * SP + n) = *reinterpret_cast<const float4 *>(s0_row(u) + n);
@@ -375,6 +376,9 @@ __global__ void __launch_bounds__(NT, 2)
                 const int e = tid + NT * m, row = e >> 4, col = (e & 15) * 4;
                 sv[m] = *reinterpret_cast<const float4 *>(s0_row(row) + col);
             }
+            // the last chunk's gradient stores must have read their staging (the S_0,
+            // v and SA slots) before the splits below overwrite it
+            if (tid == 0) bulk_wait_read();
             __syncthreads();
             __nv_bfloat16 *sh = hi_of(Bs, B_SX), *sl = lo_of(Bs, B_SX, 64);
 #pragma unroll
