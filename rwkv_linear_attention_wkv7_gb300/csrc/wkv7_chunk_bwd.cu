@@ -658,7 +658,8 @@ __global__ void __launch_bounds__(NT, 2)
                 BFrag bq[4];
                 ldb2(DYH, 0, 16 * kk, lane, bq[0], bq[1]);
                 ldb2(DSH, 0, 16 * kk, lane, bq[2], bq[3]);
-                const AFrag af = lda(mt ? VM : SAH, 0, 16 * kk, lane);
+                // v rows: with bf16 inputs their lo part is zero and is not loaded
+                const AFrag af = (mt && !kVLo) ? lda_hi(VM, 0, 16 * kk, lane) : lda(mt ? VM : SAH, 0, 16 * kk, lane);
                 const bool ds = warp & 1;
                 const BFrag gq[2] = {ds ? bq[2] : bq[0], ds ? bq[3] : bq[1]};
                 mma3n<2>(acc, af, gq);
@@ -729,7 +730,10 @@ __global__ void __launch_bounds__(NT, 2)
         for (int kk = 0; kk < 4; ++kk) {
             const AFrag gT = lda_t(SX, 16 * warp, 16 * kk, lane);
             BFrag b0, b1, b2, b3;
-            ldb2(VM, 0, 16 * kk, lane, b0, b1);
+            if constexpr (kVLo)
+                ldb2(VM, 0, 16 * kk, lane, b0, b1);
+            else
+                ldb2_hi(VM, 0, 16 * kk, lane, b0, b1);
             ldb2(SAH, 0, 16 * kk, lane, b2, b3);
             {
                 const BFrag bv[2] = {b0, b1}, bs[2] = {b2, b3};

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 ldb2(AH, 0, 16 * kk, lane, bq[2], bq[3]);
                 mma3n<4>(ya, sf, bq);
             }
-            const AFrag vA = lda_t(VM, 16 * warp, 0, lane);
+            const AFrag vA = kVLo ? lda_t(VM, 16 * warp, 0, lane) : lda_t_hi(VM, 16 * warp, 0, lane);
             {
                 BFrag bq[4];
 #pragma unroll

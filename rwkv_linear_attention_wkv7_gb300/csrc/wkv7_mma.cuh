@@ -138,6 +138,31 @@ __device__ __forceinline__ void ldb2(const HL &M, int n0, int k0, int lane, BFra
     b0.hi[0] = h[0]; b0.hi[1] = h[1]; b1.hi[0] = h[2]; b1.hi[1] = h[3];
     b0.lo[0] = l[0]; b0.lo[1] = l[1]; b1.lo[0] = l[2]; b1.lo[1] = l[3];
 }
+// The same two B fragments with hi only (lo set to zero), for a matrix whose
+// lo part is identically zero.
+__device__ __forceinline__ void ldb2_hi(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
+    const int off = (n0 + (lane & 7) + 8 * (lane >> 4)) * MS + k0 + 8 * ((lane >> 3) & 1);
+    uint32_t h[4];
+    ldsm_x4(h, M.hi + off);
+    b0.hi[0] = h[0]; b0.hi[1] = h[1]; b1.hi[0] = h[2]; b1.hi[1] = h[3];
+    b0.lo[0] = b0.lo[1] = b1.lo[0] = b1.lo[1] = 0u;
+}
+// A fragment with hi only (lo set to zero), A[m][k] = M[m0 + m][k0 + k].
+__device__ __forceinline__ AFrag lda_hi(const HL &M, int m0, int k0, int lane) {
+    const int off = (m0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + k0 + 8 * (lane >> 4);
+    AFrag f;
+    ldsm_x4(f.hi, M.hi + off);
+    f.lo[0] = f.lo[1] = f.lo[2] = f.lo[3] = 0u;
+    return f;
+}
+// A fragment with hi only (lo set to zero), A[m][k] = M[k0 + k][m0 + m].
+__device__ __forceinline__ AFrag lda_t_hi(const HL &M, int m0, int k0, int lane) {
+    const int off = (k0 + (lane & 7) + 8 * (lane >> 4)) * MS + m0 + 8 * ((lane >> 3) & 1);
+    AFrag f;
+    ldsm_x4_t(f.hi, M.hi + off);
+    f.lo[0] = f.lo[1] = f.lo[2] = f.lo[3] = 0u;
+    return f;
+}
 // B fragments of two n-tiles, B[k][n] = M[k][n] (M stored [k][n]).
 __device__ __forceinline__ void ldb2_t(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
     const int off = (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + n0 + 8 * (lane >> 4);
