@@ -272,9 +272,12 @@ __device__ __forceinline__ void prep_inverse(const float *G, float *Wm) {
 
 // W = (I - M_b)^{-1} as above, M_b read from a row-major copy with row
 // stride MBS floats (16-byte aligned rows): each row comes in with broadcast
-// 16-byte loads issued ahead of the product chain.
+// 16-byte loads issued ahead of the product chain.  Lane t holds column t of
+// W and writes it, split into bf16 hi + lo, as row t of W^T in two compact
+// 16 x 16 matrices of row stride CS (four 16-byte stores per lane).
 constexpr int MBS = 20;
-__device__ __forceinline__ void prep_inverse_v(const float *Mb, float *Wm) {
+constexpr int CS = 24;  // row stride (elements) of a compact 16 x 16 split matrix: ldmatrix rows 12 banks apart
+__device__ __forceinline__ void prep_inverse_t(const float *Mb, __nv_bfloat16 *wt_hi, __nv_bfloat16 *wt_lo) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (warp != 0 || lane >= C) return;
     const int t = lane;
@@ -293,8 +296,18 @@ __device__ __forceinline__ void prep_inverse_v(const float *Mb, float *Wm) {
         for (int u = C - 1; u > s; --u) acc = __fmaf_rn(m[u], wc[u], acc);
         wc[s] = acc;
     }
+    uint32_t h[8], l[8];
 #pragma unroll
-    for (int s = 0; s < C; ++s) Wm[s * WS + t] = wc[s];
+    for (int i = 0; i < 8; ++i) {
+        const Frag2 f = split2(wc[2 * i], wc[2 * i + 1]);
+        h[i] = f.hi;
+        l[i] = f.lo;
+    }
+    uint4 *hp = reinterpret_cast<uint4 *>(wt_hi + t * CS), *lp = reinterpret_cast<uint4 *>(wt_lo + t * CS);
+    hp[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    hp[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    lp[0] = make_uint4(l[0], l[1], l[2], l[3]);
+    lp[1] = make_uint4(l[4], l[5], l[6], l[7]);
 }
 
 }  // namespace chunk

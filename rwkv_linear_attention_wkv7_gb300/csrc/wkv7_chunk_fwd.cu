@@ -35,21 +35,24 @@ constexpr int NT = 128;
 constexpr int YS = 68;  // row stride (floats) of the y staging block
 
 // Shared-memory carve-up (byte offsets after the raw input block).  HL16 = a
-// split operand matrix (bf16 hi then lo) of 16 rows, row stride MS.
+// split operand matrix (bf16 hi then lo) of 16 rows, row stride MS; HLC = a
+// compact 16 x 16 split matrix, row stride CS.
 constexpr int HL16 = 2 * 16 * MS * 2;
+constexpr int HLC = 2 * 16 * CS * 2;
 constexpr int B_DD = 0;                              // d fp32 [C][DS]
-constexpr int B_G = B_DD + C * SP * 4;               // Gram fp32 [32][GS]
-constexpr int G_SLOT = 32 * GS * 4;
-constexpr int B_BT = B_G + ((G_SLOT + 15) / 16) * 16;  // b~ [t][j]
+constexpr int B_BT = B_DD + C * SP * 4;              // b~ [t][j]
 constexpr int B_KT = B_BT + HL16;                    // k~ [t][j]
 constexpr int B_AH = B_KT + HL16;                    // a^ [t][j]
 constexpr int B_RH = B_AH + HL16;                    // r^ [t][j]
 constexpr int B_VM = B_RH + HL16;                    // v [t][i]
 constexpr int B_Y = B_VM + HL16;                     // y staging fp32 [C][YS]
-constexpr int B_W = B_Y + C * YS * 4;                // W fp32 [C][WS]
-constexpr int B_MB = B_W + ((C * WS * 4 + 15) / 16) * 16;  // M_b fp32 [C][MBS] (for the inverse)
+constexpr int B_QB = B_Y + C * YS * 4;               // Q_b [s][t]  (compact; Q_b, M_k, Q_k in
+constexpr int B_MK = B_QB + HLC;                     // M_k [s][t]   the order of the Gram
+constexpr int B_QK = B_MK + HLC;                     // Q_k [s][t]   warps 1, 2, 3)
+constexpr int B_WT = B_QK + HLC;                     // W^T [t][s]  (compact)
+constexpr int B_MB = B_WT + HLC;                     // M_b fp32 [C][MBS] (for the inverse)
 constexpr int kBytes = B_MB + C * MBS * 4;
-static_assert(B_BT % 16 == 0 && B_Y % 128 == 0 && B_W % 16 == 0 && B_MB % 16 == 0 && YS == OS,
+static_assert(B_BT % 16 == 0 && B_Y % 128 == 0 && B_QB % 16 == 0 && B_MB % 16 == 0 && YS == OS,
               "aligned blocks; the y staging block is a tensor-store source");
 
 template <typename E>
@@ -58,6 +61,10 @@ __host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + 
 __device__ __forceinline__ HL hl(const unsigned char *base, int off) {
     const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
     return HL{p, p + 16 * MS};
+}
+__device__ __forceinline__ HL hlc(const unsigned char *base, int off) {
+    const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
+    return HL{p, p + 16 * CS};
 }
 __device__ __forceinline__ __nv_bfloat16 *hi_of(unsigned char *base, int off) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off);
@@ -73,10 +80,10 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     E *raw = reinterpret_cast<E *>(smem);
     unsigned char *Bs = smem + raw_bytes<E>();
-    float *dd = reinterpret_cast<float *>(Bs + B_DD), *G = reinterpret_cast<float *>(Bs + B_G);
-    float *ys = reinterpret_cast<float *>(Bs + B_Y), *Wm = reinterpret_cast<float *>(Bs + B_W);
+    float *dd = reinterpret_cast<float *>(Bs + B_DD), *ys = reinterpret_cast<float *>(Bs + B_Y);
     float *Mb = reinterpret_cast<float *>(Bs + B_MB);
     const HL BT = hl(Bs, B_BT), KT = hl(Bs, B_KT), AH = hl(Bs, B_AH), RH = hl(Bs, B_RH), VM = hl(Bs, B_VM);
+    const HL QB = hlc(Bs, B_QB), MK = hlc(Bs, B_MK), QK = hlc(Bs, B_QK), WT = hlc(Bs, B_WT);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -169,27 +176,30 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                     const BFrag bq[2] = {b0, b1};
                     mma3n<2>(acc, af, bq);
                 }
+                if (warp == 0) {  // b~ . a^ = M_b (its unused lower part too), fp32 for the inverse
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int col = 8 * (2 * (warp & 1) + u) + 2 * q, row = 16 * mt + g;
-                    G[row * GS + col] = acc[u][0];
-                    G[row * GS + col + 1] = acc[u][1];
-                    G[(row + 8) * GS + col] = acc[u][2];
-                    G[(row + 8) * GS + col + 1] = acc[u][3];
-                    if (warp == 0) {  // b~ . a^ tile = M_b (and its unused lower part)
-                        *reinterpret_cast<float2 *>(Mb + row * MBS + col) = make_float2(acc[u][0], acc[u][1]);
-                        *reinterpret_cast<float2 *>(Mb + (row + 8) * MBS + col) = make_float2(acc[u][2], acc[u][3]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 8 * u + 2 * q;
+                        *reinterpret_cast<float2 *>(Mb + g * MBS + col) = make_float2(acc[u][0], acc[u][1]);
+                        *reinterpret_cast<float2 *>(Mb + (g + 8) * MBS + col) = make_float2(acc[u][2], acc[u][3]);
                     }
+                } else {  // b~ . r^ = Q_b, k~ . a^ = M_k, k~ . r^ = Q_k: masked to [s <= t] ([s < t] for
+                          // M_k) and split into their compact operand matrices
+                    const int strict = warp == 2;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (g + 8 * (e >> 1) + strict > 8 * u + 2 * q + (e & 1)) acc[u][e] = 0.f;
+                    unsigned char *dst = Bs + B_QB + (warp - 1) * HLC;
+                    st_acc16<CS>(hi_of(dst, 0), reinterpret_cast<__nv_bfloat16 *>(dst) + 16 * CS, 0, 0, acc, lane);
                 }
             }
             __syncthreads();
 
             // W on warp 0 while every warp forms [Z | U] = S_0 [R^ | A^] + V [Q_k | M_k]
             // (warp 0 follows with its own rows once W is done)
-            prep_inverse_v(Mb, Wm);
-            auto mk = [&](int s, int t) { return s < t ? G[(16 + s) * GS + t] : 0.f; };        // M_k[s][t]
-            auto qk = [&](int s, int t) { return s <= t ? G[(16 + s) * GS + 16 + t] : 0.f; };  // Q_k[s][t]
-            auto qb = [&](int s, int t) { return s <= t ? G[s * GS + 16 + t] : 0.f; };         // Q_b[s][t]
+            prep_inverse_t(Mb, hi_of(Bs, B_WT), reinterpret_cast<__nv_bfloat16 *>(Bs + B_WT) + 16 * CS);
             float ya[4][4] = {};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -202,12 +212,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             const AFrag vA = kVLo ? lda_t(VM, 16 * warp, 0, lane) : lda_t_hi(VM, 16 * warp, 0, lane);
             {
                 BFrag bq[4];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = 8 * u + g;
-                    bq[u] = make_b(make_float2(qk(2 * q, t), qk(2 * q + 1, t)), make_float2(qk(2 * q + 8, t), qk(2 * q + 9, t)));
-                    bq[2 + u] = make_b(make_float2(mk(2 * q, t), mk(2 * q + 1, t)), make_float2(mk(2 * q + 8, t), mk(2 * q + 9, t)));
-                }
+                ldb2_t<CS>(QK, 0, 0, lane, bq[0], bq[1]);
+                ldb2_t<CS>(MK, 0, 0, lane, bq[2], bq[3]);
                 mma3n<4, kVLo>(ya, vA, bq);
             }
             if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
@@ -240,62 +246,38 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 const AFrag ua = make_a(make_float2(ya[2][0], ya[2][1]), make_float2(ya[2][2], ya[2][3]),
                                         make_float2(ya[3][0], ya[3][1]), make_float2(ya[3][2], ya[3][3]));
                 BFrag bw[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = 8 * u + g;
-                    bw[u] = make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
-                                   make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t]));
-                }
+                ldb2<CS>(WT, 0, 0, lane, bw[0], bw[1]);  // B[s][t] = W[s][t] = W^T[t][s]
                 mma3n<2>(sa, ua, bw);
             }
             const AFrag saf = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
                                      make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
-            {
-                BFrag bq[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int t = 8 * u + g;
-                    bq[u] = make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)), make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t)));
-                }
-                mma3n<2>(ya, saf, bq);  // Y (tiles 0, 1 of ya)
-            }
+            BFrag qbf[2];
+            ldb2_t<CS>(QB, 0, 0, lane, qbf[0], qbf[1]);
+            mma3n<2>(ya, saf, qbf);  // Y (tiles 0, 1 of ya)
             if (fc) {  // factor cache for the backward
                 st_acc2(fc + fac::kSA + 256 * warp, sa[0], sa[1], lane);
                 if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b
-                    const AFrag am = make_a(make_float2(mk(g, 2 * q), mk(g, 2 * q + 1)), make_float2(mk(g + 8, 2 * q), mk(g + 8, 2 * q + 1)),
-                                            make_float2(mk(g, 2 * q + 8), mk(g, 2 * q + 9)),
-                                            make_float2(mk(g + 8, 2 * q + 8), mk(g + 8, 2 * q + 9)));
+                    const AFrag am = lda<CS>(MK, 0, 0, lane);
+                    BFrag bw[2];
+                    ldb2<CS>(WT, 0, 0, lane, bw[0], bw[1]);
                     float cm[2][4] = {};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int t = 8 * nt + g;
-                        mma3(cm[nt], am, make_b(make_float2(Wm[(2 * q) * WS + t], Wm[(2 * q + 1) * WS + t]),
-                                                make_float2(Wm[(2 * q + 8) * WS + t], Wm[(2 * q + 9) * WS + t])));
-                    }
+                    mma3n<2>(cm, am, bw);
                     const AFrag amp = make_a(make_float2(cm[0][0], cm[0][1]), make_float2(cm[0][2], cm[0][3]),
                                              make_float2(cm[1][0], cm[1][1]), make_float2(cm[1][2], cm[1][3]));
                     float cq[2][4];
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
-                        const int tc = 8 * nt + 2 * q, t = 8 * nt + g;
-                        cq[nt][0] = qk(g, tc); cq[nt][1] = qk(g, tc + 1); cq[nt][2] = qk(g + 8, tc); cq[nt][3] = qk(g + 8, tc + 1);
-                        mma3(cq[nt], amp, make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)),
-                                                 make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t))));
+                        const int tc = 8 * nt + 2 * q;
+                        const float2 x = ld_hl<CS>(QK.hi, QK.lo, g, tc), z = ld_hl<CS>(QK.hi, QK.lo, g + 8, tc);
+                        cq[nt][0] = x.x; cq[nt][1] = x.y; cq[nt][2] = z.x; cq[nt][3] = z.y;
                     }
+                    mma3n<2>(cq, amp, qbf);
                     st_afrag(fc + fac::kMkA, amp, lane);
                     st_bfrags_acc(fc + fac::kQB, cq, lane);
                 } else if (warp == 3) {  // W (A operand of W B~) and W Q_b
-                    const AFrag wa = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
-                                            make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
-                                            make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
-                                            make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+                    const AFrag wa = lda_t<CS>(WT, 0, 0, lane);  // A[s][t] = W[s][t] = W^T[t][s]
                     float cb[2][4] = {};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int t = 8 * nt + g;
-                        mma3(cb[nt], wa, make_b(make_float2(qb(2 * q, t), qb(2 * q + 1, t)),
-                                                make_float2(qb(2 * q + 8, t), qb(2 * q + 9, t))));
-                    }
+                    mma3n<2>(cb, wa, qbf);
                     st_afrag(fc + fac::kWA, wa, lane);
                     st_bfrags_acc(fc + fac::kWQbB, cb, lane);
                 }

@@ -113,25 +113,29 @@ struct HL {  // a split operand matrix: hi and lo parts, same layout
     const __nv_bfloat16 *hi, *lo;
 };
 
-// A fragment, A[m][k] = M[m0 + m][k0 + k] (M stored [m][k]).
+// A fragment, A[m][k] = M[m0 + m][k0 + k] (M stored [m][k], row stride S).
+template <int S = MS>
 __device__ __forceinline__ AFrag lda(const HL &M, int m0, int k0, int lane) {
-    const int off = (m0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + k0 + 8 * (lane >> 4);
+    const int off = (m0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * S + k0 + 8 * (lane >> 4);
     AFrag f;
     ldsm_x4(f.hi, M.hi + off);
     ldsm_x4(f.lo, M.lo + off);
     return f;
 }
-// A fragment, A[m][k] = M[k0 + k][m0 + m] (M stored [k][m]).
+// A fragment, A[m][k] = M[k0 + k][m0 + m] (M stored [k][m], row stride S).
+template <int S = MS>
 __device__ __forceinline__ AFrag lda_t(const HL &M, int m0, int k0, int lane) {
-    const int off = (k0 + (lane & 7) + 8 * (lane >> 4)) * MS + m0 + 8 * ((lane >> 3) & 1);
+    const int off = (k0 + (lane & 7) + 8 * (lane >> 4)) * S + m0 + 8 * ((lane >> 3) & 1);
     AFrag f;
     ldsm_x4_t(f.hi, M.hi + off);
     ldsm_x4_t(f.lo, M.lo + off);
     return f;
 }
-// B fragments of two n-tiles (n0..n0+7, n0+8..n0+15), B[k][n] = M[n][k] (M stored [n][k]).
+// B fragments of two n-tiles (n0..n0+7, n0+8..n0+15), B[k][n] = M[n][k] (M stored [n][k],
+// row stride S).
+template <int S = MS>
 __device__ __forceinline__ void ldb2(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
-    const int off = (n0 + (lane & 7) + 8 * (lane >> 4)) * MS + k0 + 8 * ((lane >> 3) & 1);
+    const int off = (n0 + (lane & 7) + 8 * (lane >> 4)) * S + k0 + 8 * ((lane >> 3) & 1);
     uint32_t h[4], l[4];
     ldsm_x4(h, M.hi + off);
     ldsm_x4(l, M.lo + off);
@@ -163,9 +167,10 @@ __device__ __forceinline__ AFrag lda_t_hi(const HL &M, int m0, int k0, int lane)
     f.lo[0] = f.lo[1] = f.lo[2] = f.lo[3] = 0u;
     return f;
 }
-// B fragments of two n-tiles, B[k][n] = M[k][n] (M stored [k][n]).
+// B fragments of two n-tiles, B[k][n] = M[k][n] (M stored [k][n], row stride S).
+template <int S = MS>
 __device__ __forceinline__ void ldb2_t(const HL &M, int n0, int k0, int lane, BFrag &b0, BFrag &b1) {
-    const int off = (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * MS + n0 + 8 * (lane >> 4);
+    const int off = (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * S + n0 + 8 * (lane >> 4);
     uint32_t h[4], l[4];
     ldsm_x4_t(h, M.hi + off);
     ldsm_x4_t(l, M.lo + off);
@@ -184,9 +189,10 @@ __device__ __forceinline__ void st_hl4(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int
     *reinterpret_cast<uint2 *>(hi + row * MS + col) = make_uint2(f0.hi, f1.hi);
     *reinterpret_cast<uint2 *>(lo + row * MS + col) = make_uint2(f0.lo, f1.lo);
 }
+template <int S = MS>
 __device__ __forceinline__ float2 ld_hl(const __nv_bfloat16 *hi, const __nv_bfloat16 *lo, int row, int col) {
-    const uint32_t h = *reinterpret_cast<const uint32_t *>(hi + row * MS + col);
-    const uint32_t l = *reinterpret_cast<const uint32_t *>(lo + row * MS + col);
+    const uint32_t h = *reinterpret_cast<const uint32_t *>(hi + row * S + col);
+    const uint32_t l = *reinterpret_cast<const uint32_t *>(lo + row * S + col);
     return make_float2(__uint_as_float(h << 16) + __uint_as_float(l << 16),
                        __uint_as_float(h & 0xffff0000u) + __uint_as_float(l & 0xffff0000u));
 }
@@ -286,12 +292,13 @@ __device__ __forceinline__ void stsm_x4(void *p, uint32_t r0, uint32_t r1, uint3
                  "r"(r3)
                  : "memory");
 }
+template <int S = MS>
 __device__ __forceinline__ void st_acc16(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int row0, int col0, const float c[2][4],
                                          int lane) {
     const Frag2 f0 = split2(c[0][0], c[0][1]), f1 = split2(c[0][2], c[0][3]);
     const Frag2 f2 = split2(c[1][0], c[1][1]), f3 = split2(c[1][2], c[1][3]);
     const int k = lane >> 3, r = lane & 7;
-    const int off = (row0 + 8 * (k & 1) + r) * MS + col0 + 8 * (k >> 1);
+    const int off = (row0 + 8 * (k & 1) + r) * S + col0 + 8 * (k >> 1);
     stsm_x4(hi + off, f0.hi, f1.hi, f2.hi, f3.hi);
     stsm_x4(lo + off, f0.lo, f1.lo, f2.lo, f3.lo);
 }
