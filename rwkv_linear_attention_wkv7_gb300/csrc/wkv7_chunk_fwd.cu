@@ -88,8 +88,6 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, q = lane & 3;
     const int bh = blockIdx.x, bi = bh / p.H, h = bh % p.H;
-    const size_t tstride = (size_t)p.H * 64;
-    const size_t base0 = ((size_t)bi * p.T * p.H + h) * 64;
     const size_t sbase = (size_t)bh * 64 * 64;
     const int rA = warp * 16 + g, rB = rA + 8;  // the two state rows this lane holds
 
@@ -159,22 +157,36 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
                 st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
                 st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
-                st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
+                if (kVLo) st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
+            }
+            // bf16 v is its own hi part: its A fragment (A[i][t] = v[t][i]) comes straight
+            // from the staged input, before the barrier that lets the next chunk's copies in
+            AFrag vA;
+            if (!kVLo) {
+                const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(raw) + VV * C * RS;
+                vA = lda_t_hi(HL{rv, rv}, 16 * warp, 0, lane);
             }
             __syncthreads();
             // raw is no longer read in this chunk: fetch the next one now
             if (c + 1 < nchunks) prefetch(c + 1);
 
-            {   // Gram [B~; K~] [A^; R^]^T: warp -> m-tile (b~ | k~), n-tile pair (a^ | r^)
+            // Gram [B~; K~] [A^; R^]^T (warp -> m-tile b~ | k~, n-tile pair a^ | r^) and
+            // [Z | U] = S_0 [R^ | A^] in one pass over j: both take the same r^ / a^ fragments
+            float ya[4][4] = {};
+            {
                 const int mt = warp >> 1;
+                const bool rn = warp & 1;
                 float acc[2][4] = {};
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
+                    BFrag bq[4];
+                    ldb2(RH, 0, 16 * kk, lane, bq[0], bq[1]);
+                    ldb2(AH, 0, 16 * kk, lane, bq[2], bq[3]);
                     const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
-                    BFrag b0, b1;
-                    ldb2((warp & 1) ? RH : AH, 0, 16 * kk, lane, b0, b1);
-                    const BFrag bq[2] = {b0, b1};
-                    mma3n<2>(acc, af, bq);
+                    const BFrag gq[2] = {rn ? bq[0] : bq[2], rn ? bq[1] : bq[3]};
+                    mma3n<2>(acc, af, gq);
+                    const AFrag sf = a_from_acc(S, kk);
+                    mma3n<4>(ya, sf, bq);
                 }
                 if (warp == 0) {  // b~ . a^ = M_b (its unused lower part too), fp32 for the inverse
 #pragma unroll
@@ -197,19 +209,10 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             }
             __syncthreads();
 
-            // W on warp 0 while every warp forms [Z | U] = S_0 [R^ | A^] + V [Q_k | M_k]
-            // (warp 0 follows with its own rows once W is done)
+            // W on warp 0 while every warp adds V [Q_k | M_k] to [Z | U] (warp 0 follows
+            // with its own rows once W is done)
             prep_inverse_t(Mb, hi_of(Bs, B_WT), reinterpret_cast<__nv_bfloat16 *>(Bs + B_WT) + 16 * CS);
-            float ya[4][4] = {};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const AFrag sf = a_from_acc(S, kk);
-                BFrag bq[4];
-                ldb2(RH, 0, 16 * kk, lane, bq[0], bq[1]);
-                ldb2(AH, 0, 16 * kk, lane, bq[2], bq[3]);
-                mma3n<4>(ya, sf, bq);
-            }
-            const AFrag vA = kVLo ? lda_t(VM, 16 * warp, 0, lane) : lda_t_hi(VM, 16 * warp, 0, lane);
+            if (kVLo) vA = lda_t(VM, 16 * warp, 0, lane);
             {
                 BFrag bq[4];
                 ldb2_t<CS>(QK, 0, 0, lane, bq[0], bq[1]);
