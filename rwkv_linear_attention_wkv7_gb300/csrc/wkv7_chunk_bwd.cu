@@ -64,8 +64,8 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
         float S[8][4];
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
-            const float2 x = *reinterpret_cast<const float2 *>(S0s + rA * SP + 8 * nt + 2 * q);
-            const float2 z = *reinterpret_cast<const float2 *>(S0s + rB * SP + 8 * nt + 2 * q);
+            const float2 x = *reinterpret_cast<const float2 *>(S0s + rA * OS + 8 * nt + 2 * q);
+            const float2 z = *reinterpret_cast<const float2 *>(S0s + rB * OS + 8 * nt + 2 * q);
             S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = z.x; S[nt][3] = z.y;
         }
         float sa0 = 0.f, sa1 = 0.f;
@@ -183,7 +183,7 @@ constexpr int B_DYF = 0;                       // dy fp32 [C][SP]        (chunk 
 constexpr int B_DD = B_DYF + C * SP * 4;       // d fp32 [C][SP]
 constexpr int B_G = B_DD + C * SP * 4;         // Gram, then Gam, fp32 [32][GS] (slot C*SP floats)
 constexpr int B_W = B_G + C * SP * 4;          // W fp32 [C][WS]
-constexpr int B_SX = B_W + 1280;               // S_0 split (HL64), then G d_C (HL64), then gradient staging
+constexpr int B_SX = B_W + 1280;               // S_0 fp32 [64][OS], then G d_C (HL64), then gradient staging
 constexpr int B_BT = B_SX + HL64;              // b~, k~, a^, r^ (HL16 each) [t][j]; exact path: S_{t-1} fp32
 constexpr int B_KT = B_BT + HL16;
 constexpr int B_AH = B_KT + HL16;
@@ -200,7 +200,7 @@ static_assert(B_SX % 16 == 0 && B_BT % 16 == 0 && B_Y % 16 == 0, "16-byte aligne
 static_assert(32 * GS <= C * SP && C * WS * 4 <= 1280, "small fp32 blocks fit");
 static_assert(B_SX % 128 == 0 && B_VV % 128 == 0 && B_SAH % 128 == 0 && C * OS * 4 <= HL16,
               "gradient staging blocks: 128-byte aligned, one per 4.5 KiB slot");
-static_assert(64 * SP * 4 == HL64, "S_0 staging and its split share one slot");
+static_assert(64 * OS * 4 <= HL64, "S_0 staging and the G d_C split share one slot");
 static_assert(4 * HL16 >= 64 * SP * 4, "exact-path S_{t-1} fits the four scaled blocks");
 static_assert(5 * 4 * 64 * 4 <= 2 * HL32, "exact-path scratch fits region Y");
 
@@ -293,16 +293,24 @@ __global__ void __launch_bounds__(NT, 2)
     float carryA = 0.f, carryB = 0.f;  // dw running sum for key columns rA / rB
 
     const int nchunks = (p.T + C - 1) / C;
-    // A chunk's inputs and dy (tensor copies), start state and factor block
-    // (bulk copies) arrive on the TMA engine, completed on one mbarrier whose
-    // phase k holds the chunk processed k-th (nchunks - 1 - c).  Thread 0
-    // announces the bytes right after the previous phase completed and
-    // arrives once the last block is issued.
-    __shared__ __align__(8) uint64_t bar;
-    if (tid == 0) mbar_init(&bar, 1);
+    // A chunk's inputs and dy (tensor copies) and factor block (bulk copy)
+    // arrive on the TMA engine, completed on one mbarrier whose phase k holds
+    // the chunk processed k-th (nchunks - 1 - c).  Thread 0 announces the bytes
+    // right after the previous phase completed and arrives once the inputs are
+    // issued.  The chunk's start state comes on a second mbarrier (same phase
+    // numbering): one 2-D tensor copy of the fp32 checkpoint into the S_0 slot
+    // (rows of stride OS, the columns past 64 zero fill), issued at the chunk
+    // start once the previous chunk's gradient stores have read their staging
+    // there, and first waited for by the products that read S_0.
+    __shared__ __align__(8) uint64_t bar, bar_s;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_init(&bar_s, 1);
+    }
     __syncthreads();
     bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
-    constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + 64 * 64 * 4 + (kFac ? fac::kWords * 4 : 0));
+    constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0));
+    constexpr unsigned kS0Bytes = 64 * OS * 4;
     auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each
         if (tid == 0) {
 #pragma unroll
@@ -310,20 +318,23 @@ __global__ void __launch_bounds__(NT, 2)
             tma_rows(dyf, &maps.m[6], h, c * C, bi, &bar);
         }
     };
-    // The next chunk's start state (fp32, dense 256-byte rows) is fetched
-    // while this chunk's last products still run, into three slots idle by
-    // then: rows 0..15 -> the dy split and 16..31 -> the DSA split (once Gam
-    // and G3's S_0 part are done), 32..63 -> the first masked-Gam block (once
-    // G3 is done).
-    auto s0_row = [&](int row) -> float * {
-        const int off = row < 16 ? B_DYH + row * 256 : row < 32 ? B_DSH + (row - 16) * 256 : B_M3 + (row - 32) * 256;
-        return reinterpret_cast<float *>(Bs + off);
+    auto load_s0 = [&](int c) {  // thread 0
+        mbar_expect_tx(&bar_s, kS0Bytes);
+        tma_load_2d(S0f, &maps.m[7], (bh * p.nck + c) * 64, &bar_s);
+        mbar_arrive(&bar_s);
     };
-    auto stage_s0 = [&](int c, int r0, int r1) {  // rows r0 .. r1 - 1: whole slots
-        const float *src0 = p.ckpt_in + ((size_t)bh * p.nck + c) * 64 * 64;
-        if (tid == 0 && r0 <= 0 && r1 >= 16) bulk_g2s(s0_row(0), src0, 16 * 256, &bar);
-        if (tid == 1 && r0 <= 16 && r1 >= 32) bulk_g2s(s0_row(16), src0 + 16 * 64, 16 * 256, &bar);
-        if (tid == 2 && r0 <= 32 && r1 >= 64) bulk_g2s(s0_row(32), src0 + 32 * 64, 32 * 256, &bar);
+    // S_0 operand fragments straight from the fp32 staging, split on the way:
+    // A[m][k] = S_0[m0 + m][k0 + k] (s0_a) or S_0[k0 + k][m0 + m] (s0_at).
+    // Rows of stride OS put the 32 lanes' words in distinct banks.
+    auto ld2 = [](const float *x) { return *reinterpret_cast<const float2 *>(x); };
+    auto s0_a = [&](int m0, int k0) {
+        const float *x = S0f + (m0 + g) * OS + k0 + 2 * q;
+        return make_a(ld2(x), ld2(x + 8 * OS), ld2(x + 8), ld2(x + 8 * OS + 8));
+    };
+    auto s0_at = [&](int m0, int k0) {
+        const float *x = S0f + (k0 + 2 * q) * OS + m0 + g;
+        return make_a(make_float2(x[0], x[OS]), make_float2(x[8], x[OS + 8]), make_float2(x[8 * OS], x[9 * OS]),
+                      make_float2(x[8 * OS + 8], x[9 * OS + 8]));
     };
     const float *FC = reinterpret_cast<const float *>(Bs + B_QQ);  // factor block of the current chunk
     auto stage_fac = [&](int c) {
@@ -333,7 +344,6 @@ __global__ void __launch_bounds__(NT, 2)
     };
     if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     stage_in(nchunks - 1);
-    stage_s0(nchunks - 1, 0, 64);
     stage_fac(nchunks - 1);
     if (tid == 0) mbar_arrive(&bar);
 
@@ -341,26 +351,27 @@ __global__ void __launch_bounds__(NT, 2)
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
-        lost |= !mbar_wait(&bar, (nchunks - 1 - c) & 1, p.err);
+        const unsigned ph = (nchunks - 1 - c) & 1;
+        lost |= !mbar_wait(&bar, ph, p.err);
         __syncthreads();
-        if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
+        if (tid == 0) {
+            if (c > 0) mbar_expect_tx(&bar, kChunkBytes);
+            // the last chunk's gradient stores have read their staging (the S_0, v and SA
+            // slots): the start state may land, and (after the next barrier) the splits
+            // below may overwrite the rest
+            bulk_wait_read();
+            load_s0(c);
+        }
 
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
         if (exact) {
-            if (tid == 0) bulk_wait_read();  // the last chunk's gradient stores have read their staging
-            __syncthreads();
-            for (int e = tid; e < 64 * 16; e += NT) {  // contiguous fp32 start state for the per-token path
-                const int u = e >> 4, n = (e & 15) * 4;
-                *reinterpret_cast<float4 *>(S0f + u * SP + n) = *reinterpret_cast<const float4 *>(s0_row(u) + n);
-            }
-            __syncthreads();
+            lost |= !mbar_wait(&bar_s, ph, p.err);
             bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
             fence_proxy_async();  // the per-token path wrote into slots the copies refill
             __syncthreads();
             if (c > 0) {
                 stage_in(c - 1);
-                stage_s0(c - 1, 0, 64);
                 stage_fac(c - 1);
                 if (tid == 0) mbar_arrive(&bar);
             }
@@ -368,25 +379,7 @@ __global__ void __launch_bounds__(NT, 2)
         }
         const float *dC = dd + (C - 1) * DS;
 
-        // ================= split every operand matrix once
-        {   // S_0 in place: fp32 staging -> hi/lo
-            float4 sv[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int e = tid + NT * m, row = e >> 4, col = (e & 15) * 4;
-                sv[m] = *reinterpret_cast<const float4 *>(s0_row(row) + col);
-            }
-            // the last chunk's gradient stores must have read their staging (the S_0,
-            // v and SA slots) before the splits below overwrite it
-            if (tid == 0) bulk_wait_read();
-            __syncthreads();
-            __nv_bfloat16 *sh = hi_of(Bs, B_SX), *sl = lo_of(Bs, B_SX, 64);
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                const int e = tid + NT * m, row = e >> 4, col = (e & 15) * 4;
-                st_hl4(sh, sl, row, col, sv[m]);
-            }
-        }
+        // ================= split every operand matrix once (S_0 is split where it is read)
 #pragma unroll
         for (int m = 0; m < 2; ++m) {  // decay-scaled vectors: [t][j] quads
             // with the factor cache, warp w converts its own 16-key slab (all
@@ -413,7 +406,10 @@ __global__ void __launch_bounds__(NT, 2)
         } else {
             __syncthreads();
             // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
-            if (c > 0) stage_in(c - 1);
+            if (c > 0) {
+                stage_in(c - 1);
+                if (tid == 0) mbar_arrive(&bar);
+            }
         }
 
         // ================= per-chunk operands (no state involved)
@@ -542,7 +538,10 @@ __global__ void __launch_bounds__(NT, 2)
         }
         __syncthreads();
         if constexpr (kFac) {  // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
-            if (c > 0) stage_in(c - 1);
+            if (c > 0) {
+                stage_in(c - 1);
+                if (tid == 0) mbar_arrive(&bar);
+            }
         }
 
         // ================= state-dependent products
@@ -552,9 +551,10 @@ __global__ void __launch_bounds__(NT, 2)
         if constexpr (kFac) {  // SA from the forward
             ld_acc2(FC + fac::kSA + 256 * warp, sa[0], sa[1], lane);
         } else {
+            lost |= !mbar_wait(&bar_s, ph, p.err);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const AFrag sf = lda(SX, 16 * warp, 16 * kk, lane);
+                const AFrag sf = s0_a(16 * warp, 16 * kk);
                 BFrag b0, b1;
                 ldb2(AP, 0, 16 * kk, lane, b0, b1);
                 mma3(sa[0], sf, b0);
@@ -572,6 +572,7 @@ __global__ void __launch_bounds__(NT, 2)
 
         // the dw running sum starts at diag(dsT^T sT): sT from the last chunk's start state
         if (last && p.dsT) {
+            lost |= !mbar_wait(&bar_s, ph, p.err);
             const AFrag saA = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
                                      make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
             float part[8][2];
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int nt = 4 * half + 2 * pp + u, j0 = 8 * nt + 2 * q;
-                        const float2 x = ld_hl(SX.hi, SX.lo, rA, j0), z = ld_hl(SX.hi, SX.lo, rB, j0);
+                        const float2 x = ld2(S0f + rA * OS + j0), z = ld2(S0f + rB * OS + j0);
                         float ST[4] = {x.x, x.y, z.x, z.y};
                         mma3(ST, saA, u ? bb1 : bb0);
                         mma3(ST, vA, u ? kb1 : kb0);
@@ -653,6 +654,7 @@ __global__ void __launch_bounds__(NT, 2)
             // this loop (and its DY / DSA fragments) with Gam.
             const int mt = warp >> 1;
             float acc[2][4] = {};
+            lost |= !mbar_wait(&bar_s, ph, p.err);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 BFrag bq[4];
@@ -663,7 +665,7 @@ __global__ void __launch_bounds__(NT, 2)
                 const bool ds = warp & 1;
                 const BFrag gq[2] = {ds ? bq[2] : bq[0], ds ? bq[3] : bq[1]};
                 mma3n<2>(acc, af, gq);
-                const AFrag sT = lda_t(SX, 16 * warp, 16 * kk, lane);
+                const AFrag sT = s0_at(16 * warp, 16 * kk);
                 mma3n<4>(x3, sT, bq);
             }
             __nv_bfloat16 *h3 = hi_of(Bs, B_M3), *l3 = lo_of(Bs, B_M3, 32);
@@ -689,9 +691,7 @@ __global__ void __launch_bounds__(NT, 2)
             st_acc_t16(h4, l4, 16 * (warp & 1), mt ? 0 : 16, m4, lane);
         }
 
-        fence_proxy_async();  // the dy and DSA slots were written by ordinary stores
-        __syncthreads();      // masked Gam blocks visible; S_0, dy and DSA no longer read
-        if (c > 0) stage_s0(c - 1, 0, 32);  // next start state, rows 0..31 (dy and DSA slots)
+        __syncthreads();  // masked Gam blocks visible; S_0, dy and DSA no longer read
         // b~ and k~ of this warp's key rows as A operands, kept for the outputs
         const AFrag btA = lda_t(BT, 16 * warp, 0, lane), ktA = lda_t(KT, 16 * warp, 0, lane);
 #pragma unroll
@@ -717,12 +717,7 @@ __global__ void __launch_bounds__(NT, 2)
                 st_acc16(gh, gl, 16 * warp, 16 * pp, gd, lane);
             }
         }
-        fence_proxy_async();  // the first masked block was written by ordinary stores
-        __syncthreads();      // G d_C visible; the first masked block no longer read
-        if (c > 0) {
-            stage_s0(c - 1, 32, 64);  // rows 32..63 (first masked block's slot)
-            if (tid == 0) mbar_arrive(&bar);
-        }
+        __syncthreads();  // G d_C visible
 
         // G4: [DK | DB] (rows = key index)
         float x4[4][4] = {};
@@ -850,7 +845,10 @@ __global__ void __launch_bounds__(NT, 2)
         }
     }
     if (tid == 0) bulk_wait_all();
-    if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
+    if (lost) {
+        mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
+        mbar_wait(&bar_s, (nchunks - 1) & 1, nullptr);
+    }
     if (p.ds0) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -865,7 +863,8 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
     InputMaps maps;
     OutputMaps omaps;
-    cudaError_t e = encode_input_maps(&maps, p, p.dy);
+    cudaError_t e = encode_input_maps(&maps, p, p.dy);  // six inputs, dy, and the checkpoints (box OS x 64)
+    if (e == cudaSuccess) e = encode_ckpt_map(&maps.m[7], p.ckpt_in, (long long)p.B * p.H * p.nck * 64, 64);
     if (e == cudaSuccess) e = encode_output_maps(&omaps, p);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

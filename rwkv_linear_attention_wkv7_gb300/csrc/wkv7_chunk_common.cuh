@@ -100,6 +100,14 @@ __device__ __forceinline__ void tma_store_rows(const CUtensorMap *map, const voi
                  "r"(smem_addr(src)), "r"(0), "r"(h), "r"(t0), "r"(b)
                  : "memory");
 }
+// 2-D tensor copy into shared memory: box at (column 0, row `row`).
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int row, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar))
+        : "memory");
+}
 // 2-D tensor store: box at (column 0, row `row`).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int row) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
@@ -190,13 +198,14 @@ inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const fl
     return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
 }
 // Host: map of the checkpoints as rows of 64 fp32 (nrows = B*H*ceil(T/L)*64),
-// box OS x 8 (eight state rows of one warp from a padded staging block).
-inline cudaError_t encode_ckpt_map(CUtensorMap *m, const float *ckpt, long long nrows) {
+// box OS x box_rows (padded staging rows: eight state rows of one warp for the
+// stores, a whole 64-row state for the loads).
+inline cudaError_t encode_ckpt_map(CUtensorMap *m, const float *ckpt, long long nrows, int box_rows = 8) {
     const EncodeTiledFn encode = encode_tiled_fn();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {64, (cuuint64_t)nrows};
     const cuuint64_t strides[1] = {64ull * 4};
-    const cuuint32_t box[2] = {OS, 8};
+    const cuuint32_t box[2] = {OS, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ckpt), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
