@@ -353,17 +353,19 @@ __global__ void __launch_bounds__(NT, 2)
         const bool last = c == nchunks - 1;
         const unsigned ph = (nchunks - 1 - c) & 1;
         lost |= !mbar_wait(&bar, ph, p.err);
-        __syncthreads();
-        if (tid == 0) {
-            if (c > 0) mbar_expect_tx(&bar, kChunkBytes);
-            // the last chunk's gradient stores have read their staging (the S_0, v and SA
-            // slots): the start state may land, and (after the next barrier) the splits
-            // below may overwrite the rest
-            bulk_wait_read();
-            load_s0(c);
+        if (warp == 0) {
+            // the last chunk's gradient stores (lanes 0..5, one each) have read their
+            // staging (the S_0, v and SA slots): the start state may land, and after the
+            // barrier below the splits may overwrite the rest
+            if (lane < 6) bulk_wait_read();
+            __syncwarp();
+            if (lane == 0) {
+                if (c > 0) mbar_expect_tx(&bar, kChunkBytes);
+                load_s0(c);
+            }
         }
-
-        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
+        // the cumulative decays on warps 2 and 3, clear of warp 0's copies
+        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv, 64));
         if (exact) {
             lost |= !mbar_wait(&bar_s, ph, p.err);
             bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
@@ -837,14 +839,13 @@ __global__ void __launch_bounds__(NT, 2)
 
         fence_proxy_async();  // the staged tiles are read by the tensor stores
         __syncthreads();
-        if (tid == 0) {
-            const float *const tiles[6] = {gdr, gdw, gdk, gdv, gda, gdb};
-#pragma unroll
-            for (int o = 0; o < 6; ++o) tma_store_rows(&omaps.m[o], tiles[o], h, t0, bi);
+        if (tid < 6) {  // dr, dw, dk, dv, da, db: one tensor store per lane
+            const float *const tile = tid < 4 ? gdr + 1152 * tid : tid == 4 ? gda : gdb;
+            tma_store_rows(&omaps.m[tid], tile, h, t0, bi);
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid < 6) bulk_wait_all();
     if (lost) {
         mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
         mbar_wait(&bar_s, (nchunks - 1) & 1, nullptr);

@@ -235,15 +235,16 @@ __device__ __forceinline__ float4 rcp4(float4 a) {
     return make_float4(rcp_approx(a.x), rcp_approx(a.y), rcp_approx(a.z), rcp_approx(a.w));
 }
 
-// d_t per key column (threads 0..63); padding tokens (t >= nv) decay by 1.
+// d_t per key column (threads first_thread .. first_thread + 63); padding
+// tokens (t >= nv) decay by 1.
 // Returns true (on the calling thread) when some d_t of its column leaves
 // [1e-20, 1e20] (or is not finite): the factorised form then cannot divide
 // by d_t and the chunk takes the exact per-token path.
 template <typename E>
-__device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv) {
+__device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0) {
     bool bad = false;
-    if (threadIdx.x < 64) {
-        const int j = threadIdx.x;
+    const int j = (int)threadIdx.x - first_thread;
+    if (j >= 0 && j < 64) {
         // all loads first: the product chain then runs at FMUL latency
         float wv[C];
 #pragma unroll

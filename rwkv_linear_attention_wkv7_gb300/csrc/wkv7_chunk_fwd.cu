@@ -125,8 +125,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
         lost |= !mbar_wait(&bar, c & 1, p.err);
-        if (lane == 0) bulk_wait_read();  // this warp's checkpoint stores have left the a^ / r^ slots
-        __syncthreads();
+        // this warp's checkpoint stores have left the a^ / r^ slots (the splits write
+        // there after the barrier below)
+        if (lane == 0) bulk_wait_read();
         if (tid == 0 && c + 1 < nchunks) mbar_expect_tx(&bar, kChunkBytes);
 
         // checkpoint of the state before token t0; written once the previous
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         };
 
         float *const fc = p.fac ? p.fac + ((size_t)bh * nchunks + c) * fac::kWords : nullptr;
-        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv));
+        // the cumulative decays on warps 2 and 3 (thread 0 has just issued the y store)
+        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv, 64));
         if (!exact) {
             // ---- split the decay-scaled vectors and v once: [t][j] quads
 #pragma unroll
