@@ -311,11 +311,10 @@ __global__ void __launch_bounds__(NT, 2)
     bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
     constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0));
     constexpr unsigned kS0Bytes = 64 * OS * 4;
-    auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each
-        if (tid == 0) {
-#pragma unroll
-            for (int v = 0; v < 6; ++v) tma_rows(raw + v * C * RS, &maps.m[v], h, c * C, bi, &bar);
-            tma_rows(dyf, &maps.m[6], h, c * C, bi, &bar);
+    auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each, lanes 0..6 of warp 0
+        if (tid < 7) {
+            void *const dst = tid < 6 ? static_cast<void *>(raw + tid * C * RS) : static_cast<void *>(dyf);
+            tma_rows(dst, &maps.m[tid], h, c * C, bi, &bar);
         }
     };
     auto load_s0 = [&](int c) {  // thread 0
@@ -353,20 +352,27 @@ __global__ void __launch_bounds__(NT, 2)
         const bool last = c == nchunks - 1;
         const unsigned ph = (nchunks - 1 - c) & 1;
         lost |= !mbar_wait(&bar, ph, p.err);
-        if (warp == 0) {
-            // the last chunk's gradient stores (lanes 0..5, one each) have read their
-            // staging (the S_0, v and SA slots): the start state may land, and after the
-            // barrier below the splits may overwrite the rest
-            if (lane < 6) bulk_wait_read();
-            __syncwarp();
-            if (lane == 0) {
-                if (c > 0) mbar_expect_tx(&bar, kChunkBytes);
-                load_s0(c);
+        if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
+        // The last chunk's gradient stores (lanes 0..5 of warp 0, one each) must have
+        // read their staging (the S_0, v and SA slots) before the start state lands
+        // there and before the v split and SA, both after a later block barrier,
+        // overwrite the rest.  Warp 0 waits for them after the first splits.
+        auto drain_then_load_s0 = [&]() {
+            if (warp == 0) {
+                if (lane < 6) bulk_wait_read();
+                __syncwarp();
+                if (lane == 0) {
+                    load_s0(c);
+                    // the next start state into L2 now, so that its copy at the next
+                    // chunk start does not wait on DRAM
+                    if (c > 0) tma_prefetch_2d(&maps.m[7], (bh * p.nck + c - 1) * 64);
+                }
             }
-        }
+        };
         // the cumulative decays on warps 2 and 3, clear of warp 0's copies
         const bool exact = __syncthreads_or(prep_decay(raw, dd, nv, 64));
         if (exact) {
+            drain_then_load_s0();
             lost |= !mbar_wait(&bar_s, ph, p.err);
             bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
@@ -398,21 +404,15 @@ __global__ void __launch_bounds__(NT, 2)
             st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // v and dy: [t][i] quads
+        for (int m = 0; m < 2; ++m) {  // dy: [t][i] quads
             const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
-            st_hl4(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, j, ld_raw4(raw, VV, t, j));
             st_hl4(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
         }
-        if constexpr (kFac) {
+        drain_then_load_s0();
+        if constexpr (kFac)
             __syncwarp();
-        } else {
+        else
             __syncthreads();
-            // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
-            if (c > 0) {
-                stage_in(c - 1);
-                if (tid == 0) mbar_arrive(&bar);
-            }
-        }
 
         // ================= per-chunk operands (no state involved)
         if constexpr (!kFac) {
@@ -538,13 +538,15 @@ __global__ void __launch_bounds__(NT, 2)
             st_acc16(kh, kl, 0, 16 * warp, ck, lane);   // K' rows (tokens)
             st_acc16(kh, kl, 16, 16 * warp, cb2, lane); // B' rows
         }
-        __syncthreads();
-        if constexpr (kFac) {  // raw inputs and dy are no longer read in this chunk: fetch the previous chunk's now
-            if (c > 0) {
-                stage_in(c - 1);
-                if (tid == 0) mbar_arrive(&bar);
-            }
+        __syncthreads();  // warp 0 has drained the gradient stores: the staging slots are free
+        // v split: warp w its own 16 value columns (all tokens), which is all its vA
+        // reads; the other readers come after the barrier that follows G2
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int e = lane + 32 * m, t = e >> 2, i = 16 * warp + (e & 3) * 4;
+            st_hl4(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, i, ld_raw4(raw, VV, t, i));
         }
+        __syncwarp();
 
         // ================= state-dependent products
         // G1: SA = S_0 A' + V M_k'  (rows = value index)
@@ -643,7 +645,11 @@ __global__ void __launch_bounds__(NT, 2)
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
-        if (c > 0) stage_fac(c - 1);  // this chunk's factors are consumed
+        if (c > 0) {  // this chunk's inputs, dy and factors are consumed: fetch the previous chunk's
+            stage_in(c - 1);
+            stage_fac(c - 1);
+            if (tid == 0) mbar_arrive(&bar);
+        }
 
         // G3: [DR | DA] (rows = key index j = rA / rB)
         float x3[4][4] = {};

@@ -108,6 +108,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar))
         : "memory");
 }
+// Fetch the same box into L2 only (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int row) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(0), "r"(row)
+                 : "memory");
+}
 // 2-D tensor store: box at (column 0, row `row`).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int row) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(

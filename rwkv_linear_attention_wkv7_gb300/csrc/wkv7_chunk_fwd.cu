@@ -111,12 +111,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     __syncthreads();
     bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
     constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>();
-    auto prefetch = [&](int c) {  // chunk c's copies; thread 0 announced its bytes
-        if (tid == 0) {
-#pragma unroll
-            for (int v = 0; v < 6; ++v) tma_rows(raw + v * C * RS, &maps.m[v], h, c * C, bi, &bar);
-            mbar_arrive(&bar);
-        }
+    auto prefetch = [&](int c) {  // chunk c's copies (lanes 0..5 of warp 0); thread 0 announced its bytes
+        if (tid < 6) tma_rows(raw + tid * C * RS, &maps.m[tid], h, c * C, bi, &bar);
+        if (tid == 0) mbar_arrive(&bar);
     };
     if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     prefetch(0);
