@@ -353,13 +353,15 @@ __global__ void __launch_bounds__(NT, 2)
         const unsigned ph = (nchunks - 1 - c) & 1;
         lost |= !mbar_wait(&bar, ph, p.err);
         if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
-        // The last chunk's gradient stores (lanes 0..5 of warp 0, one each) must have
-        // read their staging (the S_0, v and SA slots) before the start state lands
-        // there and before the v split and SA, both after a later block barrier,
-        // overwrite the rest.  Warp 0 waits for them after the first splits.
+        // The last chunk's gradient stores must have read their staging before the
+        // start state lands in the S_0 slot (dr, dw, dk, dv: lanes 0..3 of warp 0)
+        // and before the v split and SA, both after a later block barrier, overwrite
+        // the v and SA slots (da, db: lanes 0..1 of warp 1).  Each issuing lane waits
+        // for its own store after the first splits.
         auto drain_then_load_s0 = [&]() {
+            if (warp == 1 && lane < 2) bulk_wait_read();
             if (warp == 0) {
-                if (lane < 6) bulk_wait_read();
+                if (lane < 4) bulk_wait_read();
                 __syncwarp();
                 if (lane == 0) {
                     load_s0(c);
@@ -845,13 +847,16 @@ __global__ void __launch_bounds__(NT, 2)
 
         fence_proxy_async();  // the staged tiles are read by the tensor stores
         __syncthreads();
-        if (tid < 6) {  // dr, dw, dk, dv, da, db: one tensor store per lane
-            const float *const tile = tid < 4 ? gdr + 1152 * tid : tid == 4 ? gda : gdb;
-            tma_store_rows(&omaps.m[tid], tile, h, t0, bi);
+        // one tensor store per lane: dr, dw, dk, dv from lanes 0..3 of warp 0, da, db
+        // from lanes 0..1 of warp 1 (the two warps issue theirs side by side)
+        const int o = warp == 0 ? lane : warp == 1 ? 4 + lane : 6;
+        if ((warp == 0 && lane < 4) || (warp == 1 && lane < 2)) {
+            const float *const tile = o < 4 ? gdr + 1152 * o : o == 4 ? gda : gdb;
+            tma_store_rows(&omaps.m[o], tile, h, t0, bi);
             bulk_commit();
         }
     }
-    if (tid < 6) bulk_wait_all();
+    if ((warp == 0 && lane < 4) || (warp == 1 && lane < 2)) bulk_wait_all();
     if (lost) {
         mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
         mbar_wait(&bar_s, (nchunks - 1) & 1, nullptr);
