@@ -34,6 +34,7 @@ from rwkv_linear_attention_wkv7_gb300 import synthetic  # noqa: E402
 METRIC = "WKV7 fwd+bwd tokens/sec at B=16,T=4096,H=32,N=64; % HBM roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_b16_t4096_h32"
+DECODE_WORKLOAD = "decode_b512_h32"
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 L2_BYTES = 126 * 2**20
@@ -251,6 +252,45 @@ def workload_of(args):
     return spec
 
 
+def bench_decode(wkv7, dev, stream, peak, world, steps=200, warmup=5):
+    """Batched streaming decode: B sequences advance one token per call from a
+    carried state of B*H heads, updated in place.  The state (B*H*16 KiB) is
+    larger than L2, so every call reads and writes it in HBM; the token
+    vectors cycle over the workload's T drawn sets."""
+    spec = synthetic.DECODE_WORKLOADS[DECODE_WORKLOAD]
+    d = synthetic.make_inputs(spec, device=dev)
+    toks = [[d[n][:, t].contiguous() for n in INPUTS] for t in range(spec.T)]
+    state = d["s0"]
+    del d
+    y = torch.empty((spec.B, spec.H, spec.N), device=dev)
+
+    def go(i):
+        wkv7.decode_step(*toks[i % spec.T], state, y=y, stream=stream)
+
+    for i in range(warmup):
+        go(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        go(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    es = 2 if spec.dtype == "bf16" else 4
+    heads = spec.B * spec.H
+    per_step = heads * (2 * spec.N * spec.N * 4 + 6 * spec.N * es + spec.N * 4)  # state in + out, vectors, y
+    gbs = per_step / (ms / 1e3) / 1e9
+    return {"workload": spec.name, "B": spec.B, "H": spec.H, "N": spec.N, "input_dtype": spec.dtype,
+            "tokens_per_s": world * spec.B / (ms / 1e3), "us_per_step": ms * 1e3, "steps": steps,
+            "launches": steps,
+            "roofline": {"bound": "hbm", "kernel": "wkv7 decode", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "algorithmic_bytes": per_step},
+            "l2": f"state ({heads * spec.N * spec.N * 4 / 1e6:.0f} MB) larger than L2, no flush"}
+
+
 def run_ours(args, world, rank, local):
     from rwkv_linear_attention_wkv7_gb300 import build, wkv7
     build()
@@ -426,6 +466,11 @@ def run_ours(args, world, rank, local):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "pipelined": True,
                "sequential_ms_per_step": seq_ms}
 
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(wkv7, dev, stream, peak, world)
+        wkv7.async_status()
+
     cpu = None
     if want_cpu:
         cpu, _ = cpu_baseline(spec, host_heads=host_heads)
@@ -444,6 +489,7 @@ def run_ours(args, world, rank, local):
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "decode": decode,
     }
     print(json.dumps(line), flush=True)
 
@@ -459,6 +505,7 @@ def main():
                     help="override B of the workload (smaller profiling cases of the same kernels)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

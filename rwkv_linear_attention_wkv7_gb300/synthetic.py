@@ -60,6 +60,13 @@ WORKLOADS: Dict[str, WorkloadSpec] = {
                                        w_shift=-3.0, with_dsT=True),
 }
 
+# Batched streaming decode: many sequences advance one token per call from a
+# carried state.  T here is the number of distinct token sets drawn (a decode
+# run cycles through them); s0 is the carried state.
+DECODE_WORKLOADS: Dict[str, WorkloadSpec] = {
+    "decode_b512_h32": WorkloadSpec("decode_b512_h32", 512, 8, 32, dtype="bf16", s0_std=0.1),
+}
+
 
 def _torch_dtype(name: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]

@@ -123,6 +123,31 @@ def test_decode_chain_matches_forward():
     assert parity.max_rel(state.double().cpu().numpy(), out["sT"].double().cpu().numpy()) <= parity.FWD_TOL
 
 
+def test_batched_decode_workload_sampled_heads():
+    """The batched streaming-decode workload at its full size (B=512
+    sequences, H=32, bf16 vectors, carried state): three chained decode calls
+    in the launch configuration the benchmark times, then sampled heads
+    against the oracle's decode step applied three times to the same head."""
+    spec = synthetic.DECODE_WORKLOADS["decode_b512_h32"]
+    d = synthetic.make_inputs(spec)
+    state = d["s0"].cuda()
+    y = torch.empty((spec.B, spec.H, spec.N), device="cuda")
+    ys = []
+    for t in range(3):
+        wkv7.decode_step(*(d[n][:, t].contiguous().cuda() for n in parity.INPUTS), state, y=y)
+        ys.append(y.cpu())
+    torch.cuda.synchronize()
+    g = np.random.default_rng(5)
+    for _ in range(12):
+        b, h = int(g.integers(0, spec.B)), int(g.integers(0, spec.H))
+        hs = d["s0"][b:b + 1, h:h + 1].clone()
+        for t in range(3):
+            vec = [d[n][b:b + 1, t, h:h + 1].contiguous() for n in parity.INPUTS]
+            ry, hs = oracle.decode_step(*vec, hs)  # the oracle carries its state in fp64
+            assert parity.max_rel(ys[t][b:b + 1, h:h + 1].double().numpy(), ry) <= parity.FWD_TOL
+        assert parity.max_rel(state[b:b + 1, h:h + 1].cpu().double().numpy(), hs) <= parity.FWD_TOL
+
+
 def test_autograd_function():
     """The torch.autograd wrapper routes gradients from the library."""
     spec = _custom(1, 33, 2)
