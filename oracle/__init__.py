@@ -116,6 +116,53 @@ class OracleLib:
         return y, st
 
 
+# ---- producers and backward epilogues fused into the recurrence's entry points
+# ("Foundry/cuda_kernels/timemix.cu" page: k_decay, k_composites, and their
+# backward halves k_wdecay_bwd, k_comp_keymod).  The fused calls take the
+# pre-activation of the decay, the normalised key kk and the in-context
+# learning-rate gate avec in place of (w, a, b):
+#     sigma = 1 / (1 + exp(-w_pre)),  w = exp(-DECAY * sigma)      (k_decay)
+#     a = -kk,  b = kk * avec                                          (k_composites)
+# and return their gradients in place of (dw, da, db):
+#     d w_pre = dw * w * (-DECAY) * sigma * (1 - sigma)               (k_wdecay_bwd)
+#     d kk = -da + avec * db,  d avec = kk * db                        (k_comp_keymod, the
+#         terms through a and b; its key-modulation terms belong to the model around)
+# Reading: w_pre is the whole pre-activation (the page adds a per-channel bias
+# w0 to the LoRA output before the sigmoid; the sum is the input here).
+DECAY = 0.606531  # the decay scale of k_decay (e^{-1/2})
+
+
+def producers(w_pre, kk, avec):
+    """(w, a, b, sigma) in float64 from the fused inputs."""
+    w_pre, kk, avec = map(_f64, (w_pre, kk, avec))
+    with np.errstate(over="ignore"):
+        sigma = 1.0 / (1.0 + np.exp(-w_pre))
+    return np.exp(-DECAY * sigma), -kk, kk * avec, sigma
+
+
+def epilogue(g, w, sigma, kk, avec):
+    """Gradients of the fused inputs from those of (w, a, b)."""
+    kk, avec = _f64(kk), _f64(avec)
+    return {"dr": g["dr"], "dw_pre": g["dw"] * w * (-DECAY) * sigma * (1.0 - sigma), "dk": g["dk"],
+            "dv": g["dv"], "dkk": -g["da"] + avec * g["db"], "davec": kk * g["db"], "ds0": g["ds0"]}
+
+
+def _forward_fused(orc, r, w_pre, k, v, kk, avec, s0=None, L: int = 16, want_ckpt: bool = True):
+    w, a, b, _ = producers(w_pre, kk, avec)
+    return orc.forward(r, w, k, v, a, b, s0=s0, L=L, want_ckpt=want_ckpt)
+
+
+def _backward_fused(orc, r, w_pre, k, v, kk, avec, dy, s0=None, dsT=None):
+    w, a, b, sigma = producers(w_pre, kk, avec)
+    return epilogue(orc.backward(r, w, k, v, a, b, dy, s0=s0, dsT=dsT), w, sigma, kk, avec)
+
+
+OracleLib.forward_fused = lambda self, *a, **kw: _forward_fused(self, *a, **kw)
+OracleLib.backward_fused = lambda self, *a, **kw: _backward_fused(self, *a, **kw)
+OracleLib.forward_fused.__doc__ = "Forward from (r, w_pre, k, v, kk, avec); returns (y, sT, ckpt)."
+OracleLib.backward_fused.__doc__ = ("Gradients dr, dw_pre, dk, dv, dkk, davec, ds0 of the fused inputs "
+                                    "(same arguments as backward, with w_pre, kk, avec).")
+
 _default = None
 
 
@@ -141,6 +188,14 @@ def backward(*args, **kw):
 
 def decode_step(*args, **kw):
     return lib().decode_step(*args, **kw)
+
+
+def forward_fused(*args, **kw):
+    return lib().forward_fused(*args, **kw)
+
+
+def backward_fused(*args, **kw):
+    return lib().backward_fused(*args, **kw)
 
 
 def per_head(fn, heads, threads=None):

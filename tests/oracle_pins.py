@@ -290,10 +290,99 @@ def pin_autograd_adjoint(orc):
     _close(gr["ds0"], ts0.grad.numpy(), 1e-11, "autograd ds0")
 
 
+# ------------------------------------------- fused producers and epilogues
+# The fused entry points take (r, w_pre, k, v, kk, avec): w = exp(-0.606531 sigmoid(w_pre)),
+# a = -kk, b = kk * avec ("timemix.cu" page, k_decay and k_composites).
+
+def _fused_inputs(g, B, T, H):
+    shp = (B, T, H, N)
+    r, k, v, w_pre = (g.standard_normal(shp) for _ in range(4))
+    kk = _unit(g.standard_normal(shp))
+    avec = 1.0 / (1.0 + np.exp(-g.standard_normal(shp)))
+    return dict(r=r, w_pre=w_pre, k=k, v=v, kk=kk, avec=avec)
+
+
+def pin_fused_constant_decay(orc):
+    """kk = 0 removes the rank-1 term; a constant pre-activation gives one decay
+    c for every key: sigmoid(0) = 1/2 gives c = exp(-0.606531/2), a saturated
+    sigmoid c = exp(-0.606531).  Then
+    y_t = c^{t+1} s0 r_t + sum_{s<=t} c^{t-s} v_s (k_s . r_t)."""
+    g = _rng(21)
+    B, T, H = 1, 8, 2
+    x = _fused_inputs(g, B, T, H)
+    x["kk"] = np.zeros_like(x["kk"])
+    s0 = g.standard_normal((B, H, N, N))
+    for wp, c in ((0.0, np.exp(-0.606531 / 2)), (60.0, np.exp(-0.606531))):
+        y, _, _ = orc.forward_fused(**{**x, "w_pre": np.full_like(x["r"], wp)}, s0=s0, L=3)
+        r, k, v = x["r"], x["k"], x["v"]
+        want = np.zeros_like(y)
+        for t in range(T):
+            acc = c ** (t + 1) * np.einsum("bhij,bhj->bhi", s0, r[:, t])
+            for s_ in range(t + 1):
+                acc = acc + c ** (t - s_) * v[:, s_] * np.sum(k[:, s_] * r[:, t], -1, keepdims=True)
+            want[:, t] = acc
+        _close(y, want, 1e-12, f"fused constant decay at w_pre={wp}")
+
+
+def pin_fused_delta_rule(orc):
+    """A very negative pre-activation gives w = 1.  With avec = 1 and k = kk
+    (unit) the step is the delta rule S <- S (I - kk kk^T) + v kk^T, so reading
+    with r = kk returns v_t; with avec = 0 the rank-1 term vanishes and the
+    read is causal linear attention."""
+    g = _rng(22)
+    B, T, H = 2, 6, 2
+    kk = _unit(g.standard_normal((B, T, H, N)))
+    v = g.standard_normal((B, T, H, N))
+    s0 = g.standard_normal((B, H, N, N))
+    w_pre = np.full_like(kk, -800.0)
+    y, _, _ = orc.forward_fused(kk, w_pre, kk, v, kk, np.ones_like(kk), s0=s0, L=2)
+    _close(y, v, 1e-12, "fused delta-rule read-back")
+    r, k = g.standard_normal(kk.shape), g.standard_normal(kk.shape)
+    y0, _, _ = orc.forward_fused(r, w_pre, k, v, kk, np.zeros_like(kk), L=2)
+    scores = np.einsum("bthn,bshn->bhts", r, k) * np.tril(np.ones((T, T)))
+    _close(y0, np.einsum("bhts,bshn->bthn", scores, v), 1e-12, "fused avec = 0 is linear attention")
+
+
+def _fused_loss(orc, x, s0, dy, dsT):
+    y, sT, _ = orc.forward_fused(**x, s0=s0, L=4, want_ckpt=False)
+    return float(np.sum(y * dy) + np.sum(sT * dsT))
+
+
+def pin_fused_finite_differences(orc):
+    """Central finite differences in float64 of the fused forward: every fused
+    gradient (dr, dw_pre, dk, dv, dkk, davec, ds0) at sampled coordinates,
+    relative error < 1e-5 (the difference quotient's rounding noise is about
+    1e-7 here; a wrong epilogue term is off by order 1)."""
+    g = _rng(23)
+    B, T, H = 1, 5, 1
+    x = _fused_inputs(g, B, T, H)
+    s0 = 0.5 * g.standard_normal((B, H, N, N))
+    dy = g.standard_normal(x["r"].shape)
+    dsT = g.standard_normal((B, H, N, N))
+    gr = orc.backward_fused(**x, dy=dy, s0=s0, dsT=dsT)
+    eps = 1e-6
+    for name in ("r", "w_pre", "k", "v", "kk", "avec", "s0"):
+        base = s0 if name == "s0" else x[name]
+        grad = gr["d" + name]
+        scale = float(np.abs(grad).max())
+        for idx in [tuple(int(g.integers(0, s)) for s in base.shape) for _ in range(8)]:
+            def loss_at(delta):
+                pert = base.copy()
+                pert[idx] += delta
+                if name == "s0":
+                    return _fused_loss(orc, x, pert, dy, dsT)
+                return _fused_loss(orc, {**x, name: pert}, s0, dy, dsT)
+            fd = (loss_at(eps) - loss_at(-eps)) / (2 * eps)
+            err = abs(fd - grad[idx]) / max(abs(grad[idx]), 1e-3 * scale)
+            assert err < 1e-5, f"d{name}{idx}: fd {fd:.9e} vs {grad[idx]:.9e} (rel {err:.2e})"
+
+
+FUSED_PINS = [pin_fused_constant_decay, pin_fused_delta_rule, pin_fused_finite_differences]
+
 ALL_PINS = [
     pin_linear_attention, pin_memoryless, pin_decay_only, pin_delta_rule_write,
     pin_projection_erases, pin_rank1_orientation, pin_empty_sequence,
     pin_checkpoints_are_prefix_states, pin_split_sequence, pin_decode_is_streaming,
     pin_linear_in_state_and_values, pin_adjoint_identity, pin_finite_differences,
     pin_autograd_adjoint,
-]
+] + FUSED_PINS

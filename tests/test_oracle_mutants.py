@@ -55,3 +55,66 @@ def test_some_pin_catches(mutant, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin catches the planted mistake: {name}"
+
+
+# Plausible mistakes in the fused producers and epilogues (Python side of the
+# oracle), each swapped in for the real function; some fused pin must trip.
+def _bad_producers(kind):
+    real = oracle.producers
+
+    def bad(w_pre, kk, avec):
+        w, a, b, sigma = real(w_pre, kk, avec)
+        kk64, avec64, wp = oracle._f64(kk), oracle._f64(avec), oracle._f64(w_pre)
+        if kind == "decay coefficient doubled":
+            w = w * w
+        elif kind == "sigmoid dropped":
+            w = oracle.np.exp(-oracle.DECAY * oracle.np.clip(wp, -50, 50))
+        elif kind == "a = +kk":
+            a = kk64
+        elif kind == "b ignores avec":
+            b = kk64
+        elif kind == "b = avec":
+            b = avec64
+        return w, a, b, sigma
+    return bad
+
+
+def _bad_epilogue(kind):
+    real = oracle.epilogue
+
+    def bad(g, w, sigma, kk, avec):
+        out = real(g, w, sigma, kk, avec)
+        kk64, avec64 = oracle._f64(kk), oracle._f64(avec)
+        if kind == "dw_pre without sigma(1 - sigma)":
+            out["dw_pre"] = g["dw"] * w * (-oracle.DECAY)
+        elif kind == "dkk sign of da":
+            out["dkk"] = g["da"] + avec64 * g["db"]
+        elif kind == "davec uses avec":
+            out["davec"] = avec64 * g["db"]
+        elif kind == "dkk drops db term":
+            out["dkk"] = -g["da"]
+        return out
+    return bad
+
+
+FUSED_MUTANTS = [("producers", k) for k in ("decay coefficient doubled", "sigmoid dropped", "a = +kk",
+                                            "b ignores avec", "b = avec")] + \
+                [("epilogue", k) for k in ("dw_pre without sigma(1 - sigma)", "dkk sign of da",
+                                           "davec uses avec", "dkk drops db term")]
+
+
+@pytest.mark.parametrize("mutant", FUSED_MUTANTS, ids=[m[1] for m in FUSED_MUTANTS])
+def test_some_fused_pin_catches(mutant, monkeypatch):
+    from tests.oracle_pins import FUSED_PINS
+    where, kind = mutant
+    if where == "producers":
+        monkeypatch.setattr(oracle, "producers", _bad_producers(kind))
+    else:
+        monkeypatch.setattr(oracle, "epilogue", _bad_epilogue(kind))
+    caught = []
+    for pin in FUSED_PINS:
+        try:
+            pin(oracle.lib())
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no fused pin catches the planted mistake: {kind}"
