@@ -127,6 +127,40 @@ int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype,
                      const void *v, const void *a, const void *b,
                      float *state, float *y, void *stream);
 
+/*
+ * The producers of w, a and b fused into the recurrence ("Foundry/cuda_kernels/
+ * timemix.cu" page: k_decay and k_composites in front of the WKV7 launch,
+ * k_wdecay_bwd and k_comp_keymod behind its backward).  Instead of (w, a, b)
+ * these entry points take, in the same [B][T][H][N] layout and dtype,
+ *   w_pre     the decay pre-activation:  w = exp(-0.606531 * sigmoid(w_pre))
+ *   kk        the normalised key:        a = -kk
+ *   avec      the in-context gate:       b = kk * avec
+ * and compute w, a, b as the inputs are staged, so that they never exist in
+ * HBM.  All other arguments are those of wkv7_forward / wkv7_backward.
+ * wkv7_forward_fused needs L a multiple of 16 (WKV7_EUNSUPPORTED otherwise).
+ * wkv7_backward_fused needs L == 16 and the factor cache of the matching
+ * wkv7_forward_fused call (WKV7_EINVAL otherwise, when T > 0), and writes the
+ * gradients of the fused inputs in place of (dw, da, db):
+ *   dw_pre    dw * w * (-0.606531) * s * (1 - s),  s = sigmoid(w_pre)
+ *   dkk       -da + avec * db
+ *   davec     kk * db
+ * (the terms of k_comp_keymod that pass through a and b; its key-modulation
+ * terms belong to the model around the recurrence).  dr, dk, dv and ds0 are
+ * as in wkv7_backward.
+ */
+int wkv7_forward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
+                       const void *r, const void *w_pre, const void *k,
+                       const void *v, const void *kk, const void *avec,
+                       const float *s0, float *y, float *sT, float *ckpt,
+                       float *factors, int L, void *stream);
+int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
+                        const void *r, const void *w_pre, const void *k,
+                        const void *v, const void *kk, const void *avec,
+                        const float *ckpt, const float *factors, int L,
+                        const float *dy, const float *dsT,
+                        float *dr, float *dw_pre, float *dk, float *dv, float *dkk, float *davec,
+                        float *ds0, void *stream);
+
 /* Largest B*H*ceil(T/16) that wkv7_forward_backward_noalloc accepts. */
 #define WKV7_NOALLOC_MAX_CHUNK_HEADS 4096
 

@@ -140,16 +140,21 @@ int wkv7_async_status(void) {
     return WKV7_OK;
 }
 
-int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+}  // extern "C"
+
+namespace {
+// prod = 1: w, a, b carry (w_pre, kk, avec) and the backward writes (dw_pre, dkk, davec)
+int forward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
-                 float *factors, int L, void *stream) {
+                 float *factors, int L, void *stream, int prod) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
     if (factors && L != 16) return fail(WKV7_EINVAL, "factors need L == 16 (got %d)", L);
+    if (prod && L % 16 != 0) return fail(WKV7_EUNSUPPORTED, "the fused producers need L a multiple of 16 (got %d)", L);
     const bool need = T > 0;
-    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
-    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
+    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, prod ? "w_pre" : "w", need)); TRY(check_ptr(k, "k", need));
+    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, prod ? "kk" : "a", need)); TRY(check_ptr(b, prod ? "avec" : "b", need));
     TRY(check_ptr(s0, "s0", false)); TRY(check_ptr(y, "y", need));
     TRY(check_ptr(sT, "sT", false)); TRY(check_ptr(ckpt, "ckpt", false));
     TRY(check_ptr(factors, "factors", false));
@@ -161,27 +166,30 @@ int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
     wkv7::SeqArgs p{};
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
-    p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt; p.fac = factors;
+    p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt; p.fac = factors; p.prod = prod;
     if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (wkv7::forward_chunk_supported(p)) return launch_status(wkv7::launch_forward_chunk(p, st), "wkv7_forward launch");
     return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
 }
 
-int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                   const void *v, const void *a, const void *b, const float *ckpt, const float *factors, int L,
                   const float *dy, const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db,
-                  float *ds0, void *stream) {
+                  float *ds0, void *stream, int prod) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
     if (factors && L != 16) return fail(WKV7_EINVAL, "factors need L == 16 (got %d)", L);
     const bool need = T > 0;
-    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, "w", need)); TRY(check_ptr(k, "k", need));
-    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, "a", need)); TRY(check_ptr(b, "b", need));
+    if (prod && need && (L != 16 || !factors))
+        return fail(WKV7_EINVAL, "the fused producers' backward needs L == 16 and the forward's factor cache");
+    TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, prod ? "w_pre" : "w", need)); TRY(check_ptr(k, "k", need));
+    TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, prod ? "kk" : "a", need)); TRY(check_ptr(b, prod ? "avec" : "b", need));
     TRY(check_ptr(ckpt, "ckpt", need)); TRY(check_ptr(factors, "factors", false));
     TRY(check_ptr(dy, "dy", need)); TRY(check_ptr(dsT, "dsT", false));
-    TRY(check_ptr(dr, "dr", need)); TRY(check_ptr(dw, "dw", need)); TRY(check_ptr(dk, "dk", need));
-    TRY(check_ptr(dv, "dv", need)); TRY(check_ptr(da, "da", need)); TRY(check_ptr(db, "db", need));
+    TRY(check_ptr(dr, "dr", need)); TRY(check_ptr(dw, prod ? "dw_pre" : "dw", need)); TRY(check_ptr(dk, "dk", need));
+    TRY(check_ptr(dv, "dv", need)); TRY(check_ptr(da, prod ? "dkk" : "da", need));
+    TRY(check_ptr(db, prod ? "davec" : "db", need));
     TRY(check_ptr(ds0, "ds0", false));
     TRY(check_device());
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -192,10 +200,41 @@ int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.ckpt_in = ckpt; p.fac_in = factors; p.dy = dy; p.dsT = dsT;
-    p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0;
+    p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0; p.prod = prod;
     if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (wkv7::backward_chunk_supported(p)) return launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward launch");
     return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");
+}
+}  // namespace
+
+extern "C" {
+
+int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                 const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
+                 float *factors, int L, void *stream) {
+    return forward_impl(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, ckpt, factors, L, stream, 0);
+}
+
+int wkv7_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                  const void *v, const void *a, const void *b, const float *ckpt, const float *factors, int L,
+                  const float *dy, const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                  float *ds0, void *stream) {
+    return backward_impl(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, L, dy, dsT, dr, dw, dk, dv, da, db,
+                         ds0, stream, 0);
+}
+
+int wkv7_forward_fused(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w_pre,
+                       const void *k, const void *v, const void *kk, const void *avec, const float *s0, float *y,
+                       float *sT, float *ckpt, float *factors, int L, void *stream) {
+    return forward_impl(B, T, H, N, dtype, r, w_pre, k, v, kk, avec, s0, y, sT, ckpt, factors, L, stream, 1);
+}
+
+int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w_pre,
+                        const void *k, const void *v, const void *kk, const void *avec, const float *ckpt,
+                        const float *factors, int L, const float *dy, const float *dsT, float *dr, float *dw_pre,
+                        float *dk, float *dv, float *dkk, float *davec, float *ds0, void *stream) {
+    return backward_impl(B, T, H, N, dtype, r, w_pre, k, v, kk, avec, ckpt, factors, L, dy, dsT, dr, dw_pre, dk, dv,
+                         dkk, davec, ds0, stream, 1);
 }
 
 int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,

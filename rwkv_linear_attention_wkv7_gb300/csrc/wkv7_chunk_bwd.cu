@@ -53,7 +53,7 @@ __device__ __forceinline__ float rows_sum(float x) {
 // rows rA/rB, columns 8nt+2q+{0,1}) enters as dL/dS_C and leaves as dL/dS_0.
 // Writes all six gradients of the chunk's tokens and returns, per lane, the
 // dw carry for columns jA/jB of the G3/G4 layout (w_0 o dw_0 + a_0 o da_0).
-template <typename E>
+template <typename E, bool kP>
 __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s, float *Sps, float *red,
                                 float G[8][4], int nv, const SeqArgs &p, size_t base0, size_t tstride, int t0,
                                 float &carryA, float &carryB) {
@@ -74,7 +74,7 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int j = 8 * nt + 2 * q;
-                const float a0 = ld_raw(raw, VA, u, j), a1 = ld_raw(raw, VA, u, j + 1);
+                const float a0 = in_a<kP>(raw, u, j), a1 = in_a<kP>(raw, u, j + 1);
                 sa0 = __fmaf_rn(S[nt][0], a0, __fmaf_rn(S[nt][1], a1, sa0));
                 sa1 = __fmaf_rn(S[nt][2], a0, __fmaf_rn(S[nt][3], a1, sa1));
             }
@@ -93,7 +93,7 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int j = 8 * nt + 2 * q + e;
-                    const float wv = ld_raw(raw, VW, u, j), kv = ld_raw(raw, VK, u, j), bv = ld_raw(raw, VB, u, j);
+                    const float wv = in_w<kP>(raw, u, j), kv = ld_raw(raw, VK, u, j), bv = in_b<kP>(raw, u, j);
                     S[nt][e] = __fmaf_rn(S[nt][e], wv, __fmaf_rn(sa0, bv, __fmul_rn(v0, kv)));
                     S[nt][2 + e] = __fmaf_rn(S[nt][2 + e], wv, __fmaf_rn(sa1, bv, __fmul_rn(v1, kv)));
                 }
@@ -107,7 +107,7 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int j = 8 * nt + 2 * q + e;
-                const float rv = ld_raw(raw, VR, t, j), kv = ld_raw(raw, VK, t, j), bv = ld_raw(raw, VB, t, j);
+                const float rv = ld_raw(raw, VR, t, j), kv = ld_raw(raw, VK, t, j), bv = in_b<kP>(raw, t, j);
                 G[nt][e] = __fmaf_rn(dy0, rv, G[nt][e]);
                 G[nt][2 + e] = __fmaf_rn(dy1, rv, G[nt][2 + e]);
                 dv0 = __fmaf_rn(G[nt][e], kv, dv0);
@@ -148,25 +148,42 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int j = 8 * nt + 2 * q + e;
-                const float wv = ld_raw(raw, VW, t, j), av = ld_raw(raw, VA, t, j);
+                const float wv = in_w<kP>(raw, t, j), av = in_a<kP>(raw, t, j);
                 G[nt][e] = __fmaf_rn(G[nt][e], wv, __fmul_rn(ds0, av));
                 G[nt][2 + e] = __fmaf_rn(G[nt][2 + e], wv, __fmul_rn(ds1, av));
             }
         __syncthreads();
-        float *outs[5] = {p.dr, p.dk, p.db, p.dw, p.da};
-        for (int o = tid; o < 5 * 64; o += NT) {
-            const int m = o >> 6, j = o & 63;
-            const float s = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
+        if constexpr (kP) {  // gradients of the producers' inputs: dw_pre, dkk, davec (k_wdecay_bwd, k_comp_keymod)
+            for (int j = tid; j < 64; j += NT) {
+                float s5[5];
+#pragma unroll
+                for (int m = 0; m < 5; ++m)
+                    s5[m] = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
                             red[(m * 4 + 3) * 64 + j];
-            outs[m][base0 + (size_t)(t0 + t) * tstride + j] = s;
+                const size_t o = base0 + (size_t)(t0 + t) * tstride + j;
+                const float sg = sigmoid_f(ld_raw(raw, VW, t, j)), kkv = ld_raw(raw, VA, t, j), avv = ld_raw(raw, VB, t, j);
+                p.dr[o] = s5[0];
+                p.dk[o] = s5[1];
+                p.db[o] = kkv * s5[2];
+                p.dw[o] = s5[3] * in_w<kP>(raw, t, j) * (-kDecayScale) * sg * (1.f - sg);
+                p.da[o] = avv * s5[2] - s5[4];
+            }
+        } else {
+            float *outs[5] = {p.dr, p.dk, p.db, p.dw, p.da};
+            for (int o = tid; o < 5 * 64; o += NT) {
+                const int m = o >> 6, j = o & 63;
+                const float s = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
+                                red[(m * 4 + 3) * 64 + j];
+                outs[m][base0 + (size_t)(t0 + t) * tstride + j] = s;
+            }
         }
         if (t == 0) {  // dw carry into the previous chunk: w_0 o dw_0 + a_0 o da_0
             const int jA = warp * 16 + g, jB = jA + 8;
             float cA = 0.f, cB = 0.f;
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {
-                cA += ld_raw(raw, VW, 0, jA) * red[(3 * 4 + w4) * 64 + jA] + ld_raw(raw, VA, 0, jA) * red[(4 * 4 + w4) * 64 + jA];
-                cB += ld_raw(raw, VW, 0, jB) * red[(3 * 4 + w4) * 64 + jB] + ld_raw(raw, VA, 0, jB) * red[(4 * 4 + w4) * 64 + jB];
+                cA += in_w<kP>(raw, 0, jA) * red[(3 * 4 + w4) * 64 + jA] + in_a<kP>(raw, 0, jA) * red[(4 * 4 + w4) * 64 + jA];
+                cB += in_w<kP>(raw, 0, jB) * red[(3 * 4 + w4) * 64 + jB] + in_a<kP>(raw, 0, jB) * red[(4 * 4 + w4) * 64 + jB];
             }
             carryA = cA;
             carryB = cB;
@@ -255,7 +272,11 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // kFac: the per-chunk factors (W, M_k', Q', W Q_b, SA) come from the
 // forward's factor cache, prefetched into the [Q'; W Q_b] slot, instead of
 // being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
-template <typename E, bool kFac>
+// kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec; see
+// in_w) and dw, da, db receive their gradients dw_pre, dkk, davec; the staged
+// rows are read once more by that epilogue, so the next chunk's copies are
+// issued at the chunk end.
+template <typename E, bool kFac, bool kP>
 __global__ void __launch_bounds__(NT, 2)
     wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
     // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
@@ -372,11 +393,11 @@ __global__ void __launch_bounds__(NT, 2)
             }
         };
         // the cumulative decays on warps 2 and 3, clear of warp 0's copies
-        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv, 64));
+        const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 64));
         if (exact) {
             drain_then_load_s0();
             lost |= !mbar_wait(&bar_s, ph, p.err);
-            bwd_chunk_exact<E>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
+            bwd_chunk_exact<E, kP>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
             fence_proxy_async();  // the per-token path wrote into slots the copies refill
             __syncthreads();
@@ -400,9 +421,9 @@ __global__ void __launch_bounds__(NT, 2)
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
-            st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(ld_raw4(raw, VB, t, j), id));
+            st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(in_b4<kP>(raw, t, j), id));
             st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
-            st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
+            st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(in_a4<kP>(raw, t, j), dp));
             st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
         }
 #pragma unroll
@@ -648,9 +669,9 @@ __global__ void __launch_bounds__(NT, 2)
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
         if (c > 0) {  // this chunk's inputs, dy and factors are consumed: fetch the previous chunk's
-            stage_in(c - 1);
+            if (!kP) stage_in(c - 1);
             stage_fac(c - 1);
-            if (tid == 0) mbar_arrive(&bar);
+            if (!kP && tid == 0) mbar_arrive(&bar);
         }
 
         // G3: [DR | DA] (rows = key index j = rA / rB)
@@ -808,9 +829,15 @@ __global__ void __launch_bounds__(NT, 2)
                     ee[nt][m] = av[vi] * xa;
                     zz[nt][m] = rv[vi] * xr + ee[nt][m] - bv[vi] * xb - kv[vi] * xk;
                     gdr[t * OS + row] = d * xr;
-                    gda[t * OS + row] = dp * xa;
                     gdk[t * OS + row] = inv * xk;
-                    gdb[t * OS + row] = inv * xb;
+                    if constexpr (kP) {  // dkk = -da + avec db, davec = kk db (k_comp_keymod)
+                        const float db_ = inv * xb;
+                        gda[t * OS + row] = ld_raw(raw, VB, t, row) * db_ - dp * xa;
+                        gdb[t * OS + row] = ld_raw(raw, VA, t, row) * db_;
+                    } else {
+                        gda[t * OS + row] = dp * xa;
+                        gdb[t * OS + row] = inv * xb;
+                    }
                 }
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
@@ -838,7 +865,12 @@ __global__ void __launch_bounds__(NT, 2)
                     const int t = tv[m];
                     const float d = dd[t * DS + row];
                     const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
-                    gdw[t * OS + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
+                    if constexpr (kP) {  // dw_pre = (w o dw) (-0.606531) sigmoid (1 - sigmoid) (k_wdecay_bwd)
+                        const float sg = sigmoid_f(ld_raw(raw, VW, t, row));
+                        gdw[t * OS + row] = (Sv[m] - ev[m]) * (-kDecayScale * sg * (1.f - sg));
+                    } else {
+                        gdw[t * OS + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
+                    }
                 }
                 const float total = __shfl_sync(kFull, S0v, 0, 4);
                 if (hr) carryB = total; else carryA = total;
@@ -847,6 +879,10 @@ __global__ void __launch_bounds__(NT, 2)
 
         fence_proxy_async();  // the staged tiles are read by the tensor stores
         __syncthreads();
+        if (kP && c > 0) {  // the epilogue has read this chunk's staged inputs
+            stage_in(c - 1);
+            if (tid == 0) mbar_arrive(&bar);
+        }
         // one tensor store per lane: dr, dw, dk, dv from lanes 0..3 of warp 0, da, db
         // from lanes 0..1 of warp 1 (the two warps issue theirs side by side)
         const int o = warp == 0 ? lane : warp == 1 ? 4 + lane : 6;
@@ -870,7 +906,7 @@ __global__ void __launch_bounds__(NT, 2)
     }
 }
 
-template <typename E, bool kFac>
+template <typename E, bool kFac, bool kP>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
     InputMaps maps;
@@ -879,9 +915,9 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     if (e == cudaSuccess) e = encode_ckpt_map(&maps.m[7], p.ckpt_in, (long long)p.B * p.H * p.nck * 64, 64);
     if (e == cudaSuccess) e = encode_output_maps(&omaps, p);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac, kP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E, kFac><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
+    wkv7_bwd_chunk_kernel<E, kFac, kP><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
     return cudaGetLastError();
 }
 
@@ -890,8 +926,12 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 bool backward_chunk_supported(const SeqArgs &p) { return p.L == C; }
 
 cudaError_t launch_backward_chunk(const SeqArgs &p, cudaStream_t st) {
-    if (p.fac_in) return p.dtype == 1 ? launch_t<__nv_bfloat16, true>(p, st) : launch_t<float, true>(p, st);
-    return p.dtype == 1 ? launch_t<__nv_bfloat16, false>(p, st) : launch_t<float, false>(p, st);
+    if (p.prod) {  // the fused producers run with the factor cache only
+        if (!p.fac_in) return cudaErrorInvalidValue;
+        return p.dtype == 1 ? launch_t<__nv_bfloat16, true, true>(p, st) : launch_t<float, true, true>(p, st);
+    }
+    if (p.fac_in) return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false>(p, st) : launch_t<float, true, false>(p, st);
+    return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false>(p, st) : launch_t<float, false, false>(p, st);
 }
 
 }  // namespace wkv7

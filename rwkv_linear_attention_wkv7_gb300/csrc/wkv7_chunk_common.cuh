@@ -142,6 +142,27 @@ __device__ __forceinline__ float ld_raw<__nv_bfloat16>(const __nv_bfloat16 *raw,
     return __bfloat162float(raw[(vec * C + t) * RS + j]);
 }
 
+// The recurrence's w, a and b at (t, j) from the staged rows.  With kP the
+// staged w, a and b rows hold the producers' inputs ("timemix.cu" page,
+// k_decay and k_composites): w = exp(-0.606531 sigmoid(w_pre)), a = -kk,
+// b = kk * avec.
+constexpr float kDecayScale = 0.606531f;
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+template <bool kP, typename E>
+__device__ __forceinline__ float in_w(const E *raw, int t, int j) {
+    const float x = ld_raw(raw, VW, t, j);
+    return kP ? expf(-kDecayScale * sigmoid_f(x)) : x;
+}
+template <bool kP, typename E>
+__device__ __forceinline__ float in_a(const E *raw, int t, int j) {
+    const float x = ld_raw(raw, VA, t, j);
+    return kP ? -x : x;
+}
+template <bool kP, typename E>
+__device__ __forceinline__ float in_b(const E *raw, int t, int j) {
+    return kP ? ld_raw(raw, VA, t, j) * ld_raw(raw, VB, t, j) : ld_raw(raw, VB, t, j);
+}
+
 // Elements j .. j + 3 (j % 4 == 0) of a staged row as one 64/128-bit load.
 template <typename E>
 __device__ __forceinline__ float4 ld_raw4(const E *raw, int vec, int t, int j);
@@ -237,6 +258,16 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 __device__ __forceinline__ float4 mul4(float4 a, float4 b) { return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w); }
+// a and b at (t, j .. j + 3), as in_a / in_b
+template <bool kP, typename E>
+__device__ __forceinline__ float4 in_a4(const E *raw, int t, int j) {
+    const float4 x = ld_raw4(raw, VA, t, j);
+    return kP ? make_float4(-x.x, -x.y, -x.z, -x.w) : x;
+}
+template <bool kP, typename E>
+__device__ __forceinline__ float4 in_b4(const E *raw, int t, int j) {
+    return kP ? mul4(ld_raw4(raw, VA, t, j), ld_raw4(raw, VB, t, j)) : ld_raw4(raw, VB, t, j);
+}
 __device__ __forceinline__ float4 rcp4(float4 a) {
     return make_float4(rcp_approx(a.x), rcp_approx(a.y), rcp_approx(a.z), rcp_approx(a.w));
 }
@@ -246,7 +277,7 @@ __device__ __forceinline__ float4 rcp4(float4 a) {
 // Returns true (on the calling thread) when some d_t of its column leaves
 // [1e-20, 1e20] (or is not finite): the factorised form then cannot divide
 // by d_t and the chunk takes the exact per-token path.
-template <typename E>
+template <bool kP, typename E>
 __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0) {
     bool bad = false;
     const int j = (int)threadIdx.x - first_thread;
@@ -254,7 +285,7 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int 
         // all loads first: the product chain then runs at FMUL latency
         float wv[C];
 #pragma unroll
-        for (int t = 0; t < C; ++t) wv[t] = t < nv ? ld_raw(raw, VW, t, j) : 1.f;
+        for (int t = 0; t < C; ++t) wv[t] = t < nv ? in_w<kP>(raw, t, j) : 1.f;
         float dc = 1.f;
 #pragma unroll
         for (int t = 0; t < C; ++t) {

@@ -73,7 +73,8 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + 16 * MS;
 }
 
-template <typename E>
+// kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec); see in_w.
+template <typename E, bool kP>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ __align__(128) unsigned char smem[];
     // bf16 inputs: v is exact in bf16, so products with v as the A operand skip its (zero) lo part
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
 
         float *const fc = p.fac ? p.fac + ((size_t)bh * nchunks + c) * fac::kWords : nullptr;
         // the cumulative decays on warps 2 and 3 (thread 0 has just issued the y store)
-        const bool exact = __syncthreads_or(prep_decay(raw, dd, nv, 64));
+        const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 64));
         if (!exact) {
             // ---- split the decay-scaled vectors and v once: [t][j] quads
 #pragma unroll
@@ -152,9 +153,9 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
                 const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
                 const float4 id = rcp4(d);
-                st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, mul4(ld_raw4(raw, VB, t, j), id));
+                st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, mul4(in_b4<kP>(raw, t, j), id));
                 st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
-                st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, mul4(ld_raw4(raw, VA, t, j), dp));
+                st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, mul4(in_a4<kP>(raw, t, j), dp));
                 st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
                 if (kVLo) st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
             }
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
                     const int j = 8 * nt + 2 * q;
-                    const float a0 = ld_raw(raw, VA, t, j), a1 = ld_raw(raw, VA, t, j + 1);
+                    const float a0 = in_a<kP>(raw, t, j), a1 = in_a<kP>(raw, t, j + 1);
                     sa0 = __fmaf_rn(S[nt][0], a0, __fmaf_rn(S[nt][1], a1, sa0));
                     sa1 = __fmaf_rn(S[nt][2], a0, __fmaf_rn(S[nt][3], a1, sa1));
                 }
@@ -339,8 +340,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int j = 8 * nt + 2 * q + e;
-                        const float wv = ld_raw(raw, VW, t, j), kv = ld_raw(raw, VK, t, j);
-                        const float bv = ld_raw(raw, VB, t, j), rv = ld_raw(raw, VR, t, j);
+                        const float wv = in_w<kP>(raw, t, j), kv = ld_raw(raw, VK, t, j);
+                        const float bv = in_b<kP>(raw, t, j), rv = ld_raw(raw, VR, t, j);
                         S[nt][e] = __fmaf_rn(S[nt][e], wv, __fmaf_rn(sa0, bv, __fmul_rn(v0, kv)));
                         S[nt][2 + e] = __fmaf_rn(S[nt][2 + e], wv, __fmaf_rn(sa1, bv, __fmul_rn(v1, kv)));
                         y0 = __fmaf_rn(S[nt][e], rv, y0);
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     }
 }
 
-template <typename E>
+template <typename E, bool kP>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = fwd_smem_bytes<E>();
     InputMaps maps;  // six inputs, and y (box OS) in the last slot
@@ -386,9 +387,9 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     if (e == cudaSuccess) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
     if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_fwd_chunk_kernel<E><<<p.B * p.H, NT, sm, st>>>(p, maps);
+    wkv7_fwd_chunk_kernel<E, kP><<<p.B * p.H, NT, sm, st>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -397,7 +398,8 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 bool forward_chunk_supported(const SeqArgs &p) { return p.L % C == 0; }
 
 cudaError_t launch_forward_chunk(const SeqArgs &p, cudaStream_t st) {
-    return p.dtype == 1 ? launch_t<__nv_bfloat16>(p, st) : launch_t<float>(p, st);
+    if (p.prod) return p.dtype == 1 ? launch_t<__nv_bfloat16, true>(p, st) : launch_t<float, true>(p, st);
+    return p.dtype == 1 ? launch_t<__nv_bfloat16, false>(p, st) : launch_t<float, false>(p, st);
 }
 
 }  // namespace wkv7

@@ -22,6 +22,10 @@ struct SeqArgs {
     const float *fac_in;  // factor cache from the forward, or NULL (recomputed)
     float *dr, *dw, *dk, *dv, *da, *db, *ds0;
     unsigned *err;  // device flag a kernel sets when a bounded wait on its copies times out
+    // 1: the inputs w, a, b hold the producers' inputs w_pre, kk, avec (w = exp(-0.606531
+    // sigmoid(w_pre)), a = -kk, b = kk * avec) and the backward writes the gradients of
+    // those (dw_pre, dkk, davec) into dw, da, db
+    int prod;
 };
 
 // Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the

@@ -72,10 +72,12 @@ def _torch_dtype(name: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
 
 
-def stream_inputs(spec: WorkloadSpec) -> Iterator[Tuple[str, Optional[torch.Tensor]]]:
+def stream_inputs(spec: WorkloadSpec, fused: bool = False) -> Iterator[Tuple[str, Optional[torch.Tensor]]]:
     """Yield (name, CPU tensor) in a fixed order, holding few tensors at once.
 
-    Names: r, k, v, a, b, w, s0, dy, dsT (s0 / dsT may be None).
+    Names: r, k, v, a, b, w, s0, dy, dsT (s0 / dsT may be None).  With
+    ``fused`` the same draws come out before the producers: kk, avec and
+    w_pre in place of a, b and w (the inputs of the fused entry points).
     """
     g = torch.Generator().manual_seed(spec.seed)
     shape = (spec.B, spec.T, spec.H, spec.N)
@@ -91,13 +93,20 @@ def stream_inputs(spec: WorkloadSpec) -> Iterator[Tuple[str, Optional[torch.Tens
     kk = torch.randn(shape, generator=g)
     kk = kk / (kk.norm(dim=-1, keepdim=True) + 1e-12)
     gate = torch.sigmoid(torch.randn(shape, generator=g))
-    yield "a", cast(-kk)
-    yield "b", cast(kk * gate)
+    if fused:
+        yield "kk", cast(kk)
+        yield "avec", cast(gate)
+    else:
+        yield "a", cast(-kk)
+        yield "b", cast(kk * gate)
     del kk, gate
     w_raw = torch.randn(shape, generator=g)
     if spec.w_shift:
         w_raw += spec.w_shift
-    yield "w", cast(torch.exp(-DECAY_COEFF * torch.sigmoid(w_raw)))
+    if fused:
+        yield "w_pre", cast(w_raw)
+    else:
+        yield "w", cast(torch.exp(-DECAY_COEFF * torch.sigmoid(w_raw)))
     del w_raw
     s0 = torch.randn(sshape, generator=g) * spec.s0_std
     yield "s0", s0 if spec.s0_std > 0 else None
@@ -106,10 +115,10 @@ def stream_inputs(spec: WorkloadSpec) -> Iterator[Tuple[str, Optional[torch.Tens
     yield "dsT", dsT if spec.with_dsT else None
 
 
-def make_inputs(spec: WorkloadSpec, device: str = "cpu") -> Dict[str, Optional[torch.Tensor]]:
+def make_inputs(spec: WorkloadSpec, device: str = "cpu", fused: bool = False) -> Dict[str, Optional[torch.Tensor]]:
     """All inputs of ``spec`` as a dict, moved to ``device`` one by one."""
     out = {}
-    for name, t in stream_inputs(spec):
+    for name, t in stream_inputs(spec, fused=fused):
         out[name] = None if t is None else t.to(device)
     return out
 

@@ -48,6 +48,10 @@ def lib() -> ctypes.CDLL:
         L.wkv7_forward.restype = ci
         L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci, fp, fp] + [fp] * 7 + [vp]
         L.wkv7_backward.restype = ci
+        L.wkv7_forward_fused.argtypes = L.wkv7_forward.argtypes
+        L.wkv7_forward_fused.restype = ci
+        L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
+        L.wkv7_backward_fused.restype = ci
         L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
         L.wkv7_decode_step.restype = ci
         L.wkv7_async_status.argtypes = []
@@ -121,7 +125,8 @@ def factor_floats(T: int) -> int:
 
 
 def forward(r, w, k, v, a, b, s0=None, L: int = 16, want_ckpt: bool = True, want_sT: bool = True,
-            want_factors: bool = False, out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+            want_factors: bool = False, out: Optional[Dict[str, torch.Tensor]] = None, stream=None,
+            _entry: str = "wkv7_forward"):
     """Run the recurrence over [B][T][H][64] inputs.
 
     Returns (y, sT, ckpt), or (y, sT, ckpt, factors) with ``want_factors``
@@ -148,9 +153,9 @@ def forward(r, w, k, v, a, b, s0=None, L: int = 16, want_ckpt: bool = True, want
         _f32(fac, (B, H, nf), dev, "factors")
     _f32(y, (B, T, H, N), dev, "y")
     _f32(s0, sshape, dev, "s0")
-    rc = lib().wkv7_forward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(y), _ptr(sT), _ptr(ck),
-                            _ptr(fac), L, _stream(stream))
-    _check("wkv7_forward", rc)
+    rc = getattr(lib(), _entry)(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(y), _ptr(sT), _ptr(ck),
+                                _ptr(fac), L, _stream(stream))
+    _check(_entry, rc)
     return (y, sT, ck, fac) if want_factors else (y, sT, ck)
 
 
@@ -158,7 +163,8 @@ GRAD_NAMES = ("dr", "dw", "dk", "dv", "da", "db")
 
 
 def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool = True, factors=None,
-             out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+             out: Optional[Dict[str, torch.Tensor]] = None, stream=None, _entry: str = "wkv7_backward",
+             _names=None) -> Dict[str, torch.Tensor]:
     """Gradients of sum(y*dy) + sum(sT*dsT) w.r.t. r, w, k, v, a, b and s0.
 
     ``factors`` is the cache of the forward call that wrote ``ckpt`` (or None
@@ -168,17 +174,37 @@ def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool =
     B, T, H, N = r.shape
     dev = r.device
     out = out or {}
-    g = {n: out.get(n) if out.get(n) is not None else torch.empty((B, T, H, N), device=dev) for n in GRAD_NAMES}
+    names = _names or GRAD_NAMES
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty((B, T, H, N), device=dev) for n in names}
     g["ds0"] = (out.get("ds0") if out.get("ds0") is not None else torch.empty((B, H, N, N), device=dev)) if want_ds0 else None
     _f32(dy, (B, T, H, N), dev, "dy")
     _f32(dsT, (B, H, N, N), dev, "dsT")
     if factors is not None:
         _f32(factors, (B, H, factor_floats(T)), dev, "factors")
-    rc = lib().wkv7_backward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), _ptr(factors), L,
-                             _ptr(dy), _ptr(dsT),
-                             *(_ptr(g[n]) for n in GRAD_NAMES), _ptr(g["ds0"]), _stream(stream))
-    _check("wkv7_backward", rc)
+    rc = getattr(lib(), _entry)(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), _ptr(factors), L,
+                                _ptr(dy), _ptr(dsT),
+                                *(_ptr(g[n]) for n in names), _ptr(g["ds0"]), _stream(stream))
+    _check(_entry, rc)
     return g
+
+
+FUSED_GRAD_NAMES = ("dr", "dw_pre", "dk", "dv", "dkk", "davec")
+
+
+def forward_fused(r, w_pre, k, v, kk, avec, s0=None, L: int = 16, want_ckpt: bool = True, want_sT: bool = True,
+                  want_factors: bool = False, out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    """``forward`` with the producers of w, a, b fused in: w = exp(-0.606531 sigmoid(w_pre)),
+    a = -kk, b = kk * avec (computed as the inputs are staged).  Needs L % 16 == 0."""
+    return forward(r, w_pre, k, v, kk, avec, s0=s0, L=L, want_ckpt=want_ckpt, want_sT=want_sT,
+                   want_factors=want_factors, out=out, stream=stream, _entry="wkv7_forward_fused")
+
+
+def backward_fused(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool = True, factors=None,
+                   out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Gradients dr, dw_pre, dk, dv, dkk, davec (and ds0) of the fused inputs; needs L == 16 and
+    the factor cache of the matching ``forward_fused`` call."""
+    return backward(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=dsT, L=L, want_ds0=want_ds0, factors=factors,
+                    out=out, stream=stream, _entry="wkv7_backward_fused", _names=FUSED_GRAD_NAMES)
 
 
 def decode_step(r, w, k, v, a, b, state, y=None, stream=None):

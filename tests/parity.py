@@ -19,6 +19,9 @@ FWD_TOL = 2e-4
 GRAD_TOL = 1e-3
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
+# the fused entry points' inputs and gradients (producers computed inside)
+INPUTS_FUSED = ("r", "w_pre", "k", "v", "kk", "avec")
+GRADS_FUSED = ("dr", "dw_pre", "dk", "dv", "dkk", "davec")
 STATE_KEYS = ("s0", "dsT", "sT", "ds0", "ckpt")
 
 
@@ -26,11 +29,11 @@ def to_dev(x, dev="cuda"):
     return None if x is None else x.to(dev).contiguous()
 
 
-def inputs_on_device(spec, heads=None, dev="cuda"):
+def inputs_on_device(spec, heads=None, dev="cuda", fused=False):
     """Draw ``spec``'s inputs, move each to the GPU as soon as it is drawn and
     keep on the host only the slices of ``heads`` (all heads if None)."""
     dev_in, host = {}, {}
-    for name, t in synthetic.stream_inputs(spec):
+    for name, t in synthetic.stream_inputs(spec, fused=fused):
         if t is None:
             dev_in[name] = None
             continue
@@ -43,12 +46,23 @@ def inputs_on_device(spec, heads=None, dev="cuda"):
     return dev_in, host
 
 
-def run_gpu(d, L=16, backward=True, factors=None):
+def run_gpu(d, L=16, backward=True, factors=None, fused=False):
     """Forward (+ backward) through the C ABI on device inputs ``d``; outputs stay on the device.
 
     ``factors``: pass the forward's per-chunk factor cache to the backward
-    (the training path); default: whenever L == 16, the stride it needs."""
+    (the training path); default: whenever L == 16, the stride it needs.
+    ``fused``: the entry points with the producers fused in (inputs
+    INPUTS_FUSED, gradients GRADS_FUSED)."""
     use_fac = (L == 16) if factors is None else factors
+    if fused:
+        res = wkv7.forward_fused(*(d[n] for n in INPUTS_FUSED), s0=d.get("s0"), L=L, want_factors=use_fac)
+        out = {"y": res[0], "sT": res[1], "ckpt": res[2]}
+        if backward:
+            out.update(wkv7.backward_fused(*(d[n] for n in INPUTS_FUSED), res[2], d["dy"], dsT=d.get("dsT"), L=L,
+                                           factors=res[3] if use_fac else None))
+        torch.cuda.synchronize()
+        wkv7.async_status()
+        return out
     res = wkv7.forward(*(d[n] for n in INPUTS), s0=d.get("s0"), L=L, want_factors=use_fac)
     y, sT, ck = res[:3]
     fac = res[3] if use_fac else None
@@ -69,13 +83,15 @@ def _head_input(host, name, b, h):
     return synthetic.head_slice(x, b, h, state=name in STATE_KEYS)
 
 
-def oracle_head(host, b, h, L=16, backward=True):
+def oracle_head(host, b, h, L=16, backward=True, fused=False):
     """Oracle results for head (b, h) only, float64 numpy in B=H=1 shapes."""
-    sl = {n: _head_input(host, n, b, h) for n in INPUTS + ("s0", "dy", "dsT")}
-    y, sT, ck = oracle.forward(*(sl[n] for n in INPUTS), s0=sl["s0"], L=L)
+    names = INPUTS_FUSED if fused else INPUTS
+    fwd, bwd = (oracle.forward_fused, oracle.backward_fused) if fused else (oracle.forward, oracle.backward)
+    sl = {n: _head_input(host, n, b, h) for n in names + ("s0", "dy", "dsT")}
+    y, sT, ck = fwd(*(sl[n] for n in names), s0=sl["s0"], L=L)
     res = {"y": y, "sT": sT, "ckpt": ck}
     if backward:
-        res.update(oracle.backward(*(sl[n] for n in INPUTS), sl["dy"], s0=sl["s0"], dsT=sl["dsT"]))
+        res.update(bwd(*(sl[n] for n in names), sl["dy"], s0=sl["s0"], dsT=sl["dsT"]))
     return res
 
 
@@ -104,7 +120,7 @@ def fro_rel(got, ref):
     return num / den if den > 0 else num
 
 
-def compare(gpu, ref, backward=True, what=""):
+def compare(gpu, ref, backward=True, what="", grads=GRADS):
     """Assert the tolerances; return the measured errors."""
     errs = {}
     for k in ("y", "sT", "ckpt"):
@@ -112,19 +128,21 @@ def compare(gpu, ref, backward=True, what=""):
             errs[k] = max_rel(gpu[k], ref[k])
             assert errs[k] <= FWD_TOL, f"{what} {k}: max err {errs[k]:.3e} x max|ref| > {FWD_TOL}"
     if backward:
-        for k in GRADS + ("ds0",):
+        for k in grads + ("ds0",):
             if k in gpu:
                 errs[k] = fro_rel(gpu[k], ref[k])
                 assert errs[k] <= GRAD_TOL, f"{what} {k}: rel Frobenius {errs[k]:.3e} > {GRAD_TOL}"
     return errs
 
 
-def check_heads(host, out, heads, L=16, backward=True, threads=None):
+def check_heads(host, out, heads, L=16, backward=True, threads=None, fused=False):
     """Oracle the given heads in parallel and compare each with the GPU result."""
-    refs = oracle.per_head(lambda b, h: oracle_head(host, b, h, L=L, backward=backward), heads, threads)
+    refs = oracle.per_head(lambda b, h: oracle_head(host, b, h, L=L, backward=backward, fused=fused), heads,
+                           threads)
     worst = {}
     for (b, h), ref in zip(heads, refs):
-        e = compare(gpu_head(out, b, h), ref, backward=backward, what=f"head (b={b}, h={h})")
+        e = compare(gpu_head(out, b, h), ref, backward=backward, what=f"head (b={b}, h={h})",
+                    grads=GRADS_FUSED if fused else GRADS)
         for k, v in e.items():
             worst[k] = max(worst.get(k, 0.0), v)
     return worst

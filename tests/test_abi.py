@@ -34,7 +34,7 @@ def lib():
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
-                     "wkv7_async_status", "wkv7_last_error"):
+                     "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused"):
         assert required in names
 
 
@@ -95,6 +95,23 @@ def test_backward_rejects_bad_arguments(lib):
     bad = list(args)
     bad[12], bad[13] = p, 8  # factors with a stride other than 16
     assert lib.wkv7_backward(*bad) == EINVAL and "L == 16" in wkv7.last_error()
+
+
+def test_fused_entry_points_reject_bad_arguments(lib):
+    """The fused producers run on the chunked path only: the forward needs L a
+    multiple of 16, the backward L == 16 and the forward's factor cache."""
+    p = ctypes.c_void_p(4096)
+    assert lib.wkv7_forward_fused(1, 4, 1, 64, 0, *([p] * 6), None, p, None, None, None, 8, None) == EUNSUPPORTED
+    assert "multiple of 16" in wkv7.last_error()
+    assert lib.wkv7_forward_fused(1, 4, 1, 64, 0, p, None, *([p] * 4), None, p, None, None, None, 16, None) == EINVAL
+    assert "w_pre is NULL" in wkv7.last_error()
+    args = [1, 4, 1, 64, 0] + [p] * 6 + [p, p, 16, p, None] + [p] * 6 + [None, None]
+    bad = list(args)
+    bad[12] = None  # no factor cache
+    assert lib.wkv7_backward_fused(*bad) == EINVAL and "factor cache" in wkv7.last_error()
+    bad = list(args)
+    bad[21] = None  # davec missing
+    assert lib.wkv7_backward_fused(*bad) == EINVAL and "davec is NULL" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

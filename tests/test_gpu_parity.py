@@ -204,3 +204,49 @@ def test_forward_paths_agree():
     torch.cuda.synchronize()
     assert parity.max_rel(y1.double().cpu().numpy(), y2.double().cpu().numpy()) <= parity.FWD_TOL
     assert parity.max_rel(s1.double().cpu().numpy(), s2.double().cpu().numpy()) <= parity.FWD_TOL
+
+
+# ---- the producers fused into the entry points (w_pre, kk, avec in; dw_pre, dkk, davec out)
+
+@pytest.mark.parametrize("name", SMALL)
+def test_fused_small_workloads_all_heads(name):
+    """Every head of the small workloads through the fused entry points:
+    forward (y, sT, checkpoints) and the gradients of the fused inputs."""
+    spec = synthetic.WORKLOADS[name]
+    d, host = parity.inputs_on_device(spec, fused=True)
+    out = parity.run_gpu(d, L=16, fused=True)
+    worst = parity.check_heads(host, out, parity.all_heads(spec.B, spec.H), L=16, fused=True)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+@pytest.mark.parametrize("T", [1, 15, 17, 130])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_ragged_lengths(T, dtype):
+    """Ragged lengths (partial chunks) with an initial state and dsT, fused path;
+    a saturating decay pre-activation shift exercises w near exp(-0.606531)."""
+    spec = synthetic.WorkloadSpec("custom", 2, T, 3, dtype=dtype, s0_std=0.1, with_dsT=True, seed=4, w_shift=2.0)
+    d, host = parity.inputs_on_device(spec, fused=True)
+    out = parity.run_gpu(d, L=16, fused=True)
+    parity.check_heads(host, out, parity.all_heads(2, 3), L=16, fused=True)
+
+
+def test_fused_forward_longer_stride():
+    """The fused forward with checkpoint stride 32 (a multiple of the chunk)."""
+    spec = synthetic.WorkloadSpec("custom", 1, 100, 2, s0_std=0.1, seed=6)
+    d, host = parity.inputs_on_device(spec, fused=True)
+    out = parity.run_gpu(d, L=32, backward=False, factors=False, fused=True)
+    assert out["ckpt"].shape[2] == 4
+    parity.check_heads(host, out, parity.all_heads(1, 2), L=32, backward=False, fused=True)
+
+
+@pytest.mark.slow
+def test_fused_full_size_sampled_heads():
+    """The fused entry points on the full-size bf16 workload (B=16, T=4096,
+    H=32), sampled heads recomputed by the oracle over all T."""
+    spec = synthetic.WORKLOADS["bf16_b16_t4096_h32"]
+    heads = parity.sample_heads(spec.B, spec.H, n=4)
+    d, host = parity.inputs_on_device(spec, heads=heads, fused=True)
+    out = parity.run_gpu(d, L=16, fused=True)
+    for k in ("y", "sT") + parity.GRADS_FUSED + ("ds0",):
+        assert bool(torch.isfinite(out[k]).all()), k
+    parity.check_heads(host, out, heads, L=16, fused=True)
