@@ -466,6 +466,57 @@ def run_ours(args, world, rank, local):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "pipelined": True,
                "sequential_ms_per_step": seq_ms}
 
+    # the producers fused into the entry points: the same step through
+    # wkv7_forward_fused / wkv7_backward_fused on the same draws taken before the
+    # producers (w_pre, kk, avec in place of w, a, b; same bytes per element)
+    fused = None
+    if not args.no_fused and use_fac:
+        fz = {}
+        for name, t in synthetic.stream_inputs(spec, fused=True):
+            if name in ("w_pre", "kk", "avec"):
+                fz[name] = t.to(dev)
+            del t
+        fx = [d["r"], fz["w_pre"], d["k"], d["v"], fz["kk"], fz["avec"]]
+        fg = {fn: gouts[gn] for fn, gn in zip(wkv7.FUSED_GRAD_NAMES, GRADS)}
+        fg["ds0"] = gouts["ds0"]
+        fev = []
+
+        def fstep(record=False):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if record else None
+            if record:
+                e[0].record(stream)
+            wkv7.forward_fused(*fx, s0=d["s0"], L=spec.L, want_factors=True, out=outs, stream=stream)
+            if record:
+                e[1].record(stream)
+            wkv7.backward_fused(*fx, outs["ckpt"], d["dy"], dsT=d["dsT"], L=spec.L, factors=outs["factors"],
+                                out=fg, stream=stream)
+            if record:
+                e[2].record(stream)
+                fev.append(e)
+
+        for _ in range(args.warmup):
+            fstep()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fstep(record=True)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        wkv7.async_status()
+        f_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
+        ff = statistics.mean(a.elapsed_time(b) for a, b, _ in fev)
+        fb = statistics.mean(b.elapsed_time(c) for _, b, c in fev)
+        fused = {"ms_per_step": f_ms, "tokens_per_s": world * spec.tokens / (f_ms / 1e3), "forward_ms": ff,
+                 "backward_ms": fb, "launches": 2 * args.steps,
+                 "roofline": {"bound": "hbm", "kernel": "wkv7 backward (fused producers)",
+                              "achieved": bwd_bytes / (fb / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                              "frac": bwd_bytes / (fb / 1e3) / 1e9 / peak, "algorithmic_bytes": bwd_bytes},
+                 "inputs": "r, w_pre, k, v, kk, avec (w, a, b computed in the kernels)"}
+        del fz, fx
+
     decode = None
     if not args.no_decode:
         decode = bench_decode(wkv7, dev, stream, peak, world)
@@ -489,7 +540,7 @@ def run_ours(args, world, rank, local):
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks,
-        "decode": decode,
+        "fused": fused, "decode": decode,
     }
     print(json.dumps(line), flush=True)
 
@@ -506,6 +557,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused-producer measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

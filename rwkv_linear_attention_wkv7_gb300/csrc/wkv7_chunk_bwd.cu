@@ -273,9 +273,11 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // forward's factor cache, prefetched into the [Q'; W Q_b] slot, instead of
 // being rebuilt from the Gram (no Gram, inverse, A' or G1 in this mode).
 // kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec; see
-// in_w) and dw, da, db receive their gradients dw_pre, dkk, davec; the staged
-// rows are read once more by that epilogue, so the next chunk's copies are
-// issued at the chunk end.
+// in_w) and dw, da, db receive their gradients dw_pre, dkk, davec.  That
+// epilogue runs after the staged rows are refilled: it takes kk from the a^
+// split (a^ = -kk d_{t-1}), the sigmoid from the decays (w_t = d_t / d_{t-1},
+// sigmoid = -ln(w_t) / 0.606531) and avec from a copy the split phase keeps in
+// the Gram / W slots, which the factor-cache path does not use otherwise.
 template <typename E, bool kFac, bool kP>
 __global__ void __launch_bounds__(NT, 2)
     wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
@@ -286,6 +288,9 @@ __global__ void __launch_bounds__(NT, 2)
     unsigned char *Bs = smem + raw_bytes<E>();
     float *dyf = reinterpret_cast<float *>(Bs + B_DYF), *dd = reinterpret_cast<float *>(Bs + B_DD);
     float *Gm = reinterpret_cast<float *>(Bs + B_G), *Wm = reinterpret_cast<float *>(Bs + B_W);
+    // kP: avec of the chunk, fp32 [C][OS], past the 256 floats the last chunk's dw carry uses
+    float *const avs = Gm + 256;
+    static_assert(256 * 4 + C * OS * 4 <= C * SP * 4 + 1280, "avec copy fits the Gram and W slots");
     float *S0f = reinterpret_cast<float *>(Bs + B_SX);
     const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, B_BT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, B_AH, 16),
              RH = hl(Bs, B_RH, 16), VM = hl(Bs, B_VV, 16), DYH = hl(Bs, B_DYH, 16), SAH = hl(Bs, B_SAH, 16),
@@ -422,6 +427,7 @@ __global__ void __launch_bounds__(NT, 2)
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
             st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(in_b4<kP>(raw, t, j), id));
+            if constexpr (kP) *reinterpret_cast<float4 *>(avs + t * OS + j) = ld_raw4(raw, VB, t, j);
             st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
             st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(in_a4<kP>(raw, t, j), dp));
             st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
@@ -669,9 +675,9 @@ __global__ void __launch_bounds__(NT, 2)
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         __syncthreads();
         if (c > 0) {  // this chunk's inputs, dy and factors are consumed: fetch the previous chunk's
-            if (!kP) stage_in(c - 1);
+            stage_in(c - 1);
             stage_fac(c - 1);
-            if (!kP && tid == 0) mbar_arrive(&bar);
+            if (tid == 0) mbar_arrive(&bar);
         }
 
         // G3: [DR | DA] (rows = key index j = rA / rB)
@@ -832,8 +838,8 @@ __global__ void __launch_bounds__(NT, 2)
                     gdk[t * OS + row] = inv * xk;
                     if constexpr (kP) {  // dkk = -da + avec db, davec = kk db (k_comp_keymod)
                         const float db_ = inv * xb;
-                        gda[t * OS + row] = ld_raw(raw, VB, t, row) * db_ - dp * xa;
-                        gdb[t * OS + row] = ld_raw(raw, VA, t, row) * db_;
+                        gda[t * OS + row] = avs[t * OS + row] * db_ - dp * xa;
+                        gdb[t * OS + row] = -av[vi] * rcp_approx(dp) * db_;
                     } else {
                         gda[t * OS + row] = dp * xa;
                         gdb[t * OS + row] = inv * xb;
@@ -866,7 +872,7 @@ __global__ void __launch_bounds__(NT, 2)
                     const float d = dd[t * DS + row];
                     const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
                     if constexpr (kP) {  // dw_pre = (w o dw) (-0.606531) sigmoid (1 - sigmoid) (k_wdecay_bwd)
-                        const float sg = sigmoid_f(ld_raw(raw, VW, t, row));
+                        const float sg = -__logf(d * rcp_approx(dp)) * (1.f / kDecayScale);
                         gdw[t * OS + row] = (Sv[m] - ev[m]) * (-kDecayScale * sg * (1.f - sg));
                     } else {
                         gdw[t * OS + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
@@ -879,10 +885,6 @@ __global__ void __launch_bounds__(NT, 2)
 
         fence_proxy_async();  // the staged tiles are read by the tensor stores
         __syncthreads();
-        if (kP && c > 0) {  // the epilogue has read this chunk's staged inputs
-            stage_in(c - 1);
-            if (tid == 0) mbar_arrive(&bar);
-        }
         // one tensor store per lane: dr, dw, dk, dv from lanes 0..3 of warp 0, da, db
         // from lanes 0..1 of warp 1 (the two warps issue theirs side by side)
         const int o = warp == 0 ? lane : warp == 1 ? 4 + lane : 6;

@@ -114,6 +114,13 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int row)
                  "r"(0), "r"(row)
                  : "memory");
 }
+// The same box into L2 only (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap *map, int h, int t0, int b) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(0), "r"(h), "r"(t0), "r"(b)
+                 : "memory");
+}
 // 2-D tensor store: box at (column 0, row `row`).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int row) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
@@ -146,12 +153,16 @@ __device__ __forceinline__ float ld_raw<__nv_bfloat16>(const __nv_bfloat16 *raw,
 // staged w, a and b rows hold the producers' inputs ("timemix.cu" page,
 // k_decay and k_composites): w = exp(-0.606531 sigmoid(w_pre)), a = -kk,
 // b = kk * avec.
+// The hardware exponential and reciprocal (__expf, __fdividef: a few ulp,
+// about 3e-7 relative here, far below the split-bf16 product error) keep
+// these off the per-chunk decay chain's critical path; the forward and the
+// backward evaluate the same expressions, so both see the same decays.
 constexpr float kDecayScale = 0.606531f;
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 template <bool kP, typename E>
 __device__ __forceinline__ float in_w(const E *raw, int t, int j) {
     const float x = ld_raw(raw, VW, t, j);
-    return kP ? expf(-kDecayScale * sigmoid_f(x)) : x;
+    return kP ? __expf(-kDecayScale * sigmoid_f(x)) : x;
 }
 template <bool kP, typename E>
 __device__ __forceinline__ float in_a(const E *raw, int t, int j) {
