@@ -509,7 +509,38 @@ def run_ours(args, world, rank, local):
         f_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
         ff = statistics.mean(a.elapsed_time(b) for a, b, _ in fev)
         fb = statistics.mean(b.elapsed_time(c) for _, b, c in fev)
+        # the same step with the producers and epilogues as separate elementwise
+        # passes around the plain entry points (torch ops writing w, a, b to HBM
+        # and reading the plain gradients back), for comparison
+        dt_in = d["r"].dtype
+
+        def ustep():
+            sig = torch.sigmoid(fz["w_pre"].float())
+            w = torch.exp(-synthetic.DECAY_COEFF * sig)
+            kk32 = fz["kk"].float()
+            a, b = (-kk32).to(dt_in), (kk32 * fz["avec"].float()).to(dt_in)
+            wkv7.forward(d["r"], w.to(dt_in), d["k"], d["v"], a, b, s0=d["s0"], L=spec.L, want_factors=True,
+                         out=outs, stream=stream)
+            gg = wkv7.backward(d["r"], w.to(dt_in), d["k"], d["v"], a, b, outs["ckpt"], d["dy"], dsT=d["dsT"],
+                               L=spec.L, factors=outs["factors"], out=gouts, stream=stream)
+            gw = gg["dw"] * w * (-synthetic.DECAY_COEFF) * sig * (1.0 - sig)
+            gk = -gg["da"] + fz["avec"].float() * gg["db"]
+            ga = kk32 * gg["db"]
+            return gw, gk, ga
+
+        for _ in range(args.warmup):
+            ustep()
+        torch.cuda.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_u = max(3, args.steps // 10)
+        u0.record(stream)
+        for _ in range(n_u):
+            ustep()
+        u1.record(stream)
+        torch.cuda.synchronize()
+        u_ms = max_over_ranks(u0.elapsed_time(u1), world) / n_u
         fused = {"ms_per_step": f_ms, "tokens_per_s": world * spec.tokens / (f_ms / 1e3), "forward_ms": ff,
+                 "separate_producers_ms_per_step": u_ms,
                  "backward_ms": fb, "launches": 2 * args.steps,
                  "roofline": {"bound": "hbm", "kernel": "wkv7 backward (fused producers)",
                               "achieved": bwd_bytes / (fb / 1e3) / 1e9, "peak": peak, "unit": "GB/s",

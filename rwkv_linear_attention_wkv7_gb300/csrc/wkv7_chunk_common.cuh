@@ -283,14 +283,39 @@ __device__ __forceinline__ float4 rcp4(float4 a) {
     return make_float4(rcp_approx(a.x), rcp_approx(a.y), rcp_approx(a.z), rcp_approx(a.w));
 }
 
-// d_t per key column (threads first_thread .. first_thread + 63); padding
-// tokens (t >= nv) decay by 1.
+// d_t per key column (threads first_thread .. first_thread + 63; with the
+// fused producers all 128 threads, two per key); padding tokens (t >= nv)
+// decay by 1.
 // Returns true (on the calling thread) when some d_t of its column leaves
 // [1e-20, 1e20] (or is not finite): the factorised form then cannot divide
 // by d_t and the chunk takes the exact per-token path.
 template <bool kP, typename E>
 __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0) {
     bool bad = false;
+    if constexpr (kP) {
+        // the producers' exponentials on all four warps: warp w holds keys
+        // 16w..16w+15, lanes 0-15 tokens 0..7 and lanes 16-31 tokens 8..15 of key
+        // 16w + lane % 16; the second half continues from the first half's
+        // product with one shuffle (first_thread is not used)
+        const int lane = threadIdx.x & 31, j = 16 * (threadIdx.x >> 5) + (lane & 15), t0 = 8 * (lane >> 4);
+        float wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = t0 + u < nv ? in_w<true>(raw, t0 + u, j) : 1.f;
+        float dl[8], dc = 1.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            dc = __fmul_rn(dc, wv[u]);
+            dl[u] = dc;
+        }
+        const float head = __shfl_sync(0xffffffffu, dc, lane & 15);  // d_7 of the key
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float d = lane >= 16 ? __fmul_rn(dl[u], head) : dl[u];
+            dd[(t0 + u) * DS + j] = d;
+            bad |= !(d >= kTiny && d <= 1.f / kTiny);
+        }
+        return bad;
+    }
     const int j = (int)threadIdx.x - first_thread;
     if (j >= 0 && j < 64) {
         // all loads first: the product chain then runs at FMUL latency
