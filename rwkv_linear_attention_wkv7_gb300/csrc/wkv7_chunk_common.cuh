@@ -114,13 +114,6 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int row)
                  "r"(0), "r"(row)
                  : "memory");
 }
-// The same box into L2 only (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap *map, int h, int t0, int b) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(0), "r"(h), "r"(t0), "r"(b)
-                 : "memory");
-}
 // 2-D tensor store: box at (column 0, row `row`).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int row) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(
