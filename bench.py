@@ -35,6 +35,8 @@ METRIC = "WKV7 fwd+bwd tokens/sec at B=16,T=4096,H=32,N=64; % HBM roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_b16_t4096_h32"
 DECODE_WORKLOAD = "decode_b512_h32"
+TIMESPLIT_WORKLOAD = "long_b1_t65536_h8"
+TIMESPLIT_SEGMENTS = 32
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 L2_BYTES = 126 * 2**20
@@ -289,6 +291,61 @@ def bench_decode(wkv7, dev, stream, peak, world, steps=200, warmup=5):
             "roofline": {"bound": "hbm", "kernel": "wkv7 decode", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "algorithmic_bytes": per_step},
             "l2": f"state ({heads * spec.N * spec.N * 4 / 1e6:.0f} MB) larger than L2, no flush"}
+
+
+def bench_timesplit(wkv7, dev, stream, peak, world, steps=3, warmup=1):
+    """Few, long sequences (8 heads of 65536 tokens): the plain entry points
+    (one thread block per head) against the time-split ones (each sequence in
+    TIMESPLIT_SEGMENTS segments side by side), fwd+bwd per step, with the
+    largest relative difference between the two results."""
+    spec = synthetic.TIMESPLIT_WORKLOADS[TIMESPLIT_WORKLOAD]
+    d = synthetic.make_inputs(spec, device=dev)
+    xs = [d[n] for n in INPUTS]
+    B, T, H, N = spec.B, spec.T, spec.H, spec.N
+    nseg = TIMESPLIT_SEGMENTS
+    outs = {"y": torch.empty((B, T, H, N), device=dev), "sT": torch.empty((B, H, N, N), device=dev),
+            "ckpt": torch.empty((B, H, wkv7.ckpt_count(T, 16), N, N), device=dev),
+            "factors": torch.empty((B, H, wkv7.factor_floats(T)), device=dev)}
+    g_plain = {n: torch.empty((B, T, H, N), device=dev) for n in GRADS}
+    g_plain["ds0"] = torch.empty((B, H, N, N), device=dev)
+    ws = torch.empty(wkv7.timesplit_workspace_floats(B, T, H, nseg), device=dev)
+    so = {"y": torch.empty((B, T, H, N), device=dev), "sT": torch.empty((B, H, N, N), device=dev)}
+    g_split = {n: torch.empty_like(v) for n, v in g_plain.items()}
+
+    def plain():
+        wkv7.forward(*xs, s0=d["s0"], L=16, want_factors=True, out=outs, stream=stream)
+        wkv7.backward(*xs, outs["ckpt"], d["dy"], dsT=d["dsT"], L=16, factors=outs["factors"], out=g_plain,
+                      stream=stream)
+
+    def split():
+        wkv7.forward_timesplit(*xs, s0=d["s0"], nseg=nseg, workspace=ws, out=so, stream=stream)
+        wkv7.backward_timesplit(*xs, d["dy"], dsT=d["dsT"], nseg=nseg, workspace=ws, out=g_split, stream=stream)
+
+    res = {}
+    for name, fn in (("plain", plain), ("split", split)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    wkv7.async_status()
+
+    def rel(a, b):
+        return float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+    diff = max([rel(so["y"], outs["y"]), rel(so["sT"], outs["sT"])] + [rel(g_split[n], g_plain[n]) for n in g_plain])
+    fwd_b, bwd_b = algorithmic_bytes(spec)
+    gbs = (fwd_b + bwd_b) / (res["split"] / 1e3) / 1e9
+    return {"workload": spec.name, "B": B, "T": T, "H": H, "input_dtype": spec.dtype, "segments": nseg,
+            "plain_ms_per_step": res["plain"], "split_ms_per_step": res["split"],
+            "plain_tokens_per_s": world * spec.tokens / (res["plain"] / 1e3),
+            "split_tokens_per_s": world * spec.tokens / (res["split"] / 1e3),
+            "split_hbm_fraction_step": gbs / peak, "max_rel_diff_split_vs_plain": diff, "steps": steps}
 
 
 def run_ours(args, world, rank, local):
@@ -548,6 +605,10 @@ def run_ours(args, world, rank, local):
                  "inputs": "r, w_pre, k, v, kk, avec (w, a, b computed in the kernels)"}
         del fz, fx
 
+    timesplit = None
+    if not args.no_timesplit:
+        timesplit = bench_timesplit(wkv7, dev, stream, peak, world)
+
     decode = None
     if not args.no_decode:
         decode = bench_decode(wkv7, dev, stream, peak, world)
@@ -571,7 +632,7 @@ def run_ours(args, world, rank, local):
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks,
-        "fused": fused, "decode": decode,
+        "fused": fused, "decode": decode, "timesplit": timesplit,
     }
     print(json.dumps(line), flush=True)
 
@@ -589,6 +650,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused-producer measurement")
+    ap.add_argument("--no-timesplit", action="store_true", help="skip the time-split measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

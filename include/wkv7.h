@@ -161,6 +161,44 @@ int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
                         float *dr, float *dw_pre, float *dk, float *dv, float *dkk, float *davec,
                         float *ds0, void *stream);
 
+/*
+ * Sequence parallelism inside one GPU for few, long sequences.  The pages
+ * give the recurrence one thread block per (b, h) over all T tokens; these
+ * entry points (which have no counterpart there) cut every sequence into
+ * nseg equal segments that run side by side, using that the recurrence is
+ * affine in the state a segment starts from (S_end = S_start M + Z, M the
+ * product of the segment's transitions diag(w_t) + a_t b_t^T):
+ *   forward   every segment from I with v = 0 (gives M) and from 0 (gives
+ *             Z), a scan S_{k+1} = S_k M_k + Z_k over each head's segments,
+ *             then every segment from its start state (y, and checkpoints
+ *             and factors kept in the workspace);
+ *   backward  every segment with no gradient at its end (gives D_k, what it
+ *             sends to its start), a reverse scan G_{k-1} = D_k + G_k M_k^T
+ *             from G = dsT, then every segment with G_k at its end.
+ * It does about three forwards' and two backwards' work, and pays off when
+ * B*H is small next to the GPU's thread-block slots.
+ *   nseg       segments per sequence; T must be a multiple of 16 * nseg.
+ *   workspace  device buffer of wkv7_timesplit_workspace_floats(B, T, H,
+ *              nseg) floats, 16-byte aligned, owned by the caller; the
+ *              backward reads what the matching forward left there, so pass
+ *              the same buffer, untouched in between, with the same inputs.
+ * Other arguments as in wkv7_forward / wkv7_backward (y required when T > 0,
+ * checkpoint stride 16 internally).  Errors as there; WKV7_EINVAL also for a
+ * bad nseg, T not a multiple of 16 * nseg, or a missing workspace.
+ */
+long long wkv7_timesplit_workspace_floats(int B, int T, int H, int nseg);
+int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype,
+                           const void *r, const void *w, const void *k,
+                           const void *v, const void *a, const void *b,
+                           const float *s0, float *y, float *sT,
+                           int nseg, float *workspace, void *stream);
+int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype,
+                            const void *r, const void *w, const void *k,
+                            const void *v, const void *a, const void *b,
+                            const float *dy, const float *dsT,
+                            float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                            float *ds0, int nseg, float *workspace, void *stream);
+
 /* Largest B*H*ceil(T/16) that wkv7_forward_backward_noalloc accepts. */
 #define WKV7_NOALLOC_MAX_CHUNK_HEADS 4096
 

@@ -1,0 +1,223 @@
+// Sequence parallelism inside one GPU: each (b, h) sequence of T tokens is cut
+// into nseg equal segments that run side by side as extra batch rows.
+//
+// Over a segment the recurrence is affine in its start state: with P_t =
+// diag(w_t) + a_t b_t^T, S_end = S_start M + Z where M = P_1 ... P_L (the end
+// state from S_start = I with v = 0) and Z is the end state from S_start = 0.
+// The [B][T][H][N] inputs read as [B*nseg][T/nseg][H][N] make every segment
+// an independent batch row, so:
+//   forward: (1) all segments from S_start = I with v = 0  -> M,
+//            (2) all segments from S_start = 0              -> Z,
+//            (3) a scan over the segments of each head, S_{k+1} = S_k M_k + Z_k,
+//            (4) all segments from their true start states -> y, checkpoints, factors;
+//   backward (the adjoint of the same decomposition, with D_k = the gradient a
+//   segment sends to its start state when nothing arrives at its end):
+//            (1) all segments with no gradient at their end -> D,
+//            (2) a reverse scan, G_{k-1} = D_k + G_k M_k^T from G_last = dsT,
+//            (3) all segments with G_k arriving at their end -> the gradients.
+// This is for few, long sequences (B*H small next to the GPU's CTA slots); it
+// does about three times the forward work and twice the backward work.
+#include <cstdio>
+
+#include <cuda_runtime.h>
+
+#include "wkv7.h"
+#include "wkv7_internal.cuh"
+
+namespace {
+
+constexpr int kN = 64;
+constexpr int kThreads = 256;  // thread (rg, cg) owns rows 4rg..4rg+3, columns 4cg..4cg+3
+constexpr int kPad = kN + 4;   // shared row stride (floats)
+
+__device__ __forceinline__ size_t seg_off(int b, int k, int h, int nseg, int H) {
+    return (((size_t)b * nseg + k) * H + h) * kN * kN;
+}
+
+// Per head (b, h): forward (kBack = false)
+//   S_0 = init or 0;  for k = 0 .. nseg-1: out_k = S_k, S_{k+1} = C_k + S_k M_k;  fin = S_nseg
+// backward (kBack = true)
+//   G = init or 0;  for k = nseg-1 .. 0: out_k = G, G = C_k + G M_k^T;  fin = G
+// (C = Z forward, D backward).  init / fin are [B][H][N][N] (either may be
+// NULL); M, C, out are [B][nseg][H][N][N].
+template <bool kBack>
+__global__ void __launch_bounds__(kThreads) wkv7_segment_scan_kernel(int H, int nseg, const float *__restrict__ M,
+                                                                     const float *__restrict__ Cadd,
+                                                                     const float *__restrict__ init,
+                                                                     float *__restrict__ out, float *__restrict__ fin) {
+    __shared__ __align__(16) float S[kN * kPad];
+    __shared__ __align__(16) float R[kN * kPad];
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int rg = threadIdx.x >> 4, cg = threadIdx.x & 15;
+    const size_t head = (size_t)bh * kN * kN;
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 x = init ? *reinterpret_cast<const float4 *>(init + head + (4 * rg + i) * kN + 4 * cg)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[i][0] = x.x; acc[i][1] = x.y; acc[i][2] = x.z; acc[i][3] = x.w;
+    }
+    for (int step = 0; step < nseg; ++step) {
+        const int k = kBack ? nseg - 1 - step : step;
+        const size_t o = seg_off(b, k, h, nseg, H);
+        // publish the current state / gradient, write it out, stage this step's right factor
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 x = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            *reinterpret_cast<float4 *>(S + (4 * rg + i) * kPad + 4 * cg) = x;
+            *reinterpret_cast<float4 *>(out + o + (4 * rg + i) * kN + 4 * cg) = x;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = 4 * rg + i;
+            const float4 mm = *reinterpret_cast<const float4 *>(M + o + row * kN + 4 * cg);
+            const float m[4] = {mm.x, mm.y, mm.z, mm.w};
+            if (kBack) {  // R = M^T
+#pragma unroll
+                for (int j = 0; j < 4; ++j) R[(4 * cg + j) * kPad + row] = m[j];
+            } else {
+                *reinterpret_cast<float4 *>(R + row * kPad + 4 * cg) = make_float4(m[0], m[1], m[2], m[3]);
+            }
+            // the additive term at this thread's block
+            const float4 c = *reinterpret_cast<const float4 *>(Cadd + o + row * kN + 4 * cg);
+            acc[i][0] = c.x; acc[i][1] = c.y; acc[i][2] = c.z; acc[i][3] = c.w;
+        }
+        __syncthreads();
+        for (int m = 0; m < kN; ++m) {
+            const float4 r = *reinterpret_cast<const float4 *>(R + m * kPad + 4 * cg);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float s = S[(4 * rg + i) * kPad + m];
+                acc[i][0] = __fmaf_rn(s, r.x, acc[i][0]);
+                acc[i][1] = __fmaf_rn(s, r.y, acc[i][1]);
+                acc[i][2] = __fmaf_rn(s, r.z, acc[i][2]);
+                acc[i][3] = __fmaf_rn(s, r.w, acc[i][3]);
+            }
+        }
+        __syncthreads();  // S and R are rewritten by the next step
+    }
+    if (fin) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4 *>(fin + head + (4 * rg + i) * kN + 4 * cg) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    }
+}
+
+// n identity matrices [n][N][N]
+__global__ void wkv7_identity_kernel(float *dst, size_t n) {
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= n * kN * kN) return;
+    const int rc = (int)(e % (kN * kN));
+    dst[e] = (rc / kN == rc % kN) ? 1.f : 0.f;
+}
+
+struct Workspace {
+    float *M, *Z, *starts, *D, *G, *ident, *zero_v, *ckpt, *fac;
+};
+
+long long state_floats(int B, int H, int nseg) { return (long long)B * nseg * H * kN * kN; }
+
+Workspace carve(float *ws, int B, int T, int H, int nseg) {
+    const long long s = state_floats(B, H, nseg);
+    const int tseg = T / nseg;
+    Workspace w;
+    w.M = ws;
+    w.Z = w.M + s;
+    w.starts = w.Z + s;
+    w.D = w.starts + s;
+    w.G = w.D + s;
+    w.ident = w.G + s;
+    w.zero_v = w.ident + s;  // B*T*H*N floats: room for a zero v of either dtype
+    w.ckpt = w.zero_v + (long long)B * T * H * kN;
+    w.fac = w.ckpt + (long long)B * nseg * H * wkv7_ckpt_count(tseg, 16) * kN * kN;
+    return w;
+}
+
+int check_split(int B, int T, int H, int nseg, const float *ws) {
+    if (B < 1 || H < 1 || T < 0) return wkv7::set_error(WKV7_EINVAL, "B, H must be >= 1 and T >= 0");
+    if (nseg < 1) return wkv7::set_error(WKV7_EINVAL, "nseg must be >= 1");
+    if (T % (16 * nseg) != 0) return wkv7::set_error(WKV7_EINVAL, "T must be a multiple of 16 * nseg");
+    if ((long long)B * nseg * H > 0x7fffffffLL) return wkv7::set_error(WKV7_EINVAL, "B * nseg * H too large");
+    if (T > 0 && !ws) return wkv7::set_error(WKV7_EINVAL, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 15u) return wkv7::set_error(WKV7_EINVAL, "workspace is not 16-byte aligned");
+    return WKV7_OK;
+}
+
+int cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return WKV7_OK;
+    char msg[160];
+    snprintf(msg, sizeof msg, "%s: %s", what, cudaGetErrorString(e));
+    return wkv7::set_error(WKV7_ECUDA, msg);
+}
+
+}  // namespace
+
+extern "C" {
+
+long long wkv7_timesplit_workspace_floats(int B, int T, int H, int nseg) {
+    if (B < 1 || H < 1 || T < 0 || nseg < 1 || T % (16 * nseg) != 0) return -1;
+    const int tseg = T / nseg;
+    const long long s = state_floats(B, H, nseg);
+    return 6 * s + (long long)B * T * H * kN + (long long)B * nseg * H * wkv7_ckpt_count(tseg, 16) * kN * kN +
+           (long long)B * nseg * H * wkv7_factor_floats(tseg);
+}
+
+int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
+                           const void *k, const void *v, const void *a, const void *b, const float *s0, float *y,
+                           float *sT, int nseg, float *workspace, void *stream) {
+    int rc = check_split(B, T, H, nseg, workspace);
+    if (rc != WKV7_OK) return rc;
+    if (T == 0) return wkv7_forward(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, nullptr, nullptr, 16, stream);
+    const int bs = B * nseg, tseg = T / nseg;
+    const Workspace ws = carve(workspace, B, T, H, nseg);
+    if (nseg == 1)  // one segment: the plain call, keeping its checkpoints and factors for the backward
+        return wkv7_forward(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, ws.ckpt, ws.fac, 16, stream);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long s = state_floats(B, H, nseg);
+    const size_t nmat = (size_t)bs * H;
+    wkv7_identity_kernel<<<(unsigned)((s + 255) / 256), 256, 0, st>>>(ws.ident, nmat);
+    if ((rc = cuda_status(cudaGetLastError(), "identity launch")) != WKV7_OK) return rc;
+    const size_t vbytes = (size_t)B * T * H * kN * (dtype == WKV7_BF16 ? 2 : 4);
+    if ((rc = cuda_status(cudaMemsetAsync(ws.zero_v, 0, vbytes, st), "zero v")) != WKV7_OK) return rc;
+    // (1) from I with v = 0 and (2) from 0: y is scratch here, written for real by (4)
+    if ((rc = wkv7_forward(bs, tseg, H, N, dtype, r, w, k, ws.zero_v, a, b, ws.ident, y, ws.M, nullptr, nullptr, 16,
+                           stream)))
+        return rc;
+    if ((rc = wkv7_forward(bs, tseg, H, N, dtype, r, w, k, v, a, b, nullptr, y, ws.Z, nullptr, nullptr, 16, stream)))
+        return rc;
+    // (3) segment start states, and the final state
+    wkv7_segment_scan_kernel<false><<<B * H, kThreads, 0, st>>>(H, nseg, ws.M, ws.Z, s0, ws.starts, sT);
+    if ((rc = cuda_status(cudaGetLastError(), "segment scan launch")) != WKV7_OK) return rc;
+    // (4) every segment from its start state; checkpoints and factors for the backward
+    return wkv7_forward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.starts, y, nullptr, ws.ckpt, ws.fac, 16, stream);
+}
+
+int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
+                            const void *k, const void *v, const void *a, const void *b, const float *dy,
+                            const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                            float *ds0, int nseg, float *workspace, void *stream) {
+    int rc = check_split(B, T, H, nseg, workspace);
+    if (rc != WKV7_OK) return rc;
+    if (T == 0) return wkv7_backward(B, 0, H, N, dtype, r, w, k, v, a, b, nullptr, nullptr, 16, dy, dsT, dr, dw, dk,
+                                     dv, da, db, ds0, stream);
+    const int bs = B * nseg, tseg = T / nseg;
+    const Workspace ws = carve(workspace, B, T, H, nseg);
+    if (nseg == 1)
+        return wkv7_backward(B, T, H, N, dtype, r, w, k, v, a, b, ws.ckpt, ws.fac, 16, dy, dsT, dr, dw, dk, dv, da, db,
+                             ds0, stream);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // (1) no gradient arriving at the segment ends: D = what each segment sends to its start
+    if ((rc = wkv7_backward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.ckpt, ws.fac, 16, dy, nullptr, dr, dw, dk, dv,
+                            da, db, ws.D, stream)))
+        return rc;
+    // (2) the gradient arriving at every segment's end, and ds0
+    wkv7_segment_scan_kernel<true><<<B * H, kThreads, 0, st>>>(H, nseg, ws.M, ws.D, dsT, ws.G, ds0);
+    if ((rc = cuda_status(cudaGetLastError(), "segment scan launch")) != WKV7_OK) return rc;
+    // (3) the gradients, each segment with its arriving gradient (its own ds0 is not needed)
+    return wkv7_backward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.ckpt, ws.fac, 16, dy, ws.G, dr, dw, dk, dv, da,
+                         db, ws.starts, stream);
+}
+
+}  // extern "C"

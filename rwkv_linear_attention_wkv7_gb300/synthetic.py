@@ -67,6 +67,12 @@ DECODE_WORKLOADS: Dict[str, WorkloadSpec] = {
     "decode_b512_h32": WorkloadSpec("decode_b512_h32", 512, 8, 32, dtype="bf16", s0_std=0.1),
 }
 
+# Few, long sequences: B*H = 8 heads of 65536 tokens (the time-split entry
+# points' case: one thread block per head would leave the GPU nearly idle).
+TIMESPLIT_WORKLOADS: Dict[str, WorkloadSpec] = {
+    "long_b1_t65536_h8": WorkloadSpec("long_b1_t65536_h8", 1, 65536, 8, dtype="bf16", s0_std=0.1, with_dsT=True),
+}
+
 
 def _torch_dtype(name: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]

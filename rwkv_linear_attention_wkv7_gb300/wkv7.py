@@ -48,6 +48,12 @@ def lib() -> ctypes.CDLL:
         L.wkv7_forward.restype = ci
         L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci, fp, fp] + [fp] * 7 + [vp]
         L.wkv7_backward.restype = ci
+        L.wkv7_timesplit_workspace_floats.argtypes = [ci, ci, ci, ci]
+        L.wkv7_timesplit_workspace_floats.restype = ctypes.c_longlong
+        L.wkv7_forward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, ci, fp, vp]
+        L.wkv7_forward_timesplit.restype = ci
+        L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
+        L.wkv7_backward_timesplit.restype = ci
         L.wkv7_forward_fused.argtypes = L.wkv7_forward.argtypes
         L.wkv7_forward_fused.restype = ci
         L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
@@ -205,6 +211,52 @@ def backward_fused(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=None, L: int = 16, wa
     the factor cache of the matching ``forward_fused`` call."""
     return backward(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=dsT, L=L, want_ds0=want_ds0, factors=factors,
                     out=out, stream=stream, _entry="wkv7_backward_fused", _names=FUSED_GRAD_NAMES)
+
+
+def timesplit_workspace_floats(B: int, T: int, H: int, nseg: int) -> int:
+    return lib().wkv7_timesplit_workspace_floats(B, T, H, nseg)
+
+
+def forward_timesplit(r, w, k, v, a, b, s0=None, nseg: int = 1, workspace=None,
+                      out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    """Forward with every sequence cut into ``nseg`` segments run side by side
+    (T a multiple of 16 * nseg).  Returns (y, sT, workspace); pass the workspace
+    to ``backward_timesplit`` with the same inputs."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+    nws = timesplit_workspace_floats(B, T, H, nseg)
+    if nws < 0:
+        raise ValueError(f"T={T} is not a multiple of 16 * nseg (nseg={nseg})")
+    ws = workspace if workspace is not None else torch.empty(max(nws, 1), device=dev)
+    y = out.get("y") if out.get("y") is not None else torch.empty((B, T, H, N), device=dev)
+    sT = out.get("sT") if out.get("sT") is not None else torch.empty((B, H, N, N), device=dev)
+    _f32(s0, (B, H, N, N), dev, "s0")
+    rc = lib().wkv7_forward_timesplit(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(y), _ptr(sT), nseg,
+                                      _ptr(ws), _stream(stream))
+    _check("wkv7_forward_timesplit", rc)
+    return y, sT, ws
+
+
+def backward_timesplit(r, w, k, v, a, b, dy, dsT=None, nseg: int = 1, workspace=None,
+                       out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Gradients (as ``backward``) from the workspace of the matching ``forward_timesplit``."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty((B, T, H, N), device=dev) for n in GRAD_NAMES}
+    g["ds0"] = out.get("ds0") if out.get("ds0") is not None else torch.empty((B, H, N, N), device=dev)
+    _f32(dy, (B, T, H, N), dev, "dy")
+    _f32(dsT, (B, H, N, N), dev, "dsT")
+    rc = lib().wkv7_backward_timesplit(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(dy), _ptr(dsT),
+                                       *(_ptr(g[n]) for n in GRAD_NAMES), _ptr(g["ds0"]), nseg, _ptr(workspace),
+                                       _stream(stream))
+    _check("wkv7_backward_timesplit", rc)
+    return g
 
 
 def decode_step(r, w, k, v, a, b, state, y=None, stream=None):
