@@ -68,7 +68,8 @@ def load_peaks():
 
 def load_traffic():
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the kernels as they are now (source hash recorded with it)."""
+    on the chunked kernels as they are now (the hash of their source files is
+    recorded with it)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return {}
@@ -78,7 +79,7 @@ def load_traffic():
     except ValueError:
         return {}
     from rwkv_linear_attention_wkv7_gb300 import _build
-    return d.get("kernels", {}) if d.get("source_hash") == _build.source_hash() else {}
+    return d.get("kernels", {}) if d.get("source_hash") == _build.source_hash(_build.CHUNK_KERNEL_FILES) else {}
 
 
 class ClockSampler:

@@ -39,11 +39,19 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def source_hash() -> str:
-    """Hash of every source and header the library is built from."""
+# The files the two chunked kernels are compiled from (their measurements are
+# keyed by a hash of these alone).
+CHUNK_KERNEL_FILES = ("wkv7_chunk_fwd.cu", "wkv7_chunk_bwd.cu", "wkv7_chunk_common.cuh", "wkv7_mma.cuh",
+                      "wkv7_internal.cuh")
+
+
+def source_hash(files=None) -> str:
+    """Hash of every source and header the library is built from, or of the
+    named csrc files only."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted(_deps()):
+    deps = _deps() if files is None else [os.path.join(CSRC, f) for f in files]
+    for p in sorted(deps):
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
             h.update(f.read())
