@@ -31,6 +31,19 @@ def lib():
     return wkv7.lib()
 
 
+def test_header_is_plain_c_and_cpp():
+    """include/wkv7.h compiles on its own as C99 and as C++17, warnings as errors."""
+    import shutil
+    import subprocess
+    hdr = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "wkv7.h")
+    for cc, lang, std in (("gcc", "c", "-std=c99"), ("g++", "c++", "-std=c++17")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not available")
+        r = subprocess.run([cc, "-fsyntax-only", "-x", lang, std, "-Wall", "-Wextra", "-Werror", hdr],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
