@@ -187,6 +187,19 @@ int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
  * bad nseg, T not a multiple of 16 * nseg, or a missing workspace.
  */
 long long wkv7_timesplit_workspace_floats(int B, int T, int H, int nseg);
+
+/*
+ * The scan that joins segments, on its own (for segments held elsewhere,
+ * e.g. spans of a sequence on other GPUs).  Per (b, h), over k = 0..nseg-1:
+ *   backward == 0:  S = init (or 0);  out_k = S;  S = C_k + S M_k;    fin = S
+ *   backward != 0:  G = init (or 0);  for k = nseg-1 .. 0: out_k = G;
+ *                   G = C_k + G M_k^T;  fin = G
+ * M, C, out  [B][nseg][H][N][N] fp32 (M, C, out required);
+ * init, fin  [B][H][N][N] fp32, or NULL.  Device pointers, 16-byte aligned.
+ */
+int wkv7_segment_scan(int B, int H, int nseg, const float *M, const float *C,
+                      const float *init, float *out, float *fin, int backward,
+                      void *stream);
 int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype,
                            const void *r, const void *w, const void *k,
                            const void *v, const void *a, const void *b,

@@ -164,6 +164,37 @@ long long wkv7_timesplit_workspace_floats(int B, int T, int H, int nseg) {
            (long long)B * nseg * H * wkv7_factor_floats(tseg);
 }
 
+int wkv7_segment_scan(int B, int H, int nseg, const float *M, const float *C, const float *init, float *out,
+                      float *fin, int backward, void *stream) {
+    if (B < 1 || H < 1 || nseg < 1) return wkv7::set_error(WKV7_EINVAL, "B, H and nseg must be >= 1");
+    if ((long long)B * H > 0x7fffffffLL) return wkv7::set_error(WKV7_EINVAL, "B * H too large");
+    const void *ptrs[5] = {M, C, init, out, fin};
+    const char *names[5] = {"M", "C", "init", "out", "fin"};
+    for (int i = 0; i < 5; ++i) {
+        if (!ptrs[i] && i < 2) return wkv7::set_error(WKV7_EINVAL, i ? "C is NULL" : "M is NULL");
+        if (reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) {
+            char msg[64];
+            snprintf(msg, sizeof msg, "%s is not 16-byte aligned", names[i]);
+            return wkv7::set_error(WKV7_EINVAL, msg);
+        }
+    }
+    if (!out) return wkv7::set_error(WKV7_EINVAL, "out is NULL");
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
+        minor != 3) {
+        cudaGetLastError();
+        return wkv7::set_error(WKV7_EUNSUPPORTED, "this library needs an sm_103a device");
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (backward)
+        wkv7_segment_scan_kernel<true><<<B * H, kThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
+    else
+        wkv7_segment_scan_kernel<false><<<B * H, kThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
+    return cuda_status(cudaGetLastError(), "segment scan launch");
+}
+
 int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
                            const void *k, const void *v, const void *a, const void *b, const float *s0, float *y,
                            float *sT, int nseg, float *workspace, void *stream) {

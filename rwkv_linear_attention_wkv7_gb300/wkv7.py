@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.wkv7_backward.restype = ci
         L.wkv7_timesplit_workspace_floats.argtypes = [ci, ci, ci, ci]
         L.wkv7_timesplit_workspace_floats.restype = ctypes.c_longlong
+        L.wkv7_segment_scan.argtypes = [ci, ci, ci, fp, fp, fp, fp, fp, ci, vp]
+        L.wkv7_segment_scan.restype = ci
         L.wkv7_forward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, ci, fp, vp]
         L.wkv7_forward_timesplit.restype = ci
         L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
@@ -257,6 +259,23 @@ def backward_timesplit(r, w, k, v, a, b, dy, dsT=None, nseg: int = 1, workspace=
                                        _stream(stream))
     _check("wkv7_backward_timesplit", rc)
     return g
+
+
+def segment_scan(M, C, init=None, backward: bool = False, out=None, fin=None, stream=None):
+    """The segment scan alone: M, C [B][nseg][H][64][64] fp32; returns (out, fin) with out_k the
+    state entering segment k (forward) or the gradient arriving at its end (backward) and fin the
+    final state / the gradient at the start (see wkv7_segment_scan)."""
+    B, nseg, H, N, _ = M.shape
+    dev = M.device
+    _f32(M, (B, nseg, H, N, N), dev, "M")
+    _f32(C, (B, nseg, H, N, N), dev, "C")
+    _f32(init, (B, H, N, N), dev, "init")
+    out = out if out is not None else torch.empty_like(M)
+    fin = fin if fin is not None else torch.empty((B, H, N, N), device=dev)
+    rc = lib().wkv7_segment_scan(B, H, nseg, _ptr(M), _ptr(C), _ptr(init), _ptr(out), _ptr(fin), int(backward),
+                                 _stream(stream))
+    _check("wkv7_segment_scan", rc)
+    return out, fin
 
 
 def decode_step(r, w, k, v, a, b, state, y=None, stream=None):
