@@ -1,5 +1,5 @@
 """Sequence parallelism across ranks (each rank one span of the T axis):
-world_size 2 on the gloo backend.  On the CPU the span computations are done
+world sizes 2 and 3 on the gloo backend.  On the CPU the span computations are done
 by the oracle (a stand-in with the solver interface), which checks the
 exchange itself; on the GPU both ranks run the library's kernels on cuda:0
 (two processes, exchanging only through gloo between launches).  Either way
@@ -95,12 +95,12 @@ def _worker(rank, world, port, use_gpu, out):
         dist.destroy_process_group()
 
 
-def _run(use_gpu):
+def _run(use_gpu, world=2):
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, use_gpu, out)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, use_gpu, out)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
@@ -109,11 +109,12 @@ def _run(use_gpu):
     return dict(out)
 
 
-def test_exchange_world2_oracle_spans():
+@pytest.mark.parametrize("world", [2, 3])
+def test_exchange_oracle_spans(world):
     """The exchange with the oracle as the span solver reproduces the
-    whole-sequence oracle to float64 rounding."""
-    res = _run(use_gpu=False)
-    assert sorted(res) == [0, 1]
+    whole-sequence oracle to float64 rounding (every rank's span, sT, ds0)."""
+    res = _run(use_gpu=False, world=world)
+    assert sorted(res) == list(range(world))
     for rank, errs in res.items():
         for k, e in errs.items():
             assert e < 1e-11, (rank, k, e)
