@@ -275,9 +275,10 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec; see
 // in_w) and dw, da, db receive their gradients dw_pre, dkk, davec.  That
 // epilogue runs after the staged rows are refilled: it takes kk from the a^
-// split (a^ = -kk d_{t-1}), the sigmoid from the decays (w_t = d_t / d_{t-1},
-// sigmoid = -ln(w_t) / 0.606531) and avec from a copy the split phase keeps in
-// the Gram / W slots, which the factor-cache path does not use otherwise.
+// split (a^ = -kk d_{t-1}), sigmoid(w_pre) (1 - sigmoid(w_pre)) from registers
+// each lane fills from w_pre before the refill, and avec from a copy the split
+// phase keeps in the Gram / W slots, which the factor-cache path does not use
+// otherwise.
 template <typename E, bool kFac, bool kP>
 __global__ void __launch_bounds__(NT, 2)
     wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
@@ -329,12 +330,14 @@ __global__ void __launch_bounds__(NT, 2)
     // start once the previous chunk's gradient stores have read their staging
     // there, and first waited for by the products that read S_0.
     __shared__ __align__(8) uint64_t bar, bar_s;
+    __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_init(&bar_s, 1);
+        lost = 0;
     }
     __syncthreads();
-    bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
+    int stuck = -1, s_phase = -1;  // the chunk whose wait ran out; the phase of the last start-state copy
     constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0));
     constexpr unsigned kS0Bytes = 64 * OS * 4;
     auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each, lanes 0..6 of warp 0
@@ -344,6 +347,7 @@ __global__ void __launch_bounds__(NT, 2)
         }
     };
     auto load_s0 = [&](int c) {  // thread 0
+        s_phase = (nchunks - 1 - c) & 1;
         mbar_expect_tx(&bar_s, kS0Bytes);
         tma_load_2d(S0f, &maps.m[7], (bh * p.nck + c) * 64, &bar_s);
         mbar_arrive(&bar_s);
@@ -377,8 +381,8 @@ __global__ void __launch_bounds__(NT, 2)
         const int nv = min(C, p.T - t0);
         const bool last = c == nchunks - 1;
         const unsigned ph = (nchunks - 1 - c) & 1;
-        lost |= !mbar_wait(&bar, ph, p.err);
-        if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes);
+        mbar_wait(&bar, ph, p.err, &lost);
+        if (tid == 0 && c > 0) mbar_expect_tx(&bar, kChunkBytes + (last ? kPhantomTx : 0u));
         // The last chunk's gradient stores must have read their staging before the
         // start state lands in the S_0 slot (dr, dw, dk, dv: lanes 0..3 of warp 0)
         // and before the v split and SA, both after a later block barrier, overwrite
@@ -398,10 +402,14 @@ __global__ void __launch_bounds__(NT, 2)
             }
         };
         // the cumulative decays on warps 2 and 3, clear of warp 0's copies
-        const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 64));
+        const bool exact = __syncthreads_or(prep_decay<kP, E, !kP>(raw, dd, nv, 64));
+        if (lost) {  // every thread has passed its wait (the barrier above): leave together
+            stuck = c;
+            break;
+        }
         if (exact) {
             drain_then_load_s0();
-            lost |= !mbar_wait(&bar_s, ph, p.err);
+            mbar_wait(&bar_s, ph, p.err, &lost);
             bwd_chunk_exact<E, kP>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
                                Gh, nv, p, base0, tstride, t0, carryA, carryB);
             fence_proxy_async();  // the per-token path wrote into slots the copies refill
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(NT, 2)
         if constexpr (kFac) {  // SA from the forward
             ld_acc2(FC + fac::kSA + 256 * warp, sa[0], sa[1], lane);
         } else {
-            lost |= !mbar_wait(&bar_s, ph, p.err);
+            mbar_wait(&bar_s, ph, p.err, &lost);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const AFrag sf = s0_a(16 * warp, 16 * kk);
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__(NT, 2)
 
         // the dw running sum starts at diag(dsT^T sT): sT from the last chunk's start state
         if (last && p.dsT) {
-            lost |= !mbar_wait(&bar_s, ph, p.err);
+            mbar_wait(&bar_s, ph, p.err, &lost);
             const AFrag saA = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
                                      make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
             float part[8][2];
@@ -673,6 +681,21 @@ __global__ void __launch_bounds__(NT, 2)
         }
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
+        // kP: -0.606531 sigmoid (1 - sigmoid) of w_pre at this lane's dw positions (key rows rA / rB,
+        // tokens 2q, 2q + 1, 8 + 2q, 9 + 2q), taken from w_pre itself while the staged rows are
+        // still this chunk's: recovering the sigmoid from the decays (-ln(w) / 0.606531) would lose
+        // its relative precision where it is small (w rounds to 1 in fp32)
+        float sgf[2][4];
+        if constexpr (kP) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int t = 8 * (m >> 1) + 2 * q + (m & 1);
+                    const float sg = sigmoid_f(ld_raw(raw, VW, t, hr ? rB : rA));
+                    sgf[hr][m] = -kDecayScale * sg * (1.f - sg);
+                }
+        }
         __syncthreads();
         if (c > 0) {  // this chunk's inputs, dy and factors are consumed: fetch the previous chunk's
             stage_in(c - 1);
@@ -691,7 +714,7 @@ __global__ void __launch_bounds__(NT, 2)
             // this loop (and its DY / DSA fragments) with Gam.
             const int mt = warp >> 1;
             float acc[2][4] = {};
-            lost |= !mbar_wait(&bar_s, ph, p.err);
+            mbar_wait(&bar_s, ph, p.err, &lost);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 BFrag bq[4];
@@ -872,8 +895,7 @@ __global__ void __launch_bounds__(NT, 2)
                     const float d = dd[t * DS + row];
                     const float dp = t ? dd[(t - 1) * DS + row] : 1.f;
                     if constexpr (kP) {  // dw_pre = (w o dw) (-0.606531) sigmoid (1 - sigmoid) (k_wdecay_bwd)
-                        const float sg = -__logf(d * rcp_approx(dp)) * (1.f / kDecayScale);
-                        gdw[t * OS + row] = (Sv[m] - ev[m]) * (-kDecayScale * sg * (1.f - sg));
+                        gdw[t * OS + row] = (Sv[m] - ev[m]) * sgf[hr][m];
                     } else {
                         gdw[t * OS + row] = (Sv[m] - ev[m]) * (dp * rcp_approx(d));
                     }
@@ -895,9 +917,9 @@ __global__ void __launch_bounds__(NT, 2)
         }
     }
     if ((warp == 0 && lane < 4) || (warp == 1 && lane < 2)) bulk_wait_all();
-    if (lost) {
-        mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
-        mbar_wait(&bar_s, (nchunks - 1) & 1, nullptr);
+    if (stuck >= 0) {
+        mbar_drain(&bar, (nchunks - 1 - stuck) & 1);
+        if (tid == 0 && s_phase >= 0) mbar_drain(&bar_s, s_phase);
     }
     if (p.ds0) {
 #pragma unroll

@@ -52,18 +52,51 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity) {
                  : "memory");
     return ok != 0;
 }
-// Polls for the completion of the mbarrier phase of this parity.  The number
-// of polls is bounded (each try_wait also suspends for a short time): when it
-// runs out, the wait records the timeout in *err (read by wkv7_async_status)
-// and returns false instead of spinning on; the caller then goes on with
-// whatever the buffers hold, so a lost copy cannot hang the GPU.
-constexpr unsigned kSpinLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *err) {
-    for (unsigned i = 0; i < kSpinLimit; ++i)
+// Bounded waits.  A wait polls for the completion of the mbarrier phase of
+// this parity for at most kWaitLimitNs of the global timer (0.5 s; a chunk's
+// copies land within microseconds).  The first wait of a CTA that runs out
+// records the timeout in *err (read by wkv7_async_status) and sets the CTA's
+// shared `lost` flag; from then on every wait of that CTA returns at once, the
+// kernel leaves its chunk loop at the next chunk start and only a final drain
+// (mbar_drain, also bounded) remains, so a lost copy costs a CTA at most two
+// limits (about 1 s) instead of hanging the GPU.
+constexpr unsigned long long kWaitLimitNs = 500ull * 1000ull * 1000ull;
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *err, volatile int *lost) {
+    if (mbar_test(bar, parity)) return true;
+    if (*lost) return false;
+    const unsigned long long t0 = global_ns();
+    for (unsigned n = 1;; ++n) {
         if (mbar_test(bar, parity)) return true;
+        if ((n & 31u) == 0) {
+            if (*lost) return false;
+            if (global_ns() - t0 > kWaitLimitNs) break;
+        }
+    }
+    *lost = 1;
     if (err) atomicOr(err, 1u);
     return false;
 }
+// Before a CTA that lost a wait exits: wait (bounded as above) for the copies
+// still addressed to this phase, so that none lands in shared memory the CTA
+// no longer owns.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    for (unsigned n = 1; !mbar_test(bar, parity); ++n)
+        if ((n & 31u) == 0 && global_ns() - t0 > kWaitLimitNs) return;
+}
+// Test-only builds (-DWKV7_TEST_PHANTOM_TX) announce kPhantomTx bytes more than
+// one chunk's copies deliver, so that the wait for that chunk runs out without
+// anything else going wrong.
+#ifdef WKV7_TEST_PHANTOM_TX
+constexpr unsigned kPhantomTx = 16;
+#else
+constexpr unsigned kPhantomTx = 0;
+#endif
 // One contiguous block, both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
@@ -281,8 +314,13 @@ __device__ __forceinline__ float4 rcp4(float4 a) {
 // decay by 1.
 // Returns true (on the calling thread) when some d_t of its column leaves
 // [1e-20, 1e20] (or is not finite): the factorised form then cannot divide
-// by d_t and the chunk takes the exact per-token path.
-template <bool kP, typename E>
+// by d_t and the chunk takes the exact per-token path.  With kMinW (the
+// plain backward) a decay w_t below kSmallW also sends the chunk there: the
+// backward recovers dw_t from the running sum of w_t o dw_t by a division by
+// w_t, which multiplies that sum's absolute rounding (about 1e-5 of the
+// largest r o dr term) by 1 / w_t.
+constexpr float kSmallW = 0.0625f;
+template <bool kP, typename E, bool kMinW = false>
 __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0) {
     bool bad = false;
     if constexpr (kP) {
@@ -321,6 +359,7 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int 
             dc = __fmul_rn(dc, wv[t]);
             dd[t * DS + j] = dc;
             bad |= !(dc >= kTiny && dc <= 1.f / kTiny);
+            if constexpr (kMinW) bad |= !(wv[t] >= kSmallW);
         }
     }
     return bad;

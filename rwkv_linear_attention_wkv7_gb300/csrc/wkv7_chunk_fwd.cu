@@ -108,9 +108,13 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     // chunk inputs arrive by tensor copies (one per input) on the TMA engine;
     // phase c of the mbarrier is chunk c
     __shared__ __align__(8) uint64_t bar;
-    if (tid == 0) mbar_init(&bar, 1);
+    __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        lost = 0;
+    }
     __syncthreads();
-    bool lost = false;  // a wait ran out: drain the copies (bounded) before exit
+    int stuck = -1;  // the chunk whose wait ran out
     constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>();
     auto prefetch = [&](int c) {  // chunk c's copies (lanes 0..5 of warp 0); thread 0 announced its bytes
         if (tid < 6) tma_rows(raw + tid * C * RS, &maps.m[tid], h, c * C, bi, &bar);
@@ -122,11 +126,11 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * C;
         const int nv = min(C, p.T - t0);
-        lost |= !mbar_wait(&bar, c & 1, p.err);
+        mbar_wait(&bar, c & 1, p.err, &lost);
         // this warp's checkpoint stores have left the a^ / r^ slots (the splits write
         // there after the barrier below)
         if (lane == 0) bulk_wait_read();
-        if (tid == 0 && c + 1 < nchunks) mbar_expect_tx(&bar, kChunkBytes);
+        if (tid == 0 && c + 1 < nchunks) mbar_expect_tx(&bar, kChunkBytes + (c == 0 ? kPhantomTx : 0u));
 
         // checkpoint of the state before token t0; written once the previous
         // chunk's state update has long completed, not at the chunk start where
@@ -145,6 +149,10 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         float *const fc = p.fac ? p.fac + ((size_t)bh * nchunks + c) * fac::kWords : nullptr;
         // the cumulative decays on warps 2 and 3 (thread 0 has just issued the y store)
         const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 64));
+        if (lost) {  // every thread has passed its wait (the barrier above): leave together
+            stuck = c;
+            break;
+        }
         if (!exact) {
             // ---- split the decay-scaled vectors and v once: [t][j] quads
 #pragma unroll
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         }
     }
     if (lane == 0) bulk_wait_all();
-    if (lost) mbar_wait(&bar, (nchunks - 1) & 1, nullptr);
+    if (stuck >= 0) mbar_drain(&bar, stuck & 1);
     if (p.sT) {
         float *dst = p.sT + sbase;
 #pragma unroll

@@ -38,36 +38,41 @@ def lib() -> ctypes.CDLL:
         path = library_path()
         if not os.path.exists(path):
             raise ImportError(f"libwkv7.so not built at {path}; run rwkv_linear_attention_wkv7_gb300.build()")
-        L = ctypes.CDLL(path)
-        vp, ci, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
-        L.wkv7_ckpt_count.argtypes = [ci, ci]
-        L.wkv7_ckpt_count.restype = ci
-        L.wkv7_factor_floats.argtypes = [ci]
-        L.wkv7_factor_floats.restype = ctypes.c_longlong
-        L.wkv7_forward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, fp, fp, ci, vp]
-        L.wkv7_forward.restype = ci
-        L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci, fp, fp] + [fp] * 7 + [vp]
-        L.wkv7_backward.restype = ci
-        L.wkv7_timesplit_workspace_floats.argtypes = [ci, ci, ci, ci]
-        L.wkv7_timesplit_workspace_floats.restype = ctypes.c_longlong
-        L.wkv7_segment_scan.argtypes = [ci, ci, ci, fp, fp, fp, fp, fp, ci, vp]
-        L.wkv7_segment_scan.restype = ci
-        L.wkv7_forward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, ci, fp, vp]
-        L.wkv7_forward_timesplit.restype = ci
-        L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
-        L.wkv7_backward_timesplit.restype = ci
-        L.wkv7_forward_fused.argtypes = L.wkv7_forward.argtypes
-        L.wkv7_forward_fused.restype = ci
-        L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
-        L.wkv7_backward_fused.restype = ci
-        L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
-        L.wkv7_decode_step.restype = ci
-        L.wkv7_async_status.argtypes = []
-        L.wkv7_async_status.restype = ci
-        L.wkv7_last_error.argtypes = []
-        L.wkv7_last_error.restype = ctypes.c_char_p
-        _lib = L
+        _lib = load(path)
     return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Open a build of the library at ``path`` with the C ABI's signatures declared."""
+    L = ctypes.CDLL(path)
+    vp, ci, fp = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    L.wkv7_ckpt_count.argtypes = [ci, ci]
+    L.wkv7_ckpt_count.restype = ci
+    L.wkv7_factor_floats.argtypes = [ci]
+    L.wkv7_factor_floats.restype = ctypes.c_longlong
+    L.wkv7_forward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, fp, fp, ci, vp]
+    L.wkv7_forward.restype = ci
+    L.wkv7_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci, fp, fp] + [fp] * 7 + [vp]
+    L.wkv7_backward.restype = ci
+    L.wkv7_timesplit_workspace_floats.argtypes = [ci, ci, ci, ci]
+    L.wkv7_timesplit_workspace_floats.restype = ctypes.c_longlong
+    L.wkv7_segment_scan.argtypes = [ci, ci, ci, fp, fp, fp, fp, fp, ci, vp]
+    L.wkv7_segment_scan.restype = ci
+    L.wkv7_forward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, fp, ci, fp, vp]
+    L.wkv7_forward_timesplit.restype = ci
+    L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
+    L.wkv7_backward_timesplit.restype = ci
+    L.wkv7_forward_fused.argtypes = L.wkv7_forward.argtypes
+    L.wkv7_forward_fused.restype = ci
+    L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
+    L.wkv7_backward_fused.restype = ci
+    L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
+    L.wkv7_decode_step.restype = ci
+    L.wkv7_async_status.argtypes = []
+    L.wkv7_async_status.restype = ci
+    L.wkv7_last_error.argtypes = []
+    L.wkv7_last_error.restype = ctypes.c_char_p
+    return L
 
 
 def last_error() -> str:

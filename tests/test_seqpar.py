@@ -87,9 +87,9 @@ def _worker(rank, world, port, use_gpu, out):
         rg = oracle.backward(*(full[n] for n in "rwkvab"), full["dy"], s0=full["s0"], dsT=full["dsT"])
         errs = {"y": parity.max_rel(y.double().cpu().numpy(), ry[:, sl]),
                 "sT": parity.max_rel(sT.double().cpu().numpy(), rsT),
-                "ds0": parity.fro_rel(g["ds0"].double().cpu().numpy(), rg["ds0"])}
+                "ds0": parity.grad_rel(g["ds0"].double().cpu().numpy(), rg["ds0"])}
         for n in parity.GRADS:
-            errs[n] = parity.fro_rel(g[n].double().cpu().numpy(), rg[n][:, sl])
+            errs[n] = parity.grad_rel(g[n].double().cpu().numpy(), rg[n][:, sl])
         out[rank] = errs
     finally:
         dist.destroy_process_group()
