@@ -40,6 +40,7 @@ TIMESPLIT_SEGMENTS = 32
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 L2_BYTES = 126 * 2**20
+MIN_TIMED_S = 1.0
 
 
 def esize(spec):
@@ -405,16 +406,24 @@ def run_ours(args, world, rank, local):
             e2.record(stream)
             ev_f.append((e0, e1, e2))
 
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(args.warmup):
         step()
+    w1.record(stream)
     torch.cuda.synchronize()
+    # the timed region repeats whole rounds of K steps until it lasts at least
+    # MIN_TIMED_S, so that the clock record sampled during it has several samples
+    # (every round is K full steps; ms_per_step divides by all timed steps)
+    warm_ms = max_over_ranks(w0.elapsed_time(w1) / max(args.warmup, 1), world)
+    rounds = max(1, -(-int(MIN_TIMED_S * 1e3) // max(int(warm_ms * args.steps), 1)))
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for _ in range(args.steps):
+        for _ in range(rounds * args.steps):
             step(record=True)
         t_end.record(stream)
         torch.cuda.synchronize()
@@ -425,7 +434,7 @@ def run_ours(args, world, rank, local):
     bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev_f)
     clocks = clk.summary()
 
-    ms_step = total_ms / args.steps
+    ms_step = total_ms / (rounds * args.steps)
     value = world * spec.tokens / (ms_step / 1e3)
     peak, peak_kind = load_peaks()
     fwd_bytes, bwd_bytes = algorithmic_bytes(spec)
@@ -623,7 +632,8 @@ def run_ours(args, world, rank, local):
         return
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "rounds": rounds, "timed_steps": rounds * args.steps, "timed_ms": total_ms,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_of(spec, args),
         "roofline": {"bound": "hbm", "kernel": f"wkv7 {dom}", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
@@ -632,7 +642,7 @@ def run_ours(args, world, rank, local):
         "forward": {"ms": fwd_ms, "tokens_per_s": spec.tokens / (fwd_ms / 1e3),
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
-        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks,
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * rounds * args.steps, "clocks": clocks,
         "fused": fused, "decode": decode, "timesplit": timesplit,
     }
     print(json.dumps(line), flush=True)
@@ -641,7 +651,7 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))

@@ -87,6 +87,14 @@ static unsigned *g_flag_ptr[64] = {};
 namespace wkv7 {
 int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
+int check_call(int B, int T, int H, int N, int dtype, const void *const *req, const char *const *req_names, int nreq,
+               const void *const *opt, const char *const *opt_names, int nopt) {
+    TRY(check_dims(B, T, H, N, dtype));
+    for (int i = 0; i < nreq; ++i) TRY(check_ptr(req[i], req_names[i], T > 0));
+    for (int i = 0; i < nopt; ++i) TRY(check_ptr(opt[i], opt_names[i], false));
+    return check_device();
+}
+
 unsigned *async_error_flag() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {

@@ -44,6 +44,12 @@ constexpr int kWords = 2048;
 
 // Record an error for wkv7_last_error() and return `code` (C ABI layer).
 int set_error(int code, const char *msg);
+// Host checks shared by every entry point, run before anything is launched:
+// sizes and dtype, the required pointers (non-NULL when T > 0) and the
+// optional ones (NULL allowed), 16-byte alignment of both, and an sm_103a
+// current device.  Returns WKV7_OK or the error code, with the message set.
+int check_call(int B, int T, int H, int N, int dtype, const void *const *req, const char *const *req_names, int nreq,
+               const void *const *opt, const char *const *opt_names, int nopt);
 // Device address of the current device's asynchronous-error flag (looked up
 // once per device), or NULL with the error recorded.
 unsigned *async_error_flag();

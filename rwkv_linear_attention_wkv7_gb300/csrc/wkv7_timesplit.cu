@@ -200,6 +200,14 @@ int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const v
                            float *sT, int nseg, float *workspace, void *stream) {
     int rc = check_split(B, T, H, nseg, workspace);
     if (rc != WKV7_OK) return rc;
+    {   // every argument is checked before the first launch or memset
+        const void *req[7] = {r, w, k, v, a, b, y};
+        const char *rn[7] = {"r", "w", "k", "v", "a", "b", "y"};
+        const void *opt[2] = {s0, sT};
+        const char *on[2] = {"s0", "sT"};
+        rc = wkv7::check_call(B, T, H, N, dtype, req, rn, 7, opt, on, 2);
+        if (rc != WKV7_OK) return rc;
+    }
     if (T == 0) return wkv7_forward(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, nullptr, nullptr, 16, stream);
     const int bs = B * nseg, tseg = T / nseg;
     const Workspace ws = carve(workspace, B, T, H, nseg);
@@ -231,6 +239,14 @@ int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const 
                             float *ds0, int nseg, float *workspace, void *stream) {
     int rc = check_split(B, T, H, nseg, workspace);
     if (rc != WKV7_OK) return rc;
+    {   // every argument is checked before the first launch
+        const void *req[13] = {r, w, k, v, a, b, dy, dr, dw, dk, dv, da, db};
+        const char *rn[13] = {"r", "w", "k", "v", "a", "b", "dy", "dr", "dw", "dk", "dv", "da", "db"};
+        const void *opt[2] = {dsT, ds0};
+        const char *on[2] = {"dsT", "ds0"};
+        rc = wkv7::check_call(B, T, H, N, dtype, req, rn, 13, opt, on, 2);
+        if (rc != WKV7_OK) return rc;
+    }
     if (T == 0) return wkv7_backward(B, 0, H, N, dtype, r, w, k, v, a, b, nullptr, nullptr, 16, dy, dsT, dr, dw, dk,
                                      dv, da, db, ds0, stream);
     const int bs = B * nseg, tseg = T / nseg;

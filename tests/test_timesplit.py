@@ -77,6 +77,15 @@ def test_workspace_size_and_argument_errors():
     assert fwd(128, 0, p) == EINVAL
     assert fwd(128, 4, None) == EINVAL and "workspace" in wkv7.last_error()
     assert fwd(128, 4, ctypes.c_void_p(4100)) == EINVAL
+    # the sizes, dtype and pointers are checked before anything is launched or zeroed
+    bad_dtype = lib.wkv7_forward_timesplit(1, 128, 2, 64, 7, *([p] * 6), None, p, None, 4, p, None)
+    assert bad_dtype == EINVAL and "dtype" in wkv7.last_error()
+    no_y = lib.wkv7_forward_timesplit(1, 128, 2, 64, 0, *([p] * 6), None, None, None, 4, p, None)
+    assert no_y == EINVAL and "y is NULL" in wkv7.last_error()
+    odd_s0 = lib.wkv7_forward_timesplit(1, 128, 2, 64, 0, *([p] * 6), ctypes.c_void_p(4104), p, None, 4, p, None)
+    assert odd_s0 == EINVAL and "s0" in wkv7.last_error()
+    no_dr = lib.wkv7_backward_timesplit(1, 128, 2, 64, 0, *([p] * 6), p, None, None, *([p] * 5), None, 4, p, None)
+    assert no_dr == EINVAL and "dr is NULL" in wkv7.last_error()
 
 
 @pytest.mark.gpu
