@@ -435,6 +435,28 @@ def run_ours(args, world, rank, local):
     clocks = clk.summary()
 
     ms_step = total_ms / (rounds * args.steps)
+
+    # head to head: the same backward launches with two of the 64-row state
+    # products on the tensor cores (tcgen05) instead of warp-level mma.sync
+    bwd_tc_ms = None
+    if spec.L == 16:
+        os.environ["WKV7_BACKWARD_KERNEL"] = "tcgen05"
+        try:
+            def bwd_only():
+                wkv7.backward(*(d[n] for n in INPUTS), outs["ckpt"], d["dy"], dsT=d["dsT"], L=spec.L,
+                              factors=outs.get("factors"), out=gouts, stream=stream)
+            for _ in range(2):
+                bwd_only()
+            m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            m0.record(stream)
+            for _ in range(args.steps):
+                bwd_only()
+            m1.record(stream)
+            torch.cuda.synchronize()
+            bwd_tc_ms = max_over_ranks(m0.elapsed_time(m1), world) / args.steps
+        finally:
+            del os.environ["WKV7_BACKWARD_KERNEL"]
+        wkv7.async_status()
     value = world * spec.tokens / (ms_step / 1e3)
     peak, peak_kind = load_peaks()
     fwd_bytes, bwd_bytes = algorithmic_bytes(spec)
@@ -641,7 +663,8 @@ def run_ours(args, world, rank, local):
         "hbm_fraction_step": step_gbs / peak,
         "forward": {"ms": fwd_ms, "tokens_per_s": spec.tokens / (fwd_ms / 1e3),
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
-        "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9},
+        "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
+                     "kernel": "mma.sync", "tcgen05_variant_ms": bwd_tc_ms},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * rounds * args.steps, "clocks": clocks,
         "fused": fused, "decode": decode, "timesplit": timesplit,
     }

@@ -24,173 +24,15 @@
 // a reverse running sum whose value past the last token is diag(dsT^T sT).
 // Chunks whose decay underflows take an exact per-token path that replays
 // the chunk from its checkpoint.
+#include <cstdlib>
+#include <cstring>
 #include <type_traits>
 
-#include "wkv7_chunk_common.cuh"
+#include "wkv7_chunk_bwd_exact.cuh"
 
 namespace wkv7 {
 namespace {
 using namespace chunk;
-
-constexpr int NT = 128;
-constexpr unsigned kFull = 0xffffffffu;
-
-
-__device__ __forceinline__ float quad_sum(float x) {
-    x += __shfl_xor_sync(kFull, x, 1);
-    x += __shfl_xor_sync(kFull, x, 2);
-    return x;
-}
-// Sum over the 8 lanes that share q (the g index), i.e. over 8 value rows.
-__device__ __forceinline__ float rows_sum(float x) {
-    x += __shfl_xor_sync(kFull, x, 4);
-    x += __shfl_xor_sync(kFull, x, 8);
-    x += __shfl_xor_sync(kFull, x, 16);
-    return x;
-}
-
-// Exact per-token backward of one chunk (decay underflow).  G (registers,
-// rows rA/rB, columns 8nt+2q+{0,1}) enters as dL/dS_C and leaves as dL/dS_0.
-// Writes all six gradients of the chunk's tokens and returns, per lane, the
-// dw carry for columns jA/jB of the G3/G4 layout (w_0 o dw_0 + a_0 o da_0).
-template <typename E, bool kP>
-__device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s, float *Sps, float *red,
-                                float G[8][4], int nv, const SeqArgs &p, size_t base0, size_t tstride, int t0,
-                                float &carryA, float &carryB) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q = lane & 3;
-    const int rA = warp * 16 + g, rB = rA + 8;
-    for (int t = nv - 1; t >= 0; --t) {
-        // replay S_0 -> S_{t-1} (kept in registers), recording nothing
-        float S[8][4];
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const float2 x = *reinterpret_cast<const float2 *>(S0s + rA * OS + 8 * nt + 2 * q);
-            const float2 z = *reinterpret_cast<const float2 *>(S0s + rB * OS + 8 * nt + 2 * q);
-            S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = z.x; S[nt][3] = z.y;
-        }
-        float sa0 = 0.f, sa1 = 0.f;
-        for (int u = 0; u <= t; ++u) {
-            sa0 = 0.f; sa1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int j = 8 * nt + 2 * q;
-                const float a0 = in_a<kP>(raw, u, j), a1 = in_a<kP>(raw, u, j + 1);
-                sa0 = __fmaf_rn(S[nt][0], a0, __fmaf_rn(S[nt][1], a1, sa0));
-                sa1 = __fmaf_rn(S[nt][2], a0, __fmaf_rn(S[nt][3], a1, sa1));
-            }
-            sa0 = quad_sum(sa0);
-            sa1 = quad_sum(sa1);
-            if (u == t) {  // keep S_{t-1} for dw and da
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    *reinterpret_cast<float2 *>(Sps + rA * SP + 8 * nt + 2 * q) = make_float2(S[nt][0], S[nt][1]);
-                    *reinterpret_cast<float2 *>(Sps + rB * SP + 8 * nt + 2 * q) = make_float2(S[nt][2], S[nt][3]);
-                }
-            }
-            const float v0 = ld_raw(raw, VV, u, rA), v1 = ld_raw(raw, VV, u, rB);
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = 8 * nt + 2 * q + e;
-                    const float wv = in_w<kP>(raw, u, j), kv = ld_raw(raw, VK, u, j), bv = in_b<kP>(raw, u, j);
-                    S[nt][e] = __fmaf_rn(S[nt][e], wv, __fmaf_rn(sa0, bv, __fmul_rn(v0, kv)));
-                    S[nt][2 + e] = __fmaf_rn(S[nt][2 + e], wv, __fmaf_rn(sa1, bv, __fmul_rn(v1, kv)));
-                }
-        }
-        // now S = S_t, sa0/sa1 = sa_t for rows rA/rB
-        const float dy0 = dys[t * SP + rA], dy1 = dys[t * SP + rB];
-        const float v0 = ld_raw(raw, VV, t, rA), v1 = ld_raw(raw, VV, t, rB);
-        float dv0 = 0.f, dv1 = 0.f, ds0 = 0.f, ds1 = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = 8 * nt + 2 * q + e;
-                const float rv = ld_raw(raw, VR, t, j), kv = ld_raw(raw, VK, t, j), bv = in_b<kP>(raw, t, j);
-                G[nt][e] = __fmaf_rn(dy0, rv, G[nt][e]);
-                G[nt][2 + e] = __fmaf_rn(dy1, rv, G[nt][2 + e]);
-                dv0 = __fmaf_rn(G[nt][e], kv, dv0);
-                dv1 = __fmaf_rn(G[nt][2 + e], kv, dv1);
-                ds0 = __fmaf_rn(G[nt][e], bv, ds0);
-                ds1 = __fmaf_rn(G[nt][2 + e], bv, ds1);
-            }
-        dv0 = quad_sum(dv0); dv1 = quad_sum(dv1);
-        ds0 = quad_sum(ds0); ds1 = quad_sum(ds1);
-        if (q == 0) {
-            p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dv0;
-            p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dv1;
-        }
-        __syncthreads();  // S_{t-1} visible in Sps
-        // column partials over this lane's two rows, reduced over the warp's 16 rows
-        // red layout: [grad 0..4][warp][64]; grads: dr, dk, db, dw, da
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = 8 * nt + 2 * q + e;
-                const float spA = Sps[rA * SP + j], spB = Sps[rB * SP + j];
-                float x[5];
-                x[0] = __fmaf_rn(S[nt][e], dy0, __fmul_rn(S[nt][2 + e], dy1));
-                x[1] = __fmaf_rn(G[nt][e], v0, __fmul_rn(G[nt][2 + e], v1));
-                x[2] = __fmaf_rn(G[nt][e], sa0, __fmul_rn(G[nt][2 + e], sa1));
-                x[3] = __fmaf_rn(G[nt][e], spA, __fmul_rn(G[nt][2 + e], spB));
-                x[4] = __fmaf_rn(spA, ds0, __fmul_rn(spB, ds1));
-#pragma unroll
-                for (int m = 0; m < 5; ++m) {
-                    const float s = rows_sum(x[m]);
-                    if (g == 0) red[(m * 4 + warp) * 64 + j] = s;
-                }
-            }
-        // carried gradient to S_{t-1}
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = 8 * nt + 2 * q + e;
-                const float wv = in_w<kP>(raw, t, j), av = in_a<kP>(raw, t, j);
-                G[nt][e] = __fmaf_rn(G[nt][e], wv, __fmul_rn(ds0, av));
-                G[nt][2 + e] = __fmaf_rn(G[nt][2 + e], wv, __fmul_rn(ds1, av));
-            }
-        __syncthreads();
-        if constexpr (kP) {  // gradients of the producers' inputs: dw_pre, dkk, davec (k_wdecay_bwd, k_comp_keymod)
-            for (int j = tid; j < 64; j += NT) {
-                float s5[5];
-#pragma unroll
-                for (int m = 0; m < 5; ++m)
-                    s5[m] = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
-                            red[(m * 4 + 3) * 64 + j];
-                const size_t o = base0 + (size_t)(t0 + t) * tstride + j;
-                const float sg = sigmoid_f(ld_raw(raw, VW, t, j)), kkv = ld_raw(raw, VA, t, j), avv = ld_raw(raw, VB, t, j);
-                p.dr[o] = s5[0];
-                p.dk[o] = s5[1];
-                p.db[o] = kkv * s5[2];
-                p.dw[o] = s5[3] * in_w<kP>(raw, t, j) * (-kDecayScale) * sg * (1.f - sg);
-                p.da[o] = avv * s5[2] - s5[4];
-            }
-        } else {
-            float *outs[5] = {p.dr, p.dk, p.db, p.dw, p.da};
-            for (int o = tid; o < 5 * 64; o += NT) {
-                const int m = o >> 6, j = o & 63;
-                const float s = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
-                                red[(m * 4 + 3) * 64 + j];
-                outs[m][base0 + (size_t)(t0 + t) * tstride + j] = s;
-            }
-        }
-        if (t == 0) {  // dw carry into the previous chunk: w_0 o dw_0 + a_0 o da_0
-            const int jA = warp * 16 + g, jB = jA + 8;
-            float cA = 0.f, cB = 0.f;
-#pragma unroll
-            for (int w4 = 0; w4 < 4; ++w4) {
-                cA += in_w<kP>(raw, 0, jA) * red[(3 * 4 + w4) * 64 + jA] + in_a<kP>(raw, 0, jA) * red[(4 * 4 + w4) * 64 + jA];
-                cB += in_w<kP>(raw, 0, jB) * red[(3 * 4 + w4) * 64 + jB] + in_a<kP>(raw, 0, jB) * red[(4 * 4 + w4) * 64 + jB];
-            }
-            carryA = cA;
-            carryB = cB;
-        }
-        __syncthreads();
-    }
-}
 
 // Shared-memory carve-up (byte offsets after the raw input block).  HL16 /
 // HL32 / HL64 = split operand matrices (bf16 hi then lo) of 16 / 32 / 64 rows
@@ -234,17 +76,6 @@ __device__ __forceinline__ __nv_bfloat16 *hi_of(unsigned char *base, int off) {
 __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off, int rows) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + rows * MS;
 }
-// split x into (hi, lo) and store both at element (row, col) of a split matrix
-// fp32 values of an A fragment's 8 elements (hi + lo), in C-tile order:
-// v[0..1] = (row g, k 2q..2q+1), v[2..3] = (row g+8, ..), v[4..5] = (row g, k 2q+8..), v[6..7] = (row g+8, ..)
-__device__ __forceinline__ void a_values(const AFrag &f, float v[8]) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        v[2 * r] = __uint_as_float(f.hi[r] << 16) + __uint_as_float(f.lo[r] << 16);
-        v[2 * r + 1] = __uint_as_float(f.hi[r] & 0xffff0000u) + __uint_as_float(f.lo[r] & 0xffff0000u);
-    }
-}
-
 // A' = W^T-weighted a^ for NS 16-key slabs starting at slab0 (M = token,
 // N = key), the slabs' MMAs issued together; written split to the A' slot.
 template <int NS>
@@ -410,8 +241,8 @@ __global__ void __launch_bounds__(NT, 2)
         if (exact) {
             drain_then_load_s0();
             mbar_wait(&bar_s, ph, p.err, &lost);
-            bwd_chunk_exact<E, kP>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT), reinterpret_cast<float *>(Bs + B_Y),
-                               Gh, nv, p, base0, tstride, t0, carryA, carryB);
+            bwd_chunk_exact<E, kP, OS>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT),
+                                       reinterpret_cast<float *>(Bs + B_Y), Gh, nv, p, base0, tstride, t0, carryA, carryB);
             fence_proxy_async();  // the per-token path wrote into slots the copies refill
             __syncthreads();
             if (c > 0) {
@@ -949,7 +780,19 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 
 bool backward_chunk_supported(const SeqArgs &p) { return p.L == C; }
 
+// With the factor cache, the backward can run the two 64-row state products
+// that feed only the gradient outputs on the fifth-generation tensor cores
+// (wkv7_chunk_bwd_tc.cu); WKV7_BACKWARD_KERNEL=tcgen05 in the environment
+// (read at each launch) selects that kernel, "mma" or nothing this file's.
+// The warp-level kernel is the default: on the bf16 B=16 T=4096 H=32 workload
+// (two CTAs per SM) it measured 2.67 ms against 3.22 ms.
+static bool tensor_core_backward() {
+    const char *v = getenv("WKV7_BACKWARD_KERNEL");
+    return v && strcmp(v, "tcgen05") == 0;
+}
+
 cudaError_t launch_backward_chunk(const SeqArgs &p, cudaStream_t st) {
+    if (backward_tc_supported(p) && tensor_core_backward()) return launch_backward_tc(p, st);
     if (p.prod) {  // the fused producers run with the factor cache only
         if (!p.fac_in) return cudaErrorInvalidValue;
         return p.dtype == 1 ? launch_t<__nv_bfloat16, true, true>(p, st) : launch_t<float, true, true>(p, st);

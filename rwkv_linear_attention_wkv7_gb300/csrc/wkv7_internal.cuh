@@ -61,6 +61,8 @@ cudaError_t launch_forward_chunk(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_backward_plain(const SeqArgs &a, cudaStream_t s);
 bool backward_chunk_supported(const SeqArgs &a);
 cudaError_t launch_backward_chunk(const SeqArgs &a, cudaStream_t s);
+bool backward_tc_supported(const SeqArgs &a);
+cudaError_t launch_backward_tc(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_decode_step(int B, int H, int dtype, const void *r, const void *w,
                                const void *k, const void *v, const void *a, const void *b,
                                float *state, float *y, cudaStream_t s);

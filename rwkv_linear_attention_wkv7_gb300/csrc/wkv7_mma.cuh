@@ -80,6 +80,16 @@ __device__ __forceinline__ BFrag make_b(float2 k0, float2 k8) {
     return f;
 }
 
+// fp32 values of an A fragment's 8 elements (hi + lo), in C-tile order:
+// v[0..1] = (row g, k 2q..2q+1), v[2..3] = (row g+8, ..), v[4..5] = (row g, k 2q+8..), v[6..7] = (row g+8, ..)
+__device__ __forceinline__ void a_values(const AFrag &f, float v[8]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        v[2 * r] = __uint_as_float(f.hi[r] << 16) + __uint_as_float(f.lo[r] << 16);
+        v[2 * r + 1] = __uint_as_float(f.hi[r] & 0xffff0000u) + __uint_as_float(f.lo[r] & 0xffff0000u);
+    }
+}
+
 // A fragment for k-tile kt from a 16-row x 64-column fp32 accumulator slab
 // held as 8 n-tiles of C fragments (c[nt][0..3]): the C layout of n-tiles
 // 2kt and 2kt+1 is exactly the A layout of k-tile kt.
