@@ -163,6 +163,81 @@ OracleLib.forward_fused.__doc__ = "Forward from (r, w_pre, k, v, kk, avec); retu
 OracleLib.backward_fused.__doc__ = ("Gradients dr, dw_pre, dk, dv, dkk, davec, ds0 of the fused inputs "
                                     "(same arguments as backward, with w_pre, kk, avec).")
 
+# ---- the output epilogue after the recurrence ("Foundry/cuda_kernels/timemix.cu"
+# page: k_groupnorm, then k_bonus; their backward halves k_bonus_bwd and
+# k_groupnorm_bwd).  Per token and head, over the head's N recurrence outputs y:
+#     mean = sum_j y_j / N,  var = sum_j (y_j - mean)^2 / N,  rstd = 1 / sqrt(var + 64e-5)
+#     g_j = (y_j - mean) rstd gn_w[h][j] + gn_b[h][j]                 (k_groupnorm: one group per head)
+#     s = sum_j r_j k_j r_k[h][j],   o_j = g_j + s v_j                  (k_bonus)
+# with the GroupNorm's per-channel weight and bias gn_w, gn_b and the bonus
+# weight r_k, each per channel c = h N + j.  Backward from do = dL/do:
+#     ds = sum_j do_j v_j;  dv += do s;  dr += ds k r_k;  dk += ds r r_k;  d r_k = sum ds r k   (k_bonus_bwd)
+#     xh = (y - mean) rstd;  dn = do gn_w
+#     dy = rstd (dn - mean_j(dn) - xh mean_j(dn xh));  d gn_w = sum do xh;  d gn_b = sum do    (k_groupnorm_bwd)
+# with the parameter gradients summed over every batch row and token.
+# Readings: r, k, v here are the recurrence's own inputs (the page's R, K, V
+# buffers feed both); the bonus is added after the GroupNorm, as the page
+# launches them; the page's output gate after the bonus belongs to the model
+# around and is not part of this epilogue.
+GN_EPS = 64e-5
+
+
+def gn_bonus(y, r, k, v, gn_w, gn_b, r_k):
+    """(o, mean, rstd) in float64.  y, r, k, v [B][T][H][N]; gn_w, gn_b, r_k [H][N];
+    mean and rstd [B][T][H]."""
+    y, r, k, v, gn_w, gn_b, r_k = map(_f64, (y, r, k, v, gn_w, gn_b, r_k))
+    n = y.shape[-1]
+    mean = y.sum(axis=-1, keepdims=True) / n
+    var = ((y - mean) ** 2).sum(axis=-1, keepdims=True) / n
+    rstd = 1.0 / np.sqrt(var + GN_EPS)
+    g = (y - mean) * rstd * gn_w + gn_b
+    s = (r * k * r_k).sum(axis=-1, keepdims=True)
+    return g + s * v, mean[..., 0], rstd[..., 0]
+
+
+def gn_bonus_backward(y, r, k, v, gn_w, r_k, do):
+    """Gradients through the epilogue from do = dL/do: dy (what the recurrence
+    receives), the bonus's own terms dr, dk, dv (added to the recurrence's),
+    and the parameter gradients dgn_w, dgn_b, dr_k [H][N]."""
+    y, r, k, v, gn_w, r_k, do = map(_f64, (y, r, k, v, gn_w, r_k, do))
+    n = y.shape[-1]
+    s = (r * k * r_k).sum(axis=-1, keepdims=True)
+    ds = (do * v).sum(axis=-1, keepdims=True)
+    out = {"dv": do * s, "dr": ds * k * r_k, "dk": ds * r * r_k, "dr_k": (ds * r * k).sum(axis=(0, 1))}
+    mean = y.sum(axis=-1, keepdims=True) / n
+    var = ((y - mean) ** 2).sum(axis=-1, keepdims=True) / n
+    rstd = 1.0 / np.sqrt(var + GN_EPS)
+    xh = (y - mean) * rstd
+    dn = do * gn_w
+    out["dy"] = rstd * (dn - dn.sum(axis=-1, keepdims=True) / n - xh * (dn * xh).sum(axis=-1, keepdims=True) / n)
+    out["dgn_w"] = (do * xh).sum(axis=(0, 1))
+    out["dgn_b"] = do.sum(axis=(0, 1))
+    return out
+
+
+def _forward_gn(orc, r, w, k, v, a, b, gn_w, gn_b, r_k, s0=None, L: int = 16, want_ckpt: bool = True):
+    y, sT, ck = orc.forward(r, w, k, v, a, b, s0=s0, L=L, want_ckpt=want_ckpt)
+    o, _, _ = gn_bonus(y, r, k, v, gn_w, gn_b, r_k)
+    return o, y, sT, ck
+
+
+def _backward_gn(orc, r, w, k, v, a, b, gn_w, r_k, do, s0=None, dsT=None):
+    y, _, _ = orc.forward(r, w, k, v, a, b, s0=s0, L=16, want_ckpt=False)
+    e = gn_bonus_backward(y, r, k, v, gn_w, r_k, do)
+    g = orc.backward(r, w, k, v, a, b, e["dy"], s0=s0, dsT=dsT)
+    for n in ("dr", "dk", "dv"):
+        g[n] = g[n] + e[n]
+    g.update({n: e[n] for n in ("dgn_w", "dgn_b", "dr_k")})
+    return g
+
+
+OracleLib.forward_gn = lambda self, *a, **kw: _forward_gn(self, *a, **kw)
+OracleLib.backward_gn = lambda self, *a, **kw: _backward_gn(self, *a, **kw)
+OracleLib.forward_gn.__doc__ = ("Recurrence, then GroupNorm + bonus: returns (o, y, sT, ckpt) from "
+                                "(r, w, k, v, a, b, gn_w, gn_b, r_k).")
+OracleLib.backward_gn.__doc__ = ("Gradients of sum(o * do) + sum(sT * dsT): dr, dw, dk, dv, da, db, ds0 "
+                                 "and dgn_w, dgn_b, dr_k; arguments (r, w, k, v, a, b, gn_w, r_k, do).")
+
 _default = None
 
 
@@ -196,6 +271,14 @@ def forward_fused(*args, **kw):
 
 def backward_fused(*args, **kw):
     return lib().backward_fused(*args, **kw)
+
+
+def forward_gn(*args, **kw):
+    return lib().forward_gn(*args, **kw)
+
+
+def backward_gn(*args, **kw):
+    return lib().backward_gn(*args, **kw)
 
 
 def per_head(fn, heads, threads=None):

@@ -379,10 +379,154 @@ def pin_fused_finite_differences(orc):
 
 FUSED_PINS = [pin_fused_constant_decay, pin_fused_delta_rule, pin_fused_finite_differences]
 
+
+# ------------------------------------------- GroupNorm + bonus output epilogue
+# ("timemix.cu" page: k_groupnorm, k_bonus and their backward kernels).  These
+# pins take the module-level oracle functions, so that planted mistakes can be
+# swapped in for them (test_oracle_mutants.py).
+
+def _gn_inputs(g, B, T, H):
+    shp = (B, T, H, N)
+    y, r, k, v = (g.standard_normal(shp) for _ in range(4))
+    gn_w, gn_b, r_k = (g.standard_normal((H, N)) for _ in range(3))
+    return dict(y=y, r=r, k=k, v=v, gn_w=gn_w, gn_b=gn_b, r_k=r_k)
+
+
+def pin_gn_library_groupnorm(orc):
+    """With r_k = 0 the epilogue is a GroupNorm with one group of N channels
+    per head over the C = H N channels of a token: torch's own group_norm in
+    float64 (eps 64e-5) gives the same output, and torch autograd through it
+    gives the same dy, dgn_w and dgn_b."""
+    import torch
+    import oracle
+    g = _rng(31)
+    B, T, H = 2, 5, 3
+    x = _gn_inputs(g, B, T, H)
+    zero = np.zeros((H, N))
+    o, _, _ = oracle.gn_bonus(x["y"], x["r"], x["k"], x["v"], x["gn_w"], x["gn_b"], zero)
+    y = torch.tensor(x["y"].reshape(B * T, H * N), requires_grad=True)
+    w = torch.tensor(x["gn_w"].reshape(-1), requires_grad=True)
+    b = torch.tensor(x["gn_b"].reshape(-1), requires_grad=True)
+    ref = torch.nn.functional.group_norm(y, H, w, b, eps=64e-5)
+    _close(o, ref.detach().numpy().reshape(B, T, H, N), 1e-12, "GroupNorm output")
+    do = g.standard_normal((B, T, H, N))
+    (ref * torch.tensor(do.reshape(B * T, H * N))).sum().backward()
+    e = oracle.gn_bonus_backward(x["y"], x["r"], x["k"], x["v"], x["gn_w"], zero, do)
+    _close(e["dy"], y.grad.numpy().reshape(B, T, H, N), 1e-12, "GroupNorm dy")
+    _close(e["dgn_w"], w.grad.numpy().reshape(H, N), 1e-12, "GroupNorm dgn_w")
+    _close(e["dgn_b"], b.grad.numpy().reshape(H, N), 1e-12, "GroupNorm dgn_b")
+
+
+def pin_gn_standardised_input(orc):
+    """y = a z + c with z of exactly zero mean and unit (biased) variance over
+    the head: with gn_w = 1, gn_b = 0, r_k = 0 the output is z a / sqrt(a^2 + 64e-5),
+    whatever c; and with y constant over the head (a = 0) it is gn_b."""
+    import oracle
+    g = _rng(32)
+    B, T, H = 1, 6, 2
+    x = _gn_inputs(g, B, T, H)
+    z = g.standard_normal((B, T, H, N))
+    z = z - z.mean(axis=-1, keepdims=True)
+    z = z / np.sqrt((z ** 2).mean(axis=-1, keepdims=True))
+    a = g.uniform(0.05, 3.0, size=(B, T, H, 1))
+    c = g.standard_normal((B, T, H, 1)) * 5
+    one, zero = np.ones((H, N)), np.zeros((H, N))
+    o, _, _ = oracle.gn_bonus(a * z + c, x["r"], x["k"], x["v"], one, zero, zero)
+    _close(o, z * a / np.sqrt(a ** 2 + 64e-5), 1e-12, "standardised input")
+    o, _, _ = oracle.gn_bonus(np.broadcast_to(c, z.shape), x["r"], x["k"], x["v"], x["gn_w"], x["gn_b"], zero)
+    _close(o, np.broadcast_to(x["gn_b"], o.shape), 1e-12, "constant input gives the bias")
+
+
+def pin_gn_bonus_one_channel(orc):
+    """A bonus weight on one channel m only (r_k = e_m) adds r_m k_m v to the
+    GroupNorm output: the bonus is the r, k product of that channel scaling
+    the whole value vector."""
+    import oracle
+    g = _rng(33)
+    B, T, H = 2, 4, 3
+    x = _gn_inputs(g, B, T, H)
+    zero = np.zeros((H, N))
+    base, _, _ = oracle.gn_bonus(x["y"], x["r"], x["k"], x["v"], x["gn_w"], x["gn_b"], zero)
+    for m in (0, 17, 63):
+        rk = np.zeros((H, N))
+        rk[:, m] = 1.0
+        o, _, _ = oracle.gn_bonus(x["y"], x["r"], x["k"], x["v"], x["gn_w"], x["gn_b"], rk)
+        want = base + (x["r"][..., m] * x["k"][..., m])[..., None] * x["v"]
+        _close(o, want, 1e-12, f"bonus on channel {m}")
+
+
+def pin_gn_finite_differences(orc):
+    """Central finite differences in float64 of sum(o do) through the
+    epilogue: dy, dr, dk, dv, dgn_w, dgn_b, dr_k at sampled coordinates,
+    relative error < 1e-6."""
+    import oracle
+    g = _rng(34)
+    B, T, H = 2, 3, 2
+    x = _gn_inputs(g, B, T, H)
+    do = g.standard_normal((B, T, H, N))
+    e = oracle.gn_bonus_backward(x["y"], x["r"], x["k"], x["v"], x["gn_w"], x["r_k"], do)
+
+    def loss(xx):
+        o, _, _ = oracle.gn_bonus(xx["y"], xx["r"], xx["k"], xx["v"], xx["gn_w"], xx["gn_b"], xx["r_k"])
+        return float(np.sum(o * do))
+    eps = 1e-6
+    for name in ("y", "r", "k", "v", "gn_w", "gn_b", "r_k"):
+        grad = e["d" + name]
+        scale = float(np.abs(grad).max())
+        for idx in [tuple(int(g.integers(0, s)) for s in x[name].shape) for _ in range(6)]:
+            def at(delta):
+                pert = x[name].copy()
+                pert[idx] += delta
+                return loss({**x, name: pert})
+            fd = (at(eps) - at(-eps)) / (2 * eps)
+            err = abs(fd - grad[idx]) / max(abs(grad[idx]), 1e-3 * scale, 1e-300)
+            assert err < 1e-6, f"d{name}{idx}: fd {fd:.9e} vs {grad[idx]:.9e} (rel {err:.2e})"
+
+
+def pin_gn_composite_finite_differences(orc):
+    """The recurrence followed by the epilogue: central finite differences of
+    sum(o do) + sum(sT dsT) for r, w, k, v, a, b, s0 and the three epilogue
+    weights against backward_gn (which adds the bonus's own dr, dk, dv to the
+    recurrence's), relative error < 1e-5."""
+    g = _rng(35)
+    B, T, H = 1, 5, 1
+    x = _realistic(g, B, T, H)
+    p = {n: g.standard_normal((H, N)) for n in ("gn_w", "gn_b", "r_k")}
+    s0 = 0.5 * g.standard_normal((B, H, N, N))
+    do = g.standard_normal((B, T, H, N))
+    dsT = g.standard_normal((B, H, N, N))
+    gr = orc.backward_gn(*(x[n] for n in "rwkvab"), p["gn_w"], p["r_k"], do, s0=s0, dsT=dsT)
+
+    def loss(xx, pp, ss):
+        o, _, sT, _ = orc.forward_gn(*(xx[n] for n in "rwkvab"), pp["gn_w"], pp["gn_b"], pp["r_k"], s0=ss, L=4,
+                                     want_ckpt=False)
+        return float(np.sum(o * do) + np.sum(sT * dsT))
+    eps = 1e-6
+    for name in ("r", "w", "k", "v", "a", "b", "s0", "gn_w", "gn_b", "r_k"):
+        base = s0 if name == "s0" else (p[name] if name in p else x[name])
+        grad = gr["d" + name]
+        scale = float(np.abs(grad).max())
+        for idx in [tuple(int(g.integers(0, s)) for s in base.shape) for _ in range(4)]:
+            def at(delta):
+                pert = base.copy()
+                pert[idx] += delta
+                if name == "s0":
+                    return loss(x, p, pert)
+                if name in p:
+                    return loss(x, {**p, name: pert}, s0)
+                return loss({**x, name: pert}, p, s0)
+            fd = (at(eps) - at(-eps)) / (2 * eps)
+            err = abs(fd - grad[idx]) / max(abs(grad[idx]), 1e-3 * scale, 1e-300)
+            assert err < 1e-5, f"d{name}{idx}: fd {fd:.9e} vs {grad[idx]:.9e} (rel {err:.2e})"
+
+
+GN_PINS = [pin_gn_library_groupnorm, pin_gn_standardised_input, pin_gn_bonus_one_channel, pin_gn_finite_differences,
+           pin_gn_composite_finite_differences]
+
 ALL_PINS = [
     pin_linear_attention, pin_memoryless, pin_decay_only, pin_delta_rule_write,
     pin_projection_erases, pin_rank1_orientation, pin_empty_sequence,
     pin_checkpoints_are_prefix_states, pin_split_sequence, pin_decode_is_streaming,
     pin_linear_in_state_and_values, pin_adjoint_identity, pin_finite_differences,
     pin_autograd_adjoint,
-] + FUSED_PINS
+] + FUSED_PINS + GN_PINS

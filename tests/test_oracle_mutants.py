@@ -118,3 +118,72 @@ def test_some_fused_pin_catches(mutant, monkeypatch):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no fused pin catches the planted mistake: {kind}"
+
+
+# Plausible mistakes in the GroupNorm + bonus epilogue (Python side of the
+# oracle), each swapped in for the real function; some epilogue pin must trip.
+def _bad_gn(kind):
+    real_f, real_b = oracle.gn_bonus, oracle.gn_bonus_backward
+    np_ = oracle.np
+
+    def fwd(y, r, k, v, gn_w, gn_b, r_k):
+        y, r, k, v, gn_w, gn_b, r_k = map(oracle._f64, (y, r, k, v, gn_w, gn_b, r_k))
+        n = y.shape[-1]
+        mean = y.mean(axis=-1, keepdims=True)
+        var = ((y - mean) ** 2).sum(axis=-1, keepdims=True) / (n - 1 if kind == "unbiased variance" else n)
+        rstd = 1.0 / (np_.sqrt(var) + oracle.GN_EPS) if kind == "eps outside the root" else \
+            1.0 / np_.sqrt(var + oracle.GN_EPS)
+        g = (y - mean) * rstd * gn_w + gn_b
+        if kind == "bonus from r twice":
+            s = (r * r * r_k).sum(axis=-1, keepdims=True)
+        elif kind == "bonus weight per value channel":
+            return g + (r * k).sum(axis=-1, keepdims=True) * r_k * v, mean[..., 0], rstd[..., 0]
+        else:
+            s = (r * k * r_k).sum(axis=-1, keepdims=True)
+        return g + s * v, mean[..., 0], rstd[..., 0]
+
+    def bwd(y, r, k, v, gn_w, r_k, do):
+        out = real_b(y, r, k, v, gn_w, r_k, do)
+        y, r, k, v, gn_w, r_k, do = map(oracle._f64, (y, r, k, v, gn_w, r_k, do))
+        n = y.shape[-1]
+        mean = y.mean(axis=-1, keepdims=True)
+        rstd = 1.0 / np_.sqrt(((y - mean) ** 2).mean(axis=-1, keepdims=True) + oracle.GN_EPS)
+        xh = (y - mean) * rstd
+        dn = do * gn_w
+        ds = (do * v).sum(axis=-1, keepdims=True)
+        if kind == "dy drops the mean of dn":
+            out["dy"] = rstd * (dn - xh * (dn * xh).mean(axis=-1, keepdims=True))
+        elif kind == "dy drops the projection on xh":
+            out["dy"] = rstd * (dn - dn.mean(axis=-1, keepdims=True))
+        elif kind == "bonus dr uses r":
+            out["dr"] = ds * r * r_k
+        elif kind == "d r_k misses k":
+            out["dr_k"] = (ds * r).sum(axis=(0, 1))
+        elif kind == "dgn_w from y":
+            out["dgn_w"] = (do * y).sum(axis=(0, 1))
+        elif kind == "dv without the bonus":
+            out["dv"] = np_.zeros_like(out["dv"])
+        return out
+
+    fwd_kinds = ("unbiased variance", "eps outside the root", "bonus from r twice", "bonus weight per value channel")
+    return (fwd if kind in fwd_kinds else real_f), (bwd if kind not in fwd_kinds else real_b)
+
+
+GN_MUTANTS = ["unbiased variance", "eps outside the root", "bonus from r twice", "bonus weight per value channel",
+              "dy drops the mean of dn", "dy drops the projection on xh", "bonus dr uses r", "d r_k misses k",
+              "dgn_w from y", "dv without the bonus"]
+
+
+@pytest.mark.parametrize("kind", GN_MUTANTS)
+def test_some_gn_pin_catches(kind, monkeypatch):
+    from tests.oracle_pins import GN_PINS
+    f, b = _bad_gn(kind)
+    monkeypatch.setattr(oracle, "gn_bonus", f)
+    monkeypatch.setattr(oracle, "gn_bonus_backward", b)
+    caught = []
+    for pin in GN_PINS:
+        try:
+            pin(oracle.lib())
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no epilogue pin catches the planted mistake: {kind}"
