@@ -162,6 +162,48 @@ int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
                         float *ds0, void *stream);
 
 /*
+ * The output epilogue of the time-mix block fused into the recurrence
+ * ("Foundry/cuda_kernels/timemix.cu" page: k_groupnorm, then k_bonus, after
+ * the WKV7 launch; k_bonus_bwd and k_groupnorm_bwd before its backward).  Per
+ * token and head, over the head's N outputs y of the recurrence,
+ *     o_j = (y_j - mean) / sqrt(var + 64e-5) * gn_w[h][j] + gn_b[h][j]
+ *           + (sum_i r_i k_i r_k[h][i]) v_j
+ * with mean and the biased variance var of y over the N channels, and the
+ * recurrence's own r, k, v.
+ *   gn_w, gn_b, r_k  [H][N] fp32: the GroupNorm's per-channel weight and bias
+ *                    (one group per head) and the bonus weight.
+ *   y                [B][T][H][N] fp32: the recurrence's output, written by the
+ *                    forward and read back by the backward.
+ *   o                [B][T][H][N] fp32: the epilogue's output.
+ * wkv7_forward_gn needs L a multiple of 16 (WKV7_EUNSUPPORTED otherwise);
+ * other arguments as in wkv7_forward.  wkv7_backward_gn takes do = dL/do in
+ * place of dy, the forward's y, and needs L == 16 and the factor cache of the
+ * matching wkv7_forward_gn call (WKV7_EINVAL otherwise, when T > 0).  It
+ * writes dr, dw, dk, dv, da, db, ds0 of the whole (recurrence + epilogue;
+ * dr, dk, dv include the bonus's own terms) and
+ *   dgn_w, dgn_b, dr_k  [H][N] fp32: parameter gradients summed over every
+ *                       batch row and token (in a fixed order, no atomics),
+ * through a caller-owned workspace of wkv7_gn_workspace_floats(B, H) floats
+ * (16-byte aligned; per-(b, h) partial sums).  No fused producers here.
+ */
+long long wkv7_gn_workspace_floats(int B, int H);
+int wkv7_forward_gn(int B, int T, int H, int N, wkv7_dtype dtype,
+                    const void *r, const void *w, const void *k,
+                    const void *v, const void *a, const void *b,
+                    const float *s0, const float *gn_w, const float *gn_b, const float *r_k,
+                    float *y, float *o, float *sT, float *ckpt,
+                    float *factors, int L, void *stream);
+int wkv7_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype,
+                     const void *r, const void *w, const void *k,
+                     const void *v, const void *a, const void *b,
+                     const float *ckpt, const float *factors, int L,
+                     const float *y, const float *do_, const float *dsT,
+                     const float *gn_w, const float *r_k,
+                     float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                     float *ds0, float *dgn_w, float *dgn_b, float *dr_k,
+                     float *workspace, void *stream);
+
+/*
  * Sequence parallelism inside one GPU for few, long sequences.  The pages
  * give the recurrence one thread block per (b, h) over all T tokens; these
  * entry points (which have no counterpart there) cut every sequence into

@@ -151,15 +151,29 @@ int wkv7_async_status(void) {
 }  // extern "C"
 
 namespace {
+// The output epilogue's arguments (wkv7_forward_gn / wkv7_backward_gn); all NULL otherwise.
+struct GnArgs {
+    const float *gn_w = nullptr, *gn_b = nullptr, *r_k = nullptr;
+    float *o = nullptr;                                          // forward
+    const float *y = nullptr;                                    // backward: the forward's y
+    float *dgn_w = nullptr, *dgn_b = nullptr, *dr_k = nullptr, *ws = nullptr;
+};
+
 // prod = 1: w, a, b carry (w_pre, kk, avec) and the backward writes (dw_pre, dkk, davec)
 int forward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,
-                 float *factors, int L, void *stream, int prod) {
+                 float *factors, int L, void *stream, int prod, const GnArgs &gn = GnArgs()) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
     if (factors && L != 16) return fail(WKV7_EINVAL, "factors need L == 16 (got %d)", L);
     if (prod && L % 16 != 0) return fail(WKV7_EUNSUPPORTED, "the fused producers need L a multiple of 16 (got %d)", L);
+    const bool epi = gn.gn_w || gn.gn_b || gn.r_k || gn.o;
+    if (epi && L % 16 != 0) return fail(WKV7_EUNSUPPORTED, "the fused epilogue needs L a multiple of 16 (got %d)", L);
+    if (epi) {
+        TRY(check_ptr(gn.gn_w, "gn_w", T > 0)); TRY(check_ptr(gn.gn_b, "gn_b", T > 0));
+        TRY(check_ptr(gn.r_k, "r_k", T > 0)); TRY(check_ptr(gn.o, "o", T > 0));
+    }
     const bool need = T > 0;
     TRY(check_ptr(r, "r", need)); TRY(check_ptr(w, prod ? "w_pre" : "w", need)); TRY(check_ptr(k, "k", need));
     TRY(check_ptr(v, "v", need)); TRY(check_ptr(a, prod ? "kk" : "a", need)); TRY(check_ptr(b, prod ? "avec" : "b", need));
@@ -175,6 +189,7 @@ int forward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.s0 = s0; p.y = y; p.sT = sT; p.ckpt = ckpt; p.fac = factors; p.prod = prod;
+    p.gn_w = gn.gn_w; p.gn_b = gn.gn_b; p.r_k = gn.r_k; p.o = gn.o;
     if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (wkv7::forward_chunk_supported(p)) return launch_status(wkv7::launch_forward_chunk(p, st), "wkv7_forward launch");
     return launch_status(wkv7::launch_forward_plain(p, st), "wkv7_forward launch");
@@ -183,7 +198,7 @@ int forward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, co
 int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                   const void *v, const void *a, const void *b, const float *ckpt, const float *factors, int L,
                   const float *dy, const float *dsT, float *dr, float *dw, float *dk, float *dv, float *da, float *db,
-                  float *ds0, void *stream, int prod) {
+                  float *ds0, void *stream, int prod, const GnArgs &gn = GnArgs()) {
     g_err[0] = '\0';
     TRY(check_dims(B, T, H, N, dtype));
     if (L < 1) return fail(WKV7_EINVAL, "L must be >= 1 (got %d)", L);
@@ -199,17 +214,39 @@ int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     TRY(check_ptr(dv, "dv", need)); TRY(check_ptr(da, prod ? "dkk" : "da", need));
     TRY(check_ptr(db, prod ? "davec" : "db", need));
     TRY(check_ptr(ds0, "ds0", false));
+    const bool epi = gn.gn_w != nullptr;
+    if (epi) {
+        if (need && (L != 16 || !factors))
+            return fail(WKV7_EINVAL, "the fused epilogue's backward needs L == 16 and the forward's factor cache");
+        TRY(check_ptr(gn.y, "y", need)); TRY(check_ptr(gn.gn_w, "gn_w", true)); TRY(check_ptr(gn.r_k, "r_k", true));
+        TRY(check_ptr(gn.dgn_w, "dgn_w", true)); TRY(check_ptr(gn.dgn_b, "dgn_b", true));
+        TRY(check_ptr(gn.dr_k, "dr_k", true)); TRY(check_ptr(gn.ws, "workspace", true));
+    }
     TRY(check_device());
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();
-    if (T == 0) return copy_state(dsT, ds0, B, H, st);
+    if (T == 0) {
+        if (epi) {  // no token: the parameter gradients are zero
+            const size_t bytes = (size_t)H * WKV7_HEAD_SIZE * sizeof(float);
+            TRY(launch_status(cudaMemsetAsync(gn.dgn_w, 0, bytes, st), "dgn_w"));
+            TRY(launch_status(cudaMemsetAsync(gn.dgn_b, 0, bytes, st), "dgn_b"));
+            TRY(launch_status(cudaMemsetAsync(gn.dr_k, 0, bytes, st), "dr_k"));
+        }
+        return copy_state(dsT, ds0, B, H, st);
+    }
 
     wkv7::SeqArgs p{};
     p.B = B; p.T = T; p.H = H; p.L = L; p.nck = wkv7_ckpt_count(T, L); p.dtype = dtype;
     p.r = r; p.w = w; p.k = k; p.v = v; p.a = a; p.b = b;
     p.ckpt_in = ckpt; p.fac_in = factors; p.dy = dy; p.dsT = dsT;
     p.dr = dr; p.dw = dw; p.dk = dk; p.dv = dv; p.da = da; p.db = db; p.ds0 = ds0; p.prod = prod;
+    p.gn_w = gn.gn_w; p.r_k = gn.r_k; p.y_in = gn.y; p.gn_part = gn.ws;
     if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
+    if (epi) {
+        TRY(launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward_gn launch"));
+        return launch_status(wkv7::launch_gn_param_reduce(B, H, gn.ws, gn.dgn_w, gn.dgn_b, gn.dr_k, st),
+                             "wkv7_backward_gn parameter reduction");
+    }
     if (wkv7::backward_chunk_supported(p)) return launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward launch");
     return launch_status(wkv7::launch_backward_plain(p, st), "wkv7_backward launch");
 }
@@ -243,6 +280,39 @@ int wkv7_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype, const void
                         float *dk, float *dv, float *dkk, float *davec, float *ds0, void *stream) {
     return backward_impl(B, T, H, N, dtype, r, w_pre, k, v, kk, avec, ckpt, factors, L, dy, dsT, dr, dw_pre, dk, dv,
                          dkk, davec, ds0, stream, 1);
+}
+
+long long wkv7_gn_workspace_floats(int B, int H) {
+    if (B < 1 || H < 1) return -1;
+    return (long long)B * H * 3 * WKV7_HEAD_SIZE;
+}
+
+int wkv7_forward_gn(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                    const void *v, const void *a, const void *b, const float *s0, const float *gn_w,
+                    const float *gn_b, const float *r_k, float *y, float *o, float *sT, float *ckpt, float *factors,
+                    int L, void *stream) {
+    GnArgs gn;
+    gn.gn_w = gn_w; gn.gn_b = gn_b; gn.r_k = r_k; gn.o = o;
+    if (T > 0 && !(gn_w && gn_b && r_k && o)) {
+        g_err[0] = '\0';
+        return fail(WKV7_EINVAL, "gn_w, gn_b, r_k and o are required");
+    }
+    return forward_impl(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, ckpt, factors, L, stream, 0, gn);
+}
+
+int wkv7_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                     const void *v, const void *a, const void *b, const float *ckpt, const float *factors, int L,
+                     const float *y, const float *do_, const float *dsT, const float *gn_w, const float *r_k,
+                     float *dr, float *dw, float *dk, float *dv, float *da, float *db, float *ds0, float *dgn_w,
+                     float *dgn_b, float *dr_k, float *workspace, void *stream) {
+    GnArgs gn;
+    gn.gn_w = gn_w; gn.r_k = r_k; gn.y = y; gn.dgn_w = dgn_w; gn.dgn_b = dgn_b; gn.dr_k = dr_k; gn.ws = workspace;
+    if (!gn_w) {
+        g_err[0] = '\0';
+        return fail(WKV7_EINVAL, "gn_w is NULL");
+    }
+    return backward_impl(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, L, do_, dsT, dr, dw, dk, dv, da, db, ds0,
+                         stream, 0, gn);
 }
 
 int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,

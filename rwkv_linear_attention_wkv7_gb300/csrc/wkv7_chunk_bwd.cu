@@ -110,9 +110,20 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // each lane fills from w_pre before the refill, and avec from a copy the split
 // phase keeps in the Gram / W slots, which the factor-cache path does not use
 // otherwise.
-template <typename E, bool kFac, bool kP>
+// kGN (with kFac, without kP): the backward of the GroupNorm + bonus output
+// epilogue ("timemix.cu" page, k_bonus_bwd and k_groupnorm_bwd) is fused in
+// front: the staged dy rows hold do = dL/do and the forward's y of the chunk
+// arrives in the Gram slot (idle on the factor-cache path); each warp turns
+// four tokens of do into the recurrence's dy in place (GroupNorm backward,
+// reductions over the head's 64 channels), leaves do s (the bonus's dv) in
+// the y slot and sum_j do_j v_j per token for the bonus's dr and dk, and
+// accumulates the parameter gradients of its lanes' two channels over every
+// token; per-(b,h) partial sums leave at the end (summed over batch rows by
+// wkv7_gn_param_reduce_kernel, no atomics).
+template <typename E, bool kFac, bool kP, bool kGN>
 __global__ void __launch_bounds__(NT, 2)
     wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
+    static_assert(!kGN || (kFac && !kP), "the epilogue's backward runs on the factor-cache path without producers");
     // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -169,12 +180,30 @@ __global__ void __launch_bounds__(NT, 2)
     }
     __syncthreads();
     int stuck = -1, s_phase = -1;  // the chunk whose wait ran out; the phase of the last start-state copy
-    constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0));
+    constexpr unsigned kChunkBytes =
+        (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
+    // kGN: per-lane channel constants (channels 2 lane, 2 lane + 1; key rows rA, rB) and
+    // parameter-gradient sums; per-token sum_j do_j v_j past the dw carry in the W slot
+    float2 gwc = {}, rkc = {}, pgw = {}, pgb = {}, prk = {};
+    float rkA = 0.f, rkB = 0.f;
+    float *const dsv = Wm + 256;
+    static_assert(256 * 4 + C * 4 <= 1280, "the dw carry and the per-token sums fit the W slot");
+    if constexpr (kGN) {
+        gwc = __ldg(reinterpret_cast<const float2 *>(p.gn_w + h * 64 + 2 * lane));
+        rkc = __ldg(reinterpret_cast<const float2 *>(p.r_k + h * 64 + 2 * lane));
+        rkA = __ldg(p.r_k + h * 64 + rA);
+        rkB = __ldg(p.r_k + h * 64 + rB);
+    }
+    // the last chunk's dw carry partials: the Gram slot, or the W slot when the Gram slot stages y
+    float *const carp = kGN ? Wm : Gm;
     constexpr unsigned kS0Bytes = 64 * OS * 4;
     auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each, lanes 0..6 of warp 0
         if (tid < 7) {
             void *const dst = tid < 6 ? static_cast<void *>(raw + tid * C * RS) : static_cast<void *>(dyf);
             tma_rows(dst, &maps.m[tid], h, c * C, bi, &bar);
+        }
+        if constexpr (kGN) {  // and the forward's y of the chunk (lane 7)
+            if (tid == 7) tma_rows(Gm, &maps.m[8], h, c * C, bi, &bar);
         }
     };
     auto load_s0 = [&](int c) {  // thread 0
@@ -238,11 +267,40 @@ __global__ void __launch_bounds__(NT, 2)
             stuck = c;
             break;
         }
+        if constexpr (kGN) {  // do -> dy through the epilogue, four tokens per warp (channels 2 lane, +1)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * warp + u, j = 2 * lane;
+                const float2 yv = *reinterpret_cast<const float2 *>(Gm + t * SP + j);
+                const float2 dov = *reinterpret_cast<const float2 *>(dyf + t * SP + j);
+                const float v0 = ld_raw(raw, VV, t, j), v1 = ld_raw(raw, VV, t, j + 1);
+                const float r0 = ld_raw(raw, VR, t, j), r1 = ld_raw(raw, VR, t, j + 1);
+                const float k0 = ld_raw(raw, VK, t, j), k1 = ld_raw(raw, VK, t, j + 1);
+                const float mean = warp_allsum(yv.x + yv.y) * (1.f / 64.f);
+                const float c0 = yv.x - mean, c1 = yv.y - mean;
+                const float rstd = 1.f / sqrtf(warp_allsum(c0 * c0 + c1 * c1) * (1.f / 64.f) + kGnEps);
+                const float x0 = c0 * rstd, x1 = c1 * rstd;
+                const float n0 = dov.x * gwc.x, n1 = dov.y * gwc.y;
+                const float mn = warp_allsum(n0 + n1) * (1.f / 64.f);
+                const float mx = warp_allsum(n0 * x0 + n1 * x1) * (1.f / 64.f);
+                const float sb = warp_allsum(r0 * k0 * rkc.x + r1 * k1 * rkc.y);
+                const float ds = warp_allsum(dov.x * v0 + dov.y * v1);
+                *reinterpret_cast<float2 *>(dyf + t * SP + j) =
+                    make_float2(rstd * (n0 - mn - x0 * mx), rstd * (n1 - mn - x1 * mx));
+                *reinterpret_cast<float2 *>(Gm + t * SP + j) = make_float2(dov.x * sb, dov.y * sb);
+                if (lane == 0) dsv[t] = ds;
+                pgw.x += dov.x * x0; pgw.y += dov.y * x1;
+                pgb.x += dov.x; pgb.y += dov.y;
+                prk.x += ds * r0 * k0; prk.y += ds * r1 * k1;
+            }
+            __syncthreads();
+        }
         if (exact) {
             drain_then_load_s0();
             mbar_wait(&bar_s, ph, p.err, &lost);
-            bwd_chunk_exact<E, kP, OS>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT),
-                                       reinterpret_cast<float *>(Bs + B_Y), Gh, nv, p, base0, tstride, t0, carryA, carryB);
+            bwd_chunk_exact<E, kP, OS, kGN>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT),
+                                            reinterpret_cast<float *>(Bs + B_Y), Gh, nv, p, base0, tstride, t0,
+                                            carryA, carryB, Gm, dsv, p.r_k + h * 64);
             fence_proxy_async();  // the per-token path wrote into slots the copies refill
             __syncthreads();
             if (c > 0) {
@@ -475,13 +533,13 @@ __global__ void __launch_bounds__(NT, 2)
             if (g == 0) {
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
-                    Gm[warp * 64 + 8 * nt + 2 * q] = part[nt][0];
-                    Gm[warp * 64 + 8 * nt + 2 * q + 1] = part[nt][1];
+                    carp[warp * 64 + 8 * nt + 2 * q] = part[nt][0];
+                    carp[warp * 64 + 8 * nt + 2 * q + 1] = part[nt][1];
                 }
             }
             __syncthreads();
-            carryA = Gm[rA] + Gm[64 + rA] + Gm[128 + rA] + Gm[192 + rA];
-            carryB = Gm[rB] + Gm[64 + rB] + Gm[128 + rB] + Gm[192 + rB];
+            carryA = carp[rA] + carp[64 + rA] + carp[128 + rA] + carp[192 + rA];
+            carryB = carp[rB] + carp[64 + rB] + carp[128 + rB] + carp[192 + rB];
         }
 
         // G2: [DV | DSA] = G [K' | B'] + DY [Q'^T | (W Q_b)^T]
@@ -505,6 +563,16 @@ __global__ void __launch_bounds__(NT, 2)
                 ldb2(QQ, 16, 0, lane, b2, b3);
             }
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(dvs, dyA, bq); }
+        }
+        if constexpr (kGN) {  // + the bonus's own dv, do s, from the y slot (before the next copies refill it)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = 8 * nt + 2 * q;
+                dvs[nt][0] += Gm[t * SP + rA];
+                dvs[nt][1] += Gm[(t + 1) * SP + rA];
+                dvs[nt][2] += Gm[t * SP + rB];
+                dvs[nt][3] += Gm[(t + 1) * SP + rB];
+            }
         }
         {
             __nv_bfloat16 *dhh = hi_of(Bs, B_DSH), *dhl = lo_of(Bs, B_DSH, 16);
@@ -688,8 +756,14 @@ __global__ void __launch_bounds__(NT, 2)
                     // r o dr = r^ o X3_r, a o da = a^ o X3_a, b o db = b~ o X4_b, k o dk = k~ o X4_k
                     ee[nt][m] = av[vi] * xa;
                     zz[nt][m] = rv[vi] * xr + ee[nt][m] - bv[vi] * xb - kv[vi] * xk;
-                    gdr[t * OS + row] = d * xr;
-                    gdk[t * OS + row] = inv * xk;
+                    if constexpr (kGN) {  // + the bonus's dr = ds k r_k and dk = ds r r_k
+                        const float rkr = m < 2 ? rkA : rkB;
+                        gdr[t * OS + row] = d * xr + dsv[t] * (kv[vi] * d) * rkr;
+                        gdk[t * OS + row] = inv * xk + dsv[t] * (rv[vi] * inv) * rkr;
+                    } else {
+                        gdr[t * OS + row] = d * xr;
+                        gdk[t * OS + row] = inv * xk;
+                    }
                     if constexpr (kP) {  // dkk = -da + avec db, davec = kk db (k_comp_keymod)
                         const float db_ = inv * xb;
                         gda[t * OS + row] = avs[t * OS + row] * db_ - dp * xa;
@@ -752,6 +826,16 @@ __global__ void __launch_bounds__(NT, 2)
         mbar_drain(&bar, (nchunks - 1 - stuck) & 1);
         if (tid == 0 && s_phase >= 0) mbar_drain(&bar_s, s_phase);
     }
+    if constexpr (kGN) {  // this head's parameter-gradient sums: the four warps' token groups combined
+        __syncthreads();
+        float *const sc = Gm;  // [warp][3][64]
+        *reinterpret_cast<float2 *>(sc + (warp * 3 + 0) * 64 + 2 * lane) = pgw;
+        *reinterpret_cast<float2 *>(sc + (warp * 3 + 1) * 64 + 2 * lane) = pgb;
+        *reinterpret_cast<float2 *>(sc + (warp * 3 + 2) * 64 + 2 * lane) = prk;
+        __syncthreads();
+        for (int o = tid; o < 3 * 64; o += NT)
+            p.gn_part[(size_t)bh * 192 + o] = sc[o] + sc[192 + o] + sc[384 + o] + sc[576 + o];
+    }
     if (p.ds0) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -761,19 +845,31 @@ __global__ void __launch_bounds__(NT, 2)
     }
 }
 
-template <typename E, bool kFac, bool kP>
+template <typename E, bool kFac, bool kP, bool kGN = false>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = bwd_smem_bytes<E>();
     InputMaps maps;
     OutputMaps omaps;
-    cudaError_t e = encode_input_maps(&maps, p, p.dy);  // six inputs, dy, and the checkpoints (box OS x 64)
+    cudaError_t e = encode_input_maps(&maps, p, p.dy);  // six inputs, dy (or do), and the checkpoints (box OS x 64)
     if (e == cudaSuccess) e = encode_ckpt_map(&maps.m[7], p.ckpt_in, (long long)p.B * p.H * p.nck * 64, 64);
+    if (e == cudaSuccess && kGN) e = encode_rows_map(&maps.m[8], p.y_in, 4, p.B, p.T, p.H);  // the forward's y
     if (e == cudaSuccess) e = encode_output_maps(&omaps, p);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac, kP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac, kP, kGN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E, kFac, kP><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
+    wkv7_bwd_chunk_kernel<E, kFac, kP, kGN><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
     return cudaGetLastError();
+}
+
+// Sum of the per-(b,h) parameter-gradient partials over the batch rows, in a
+// fixed order (no atomics): one thread per (h, parameter, channel).
+__global__ void wkv7_gn_param_reduce_kernel(int B, int H, const float *part, float *dgn_w, float *dgn_b, float *dr_k) {
+    const int h = blockIdx.x, o = threadIdx.x;  // o = parameter * 64 + channel
+    float s = 0.f;
+    for (int b = 0; b < B; ++b) s += part[((size_t)b * H + h) * 192 + o];
+    float *const dst[3] = {dgn_w, dgn_b, dr_k};
+    dst[o >> 6][h * 64 + (o & 63)] = s;
 }
 
 }  // namespace
@@ -791,7 +887,17 @@ static bool tensor_core_backward() {
     return v && strcmp(v, "tcgen05") == 0;
 }
 
+cudaError_t launch_gn_param_reduce(int B, int H, const float *part, float *dgn_w, float *dgn_b, float *dr_k,
+                                   cudaStream_t st) {
+    wkv7_gn_param_reduce_kernel<<<H, 192, 0, st>>>(B, H, part, dgn_w, dgn_b, dr_k);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_backward_chunk(const SeqArgs &p, cudaStream_t st) {
+    if (p.gn_w) {  // the output epilogue's backward in front: factor-cache path, no fused producers
+        if (!p.fac_in || p.prod) return cudaErrorInvalidValue;
+        return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false, true>(p, st) : launch_t<float, true, false, true>(p, st);
+    }
     if (backward_tc_supported(p) && tensor_core_backward()) return launch_backward_tc(p, st);
     if (p.prod) {  // the fused producers run with the factor cache only
         if (!p.fac_in) return cudaErrorInvalidValue;

@@ -31,10 +31,13 @@ __device__ __forceinline__ float rows_sum(float x) {
 // column partial sums in red (5 x 4 x 64 fp32).  Writes all six gradients of
 // the chunk's tokens and returns, per lane, the dw carry for columns jA/jB of
 // the key-row layout (w_0 o dw_0 + a_0 o da_0).
-template <typename E, bool kP, int S0S>
+// kGN: the output epilogue's own terms join dv, dr, dk: gpost ([C][SP]) holds
+// do s per (token, value), dsv the per-token sum_j do_j v_j, rkh the head's r_k.
+template <typename E, bool kP, int S0S, bool kGN = false>
 __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s, float *Sps, float *red,
                                 float G[8][4], int nv, const SeqArgs &p, size_t base0, size_t tstride, int t0,
-                                float &carryA, float &carryB) {
+                                float &carryA, float &carryB, const float *gpost = nullptr,
+                                const float *dsv = nullptr, const float *rkh = nullptr) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q = lane & 3;
     const int rA = warp * 16 + g, rB = rA + 8;
     for (int t = nv - 1; t >= 0; --t) {
@@ -96,8 +99,8 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
         dv0 = quad_sum(dv0); dv1 = quad_sum(dv1);
         ds0 = quad_sum(ds0); ds1 = quad_sum(ds1);
         if (q == 0) {
-            p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dv0;
-            p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dv1;
+            p.dv[base0 + (size_t)(t0 + t) * tstride + rA] = dv0 + (kGN ? gpost[t * SP + rA] : 0.f);
+            p.dv[base0 + (size_t)(t0 + t) * tstride + rB] = dv1 + (kGN ? gpost[t * SP + rB] : 0.f);
         }
         __syncthreads();  // S_{t-1} visible in Sps
         // column partials over this lane's two rows, reduced over the warp's 16 rows
@@ -150,8 +153,12 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
             float *outs[5] = {p.dr, p.dk, p.db, p.dw, p.da};
             for (int o = tid; o < 5 * 64; o += NT) {
                 const int m = o >> 6, j = o & 63;
-                const float s = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
-                                red[(m * 4 + 3) * 64 + j];
+                float s = red[(m * 4 + 0) * 64 + j] + red[(m * 4 + 1) * 64 + j] + red[(m * 4 + 2) * 64 + j] +
+                          red[(m * 4 + 3) * 64 + j];
+                if constexpr (kGN) {  // the bonus's dr = ds k r_k, dk = ds r r_k
+                    if (m == 0) s += dsv[t] * ld_raw(raw, VK, t, j) * rkh[j];
+                    if (m == 1) s += dsv[t] * ld_raw(raw, VR, t, j) * rkh[j];
+                }
                 outs[m][base0 + (size_t)(t0 + t) * tstride + j] = s;
             }
         }

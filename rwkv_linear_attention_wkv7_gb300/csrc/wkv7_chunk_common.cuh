@@ -109,7 +109,9 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
 // fills a padded [C][RS] staging block; the columns past 64 and the tokens
 // past T are out of range and arrive as zeros.
 struct InputMaps {
-    CUtensorMap m[8];  // r, w, k, v, a, b; then dy (backward) or y; then the checkpoints (forward)
+    // r, w, k, v, a, b; then dy (backward) or y; then the checkpoints (forward); then the
+    // epilogue's o (forward) or the forward's y (backward) of the GroupNorm + bonus calls
+    CUtensorMap m[9];
 };
 __device__ __forceinline__ void tma_rows(void *dst, const CUtensorMap *map, int h, int t0, int b, uint64_t *bar) {
     asm volatile(
@@ -286,6 +288,15 @@ inline cudaError_t encode_output_maps(OutputMaps *maps, const SeqArgs &p) {
     return cudaSuccess;
 }
 
+// Sum over the 32 lanes of a warp, returned to every lane.
+__device__ __forceinline__ float warp_allsum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+// The GroupNorm epsilon of the output epilogue ("timemix.cu" page, k_groupnorm).
+constexpr float kGnEps = 64e-5f;
+
 // Hardware approximate reciprocal (rcp.approx, about 1 ulp); used for 1/d_t,
 // whose rounding is far below the split-bf16 product error.
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -386,11 +397,12 @@ __device__ __forceinline__ void prep_inverse(const float *G, float *Wm) {
 }
 
 // W = (I - M_b)^{-1} as above, M_b read from a row-major copy with row
-// stride MBS floats (16-byte aligned rows): each row comes in with broadcast
+// stride MBS floats (16-byte aligned rows, unpadded: every lane reads the
+// same row, a broadcast): each row comes in with broadcast
 // 16-byte loads issued ahead of the product chain.  Lane t holds column t of
 // W and writes it, split into bf16 hi + lo, as row t of W^T in two compact
 // 16 x 16 matrices of row stride CS (four 16-byte stores per lane).
-constexpr int MBS = 20;
+constexpr int MBS = 16;
 constexpr int CS = 24;  // row stride (elements) of a compact 16 x 16 split matrix: ldmatrix rows 12 banks apart
 __device__ __forceinline__ void prep_inverse_t(const float *Mb, __nv_bfloat16 *wt_hi, __nv_bfloat16 *wt_lo) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -23,6 +23,13 @@
 //
 // A chunk whose cumulative decay leaves [1e-20, 1e20] (e.g. w = 0) cannot use
 // 1/d_t; it takes the exact per-token recurrence on the same register layout.
+//
+// kGN: the output epilogue of the "timemix.cu" page (k_groupnorm, then
+// k_bonus) is fused in: while a chunk's rows are staged, the bonus
+// (sum_j r_j k_j r_k[j]) v of each token goes into a [C][64] tile; once the
+// chunk's y is staged, each warp normalises four tokens over the head's 64
+// outputs (biased variance, eps 64e-5, per-channel weight and bias) and adds
+// the bonus in place; y and the epilogue output o leave by two tensor stores.
 #include <type_traits>
 
 #include "wkv7_chunk_common.cuh"
@@ -55,8 +62,9 @@ constexpr int kBytes = B_MB + C * MBS * 4;
 static_assert(B_BT % 16 == 0 && B_Y % 128 == 0 && B_QB % 16 == 0 && B_MB % 16 == 0 && YS == OS,
               "aligned blocks; the y staging block is a tensor-store source");
 
-template <typename E>
-__host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
+constexpr int kBonusBytes = C * 64 * 4;  // kGN: bonus, then epilogue output, tile [C][64] fp32 (after kBytes)
+template <typename E, bool kGN>
+__host__ __device__ constexpr size_t fwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes + (kGN ? kBonusBytes : 0); }
 
 __device__ __forceinline__ HL hl(const unsigned char *base, int off) {
     const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
@@ -74,7 +82,8 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
 }
 
 // kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec); see in_w.
-template <typename E, bool kP>
+// kGN: the GroupNorm + bonus output epilogue (see the file header).
+template <typename E, bool kP, bool kGN>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
     extern __shared__ __align__(128) unsigned char smem[];
     // bf16 inputs: v is exact in bf16, so products with v as the A operand skip its (zero) lo part
@@ -83,6 +92,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     unsigned char *Bs = smem + raw_bytes<E>();
     float *dd = reinterpret_cast<float *>(Bs + B_DD), *ys = reinterpret_cast<float *>(Bs + B_Y);
     float *Mb = reinterpret_cast<float *>(Bs + B_MB);
+    float *bon = reinterpret_cast<float *>(Bs + kBytes);  // kGN: bonus / epilogue output tile [C][64]
     const HL BT = hl(Bs, B_BT), KT = hl(Bs, B_KT), AH = hl(Bs, B_AH), RH = hl(Bs, B_RH), VM = hl(Bs, B_VM);
     const HL QB = hlc(Bs, B_QB), MK = hlc(Bs, B_MK), QK = hlc(Bs, B_QK), WT = hlc(Bs, B_WT);
 
@@ -122,6 +132,21 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     };
     if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     prefetch(0);
+    // kGN: bonus tile of the staged chunk, bon[t][j] = (sum_i r_i k_i r_k[i]) v_j; thread
+    // (t = e / 16, j = 4 (e % 16)) sums its four channels, the 16 lanes of a token finish it
+    auto write_bonus = [&]() {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
+            const float4 rr = ld_raw4(raw, VR, t, j), kq = ld_raw4(raw, VK, t, j);
+            const float4 rk = __ldg(reinterpret_cast<const float4 *>(p.r_k + h * 64 + j));
+            float sb = rr.x * kq.x * rk.x + rr.y * kq.y * rk.y + rr.z * kq.z * rk.z + rr.w * kq.w * rk.w;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) sb += __shfl_xor_sync(0xffffffffu, sb, o);
+            const float4 vv = ld_raw4(raw, VV, t, j);
+            *reinterpret_cast<float4 *>(bon + t * 64 + j) = make_float4(sb * vv.x, sb * vv.y, sb * vv.z, sb * vv.w);
+        }
+    };
 
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * C;
@@ -167,6 +192,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
                 if (kVLo) st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
             }
+            if constexpr (kGN) write_bonus();
             // bf16 v is its own hi part: its A fragment (A[i][t] = v[t][i]) comes straight
             // from the staged input, before the barrier that lets the next chunk's copies in
             AFrag vA;
@@ -325,6 +351,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             }
         } else {
             // exact per-token recurrence for a chunk whose decay leaves the factorisable range
+            if constexpr (kGN) write_bonus();
             write_ckpt();
             if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();
@@ -370,8 +397,26 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         }
         fence_proxy_async();  // the staged y tile is read by a tensor store
         __syncthreads();
-        if (tid == 0) {  // y of the chunk: one tensor store (tokens past T are not written)
+        if constexpr (kGN) {  // o = GroupNorm(y) + bonus, four tokens per warp, in place over the bonus tile
+            const float2 gw = __ldg(reinterpret_cast<const float2 *>(p.gn_w + h * 64 + 2 * lane));
+            const float2 gb = __ldg(reinterpret_cast<const float2 *>(p.gn_b + h * 64 + 2 * lane));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 4 * warp + u;
+                const float2 yv = *reinterpret_cast<const float2 *>(ys + t * YS + 2 * lane);
+                const float mean = warp_allsum(yv.x + yv.y) * (1.f / 64.f);
+                const float c0 = yv.x - mean, c1 = yv.y - mean;
+                const float rstd = 1.f / sqrtf(warp_allsum(c0 * c0 + c1 * c1) * (1.f / 64.f) + kGnEps);
+                float2 *ob = reinterpret_cast<float2 *>(bon + t * 64 + 2 * lane);
+                const float2 bv = *ob;
+                *ob = make_float2(c0 * rstd * gw.x + gb.x + bv.x, c1 * rstd * gw.y + gb.y + bv.y);
+            }
+            fence_proxy_async();
+            __syncthreads();
+        }
+        if (tid == 0) {  // y (and o) of the chunk: one tensor store each (tokens past T are not written)
             tma_store_rows(&maps.m[6], ys, h, t0, bi);
+            if constexpr (kGN) tma_store_rows(&maps.m[8], bon, h, t0, bi);
             bulk_commit();
         }
     }
@@ -387,17 +432,18 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     }
 }
 
-template <typename E, bool kP>
+template <typename E, bool kP, bool kGN>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
-    const size_t sm = fwd_smem_bytes<E>();
-    InputMaps maps;  // six inputs, and y (box OS) in the last slot
+    const size_t sm = fwd_smem_bytes<E, kGN>();
+    InputMaps maps;  // six inputs, y (box OS), the checkpoints, and o (box 64) with kGN
     cudaError_t e = encode_input_maps(&maps, p, nullptr);
     if (e == cudaSuccess) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
     if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64);
+    if (e == cudaSuccess && kGN) e = encode_rows_map(&maps.m[8], p.o, 4, p.B, p.T, p.H, 64);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP, kGN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_fwd_chunk_kernel<E, kP><<<p.B * p.H, NT, sm, st>>>(p, maps);
+    wkv7_fwd_chunk_kernel<E, kP, kGN><<<p.B * p.H, NT, sm, st>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -406,8 +452,9 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 bool forward_chunk_supported(const SeqArgs &p) { return p.L % C == 0; }
 
 cudaError_t launch_forward_chunk(const SeqArgs &p, cudaStream_t st) {
-    if (p.prod) return p.dtype == 1 ? launch_t<__nv_bfloat16, true>(p, st) : launch_t<float, true>(p, st);
-    return p.dtype == 1 ? launch_t<__nv_bfloat16, false>(p, st) : launch_t<float, false>(p, st);
+    if (p.gn_w) return p.dtype == 1 ? launch_t<__nv_bfloat16, false, true>(p, st) : launch_t<float, false, true>(p, st);
+    if (p.prod) return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false>(p, st) : launch_t<float, true, false>(p, st);
+    return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false>(p, st) : launch_t<float, false, false>(p, st);
 }
 
 }  // namespace wkv7

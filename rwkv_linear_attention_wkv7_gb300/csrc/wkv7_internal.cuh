@@ -26,6 +26,14 @@ struct SeqArgs {
     // sigmoid(w_pre)), a = -kk, b = kk * avec) and the backward writes the gradients of
     // those (dw_pre, dkk, davec) into dw, da, db
     int prod;
+    // GroupNorm + bonus output epilogue (wkv7_forward_gn / wkv7_backward_gn), else NULL:
+    // per-channel weights [H][64]; the forward's epilogue output o; the backward reads
+    // the forward's y (y_in), takes do in dy, and writes per-(b,h) partial sums of
+    // dgn_w, dgn_b, dr_k ([B*H][3][64]) into gn_part
+    const float *gn_w, *gn_b, *r_k;
+    float *o;
+    const float *y_in;
+    float *gn_part;
 };
 
 // Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the
@@ -63,6 +71,8 @@ bool backward_chunk_supported(const SeqArgs &a);
 cudaError_t launch_backward_chunk(const SeqArgs &a, cudaStream_t s);
 bool backward_tc_supported(const SeqArgs &a);
 cudaError_t launch_backward_tc(const SeqArgs &a, cudaStream_t s);
+cudaError_t launch_gn_param_reduce(int B, int H, const float *part, float *dgn_w, float *dgn_b, float *dr_k,
+                                   cudaStream_t s);
 cudaError_t launch_decode_step(int B, int H, int dtype, const void *r, const void *w,
                                const void *k, const void *v, const void *a, const void *b,
                                float *state, float *y, cudaStream_t s);

@@ -121,6 +121,18 @@ def stream_inputs(spec: WorkloadSpec, fused: bool = False) -> Iterator[Tuple[str
     yield "dsT", dsT if spec.with_dsT else None
 
 
+def gn_params(H: int, N: int = 64, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """Seeded weights of the GroupNorm + bonus output epilogue, each [H][N]
+    fp32 (one generator, draw order gn_w, gn_b, r_k): gn_w = 1 + 0.5 N(0,1),
+    gn_b = 0.5 N(0,1), r_k = 0.5 N(0,1) -- trained-looking scales around the
+    identity GroupNorm, with no trained values involved."""
+    g = torch.Generator().manual_seed(seed)
+    gn_w = 1.0 + 0.5 * torch.randn((H, N), generator=g)
+    gn_b = 0.5 * torch.randn((H, N), generator=g)
+    r_k = 0.5 * torch.randn((H, N), generator=g)
+    return {"gn_w": gn_w, "gn_b": gn_b, "r_k": r_k}
+
+
 def make_inputs(spec: WorkloadSpec, device: str = "cpu", fused: bool = False) -> Dict[str, Optional[torch.Tensor]]:
     """All inputs of ``spec`` as a dict, moved to ``device`` one by one."""
     out = {}

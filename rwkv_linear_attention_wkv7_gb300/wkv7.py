@@ -66,6 +66,12 @@ def load(path: str) -> ctypes.CDLL:
     L.wkv7_forward_fused.restype = ci
     L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
     L.wkv7_backward_fused.restype = ci
+    L.wkv7_gn_workspace_floats.argtypes = [ci, ci]
+    L.wkv7_gn_workspace_floats.restype = ctypes.c_longlong
+    L.wkv7_forward_gn.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp] * 4 + [fp] * 5 + [ci, vp]
+    L.wkv7_forward_gn.restype = ci
+    L.wkv7_backward_gn.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp, ci] + [fp] * 5 + [fp] * 7 + [fp] * 4 + [vp]
+    L.wkv7_backward_gn.restype = ci
     L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
     L.wkv7_decode_step.restype = ci
     L.wkv7_async_status.argtypes = []
@@ -218,6 +224,62 @@ def backward_fused(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=None, L: int = 16, wa
     the factor cache of the matching ``forward_fused`` call."""
     return backward(r, w_pre, k, v, kk, avec, ckpt, dy, dsT=dsT, L=L, want_ds0=want_ds0, factors=factors,
                     out=out, stream=stream, _entry="wkv7_backward_fused", _names=FUSED_GRAD_NAMES)
+
+
+def forward_gn(r, w, k, v, a, b, gn_w, gn_b, r_k, s0=None, L: int = 16, want_factors: bool = True,
+               out: Optional[Dict[str, torch.Tensor]] = None, stream=None):
+    """The recurrence with the GroupNorm + bonus output epilogue fused in
+    (gn_w, gn_b, r_k [H][64] fp32).  Returns (o, y, sT, ckpt, factors): o the
+    epilogue's output, y the recurrence's (read back by ``backward_gn``)."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+    for n, t in (("gn_w", gn_w), ("gn_b", gn_b), ("r_k", r_k)):
+        _f32(t, (H, N), dev, n)
+    y = out.get("y") if out.get("y") is not None else torch.empty((B, T, H, N), device=dev)
+    o = out.get("o") if out.get("o") is not None else torch.empty((B, T, H, N), device=dev)
+    sT = out.get("sT") if out.get("sT") is not None else torch.empty((B, H, N, N), device=dev)
+    ck = out.get("ckpt") if out.get("ckpt") is not None else torch.empty((B, H, ckpt_count(T, L), N, N), device=dev)
+    fac = None
+    if want_factors:
+        fac = out.get("factors") if out.get("factors") is not None else torch.empty((B, H, factor_floats(T)),
+                                                                                  device=dev)
+    _f32(s0, (B, H, N, N), dev, "s0")
+    rc = lib().wkv7_forward_gn(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(gn_w), _ptr(gn_b), _ptr(r_k),
+                               _ptr(y), _ptr(o), _ptr(sT), _ptr(ck), _ptr(fac), L, _stream(stream))
+    _check("wkv7_forward_gn", rc)
+    return o, y, sT, ck, fac
+
+
+def gn_workspace_floats(B: int, H: int) -> int:
+    return lib().wkv7_gn_workspace_floats(B, H)
+
+
+def backward_gn(r, w, k, v, a, b, ckpt, factors, y, do, gn_w, r_k, dsT=None, L: int = 16, workspace=None,
+                out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Gradients of sum(o * do) + sum(sT * dsT) through the epilogue and the
+    recurrence: dr, dw, dk, dv, da, db, ds0 and dgn_w, dgn_b, dr_k ([H][64])."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+    g = {n: out.get(n) if out.get(n) is not None else torch.empty((B, T, H, N), device=dev) for n in GRAD_NAMES}
+    g["ds0"] = out.get("ds0") if out.get("ds0") is not None else torch.empty((B, H, N, N), device=dev)
+    for n in ("dgn_w", "dgn_b", "dr_k"):
+        g[n] = out.get(n) if out.get(n) is not None else torch.empty((H, N), device=dev)
+    ws = workspace if workspace is not None else torch.empty(gn_workspace_floats(B, H), device=dev)
+    _f32(y, (B, T, H, N), dev, "y")
+    _f32(do, (B, T, H, N), dev, "do")
+    _f32(dsT, (B, H, N, N), dev, "dsT")
+    rc = lib().wkv7_backward_gn(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(ckpt), _ptr(factors), L, _ptr(y),
+                                _ptr(do), _ptr(dsT), _ptr(gn_w), _ptr(r_k), *(_ptr(g[n]) for n in GRAD_NAMES),
+                                _ptr(g["ds0"]), _ptr(g["dgn_w"]), _ptr(g["dgn_b"]), _ptr(g["dr_k"]), _ptr(ws),
+                                _stream(stream))
+    _check("wkv7_backward_gn", rc)
+    return g
 
 
 def timesplit_workspace_floats(B: int, T: int, H: int, nseg: int) -> int:

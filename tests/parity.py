@@ -168,3 +168,58 @@ def sample_heads(B, H, n=6, seed=0):
     while len(heads) < min(n, B * H):
         heads.add((int(g.integers(0, B)), int(g.integers(0, H))))
     return sorted(heads)
+
+
+# ---- the GroupNorm + bonus output epilogue (wkv7_forward_gn / wkv7_backward_gn)
+GN_PARAMS = ("gn_w", "gn_b", "r_k")
+GN_GRADS = ("dgn_w", "dgn_b", "dr_k")
+
+
+def run_gpu_gn(d, gp):
+    """Forward + backward through the epilogue entry points; ``d["dy"]`` serves as do."""
+    xs = [d[n] for n in INPUTS]
+    o, y, sT, ck, fac = wkv7.forward_gn(*xs, gp["gn_w"], gp["gn_b"], gp["r_k"], s0=d.get("s0"), L=16)
+    g = wkv7.backward_gn(*xs, ck, fac, y, d["dy"], gp["gn_w"], gp["r_k"], dsT=d.get("dsT"))
+    torch.cuda.synchronize()
+    wkv7.async_status()
+    return {"o": o, "y": y, "sT": sT, "ckpt": ck, **g}
+
+
+def oracle_head_gn(host, gp, b, h):
+    """Oracle results of head (b, h) through recurrence + epilogue (B=H=1 shapes);
+    the parameter gradients are this head's share of the sum over batch rows."""
+    sl = {n: _head_input(host, n, b, h) for n in INPUTS + ("s0", "dy", "dsT")}
+    p = {n: gp[n][h:h + 1] for n in GN_PARAMS}
+    o, y, sT, ck = oracle.forward_gn(*(sl[n] for n in INPUTS), p["gn_w"], p["gn_b"], p["r_k"], s0=sl["s0"], L=16)
+    res = {"o": o, "y": y, "sT": sT, "ckpt": ck}
+    res.update(oracle.backward_gn(*(sl[n] for n in INPUTS), p["gn_w"], p["r_k"], sl["dy"], s0=sl["s0"], dsT=sl["dsT"]))
+    return res
+
+
+def check_heads_gn(host, gp, out, heads, B):
+    """Every listed head element by element (o, y, sT, checkpoints at the forward
+    bar; all gradients at the gradient bar), and the parameter gradients of every
+    head index h that appears with all B batch rows, summed over them."""
+    refs = oracle.per_head(lambda b, h: oracle_head_gn(host, gp, b, h), heads)
+    worst = {}
+    psum = {}
+    for (b, h), ref in zip(heads, refs):
+        got = gpu_head({k: v for k, v in out.items() if k not in GN_GRADS}, b, h)
+        for k in ("o", "y", "sT", "ckpt"):
+            e = max_rel(got[k], ref[k])
+            assert e <= FWD_TOL, f"head ({b}, {h}) {k}: max err {e:.3e}"
+            worst[k] = max(worst.get(k, 0.0), e)
+        for k in GRADS + ("ds0",):
+            e = grad_rel(got[k], ref[k])
+            assert e <= GRAD_TOL, f"head ({b}, {h}) {k}: err {e:.3e}"
+            worst[k] = max(worst.get(k, 0.0), e)
+        for k in GN_GRADS:
+            psum.setdefault(h, {}).setdefault(k, []).append(ref[k][0])
+    for h, d in psum.items():
+        if len(d["dgn_w"]) != B:
+            continue
+        for k in GN_GRADS:
+            e = grad_rel(out[k][h].double().cpu().numpy(), np.sum(d[k], axis=0))
+            assert e <= GRAD_TOL, f"h={h} {k}: err {e:.3e}"
+            worst[k] = max(worst.get(k, 0.0), e)
+    return worst

@@ -47,7 +47,8 @@ def test_header_is_plain_c_and_cpp():
 def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
-                     "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused"):
+                     "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused",
+                     "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats"):
         assert required in names
 
 
@@ -125,6 +126,38 @@ def test_fused_entry_points_reject_bad_arguments(lib):
     bad = list(args)
     bad[21] = None  # davec missing
     assert lib.wkv7_backward_fused(*bad) == EINVAL and "davec is NULL" in wkv7.last_error()
+
+
+def test_gn_entry_points_reject_bad_arguments(lib):
+    """The fused output epilogue: forward needs its three weights, o and L a
+    multiple of 16; backward needs L == 16, the factor cache, y, the weights,
+    the parameter-gradient outputs and the workspace."""
+    p = ctypes.c_void_p(4096)
+    assert lib.wkv7_gn_workspace_floats(2, 3) == 2 * 3 * 3 * 64
+    assert lib.wkv7_gn_workspace_floats(0, 3) == -1
+    fwd = [1, 4, 1, 64, 0] + [p] * 6 + [None, p, p, p] + [p, p, None, None, None, 16, None]
+    bad = list(fwd)
+    bad[14] = None  # r_k
+    assert lib.wkv7_forward_gn(*bad) == EINVAL and "required" in wkv7.last_error()
+    bad = list(fwd)
+    bad[20] = 8  # stride
+    assert lib.wkv7_forward_gn(*bad) == EUNSUPPORTED and "multiple of 16" in wkv7.last_error()
+    bad = list(fwd)
+    bad[12] = ctypes.c_void_p(4100)  # gn_w misaligned
+    assert lib.wkv7_forward_gn(*bad) == EINVAL and "gn_w" in wkv7.last_error()
+    bwd = [1, 4, 1, 64, 0] + [p] * 6 + [p, p, 16, p, p, None, p, p] + [p] * 6 + [None] + [p] * 3 + [p, None]
+    bad = list(bwd)
+    bad[12] = None  # no factor cache
+    assert lib.wkv7_backward_gn(*bad) == EINVAL and "factor cache" in wkv7.last_error()
+    bad = list(bwd)
+    bad[14] = None  # y
+    assert lib.wkv7_backward_gn(*bad) == EINVAL and "y is NULL" in wkv7.last_error()
+    bad = list(bwd)
+    bad[29] = None  # workspace
+    assert lib.wkv7_backward_gn(*bad) == EINVAL and "workspace" in wkv7.last_error()
+    bad = list(bwd)
+    bad[17] = None  # gn_w
+    assert lib.wkv7_backward_gn(*bad) == EINVAL and "gn_w" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

@@ -307,3 +307,63 @@ def test_fused_full_size_sampled_heads():
     for k in ("y", "sT") + parity.GRADS_FUSED + ("ds0",):
         assert bool(torch.isfinite(out[k]).all()), k
     parity.check_heads(host, out, heads, L=16, fused=True)
+
+
+# ---- the GroupNorm + bonus output epilogue fused into the recurrence
+
+def _gn_case(spec, seed=5):
+    d, host = parity.inputs_on_device(spec)
+    gp = synthetic.gn_params(spec.H, seed=seed)
+    return d, host, gp, {n: t.cuda() for n, t in gp.items()}
+
+
+@pytest.mark.parametrize("name", ["tiny_b1_t64_h4", "mid_b8_t1024_h12"])
+def test_gn_epilogue_all_heads(name):
+    """Recurrence + GroupNorm + bonus against the oracle composite on every
+    head: o, y, sT, checkpoints, the seven gradients (dr, dk, dv with the
+    bonus's own terms) and the parameter gradients summed over batch rows."""
+    spec = synthetic.WORKLOADS[name]
+    d, host, gp, gpd = _gn_case(spec)
+    out = parity.run_gpu_gn(d, gpd)
+    worst = parity.check_heads_gn(host, gp, out, parity.all_heads(spec.B, spec.H), spec.B)
+    print(name, {k: f"{v:.2e}" for k, v in worst.items()})
+
+
+@pytest.mark.parametrize("T", [1, 15, 17, 130])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gn_epilogue_ragged(T, dtype):
+    """Ragged lengths (padding tokens of the last chunk must not reach the
+    parameter sums), with an initial state and dsT."""
+    spec = _custom(2, T, 3, dtype=dtype, seed=17)
+    d, host, gp, gpd = _gn_case(spec, seed=6)
+    out = parity.run_gpu_gn(d, gpd)
+    parity.check_heads_gn(host, gp, out, parity.all_heads(2, 3), 2)
+
+
+def test_gn_epilogue_extreme_decay_chunk():
+    """A chunk on the exact per-token path (w = 0 for a token) adds the
+    bonus's terms there too."""
+    spec = _custom(2, 48, 2, dtype="bf16", seed=18)
+    d, host, gp, gpd = _gn_case(spec, seed=7)
+    for x in (d, host):
+        w = x["w"].clone()
+        w[1, 20, 0, :] = 0.0
+        x["w"] = w.to(x["w"].device)
+    out = parity.run_gpu_gn(d, gpd)
+    parity.check_heads_gn(host, gp, out, parity.all_heads(2, 2), 2)
+
+
+@pytest.mark.slow
+def test_gn_epilogue_full_size():
+    """The bf16 B=16 T=4096 H=32 workload through the epilogue entry points:
+    two head indices over all 16 batch rows (per-token tensors and the
+    parameter sums of those heads)."""
+    spec = synthetic.WORKLOADS["bf16_b16_t4096_h32"]
+    heads = [(b, h) for h in (0, 31) for b in range(spec.B)]
+    d, host = parity.inputs_on_device(spec, heads=heads)
+    gp = synthetic.gn_params(spec.H, seed=8)
+    out = parity.run_gpu_gn(d, {n: t.cuda() for n, t in gp.items()})
+    for k in ("o", "y") + parity.GRADS + parity.GN_GRADS:
+        assert bool(torch.isfinite(out[k]).all()), k
+    worst = parity.check_heads_gn(host, gp, out, heads, spec.B)
+    print({k: f"{v:.2e}" for k, v in worst.items()})
