@@ -637,6 +637,78 @@ def run_ours(args, world, rank, local):
                  "inputs": "r, w_pre, k, v, kk, avec (w, a, b computed in the kernels)"}
         del fz, fx
 
+    # the GroupNorm + bonus output epilogue fused into the step (wkv7_forward_gn +
+    # wkv7_backward_gn, do = the same dy draw), beside the plain step with the
+    # epilogue as separate torch passes (group_norm and the bonus, and their
+    # autograd backward) around the plain entry points
+    gnres = None
+    if not args.no_gn and use_fac:
+        gp = {n: t.to(dev) for n, t in synthetic.gn_params(H, seed=0).items()}
+        xs = [d[n] for n in INPUTS]
+        go = {"y": outs["y"], "o": torch.empty_like(outs["y"]), "sT": outs["sT"], "ckpt": outs["ckpt"],
+              "factors": outs["factors"]}
+        gg = dict(gouts)
+        gg.update({n: torch.empty((H, N), device=dev) for n in ("dgn_w", "dgn_b", "dr_k")})
+        gws = torch.empty(wkv7.gn_workspace_floats(B, H), device=dev)
+        gev = []
+
+        def gstep(record=False):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if record else None
+            if record:
+                e[0].record(stream)
+            wkv7.forward_gn(*xs, gp["gn_w"], gp["gn_b"], gp["r_k"], s0=d["s0"], L=16, out=go, stream=stream)
+            if record:
+                e[1].record(stream)
+            wkv7.backward_gn(*xs, go["ckpt"], go["factors"], go["y"], d["dy"], gp["gn_w"], gp["r_k"], dsT=d["dsT"],
+                             workspace=gws, out=gg, stream=stream)
+            if record:
+                e[2].record(stream)
+                gev.append(e)
+
+        for _ in range(args.warmup):
+            gstep()
+        torch.cuda.synchronize()
+        barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            gstep(record=True)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        wkv7.async_status()
+        g_ms = max_over_ranks(g0.elapsed_time(g1), world) / args.steps
+        gf = statistics.mean(a.elapsed_time(b) for a, b, _ in gev)
+        gb = statistics.mean(b.elapsed_time(c) for _, b, c in gev)
+
+        def sstep():
+            y_, _, ck_, fac_ = wkv7.forward(*xs, s0=d["s0"], L=16, want_factors=True, out=outs, stream=stream)
+            yv = y_.detach().requires_grad_(True)
+            o_ = torch.nn.functional.group_norm(yv.reshape(B * T, H * N), H, gp["gn_w"].reshape(-1),
+                                                gp["gn_b"].reshape(-1), eps=64e-5).reshape(B, T, H, N)
+            o_ = o_ + (xs[0].float() * xs[2].float() * gp["r_k"]).sum(-1, keepdim=True) * xs[3].float()
+            o_.backward(d["dy"])
+            wkv7.backward(*xs, ck_, yv.grad, dsT=d["dsT"], L=16, factors=fac_, out=gouts, stream=stream)
+
+        for _ in range(2):
+            sstep()
+        torch.cuda.synchronize()
+        s0_, s1_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_s = max(3, args.steps // 10)
+        s0_.record(stream)
+        for _ in range(n_s):
+            sstep()
+        s1_.record(stream)
+        torch.cuda.synchronize()
+        sep_ms = max_over_ranks(s0_.elapsed_time(s1_), world) / n_s
+        gbytes = bwd_bytes + spec.elems * 4  # + the forward's y, read back by the epilogue's backward
+        gnres = {"ms_per_step": g_ms, "tokens_per_s": world * spec.tokens / (g_ms / 1e3), "forward_ms": gf,
+                 "backward_ms": gb, "separate_epilogue_ms_per_step": sep_ms, "launches": 3 * args.steps,
+                 "roofline": {"bound": "hbm", "kernel": "wkv7 backward with the epilogue's backward",
+                              "achieved": gbytes / (gb / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                              "frac": gbytes / (gb / 1e3) / 1e9 / peak, "algorithmic_bytes": gbytes},
+                 "outputs": "o (GroupNorm + bonus) and y; dgn_w, dgn_b, dr_k beside the seven gradients"}
+        del go, gg, gws
+
     timesplit = None
     if not args.no_timesplit:
         timesplit = bench_timesplit(wkv7, dev, stream, peak, world)
@@ -666,7 +738,7 @@ def run_ours(args, world, rank, local):
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
                      "kernel": "mma.sync", "tcgen05_variant_ms": bwd_tc_ms},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * rounds * args.steps, "clocks": clocks,
-        "fused": fused, "decode": decode, "timesplit": timesplit,
+        "fused": fused, "gn_epilogue": gnres, "decode": decode, "timesplit": timesplit,
     }
     print(json.dumps(line), flush=True)
 
@@ -685,6 +757,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")
     ap.add_argument("--no-fused", action="store_true", help="skip the fused-producer measurement")
     ap.add_argument("--no-timesplit", action="store_true", help="skip the time-split measurement")
+    ap.add_argument("--no-gn", action="store_true", help="skip the fused output-epilogue measurement")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -87,6 +87,16 @@ static unsigned *g_flag_ptr[64] = {};
 namespace wkv7 {
 int set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 
+int forward_state(int B, int T, int H, int dtype, const void *w, const void *k, const void *v, const void *a,
+                  const void *b, const float *s0, float *sT, int state_only, cudaStream_t st) {
+    SeqArgs p{};
+    p.B = B; p.T = T; p.H = H; p.L = 16; p.nck = wkv7_ckpt_count(T, 16); p.dtype = dtype;
+    p.r = w; p.w = w; p.k = state_only == 1 ? k : w; p.v = state_only == 1 ? v : w; p.a = a; p.b = b;  // unread rows: any valid map
+    p.s0 = s0; p.sT = sT; p.state_only = state_only;
+    if (!(p.err = async_error_flag())) return WKV7_ECUDA;
+    return launch_status(launch_forward_chunk(p, st), "segment pass launch");
+}
+
 int check_call(int B, int T, int H, int N, int dtype, const void *const *req, const char *const *req_names, int nreq,
                const void *const *opt, const char *const *opt_names, int nopt) {
     TRY(check_dims(B, T, H, N, dtype));

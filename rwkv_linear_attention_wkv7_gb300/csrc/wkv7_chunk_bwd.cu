@@ -113,12 +113,12 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // kGN (with kFac, without kP): the backward of the GroupNorm + bonus output
 // epilogue ("timemix.cu" page, k_bonus_bwd and k_groupnorm_bwd) is fused in
 // front: the staged dy rows hold do = dL/do and the forward's y of the chunk
-// arrives in the Gram slot (idle on the factor-cache path); each warp turns
-// four tokens of do into the recurrence's dy in place (GroupNorm backward,
-// reductions over the head's 64 channels), leaves do s (the bonus's dv) in
-// the y slot and sum_j do_j v_j per token for the bonus's dr and dk, and
-// accumulates the parameter gradients of its lanes' two channels over every
-// token; per-(b,h) partial sums leave at the end (summed over batch rows by
+// arrives in the Gram slot (idle on the factor-cache path); 16 lanes per
+// token turn do into the recurrence's dy in place (GroupNorm backward,
+// reductions over the head's 64 channels), leave do s (the bonus's dv) in the
+// y slot and sum_j do_j v_j per token for the bonus's dr and dk, and
+// accumulate the parameter gradients of their four channels over every token;
+// per-(b,h) partial sums leave at the end (summed over batch rows by
 // wkv7_gn_param_reduce_kernel, no atomics).
 template <typename E, bool kFac, bool kP, bool kGN>
 __global__ void __launch_bounds__(NT, 2)
@@ -182,15 +182,14 @@ __global__ void __launch_bounds__(NT, 2)
     int stuck = -1, s_phase = -1;  // the chunk whose wait ran out; the phase of the last start-state copy
     constexpr unsigned kChunkBytes =
         (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
-    // kGN: per-lane channel constants (channels 2 lane, 2 lane + 1; key rows rA, rB) and
-    // parameter-gradient sums; per-token sum_j do_j v_j past the dw carry in the W slot
-    float2 gwc = {}, rkc = {}, pgw = {}, pgb = {}, prk = {};
+    // kGN: parameter-gradient sums of this lane's channels 4 (lane % 16) .. + 3 (over the
+    // tokens it converts), the bonus weights of its key rows rA, rB; per-token
+    // sum_j do_j v_j past the dw carry in the W slot
+    float4 pgw = {}, pgb = {}, prk = {};
     float rkA = 0.f, rkB = 0.f;
     float *const dsv = Wm + 256;
     static_assert(256 * 4 + C * 4 <= 1280, "the dw carry and the per-token sums fit the W slot");
     if constexpr (kGN) {
-        gwc = __ldg(reinterpret_cast<const float2 *>(p.gn_w + h * 64 + 2 * lane));
-        rkc = __ldg(reinterpret_cast<const float2 *>(p.r_k + h * 64 + 2 * lane));
         rkA = __ldg(p.r_k + h * 64 + rA);
         rkB = __ldg(p.r_k + h * 64 + rB);
     }
@@ -267,31 +266,47 @@ __global__ void __launch_bounds__(NT, 2)
             stuck = c;
             break;
         }
-        if constexpr (kGN) {  // do -> dy through the epilogue, four tokens per warp (channels 2 lane, +1)
+        if constexpr (kGN) {  // do -> dy through the epilogue: 16 lanes per token (four channels each),
+                              // two tokens per warp at a time; statistics in two shuffle levels
+            const int j = 4 * (lane & 15);
+            const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.gn_w + h * 64 + j));
+            const float4 rk = __ldg(reinterpret_cast<const float4 *>(p.r_k + h * 64 + j));
+            auto sum16 = [](float x) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * warp + u, j = 2 * lane;
-                const float2 yv = *reinterpret_cast<const float2 *>(Gm + t * SP + j);
-                const float2 dov = *reinterpret_cast<const float2 *>(dyf + t * SP + j);
-                const float v0 = ld_raw(raw, VV, t, j), v1 = ld_raw(raw, VV, t, j + 1);
-                const float r0 = ld_raw(raw, VR, t, j), r1 = ld_raw(raw, VR, t, j + 1);
-                const float k0 = ld_raw(raw, VK, t, j), k1 = ld_raw(raw, VK, t, j + 1);
-                const float mean = warp_allsum(yv.x + yv.y) * (1.f / 64.f);
-                const float c0 = yv.x - mean, c1 = yv.y - mean;
-                const float rstd = 1.f / sqrtf(warp_allsum(c0 * c0 + c1 * c1) * (1.f / 64.f) + kGnEps);
-                const float x0 = c0 * rstd, x1 = c1 * rstd;
-                const float n0 = dov.x * gwc.x, n1 = dov.y * gwc.y;
-                const float mn = warp_allsum(n0 + n1) * (1.f / 64.f);
-                const float mx = warp_allsum(n0 * x0 + n1 * x1) * (1.f / 64.f);
-                const float sb = warp_allsum(r0 * k0 * rkc.x + r1 * k1 * rkc.y);
-                const float ds = warp_allsum(dov.x * v0 + dov.y * v1);
-                *reinterpret_cast<float2 *>(dyf + t * SP + j) =
-                    make_float2(rstd * (n0 - mn - x0 * mx), rstd * (n1 - mn - x1 * mx));
-                *reinterpret_cast<float2 *>(Gm + t * SP + j) = make_float2(dov.x * sb, dov.y * sb);
-                if (lane == 0) dsv[t] = ds;
-                pgw.x += dov.x * x0; pgw.y += dov.y * x1;
-                pgb.x += dov.x; pgb.y += dov.y;
-                prk.x += ds * r0 * k0; prk.y += ds * r1 * k1;
+                for (int o = 1; o < 16; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                return x;
+            };
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = 4 * warp + 2 * u + (lane >> 4);
+                const float4 y4 = *reinterpret_cast<const float4 *>(Gm + t * SP + j);
+                const float4 d4 = *reinterpret_cast<const float4 *>(dyf + t * SP + j);
+                const float4 v4 = ld_raw4(raw, VV, t, j), r4 = ld_raw4(raw, VR, t, j), k4 = ld_raw4(raw, VK, t, j);
+                const float dn[4] = {d4.x * gw.x, d4.y * gw.y, d4.z * gw.z, d4.w * gw.w};
+                // sums that need nothing else first: y, dn, the bonus r k r_k, do . v
+                const float sy = sum16(y4.x + y4.y + y4.z + y4.w);
+                const float sdn = sum16(dn[0] + dn[1] + dn[2] + dn[3]);
+                const float sb = sum16(r4.x * k4.x * rk.x + r4.y * k4.y * rk.y + r4.z * k4.z * rk.z + r4.w * k4.w * rk.w);
+                const float ds = sum16(d4.x * v4.x + d4.y * v4.y + d4.z * v4.z + d4.w * v4.w);
+                const float mean = sy * (1.f / 64.f);
+                const float c[4] = {y4.x - mean, y4.y - mean, y4.z - mean, y4.w - mean};
+                // then the variance and sum(dn xh) = rstd sum(dn (y - mean))
+                const float scc = sum16(c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3]);
+                const float sdc = sum16(dn[0] * c[0] + dn[1] * c[1] + dn[2] * c[2] + dn[3] * c[3]);
+                const float rstd = 1.f / sqrtf(scc * (1.f / 64.f) + kGnEps);
+                const float mn = sdn * (1.f / 64.f), mx = rstd * sdc * (1.f / 64.f);
+                float x[4], dy[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[i] = c[i] * rstd;
+                    dy[i] = rstd * (dn[i] - mn - x[i] * mx);
+                }
+                *reinterpret_cast<float4 *>(dyf + t * SP + j) = make_float4(dy[0], dy[1], dy[2], dy[3]);
+                *reinterpret_cast<float4 *>(Gm + t * SP + j) = make_float4(d4.x * sb, d4.y * sb, d4.z * sb, d4.w * sb);
+                if ((lane & 15) == 0) dsv[t] = ds;
+                pgw.x += d4.x * x[0]; pgw.y += d4.y * x[1]; pgw.z += d4.z * x[2]; pgw.w += d4.w * x[3];
+                pgb.x += d4.x; pgb.y += d4.y; pgb.z += d4.z; pgb.w += d4.w;
+                prk.x += ds * r4.x * k4.x; prk.y += ds * r4.y * k4.y; prk.z += ds * r4.z * k4.z; prk.w += ds * r4.w * k4.w;
             }
             __syncthreads();
         }
@@ -826,12 +841,23 @@ __global__ void __launch_bounds__(NT, 2)
         mbar_drain(&bar, (nchunks - 1 - stuck) & 1);
         if (tid == 0 && s_phase >= 0) mbar_drain(&bar_s, s_phase);
     }
-    if constexpr (kGN) {  // this head's parameter-gradient sums: the four warps' token groups combined
+    if constexpr (kGN) {  // this head's parameter-gradient sums: both half-warps, then the four warps
+        float4 *const acc3[3] = {&pgw, &pgb, &prk};
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            float4 &v = *acc3[a];
+            v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
+            v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
+            v.z += __shfl_xor_sync(0xffffffffu, v.z, 16);
+            v.w += __shfl_xor_sync(0xffffffffu, v.w, 16);
+        }
         __syncthreads();
         float *const sc = Gm;  // [warp][3][64]
-        *reinterpret_cast<float2 *>(sc + (warp * 3 + 0) * 64 + 2 * lane) = pgw;
-        *reinterpret_cast<float2 *>(sc + (warp * 3 + 1) * 64 + 2 * lane) = pgb;
-        *reinterpret_cast<float2 *>(sc + (warp * 3 + 2) * 64 + 2 * lane) = prk;
+        if (lane < 16) {
+            *reinterpret_cast<float4 *>(sc + (warp * 3 + 0) * 64 + 4 * lane) = pgw;
+            *reinterpret_cast<float4 *>(sc + (warp * 3 + 1) * 64 + 4 * lane) = pgb;
+            *reinterpret_cast<float4 *>(sc + (warp * 3 + 2) * 64 + 4 * lane) = prk;
+        }
         __syncthreads();
         for (int o = tid; o < 3 * 64; o += NT)
             p.gn_part[(size_t)bh * 192 + o] = sc[o] + sc[192 + o] + sc[384 + o] + sc[576 + o];

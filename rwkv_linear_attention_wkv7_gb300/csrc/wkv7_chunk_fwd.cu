@@ -27,9 +27,10 @@
 // kGN: the output epilogue of the "timemix.cu" page (k_groupnorm, then
 // k_bonus) is fused in: while a chunk's rows are staged, the bonus
 // (sum_j r_j k_j r_k[j]) v of each token goes into a [C][64] tile; once the
-// chunk's y is staged, each warp normalises four tokens over the head's 64
-// outputs (biased variance, eps 64e-5, per-channel weight and bias) and adds
-// the bonus in place; y and the epilogue output o leave by two tensor stores.
+// chunk's y is staged, the warps normalise each token over the head's 64
+// outputs (biased variance, eps 64e-5, per-channel weight and bias; eight
+// lanes per token) and adds the bonus in place; y and the epilogue output o
+// leave by two tensor stores.
 #include <type_traits>
 
 #include "wkv7_chunk_common.cuh"
@@ -83,8 +84,14 @@ __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off) {
 
 // kP: the staged w, a, b rows hold the producers' inputs (w_pre, kk, avec); see in_w.
 // kGN: the GroupNorm + bonus output epilogue (see the file header).
-template <typename E, bool kP, bool kGN>
+// kMode (for the time split's segment passes, which need only a segment's end
+// state): 0 the whole forward; 1 the end state only (no y: r is not staged, and
+// Z, Y, Q_b, Q_k are not formed); 2 the end state with v = 0, i.e. the product
+// of the transitions applied to s0 (k and v are not staged either, M_k and
+// every V product are skipped).
+template <typename E, bool kP, bool kGN, int kMode = 0>
 __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps) {
+    static_assert(kMode == 0 || (!kP && !kGN), "the state-only passes run on plain inputs");
     extern __shared__ __align__(128) unsigned char smem[];
     // bf16 inputs: v is exact in bf16, so products with v as the A operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
@@ -125,9 +132,12 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     }
     __syncthreads();
     int stuck = -1;  // the chunk whose wait ran out
-    constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>();
+    // the staged rows this mode reads: all six; w, k, v, a, b; or w, a, b
+    constexpr unsigned kRows = kMode == 0 ? 6 : kMode == 1 ? 5 : 3;
+    constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>() / 6 * kRows;
+    auto staged = [](int vec) { return kMode == 0 || (vec != VR && (kMode == 1 || (vec != VK && vec != VV))); };
     auto prefetch = [&](int c) {  // chunk c's copies (lanes 0..5 of warp 0); thread 0 announced its bytes
-        if (tid < 6) tma_rows(raw + tid * C * RS, &maps.m[tid], h, c * C, bi, &bar);
+        if (tid < 6 && staged(tid)) tma_rows(raw + tid * C * RS, &maps.m[tid], h, c * C, bi, &bar);
         if (tid == 0) mbar_arrive(&bar);
     };
     if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
@@ -187,16 +197,16 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
                 const float4 id = rcp4(d);
                 st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT), t, j, mul4(in_b4<kP>(raw, t, j), id));
-                st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
+                if (kMode < 2) st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT), t, j, mul4(ld_raw4(raw, VK, t, j), id));
                 st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH), t, j, mul4(in_a4<kP>(raw, t, j), dp));
-                st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
-                if (kVLo) st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
+                if (kMode == 0) st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH), t, j, mul4(ld_raw4(raw, VR, t, j), d));
+                if (kVLo && kMode < 2) st_hl4(hi_of(Bs, B_VM), lo_of(Bs, B_VM), t, j, ld_raw4(raw, VV, t, j));
             }
             if constexpr (kGN) write_bonus();
             // bf16 v is its own hi part: its A fragment (A[i][t] = v[t][i]) comes straight
             // from the staged input, before the barrier that lets the next chunk's copies in
             AFrag vA;
-            if (!kVLo) {
+            if (!kVLo && kMode < 2) {
                 const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(raw) + VV * C * RS;
                 vA = lda_t_hi(HL{rv, rv}, 16 * warp, 0, lane);
             }
@@ -212,15 +222,23 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 const bool rn = warp & 1;
                 float acc[2][4] = {};
 #pragma unroll
+                // the Gram blocks each mode needs: M_b (warp 0) always, M_k (warp 2) unless v = 0,
+                // Q_b and Q_k (warps 1, 3) only with y
+                const bool gram = kMode == 0 || warp == 0 || (kMode == 1 && warp == 2);
                 for (int kk = 0; kk < 4; ++kk) {
                     BFrag bq[4];
-                    ldb2(RH, 0, 16 * kk, lane, bq[0], bq[1]);
+                    if (kMode == 0) ldb2(RH, 0, 16 * kk, lane, bq[0], bq[1]);
                     ldb2(AH, 0, 16 * kk, lane, bq[2], bq[3]);
-                    const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
-                    const BFrag gq[2] = {rn ? bq[0] : bq[2], rn ? bq[1] : bq[3]};
-                    mma3n<2>(acc, af, gq);
+                    if (gram) {
+                        const AFrag af = lda(mt ? KT : BT, 0, 16 * kk, lane);
+                        const BFrag gq[2] = {rn ? bq[0] : bq[2], rn ? bq[1] : bq[3]};
+                        mma3n<2>(acc, af, gq);
+                    }
                     const AFrag sf = a_from_acc(S, kk);
-                    mma3n<4>(ya, sf, bq);
+                    if (kMode == 0)
+                        mma3n<4>(ya, sf, bq);
+                    else
+                        mma3n<2>(ya + 2, sf, bq + 2);  // U only
                 }
                 if (warp == 0) {  // b~ . a^ = M_b (its unused lower part too), fp32 for the inverse
 #pragma unroll
@@ -229,8 +247,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                         *reinterpret_cast<float2 *>(Mb + g * MBS + col) = make_float2(acc[u][0], acc[u][1]);
                         *reinterpret_cast<float2 *>(Mb + (g + 8) * MBS + col) = make_float2(acc[u][2], acc[u][3]);
                     }
-                } else {  // b~ . r^ = Q_b, k~ . a^ = M_k, k~ . r^ = Q_k: masked to [s <= t] ([s < t] for
-                          // M_k) and split into their compact operand matrices
+                } else if (gram) {  // b~ . r^ = Q_b, k~ . a^ = M_k, k~ . r^ = Q_k: masked to [s <= t] ([s < t] for
+                                    // M_k) and split into their compact operand matrices
                     const int strict = warp == 2;
 #pragma unroll
                     for (int u = 0; u < 2; ++u)
@@ -246,12 +264,16 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             // W on warp 0 while every warp adds V [Q_k | M_k] to [Z | U] (warp 0 follows
             // with its own rows once W is done)
             prep_inverse_t(Mb, hi_of(Bs, B_WT), reinterpret_cast<__nv_bfloat16 *>(Bs + B_WT) + 16 * CS);
-            if (kVLo) vA = lda_t(VM, 16 * warp, 0, lane);
-            {
+            if (kVLo && kMode < 2) vA = lda_t(VM, 16 * warp, 0, lane);
+            if constexpr (kMode == 0) {
                 BFrag bq[4];
                 ldb2_t<CS>(QK, 0, 0, lane, bq[0], bq[1]);
                 ldb2_t<CS>(MK, 0, 0, lane, bq[2], bq[3]);
                 mma3n<4, kVLo>(ya, vA, bq);
+            } else if constexpr (kMode == 1) {  // V M_k into U only
+                BFrag bq[2];
+                ldb2_t<CS>(MK, 0, 0, lane, bq[0], bq[1]);
+                mma3n<2, kVLo>(ya + 2, vA, bq);
             }
             if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();  // W
@@ -289,9 +311,11 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             const AFrag saf = make_a(make_float2(sa[0][0], sa[0][1]), make_float2(sa[0][2], sa[0][3]),
                                      make_float2(sa[1][0], sa[1][1]), make_float2(sa[1][2], sa[1][3]));
             BFrag qbf[2];
-            ldb2_t<CS>(QB, 0, 0, lane, qbf[0], qbf[1]);
-            mma3n<2>(ya, saf, qbf);  // Y (tiles 0, 1 of ya)
-            if (fc) {  // factor cache for the backward
+            if constexpr (kMode == 0) {
+                ldb2_t<CS>(QB, 0, 0, lane, qbf[0], qbf[1]);
+                mma3n<2>(ya, saf, qbf);  // Y (tiles 0, 1 of ya)
+            }
+            if (kMode == 0 && fc) {  // factor cache for the backward
                 st_acc2(fc + fac::kSA + 256 * warp, sa[0], sa[1], lane);
                 if (warp == 1) {  // M_k' = M_k W and Q' = Q_k + M_k' Q_b
                     const AFrag am = lda<CS>(MK, 0, 0, lane);
@@ -327,12 +351,16 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             // ---- S_C = (S_0 + SA B~^T + V K~^T) diag(d_C)
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
-                BFrag bb0, bb1, kb0, kb1;
+                BFrag bb0, bb1;
                 ldb2_t(BT, 16 * pp, 0, lane, bb0, bb1);
-                ldb2_t(KT, 16 * pp, 0, lane, kb0, kb1);
-                const BFrag bq[2] = {bb0, bb1}, kq[2] = {kb0, kb1};
+                const BFrag bq[2] = {bb0, bb1};
                 mma3n<2>(S + 2 * pp, saf, bq);
-                mma3n<2, kVLo>(S + 2 * pp, vA, kq);
+                if constexpr (kMode < 2) {
+                    BFrag kb0, kb1;
+                    ldb2_t(KT, 16 * pp, 0, lane, kb0, kb1);
+                    const BFrag kq[2] = {kb0, kb1};
+                    mma3n<2, kVLo>(S + 2 * pp, vA, kq);
+                }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int nt = 2 * pp + u;
@@ -341,13 +369,15 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 }
             }
             // y of the chunk -> staging [t][row]
+            if constexpr (kMode == 0) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t = 8 * nt + 2 * q;
-                ys[t * YS + rA] = ya[nt][0];
-                ys[(t + 1) * YS + rA] = ya[nt][1];
-                ys[t * YS + rB] = ya[nt][2];
-                ys[(t + 1) * YS + rB] = ya[nt][3];
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int t = 8 * nt + 2 * q;
+                    ys[t * YS + rA] = ya[nt][0];
+                    ys[(t + 1) * YS + rA] = ya[nt][1];
+                    ys[t * YS + rB] = ya[nt][2];
+                    ys[(t + 1) * YS + rB] = ya[nt][3];
+                }
             }
         } else {
             // exact per-token recurrence for a chunk whose decay leaves the factorisable range
@@ -368,28 +398,35 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 sa0 += __shfl_xor_sync(0xffffffffu, sa0, 2);
                 sa1 += __shfl_xor_sync(0xffffffffu, sa1, 1);
                 sa1 += __shfl_xor_sync(0xffffffffu, sa1, 2);
-                const float v0 = ld_raw(raw, VV, t, rA), v1 = ld_raw(raw, VV, t, rB);
+                // v and k are not staged with kMode 2 (v = 0), r only with kMode 0 (y)
+                const float v0 = kMode < 2 ? ld_raw(raw, VV, t, rA) : 0.f;
+                const float v1 = kMode < 2 ? ld_raw(raw, VV, t, rB) : 0.f;
                 float y0 = 0.f, y1 = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int j = 8 * nt + 2 * q + e;
-                        const float wv = in_w<kP>(raw, t, j), kv = ld_raw(raw, VK, t, j);
-                        const float bv = in_b<kP>(raw, t, j), rv = ld_raw(raw, VR, t, j);
+                        const float wv = in_w<kP>(raw, t, j), bv = in_b<kP>(raw, t, j);
+                        const float kv = kMode < 2 ? ld_raw(raw, VK, t, j) : 0.f;
                         S[nt][e] = __fmaf_rn(S[nt][e], wv, __fmaf_rn(sa0, bv, __fmul_rn(v0, kv)));
                         S[nt][2 + e] = __fmaf_rn(S[nt][2 + e], wv, __fmaf_rn(sa1, bv, __fmul_rn(v1, kv)));
-                        y0 = __fmaf_rn(S[nt][e], rv, y0);
-                        y1 = __fmaf_rn(S[nt][2 + e], rv, y1);
+                        if (kMode == 0) {
+                            const float rv = ld_raw(raw, VR, t, j);
+                            y0 = __fmaf_rn(S[nt][e], rv, y0);
+                            y1 = __fmaf_rn(S[nt][2 + e], rv, y1);
+                        }
                     }
                 }
-                y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
-                y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
-                y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-                y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
-                if (q == 0) {
-                    ys[t * YS + rA] = y0;
-                    ys[t * YS + rB] = y1;
+                if (kMode == 0) {
+                    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+                    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+                    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+                    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+                    if (q == 0) {
+                        ys[t * YS + rA] = y0;
+                        ys[t * YS + rB] = y1;
+                    }
                 }
             }
             __syncthreads();
@@ -397,24 +434,41 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         }
         fence_proxy_async();  // the staged y tile is read by a tensor store
         __syncthreads();
-        if constexpr (kGN) {  // o = GroupNorm(y) + bonus, four tokens per warp, in place over the bonus tile
-            const float2 gw = __ldg(reinterpret_cast<const float2 *>(p.gn_w + h * 64 + 2 * lane));
-            const float2 gb = __ldg(reinterpret_cast<const float2 *>(p.gn_b + h * 64 + 2 * lane));
+        if constexpr (kGN) {  // o = GroupNorm(y) + bonus in place over the bonus tile: eight lanes per token,
+                              // eight channels each (the statistics take three shuffle levels)
+            const int t = tid >> 3, j0 = (tid & 7) * 8;
+            const float4 ya0 = *reinterpret_cast<const float4 *>(ys + t * YS + j0);
+            const float4 ya1 = *reinterpret_cast<const float4 *>(ys + t * YS + j0 + 4);
+            const float yv[8] = {ya0.x, ya0.y, ya0.z, ya0.w, ya1.x, ya1.y, ya1.z, ya1.w};
+            float sum = 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 4 * warp + u;
-                const float2 yv = *reinterpret_cast<const float2 *>(ys + t * YS + 2 * lane);
-                const float mean = warp_allsum(yv.x + yv.y) * (1.f / 64.f);
-                const float c0 = yv.x - mean, c1 = yv.y - mean;
-                const float rstd = 1.f / sqrtf(warp_allsum(c0 * c0 + c1 * c1) * (1.f / 64.f) + kGnEps);
-                float2 *ob = reinterpret_cast<float2 *>(bon + t * 64 + 2 * lane);
-                const float2 bv = *ob;
-                *ob = make_float2(c0 * rstd * gw.x + gb.x + bv.x, c1 * rstd * gw.y + gb.y + bv.y);
+            for (int i = 0; i < 8; ++i) sum += yv[i];
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float mean = sum * (1.f / 64.f);
+            float cv[8], sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cv[i] = yv[i] - mean;
+                sq += cv[i] * cv[i];
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float rstd = 1.f / sqrtf(sq * (1.f / 64.f) + kGnEps);
+            const float4 *gw4 = reinterpret_cast<const float4 *>(p.gn_w + h * 64 + j0);
+            const float4 *gb4 = reinterpret_cast<const float4 *>(p.gn_b + h * 64 + j0);
+            float4 *ob = reinterpret_cast<float4 *>(bon + t * 64 + j0);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float4 gw = __ldg(gw4 + hf), gb = __ldg(gb4 + hf), bv = ob[hf];
+                const float *c = cv + 4 * hf;
+                ob[hf] = make_float4(c[0] * rstd * gw.x + gb.x + bv.x, c[1] * rstd * gw.y + gb.y + bv.y,
+                                     c[2] * rstd * gw.z + gb.z + bv.z, c[3] * rstd * gw.w + gb.w + bv.w);
             }
             fence_proxy_async();
             __syncthreads();
         }
-        if (tid == 0) {  // y (and o) of the chunk: one tensor store each (tokens past T are not written)
+        if (kMode == 0 && tid == 0) {  // y (and o) of the chunk: one tensor store each (tokens past T are not written)
             tma_store_rows(&maps.m[6], ys, h, t0, bi);
             if constexpr (kGN) tma_store_rows(&maps.m[8], bon, h, t0, bi);
             bulk_commit();
@@ -432,18 +486,19 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     }
 }
 
-template <typename E, bool kP, bool kGN>
+template <typename E, bool kP, bool kGN, int kMode = 0>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     const size_t sm = fwd_smem_bytes<E, kGN>();
     InputMaps maps;  // six inputs, y (box OS), the checkpoints, and o (box 64) with kGN
     cudaError_t e = encode_input_maps(&maps, p, nullptr);
-    if (e == cudaSuccess) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
+    if (e == cudaSuccess && kMode == 0) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
     if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64);
     if (e == cudaSuccess && kGN) e = encode_rows_map(&maps.m[8], p.o, 4, p.B, p.T, p.H, 64);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP, kGN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP, kGN, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_fwd_chunk_kernel<E, kP, kGN><<<p.B * p.H, NT, sm, st>>>(p, maps);
+    wkv7_fwd_chunk_kernel<E, kP, kGN, kMode><<<p.B * p.H, NT, sm, st>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -452,6 +507,10 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
 bool forward_chunk_supported(const SeqArgs &p) { return p.L % C == 0; }
 
 cudaError_t launch_forward_chunk(const SeqArgs &p, cudaStream_t st) {
+    if (p.state_only == 1)
+        return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false, 1>(p, st) : launch_t<float, false, false, 1>(p, st);
+    if (p.state_only == 2)
+        return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false, 2>(p, st) : launch_t<float, false, false, 2>(p, st);
     if (p.gn_w) return p.dtype == 1 ? launch_t<__nv_bfloat16, false, true>(p, st) : launch_t<float, false, true>(p, st);
     if (p.prod) return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false>(p, st) : launch_t<float, true, false>(p, st);
     return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false>(p, st) : launch_t<float, false, false>(p, st);

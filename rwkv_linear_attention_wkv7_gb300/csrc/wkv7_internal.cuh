@@ -34,6 +34,10 @@ struct SeqArgs {
     float *o;
     const float *y_in;
     float *gn_part;
+    // the time split's segment passes: 0 the whole forward; 1 only the end state sT
+    // (no y); 2 only the end state with v = 0 (the product of the transitions
+    // applied to s0; v and k are not read)
+    int state_only;
 };
 
 // Per-chunk factor cache: 2048 32-bit words per (b, h, 16-token chunk), in the
@@ -52,6 +56,11 @@ constexpr int kWords = 2048;
 
 // Record an error for wkv7_last_error() and return `code` (C ABI layer).
 int set_error(int code, const char *msg);
+// The time split's segment passes: the chunked forward of B*T*H inputs from s0
+// (NULL: zeros), writing only sT; state_only 1 reads w, k, v, a, b, state_only 2
+// reads w, a, b (v = 0).  Arguments already checked by the caller.
+int forward_state(int B, int T, int H, int dtype, const void *w, const void *k, const void *v, const void *a,
+                  const void *b, const float *s0, float *sT, int state_only, cudaStream_t s);
 // Host checks shared by every entry point, run before anything is launched:
 // sizes and dtype, the required pointers (non-NULL when T > 0) and the
 // optional ones (NULL allowed), 16-byte alignment of both, and an sm_103a

@@ -114,7 +114,7 @@ __global__ void wkv7_identity_kernel(float *dst, size_t n) {
 }
 
 struct Workspace {
-    float *M, *Z, *starts, *D, *G, *ident, *zero_v, *ckpt, *fac;
+    float *M, *Z, *starts, *D, *G, *ident, *ckpt, *fac;
 };
 
 long long state_floats(int B, int H, int nseg) { return (long long)B * nseg * H * kN * kN; }
@@ -129,8 +129,7 @@ Workspace carve(float *ws, int B, int T, int H, int nseg) {
     w.D = w.starts + s;
     w.G = w.D + s;
     w.ident = w.G + s;
-    w.zero_v = w.ident + s;  // B*T*H*N floats: room for a zero v of either dtype
-    w.ckpt = w.zero_v + (long long)B * T * H * kN;
+    w.ckpt = w.ident + s;
     w.fac = w.ckpt + (long long)B * nseg * H * wkv7_ckpt_count(tseg, 16) * kN * kN;
     return w;
 }
@@ -160,7 +159,7 @@ long long wkv7_timesplit_workspace_floats(int B, int T, int H, int nseg) {
     if (B < 1 || H < 1 || T < 0 || nseg < 1 || T % (16 * nseg) != 0) return -1;
     const int tseg = T / nseg;
     const long long s = state_floats(B, H, nseg);
-    return 6 * s + (long long)B * T * H * kN + (long long)B * nseg * H * wkv7_ckpt_count(tseg, 16) * kN * kN +
+    return 6 * s + (long long)B * nseg * H * wkv7_ckpt_count(tseg, 16) * kN * kN +
            (long long)B * nseg * H * wkv7_factor_floats(tseg);
 }
 
@@ -218,14 +217,10 @@ int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const v
     const size_t nmat = (size_t)bs * H;
     wkv7_identity_kernel<<<(unsigned)((s + 255) / 256), 256, 0, st>>>(ws.ident, nmat);
     if ((rc = cuda_status(cudaGetLastError(), "identity launch")) != WKV7_OK) return rc;
-    const size_t vbytes = (size_t)B * T * H * kN * (dtype == WKV7_BF16 ? 2 : 4);
-    if ((rc = cuda_status(cudaMemsetAsync(ws.zero_v, 0, vbytes, st), "zero v")) != WKV7_OK) return rc;
-    // (1) from I with v = 0 and (2) from 0: y is scratch here, written for real by (4)
-    if ((rc = wkv7_forward(bs, tseg, H, N, dtype, r, w, k, ws.zero_v, a, b, ws.ident, y, ws.M, nullptr, nullptr, 16,
-                           stream)))
-        return rc;
-    if ((rc = wkv7_forward(bs, tseg, H, N, dtype, r, w, k, v, a, b, nullptr, y, ws.Z, nullptr, nullptr, 16, stream)))
-        return rc;
+    // (1) M: every segment from I with v = 0 -- the segment pass that reads only w, a, b
+    // and forms no V product and no y; (2) Z: every segment from 0 (end state only, no y)
+    if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, ws.ident, ws.M, 2, st))) return rc;
+    if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, nullptr, ws.Z, 1, st))) return rc;
     // (3) segment start states, and the final state
     wkv7_segment_scan_kernel<false><<<B * H, kThreads, 0, st>>>(H, nseg, ws.M, ws.Z, s0, ws.starts, sT);
     if ((rc = cuda_status(cudaGetLastError(), "segment scan launch")) != WKV7_OK) return rc;

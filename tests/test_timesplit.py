@@ -70,7 +70,7 @@ def test_workspace_size_and_argument_errors():
     assert lib.wkv7_timesplit_workspace_floats(1, 100, 2, 4) == -1  # T not a multiple of 16 * nseg
     assert lib.wkv7_timesplit_workspace_floats(1, 128, 2, 0) == -1
     n = lib.wkv7_timesplit_workspace_floats(1, 128, 2, 4)
-    assert n == 6 * 4 * 2 * 4096 + 128 * 2 * 64 + 4 * 2 * 2 * 4096 + 4 * 2 * 2 * 2048
+    assert n == 6 * 4 * 2 * 4096 + 4 * 2 * 2 * 4096 + 4 * 2 * 2 * 2048  # 6 state sets, checkpoints, factors
     p = ctypes.c_void_p(4096)
     fwd = lambda T, nseg, ws: lib.wkv7_forward_timesplit(1, T, 2, 64, 0, *([p] * 6), None, p, None, nseg, ws, None)
     assert fwd(100, 4, p) == EINVAL and "multiple of 16 * nseg" in wkv7.last_error()
