@@ -40,7 +40,6 @@ TIMESPLIT_SEGMENTS = 32
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 L2_BYTES = 126 * 2**20
-MIN_TIMED_S = 1.0
 
 
 def esize(spec):
@@ -413,10 +412,10 @@ def run_ours(args, world, rank, local):
     w1.record(stream)
     torch.cuda.synchronize()
     # the timed region repeats whole rounds of K steps until it lasts at least
-    # MIN_TIMED_S, so that the clock record sampled during it has several samples
+    # --min-timed-s, so that the clock record sampled during it has several samples
     # (every round is K full steps; ms_per_step divides by all timed steps)
     warm_ms = max_over_ranks(w0.elapsed_time(w1) / max(args.warmup, 1), world)
-    rounds = max(1, -(-int(MIN_TIMED_S * 1e3) // max(int(warm_ms * args.steps), 1)))
+    rounds = max(1, -(-int(args.min_timed_s * 1e3) // max(int(warm_ms * args.steps), 1)))
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -758,6 +757,8 @@ def main():
     ap.add_argument("--no-fused", action="store_true", help="skip the fused-producer measurement")
     ap.add_argument("--no-timesplit", action="store_true", help="skip the time-split measurement")
     ap.add_argument("--no-gn", action="store_true", help="skip the fused output-epilogue measurement")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat rounds of --steps steps until the timed region lasts this long (0: one round)")
     args = ap.parse_args()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

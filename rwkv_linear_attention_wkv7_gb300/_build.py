@@ -41,8 +41,8 @@ def _deps():
 
 # The files the two chunked kernels are compiled from (their measurements are
 # keyed by a hash of these alone).
-CHUNK_KERNEL_FILES = ("wkv7_chunk_fwd.cu", "wkv7_chunk_bwd.cu", "wkv7_chunk_common.cuh", "wkv7_mma.cuh",
-                      "wkv7_internal.cuh")
+CHUNK_KERNEL_FILES = ("wkv7_chunk_fwd.cu", "wkv7_chunk_bwd.cu", "wkv7_chunk_bwd_exact.cuh", "wkv7_chunk_common.cuh",
+                      "wkv7_mma.cuh", "wkv7_internal.cuh")
 
 
 def source_hash(files=None) -> str:
