@@ -23,15 +23,33 @@
 
 #include "wkv7.h"
 #include "wkv7_internal.cuh"
+#include "wkv7_mma.cuh"
 
 namespace {
+using wkv7::AFrag;
+using wkv7::BFrag;
+using wkv7::make_a;
+using wkv7::make_b;
+using wkv7::mma3;
 
 constexpr int kN = 64;
-constexpr int kThreads = 256;  // thread (rg, cg) owns rows 4rg..4rg+3, columns 4cg..4cg+3
-constexpr int kPad = kN + 4;   // shared row stride (floats)
+constexpr int kPad = kN + 4;     // shared row stride (floats)
+constexpr int kScanRows = 16;    // state rows per scan CTA
+constexpr int kScanThreads = 128;
 
 __device__ __forceinline__ size_t seg_off(int b, int k, int h, int nseg, int H) {
     return (((size_t)b * nseg + k) * H + h) * kN * kN;
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Per head (b, h): forward (kBack = false)
@@ -40,68 +58,111 @@ __device__ __forceinline__ size_t seg_off(int b, int k, int h, int nseg, int H) 
 //   G = init or 0;  for k = nseg-1 .. 0: out_k = G, G = C_k + G M_k^T;  fin = G
 // (C = Z forward, D backward).  init / fin are [B][H][N][N] (either may be
 // NULL); M, C, out are [B][nseg][H][N][N].
+// Row i of the next state depends on row i of the current one only, so a
+// head's 64 rows run as 4 CTAs of 16 (blockIdx.y); warp w of a CTA owns
+// columns 16w .. 16w + 15.  Each step's 16 x 64 x 64 product runs on the
+// tensor cores with split operands (bf16x3, fp32 accumulation); the next
+// step's M arrives by cp.async into the other buffer during the products.
 template <bool kBack>
-__global__ void __launch_bounds__(kThreads) wkv7_segment_scan_kernel(int H, int nseg, const float *__restrict__ M,
-                                                                     const float *__restrict__ Cadd,
-                                                                     const float *__restrict__ init,
-                                                                     float *__restrict__ out, float *__restrict__ fin) {
-    __shared__ __align__(16) float S[kN * kPad];
-    __shared__ __align__(16) float R[kN * kPad];
-    const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int rg = threadIdx.x >> 4, cg = threadIdx.x & 15;
+__global__ void __launch_bounds__(kScanThreads) wkv7_segment_scan_kernel(int H, int nseg, const float *__restrict__ M,
+                                                                         const float *__restrict__ Cadd,
+                                                                         const float *__restrict__ init,
+                                                                         float *__restrict__ out,
+                                                                         float *__restrict__ fin) {
+    __shared__ __align__(16) float Ms[2][kN * kPad];         // M_k, double-buffered
+    __shared__ __align__(16) float Ss[2][kScanRows * kPad];  // this CTA's rows of the current state
+    const int bh = blockIdx.x, b = bh / H, h = bh % H, row0 = kScanRows * blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q = lane & 3;
     const size_t head = (size_t)bh * kN * kN;
-
-    float acc[4][4];
+    auto seg = [&](int step) { return kBack ? nseg - 1 - step : step; };
+    auto stage_m = [&](int step, float *dst) {  // 1024 16-byte pieces, 8 per thread
+        const float *src = M + seg_off(b, seg(step), h, nseg, H);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 x = init ? *reinterpret_cast<const float4 *>(init + head + (4 * rg + i) * kN + 4 * cg)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        acc[i][0] = x.x; acc[i][1] = x.y; acc[i][2] = x.z; acc[i][3] = x.w;
-    }
-    for (int step = 0; step < nseg; ++step) {
-        const int k = kBack ? nseg - 1 - step : step;
+        for (int m = 0; m < 8; ++m) {
+            const int e = tid + kScanThreads * m, row = e >> 4, c4 = (e & 15) * 4;
+            cp_async16(dst + row * kPad + c4, src + row * kN + c4);
+        }
+        cp_async_commit();
+    };
+    // every step's operands are independent of the scan: ask L2 for all of them now (each
+    // of a head's four CTAs a quarter of the M_k, and its own rows of every C_k), so that
+    // the steps' copies do not wait on DRAM
+    for (int k = tid; k < nseg; k += kScanThreads) {
         const size_t o = seg_off(b, k, h, nseg, H);
-        // publish the current state / gradient, write it out, stage this step's right factor
+        if ((k & 3) == (int)blockIdx.y) prefetch_l2(M + o, kN * kN * 4);
+        prefetch_l2(Cadd + o + (size_t)row0 * kN, kScanRows * kN * 4);
+    }
+    stage_m(0, Ms[0]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float4 x = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-            *reinterpret_cast<float4 *>(S + (4 * rg + i) * kPad + 4 * cg) = x;
-            *reinterpret_cast<float4 *>(out + o + (4 * rg + i) * kN + 4 * cg) = x;
+    for (int m = 0; m < 2; ++m) {
+        const int e = tid + kScanThreads * m, r = e >> 4, c4 = (e & 15) * 4;
+        const float4 x = init ? *reinterpret_cast<const float4 *>(init + head + (row0 + r) * kN + c4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(Ss[0] + r * kPad + c4) = x;
+    }
+    auto load_c = [&](int step, float (*c)[4]) {  // the additive term at this lane's positions
+        const float *cb = Cadd + seg_off(b, seg(step), h, nseg, H) + (size_t)(row0 + g) * kN + 16 * warp + 2 * q;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float2 x = *reinterpret_cast<const float2 *>(cb + 8 * u);
+            const float2 z = *reinterpret_cast<const float2 *>(cb + 8 * u + 8 * kN);
+            c[u][0] = x.x; c[u][1] = x.y; c[u][2] = z.x; c[u][3] = z.y;
+        }
+    };
+    float acc[2][4];  // the next state at rows row0 + g (+8), columns 16 warp + 8u + 2q (+1)
+    float cn[2][4];   // the next step's additive term, loaded a step ahead
+    load_c(0, cn);
+    for (int step = 0; step < nseg; ++step) {
+        const int cur = step & 1;
+        const size_t o = seg_off(b, seg(step), h, nseg, H);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[u][e] = cn[u][e];
+        cp_async_wait_all();
+        __syncthreads();  // M_k and the current rows are visible; step - 1 no longer reads the other buffers
+        if (step + 1 < nseg) {
+            stage_m(step + 1, Ms[cur ^ 1]);
+            load_c(step + 1, cn);
+        }
+        const float *Mk = Ms[cur], *Sk = Ss[cur];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // out_k = the current rows
+            const int e = tid + kScanThreads * m, r = e >> 4, c4 = (e & 15) * 4;
+            *reinterpret_cast<float4 *>(out + o + (row0 + r) * kN + c4) = *reinterpret_cast<const float4 *>(Sk + r * kPad + c4);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = 4 * rg + i;
-            const float4 mm = *reinterpret_cast<const float4 *>(M + o + row * kN + 4 * cg);
-            const float m[4] = {mm.x, mm.y, mm.z, mm.w};
-            if (kBack) {  // R = M^T
+        for (int kk = 0; kk < 4; ++kk) {
+            const float *a = Sk + g * kPad + 16 * kk + 2 * q;
+            auto ld2 = [](const float *x) { return *reinterpret_cast<const float2 *>(x); };
+            const AFrag af = make_a(ld2(a), ld2(a + 8 * kPad), ld2(a + 8), ld2(a + 8 * kPad + 8));
 #pragma unroll
-                for (int j = 0; j < 4; ++j) R[(4 * cg + j) * kPad + row] = m[j];
-            } else {
-                *reinterpret_cast<float4 *>(R + row * kPad + 4 * cg) = make_float4(m[0], m[1], m[2], m[3]);
+            for (int u = 0; u < 2; ++u) {
+                const int n = 16 * warp + 8 * u + g, k0 = 16 * kk + 2 * q;
+                BFrag bf;
+                if (kBack)  // B[k][n] = M[n][k]
+                    bf = make_b(ld2(Mk + n * kPad + k0), ld2(Mk + n * kPad + k0 + 8));
+                else        // B[k][n] = M[k][n]
+                    bf = make_b(make_float2(Mk[k0 * kPad + n], Mk[(k0 + 1) * kPad + n]),
+                                make_float2(Mk[(k0 + 8) * kPad + n], Mk[(k0 + 9) * kPad + n]));
+                mma3(acc[u], af, bf);
             }
-            // the additive term at this thread's block
-            const float4 c = *reinterpret_cast<const float4 *>(Cadd + o + row * kN + 4 * cg);
-            acc[i][0] = c.x; acc[i][1] = c.y; acc[i][2] = c.z; acc[i][3] = c.w;
         }
-        __syncthreads();
-        for (int m = 0; m < kN; ++m) {
-            const float4 r = *reinterpret_cast<const float4 *>(R + m * kPad + 4 * cg);
+        float *Sn = Ss[cur ^ 1];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float s = S[(4 * rg + i) * kPad + m];
-                acc[i][0] = __fmaf_rn(s, r.x, acc[i][0]);
-                acc[i][1] = __fmaf_rn(s, r.y, acc[i][1]);
-                acc[i][2] = __fmaf_rn(s, r.z, acc[i][2]);
-                acc[i][3] = __fmaf_rn(s, r.w, acc[i][3]);
-            }
+        for (int u = 0; u < 2; ++u) {
+            const int c = 16 * warp + 8 * u + 2 * q;
+            *reinterpret_cast<float2 *>(Sn + g * kPad + c) = make_float2(acc[u][0], acc[u][1]);
+            *reinterpret_cast<float2 *>(Sn + (g + 8) * kPad + c) = make_float2(acc[u][2], acc[u][3]);
         }
-        __syncthreads();  // S and R are rewritten by the next step
     }
     if (fin) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float4 *>(fin + head + (4 * rg + i) * kN + 4 * cg) =
-                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        for (int u = 0; u < 2; ++u) {
+            float *fp = fin + head + (size_t)(row0 + g) * kN + 16 * warp + 8 * u + 2 * q;
+            *reinterpret_cast<float2 *>(fp) = make_float2(acc[u][0], acc[u][1]);
+            *reinterpret_cast<float2 *>(fp + 8 * kN) = make_float2(acc[u][2], acc[u][3]);
+        }
     }
 }
 
@@ -187,10 +248,11 @@ int wkv7_segment_scan(int B, int H, int nseg, const float *M, const float *C, co
         return wkv7::set_error(WKV7_EUNSUPPORTED, "this library needs an sm_103a device");
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const dim3 grid(B * H, kN / kScanRows);
     if (backward)
-        wkv7_segment_scan_kernel<true><<<B * H, kThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
+        wkv7_segment_scan_kernel<true><<<grid, kScanThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
     else
-        wkv7_segment_scan_kernel<false><<<B * H, kThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
+        wkv7_segment_scan_kernel<false><<<grid, kScanThreads, 0, st>>>(H, nseg, M, C, init, out, fin);
     return cuda_status(cudaGetLastError(), "segment scan launch");
 }
 
@@ -222,7 +284,8 @@ int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const v
     if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, ws.ident, ws.M, 2, st))) return rc;
     if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, nullptr, ws.Z, 1, st))) return rc;
     // (3) segment start states, and the final state
-    wkv7_segment_scan_kernel<false><<<B * H, kThreads, 0, st>>>(H, nseg, ws.M, ws.Z, s0, ws.starts, sT);
+    wkv7_segment_scan_kernel<false><<<dim3(B * H, kN / kScanRows), kScanThreads, 0, st>>>(H, nseg, ws.M, ws.Z, s0,
+                                                                                           ws.starts, sT);
     if ((rc = cuda_status(cudaGetLastError(), "segment scan launch")) != WKV7_OK) return rc;
     // (4) every segment from its start state; checkpoints and factors for the backward
     return wkv7_forward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.starts, y, nullptr, ws.ckpt, ws.fac, 16, stream);
@@ -255,7 +318,8 @@ int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const 
                             da, db, ws.D, stream)))
         return rc;
     // (2) the gradient arriving at every segment's end, and ds0
-    wkv7_segment_scan_kernel<true><<<B * H, kThreads, 0, st>>>(H, nseg, ws.M, ws.D, dsT, ws.G, ds0);
+    wkv7_segment_scan_kernel<true><<<dim3(B * H, kN / kScanRows), kScanThreads, 0, st>>>(H, nseg, ws.M, ws.D, dsT,
+                                                                                          ws.G, ds0);
     if ((rc = cuda_status(cudaGetLastError(), "segment scan launch")) != WKV7_OK) return rc;
     // (3) the gradients, each segment with its arriving gradient (its own ds0 is not needed)
     return wkv7_backward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.ckpt, ws.fac, 16, dy, ws.G, dr, dw, dk, dv, da,

@@ -102,3 +102,39 @@ def test_timesplit_matches_whole_sequence_oracle(B, T, H, nseg, dtype):
     wkv7.async_status()
     out = {"y": y, "sT": sT, **g}
     parity.check_heads(host, out, parity.all_heads(B, H), L=16)
+
+
+def _scan_reference(M, C, init, backward):
+    """The segment scan by its definition, in float64 on the CPU."""
+    M, C = M.double().cpu(), C.double().cpu()
+    B, nseg, H, N, _ = M.shape
+    S = init.double().cpu().clone() if init is not None else torch.zeros((B, H, N, N), dtype=torch.float64)
+    out = torch.empty_like(M)
+    for step in range(nseg):
+        k = nseg - 1 - step if backward else step
+        out[:, k] = S
+        S = C[:, k] + S @ (M[:, k].transpose(-1, -2) if backward else M[:, k])
+    return out, S
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("backward", [False, True])
+@pytest.mark.parametrize("B,H,nseg,with_init", [(2, 3, 5, True), (1, 2, 1, False), (3, 1, 33, True)])
+def test_segment_scan_against_its_definition(B, H, nseg, with_init, backward):
+    """wkv7_segment_scan (split-operand tensor-core products, 16 rows per CTA)
+    against S_{k+1} = C_k + S_k M_k (M_k^T backward) in float64.  The M_k are
+    0.95 x random orthogonal matrices, so the states keep their scale over the
+    steps; each split product is within about 3 * 2^-18 |a| |b| of the exact
+    one, so 1e-4 of the largest entry bounds the error after 33 steps."""
+    build()
+    g = torch.Generator().manual_seed(5)
+    Q, _ = torch.linalg.qr(torch.randn((B, nseg, H, 64, 64), generator=g, dtype=torch.float64))
+    M = (0.95 * Q).float().contiguous()
+    C = (0.1 * torch.randn((B, nseg, H, 64, 64), generator=g)).float()
+    init = torch.randn((B, H, 64, 64), generator=g) if with_init else None
+    out, fin = wkv7.segment_scan(M.cuda(), C.cuda(), init=None if init is None else init.cuda(), backward=backward)
+    torch.cuda.synchronize()
+    ref_out, ref_fin = _scan_reference(M, C, init, backward)
+    for got, ref in ((out, ref_out), (fin, ref_fin)):
+        err = (got.double().cpu() - ref).abs().max().item()
+        assert err <= 1e-4 * ref.abs().max().item(), (err, ref.abs().max().item())
