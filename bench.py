@@ -550,9 +550,39 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         seq_ms = max_over_ranks(b0.elapsed_time(b1), world) / 3
         wkv7.async_status()
+        # the host link itself: one output tensor out, and dy in, each alone and both at
+        # once; the step's copies cannot take less than link_bound_ms
+        yb = host_out["y"].numel() * 4
+        dyb = pinned["dy"].numel() * pinned["dy"].element_size()
+        dsts = sets[0][0]["dy"]
+
+        def timed(fn):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            fn()
+            torch.cuda.synchronize()
+            e[0].record(stream)
+            fn()
+            e[1].record(stream)
+            torch.cuda.synchronize()
+            return e[0].elapsed_time(e[1]) / 1e3
+
+        def both():
+            with torch.cuda.stream(sd):
+                sd.wait_stream(stream)
+                host_out["y"].copy_(outs["y"], non_blocking=True)
+            dsts.copy_(pinned["dy"], non_blocking=True)
+            stream.wait_stream(sd)
+
+        d2h_gbs = yb / timed(lambda: host_out["y"].copy_(outs["y"], non_blocking=True)) / 1e9
+        h2d_gbs = dyb / timed(lambda: dsts.copy_(pinned["dy"], non_blocking=True)) / 1e9
+        both_gbs = (yb + dyb) / timed(both) / 1e9
+        # neither direction beats its own rate, nor both together their joint rate
+        link_ms = 1e3 * max(d2h / (d2h_gbs * 1e9), h2d / (h2d_gbs * 1e9), (h2d + d2h) / (both_gbs * 1e9))
         e2e = {"value": world * spec.tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "pipelined": True,
-               "sequential_ms_per_step": seq_ms}
+               "sequential_ms_per_step": seq_ms,
+               "link": {"d2h_gbs": d2h_gbs, "h2d_gbs": h2d_gbs, "both_directions_gbs": both_gbs,
+                        "link_bound_ms": link_ms, "frac_of_link_bound": link_ms / e2e_ms}}
 
     # the producers fused into the entry points: the same step through
     # wkv7_forward_fused / wkv7_backward_fused on the same draws taken before the
