@@ -173,15 +173,16 @@ __global__ void __launch_bounds__(NT, 2)
     // there, and first waited for by the products that read S_0.
     __shared__ __align__(8) uint64_t bar, bar_s;
     __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
+    constexpr unsigned kChunkBytes =
+        (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_init(&bar_s, 1);
+        mbar_expect_tx(&bar, kChunkBytes);  // the last chunk's bytes, before any copy is issued
         lost = 0;
     }
     __syncthreads();
     int stuck = -1, s_phase = -1;  // the chunk whose wait ran out; the phase of the last start-state copy
-    constexpr unsigned kChunkBytes =
-        (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
     // kGN: parameter-gradient sums of this lane's channels 4 (lane % 16) .. + 3 (over the
     // tokens it converts), the bonus weights of its key rows rA, rB; per-token
     // sum_j do_j v_j past the dw carry in the W slot
@@ -196,13 +197,18 @@ __global__ void __launch_bounds__(NT, 2)
     // the last chunk's dw carry partials: the Gram slot, or the W slot when the Gram slot stages y
     float *const carp = kGN ? Wm : Gm;
     constexpr unsigned kS0Bytes = 64 * OS * 4;
-    auto stage_in = [&](int c) {  // inputs and dy of chunk c: one tensor copy each, lanes 0..6 of warp 0
-        if (tid < 7) {
-            void *const dst = tid < 6 ? static_cast<void *>(raw + tid * C * RS) : static_cast<void *>(dyf);
-            tma_rows(dst, &maps.m[tid], h, c * C, bi, &bar);
+    // A chunk's copies come from lanes 0..2 of warps 1..3, copy 3 (w - 1) + l: the six
+    // inputs, dy, the factor block, and (kGN) the forward's y.  Warp 0 issues the
+    // gradient stores and the start-state copy; thread 0 announces the bytes (before a
+    // block barrier that precedes every issue) and arrives once.
+    const int ccopy = warp >= 1 && lane < 3 ? 3 * (warp - 1) + lane : -1;
+    auto stage_in = [&](int c) {  // inputs and dy of chunk c (and y): one tensor copy each
+        if (ccopy >= 0 && ccopy < 7) {
+            void *const dst = ccopy < 6 ? static_cast<void *>(raw + ccopy * C * RS) : static_cast<void *>(dyf);
+            tma_rows(dst, &maps.m[ccopy], h, c * C, bi, &bar);
         }
-        if constexpr (kGN) {  // and the forward's y of the chunk (lane 7)
-            if (tid == 7) tma_rows(Gm, &maps.m[8], h, c * C, bi, &bar);
+        if constexpr (kGN) {
+            if (ccopy == 8) tma_rows(Gm, &maps.m[8], h, c * C, bi, &bar);
         }
     };
     auto load_s0 = [&](int c) {  // thread 0
@@ -227,10 +233,9 @@ __global__ void __launch_bounds__(NT, 2)
     const float *FC = reinterpret_cast<const float *>(Bs + B_QQ);  // factor block of the current chunk
     auto stage_fac = [&](int c) {
         if constexpr (kFac) {
-            if (tid == 3) bulk_g2s(Bs + B_QQ, p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords, fac::kWords * 4, &bar);
+            if (ccopy == 7) bulk_g2s(Bs + B_QQ, p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords, fac::kWords * 4, &bar);
         }
     };
-    if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     stage_in(nchunks - 1);
     stage_fac(nchunks - 1);
     if (tid == 0) mbar_arrive(&bar);

@@ -41,6 +41,9 @@ using namespace chunk;
 
 constexpr int NT = 128;
 constexpr int YS = 68;  // row stride (floats) of the y staging block
+// Lane 0 of warp 3 issues the y (and o) stores: warp 0 forms the inverse, the
+// chunk's critical path.
+constexpr int kYStoreThread = 96;
 
 // Shared-memory carve-up (byte offsets after the raw input block).  HL16 = a
 // split operand matrix (bf16 hi then lo) of 16 rows, row stride MS; HLC = a
@@ -126,21 +129,26 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
     // phase c of the mbarrier is chunk c
     __shared__ __align__(8) uint64_t bar;
     __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
+    // the staged rows this mode reads: all six; w, k, v, a, b; or w, a, b
+    constexpr unsigned kRows = kMode == 0 ? 6 : kMode == 1 ? 5 : 3;
+    constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>() / 6 * kRows;
     if (tid == 0) {
         mbar_init(&bar, 1);
+        mbar_expect_tx(&bar, kChunkBytes);  // chunk 0's bytes, before any copy is issued
         lost = 0;
     }
     __syncthreads();
     int stuck = -1;  // the chunk whose wait ran out
-    // the staged rows this mode reads: all six; w, k, v, a, b; or w, a, b
-    constexpr unsigned kRows = kMode == 0 ? 6 : kMode == 1 ? 5 : 3;
-    constexpr unsigned kChunkBytes = (unsigned)raw_bytes<E>() / 6 * kRows;
     auto staged = [](int vec) { return kMode == 0 || (vec != VR && (kMode == 1 || (vec != VK && vec != VV))); };
-    auto prefetch = [&](int c) {  // chunk c's copies (lanes 0..5 of warp 0); thread 0 announced its bytes
-        if (tid < 6 && staged(tid)) tma_rows(raw + tid * C * RS, &maps.m[tid], h, c * C, bi, &bar);
+    // chunk c's copies, input 2 (w - 1) + l from lane l < 2 of warp w >= 1: warp 0, which
+    // forms the inverse right after the copies are issued, issues none.  Thread 0
+    // announced the bytes (before a block barrier that precedes every issue) and
+    // arrives once.
+    const int cvec = warp >= 1 && lane < 2 ? 2 * (warp - 1) + lane : -1;
+    auto prefetch = [&](int c) {
+        if (cvec >= 0 && staged(cvec)) tma_rows(raw + cvec * C * RS, &maps.m[cvec], h, c * C, bi, &bar);
         if (tid == 0) mbar_arrive(&bar);
     };
-    if (tid == 0) mbar_expect_tx(&bar, kChunkBytes);
     prefetch(0);
     // kGN: bonus tile of the staged chunk, bon[t][j] = (sum_i r_i k_i r_k[i]) v_j; thread
     // (t = e / 16, j = 4 (e % 16)) sums its four channels, the 16 lanes of a token finish it
@@ -182,8 +190,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         };
 
         float *const fc = p.fac ? p.fac + ((size_t)bh * nchunks + c) * fac::kWords : nullptr;
-        // the cumulative decays on warps 2 and 3 (thread 0 has just issued the y store)
-        const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 64));
+        // the cumulative decays on warps 1 and 2 (lane 0 of warp 3 has just issued the y store)
+        const bool exact = __syncthreads_or(prep_decay<kP>(raw, dd, nv, 32));
         if (lost) {  // every thread has passed its wait (the barrier above): leave together
             stuck = c;
             break;
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
                 ldb2_t<CS>(MK, 0, 0, lane, bq[0], bq[1]);
                 mma3n<2, kVLo>(ya + 2, vA, bq);
             }
-            if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
+            if (tid == kYStoreThread) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();  // W
 
             // Checkpoint of S_0 (before P2 updates S): each warp stages its 16 rows,
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             // exact per-token recurrence for a chunk whose decay leaves the factorisable range
             if constexpr (kGN) write_bonus();
             write_ckpt();
-            if (tid == 0) bulk_wait_read();  // the previous y tile has left the staging block
+            if (tid == kYStoreThread) bulk_wait_read();  // the previous y tile has left the staging block
             __syncthreads();
             for (int t = 0; t < nv; ++t) {
                 float sa0 = 0.f, sa1 = 0.f;
@@ -468,7 +476,8 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             fence_proxy_async();
             __syncthreads();
         }
-        if (kMode == 0 && tid == 0) {  // y (and o) of the chunk: one tensor store each (tokens past T are not written)
+        if (kMode == 0 && tid == kYStoreThread) {  // y (and o) of the chunk: one tensor store each (tokens past T
+                                                   // are not written)
             tma_store_rows(&maps.m[6], ys, h, t0, bi);
             if constexpr (kGN) tma_store_rows(&maps.m[8], bon, h, t0, bi);
             bulk_commit();
