@@ -66,10 +66,10 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def load_traffic():
+def load_traffic(workload: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the chunked kernels as they are now (the hash of their source files is
-    recorded with it)."""
+    on this workload and on the chunked kernels as they are now (the hash of
+    their source files is recorded with it)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return {}
@@ -79,7 +79,9 @@ def load_traffic():
     except ValueError:
         return {}
     from rwkv_linear_attention_wkv7_gb300 import _build
-    return d.get("kernels", {}) if d.get("source_hash") == _build.source_hash(_build.CHUNK_KERNEL_FILES) else {}
+    if d.get("workload") != workload or d.get("source_hash") != _build.source_hash(_build.CHUNK_KERNEL_FILES):
+        return {}
+    return d.get("kernels", {})
 
 
 class ClockSampler:
@@ -249,9 +251,11 @@ def config_of(spec, args):
 
 def workload_of(args):
     spec = synthetic.WORKLOADS[args.workload]
+    import dataclasses
     if args.batch:
-        import dataclasses
         spec = dataclasses.replace(spec, B=args.batch, name=f"{spec.name}@B={args.batch}")
+    if args.seq_len:
+        spec = dataclasses.replace(spec, T=args.seq_len, name=f"{spec.name}@T={args.seq_len}")
     return spec
 
 
@@ -459,7 +463,7 @@ def run_ours(args, world, rank, local):
     value = world * spec.tokens / (ms_step / 1e3)
     peak, peak_kind = load_peaks()
     fwd_bytes, bwd_bytes = algorithmic_bytes(spec)
-    traffic = load_traffic()
+    traffic = load_traffic(spec.name)
     dom = "backward" if bwd_ms >= fwd_ms else "forward"
     dom_ms, dom_bytes = (bwd_ms, bwd_bytes) if dom == "backward" else (fwd_ms, fwd_bytes)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -781,6 +785,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller profiling cases of the same kernels)")
+    ap.add_argument("--seq-len", type=int, default=None, help="override T of the workload (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")
