@@ -12,8 +12,9 @@
 // stay on warp-level mma.sync spread over the four warps: as chains of
 // single-thread tcgen05.mma (12 and 6 dependent MMAs of about 50 cycles each)
 // they lengthened every chunk's critical path and the kernel measured slower
-// (3.53 against 2.67 ms on the bf16 B=16 T=4096 H=32 workload).  The two that
-// only feed the gradient outputs,
+// (3.53 ms on the bf16 B=16 T=4096 H=32 workload, against 2.67 ms for the
+// warp-level kernel as it then was).  The two that only feed the gradient
+// outputs,
 //   G3  S_0^T [DY | DSA]   (M = 64 keys, N = 32, K = 64 value rows)
 //   G4  G^T [V | SA]       (M = 64 keys, N = 32, K = 64 value rows; scaled by d_C per key after)
 // are issued by one thread as tcgen05.mma (bf16 operands split hi + lo, three
