@@ -264,14 +264,16 @@ inline cudaError_t encode_input_maps(InputMaps *maps, const SeqArgs &p, const fl
     return dy ? encode_rows_map(&maps->m[6], dy, 4, p.B, p.T, p.H) : cudaSuccess;
 }
 // Host: map of the checkpoints as rows of 64 fp32 (nrows = B*H*ceil(T/L)*64),
-// box OS x box_rows (padded staging rows: eight state rows of one warp for the
+// box box_cols x box_rows (padded staging rows, the columns past 64 clipped on
+// stores and zero-filled on loads: eight state rows of one warp for the
 // stores, a whole 64-row state for the loads).
-inline cudaError_t encode_ckpt_map(CUtensorMap *m, const float *ckpt, long long nrows, int box_rows = 8) {
+inline cudaError_t encode_ckpt_map(CUtensorMap *m, const float *ckpt, long long nrows, int box_rows = 8,
+                                   int box_cols = OS) {
     const EncodeTiledFn encode = encode_tiled_fn();
     if (!encode) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {64, (cuuint64_t)nrows};
     const cuuint64_t strides[1] = {64ull * 4};
-    const cuuint32_t box[2] = {OS, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ckpt), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

@@ -44,6 +44,11 @@ constexpr int YS = 68;  // row stride (floats) of the y staging block
 // Lane 0 of warp 3 issues the y (and o) stores: warp 0 forms the inverse, the
 // chunk's critical path.
 constexpr int kYStoreThread = 96;
+// Row pitch (floats) of the checkpoint staging: a half-warp's float2 stores of
+// accumulator rows g, g + 1, ... then fall in distinct banks (with OS = 68 two
+// rows four banks apart overlap).  Two warps' eight-row halves fill one split
+// operand slot exactly.
+constexpr int CKS = 72;
 
 // Shared-memory carve-up (byte offsets after the raw input block).  HL16 = a
 // split operand matrix (bf16 hi then lo) of 16 rows, row stride MS; HLC = a
@@ -63,6 +68,7 @@ constexpr int B_QK = B_MK + HLC;                     // Q_k [s][t]   warps 1, 2,
 constexpr int B_WT = B_QK + HLC;                     // W^T [t][s]  (compact)
 constexpr int B_MB = B_WT + HLC;                     // M_b fp32 [C][MBS] (for the inverse)
 constexpr int kBytes = B_MB + C * MBS * 4;
+static_assert(2 * 8 * 72 * 4 <= HL16, "two warps' checkpoint halves fit one split operand slot");
 static_assert(B_BT % 16 == 0 && B_Y % 128 == 0 && B_QB % 16 == 0 && B_MB % 16 == 0 && YS == OS,
               "aligned blocks; the y staging block is a tensor-store source");
 
@@ -291,12 +297,12 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             // U/Z is done) and writes them with 2-D tensor stores; the second half
             // waits for the first to have left the staging block.
             const bool ck = p.ckpt && t0 % p.L == 0;
-            float *const ckst = reinterpret_cast<float *>(Bs + (warp < 2 ? B_AH : B_RH)) + (warp & 1) * 8 * OS;
+            float *const ckst = reinterpret_cast<float *>(Bs + (warp < 2 ? B_AH : B_RH)) + (warp & 1) * 8 * CKS;
             const int ckrow = (bh * p.nck + t0 / p.L) * 64 + 16 * warp;
             auto stage_ck = [&](int half) {
 #pragma unroll
                 for (int nt = 0; nt < 8; ++nt)
-                    *reinterpret_cast<float2 *>(ckst + g * OS + 8 * nt + 2 * q) =
+                    *reinterpret_cast<float2 *>(ckst + g * CKS + 8 * nt + 2 * q) =
                         make_float2(S[nt][2 * half], S[nt][2 * half + 1]);
                 fence_proxy_async();
                 __syncwarp();
@@ -501,7 +507,7 @@ cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
     InputMaps maps;  // six inputs, y (box OS), the checkpoints, and o (box 64) with kGN
     cudaError_t e = encode_input_maps(&maps, p, nullptr);
     if (e == cudaSuccess && kMode == 0) e = encode_rows_map(&maps.m[6], p.y, 4, p.B, p.T, p.H, OS);
-    if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64);
+    if (e == cudaSuccess && p.ckpt) e = encode_ckpt_map(&maps.m[7], p.ckpt, (long long)p.B * p.H * p.nck * 64, 8, CKS);
     if (e == cudaSuccess && kGN) e = encode_rows_map(&maps.m[8], p.o, 4, p.B, p.T, p.H, 64);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(wkv7_fwd_chunk_kernel<E, kP, kGN, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
