@@ -18,6 +18,8 @@
 //   [DR | DA]   = [d | d_prev] o (S_0^T [DY | DSA] + [B~ | K~] mask(Gam))
 //   [DK | DB]   = (1/d) o (Gd^T [V | SA] + [R^ | A^] mask(Gam^T))
 //   G_prev      = Gd + [DY | DSA] [R^ | A^]^T
+// ([DV | DSA] is evaluated as X = Gd [K~ | B~]^T, DV = X_K + X_B M_k'^T + DY Q'^T,
+// DSA = X_B W^T + DY Q_b'^T: K' and B' are never formed.)
 // dw needs no contraction of its own: summing H_t o S_t over the value rows
 // in two ways gives, per key column,
 //   w_t o dw_t = r_t o dr_t - b_t o db_t - k_t o dk_t + (w o dw + a o da)_{t+1},
@@ -51,8 +53,8 @@ constexpr int B_VV = B_RH + HL16;              // v [t][i]
 constexpr int B_DYH = B_VV + HL16;             // dy [t][i]
 constexpr int B_SAH = B_DYH + HL16;            // SA [t][i]
 constexpr int B_DSH = B_SAH + HL16;            // DSA [t][i]
-constexpr int B_Y = B_DSH + HL16;              // A' [t][j] (HL16), M_k' [s][t] (HL16), [K'; B'] (HL32), [Q'; W Q_b] (HL32)
-constexpr int B_AP = B_Y, B_MK = B_Y + HL16, B_KB = B_Y + 2 * HL16, B_QQ = B_KB + HL32;
+constexpr int B_Y = B_DSH + HL16;              // A' [t][j] (HL16), M_k' [s][t] (HL16), an HL32 slot, [Q'; W Q_b] (HL32)
+constexpr int B_AP = B_Y, B_MK = B_Y + HL16, B_QQ = B_Y + 2 * HL32;
 constexpr int B_M3 = B_Y, B_M4 = B_Y + HL32;   // masked Gam blocks [k][n] (HL32 each), after G1/G2
 constexpr int kBytes = B_QQ + HL32;
 static_assert(B_SX % 16 == 0 && B_BT % 16 == 0 && B_Y % 16 == 0, "16-byte aligned operand matrices");
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(NT, 2)
     float *S0f = reinterpret_cast<float *>(Bs + B_SX);
     const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, B_BT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, B_AH, 16),
              RH = hl(Bs, B_RH, 16), VM = hl(Bs, B_VV, 16), DYH = hl(Bs, B_DYH, 16), SAH = hl(Bs, B_SAH, 16),
-             DSH = hl(Bs, B_DSH, 16), AP = hl(Bs, B_AP, 16), MK = hl(Bs, B_MK, 16), KB = hl(Bs, B_KB, 32),
+             DSH = hl(Bs, B_DSH, 16), AP = hl(Bs, B_AP, 16), MK = hl(Bs, B_MK, 16),
              QQ = hl(Bs, B_QQ, 32), M3 = hl(Bs, B_M3, 32), M4 = hl(Bs, B_M4, 32);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -336,8 +338,7 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
         for (int m = 0; m < 2; ++m) {  // decay-scaled vectors: [t][j] quads
             // with the factor cache, warp w converts its own 16-key slab (all
-            // tokens), which is all its K'/B' products read: no block barrier
-            // between the split and K'/B'
+            // tokens); the block barrier after the splits shows every slab to G2
             const int e = kFac ? lane + 32 * m : tid + NT * m;
             const int t = kFac ? e >> 2 : e >> 4, j = kFac ? 16 * warp + (e & 3) * 4 : (e & 15) * 4;
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
@@ -450,41 +451,7 @@ __global__ void __launch_bounds__(NT, 2)
         }
         __syncthreads();
         }
-        {   // K' = d_C o (K~ + M_k' B~), B' = d_C o (W B~) (M = token, N = key; warp w owns keys 16w..)
-            AFrag amk, awn;
-            if constexpr (kFac) {
-                amk = ld_afrag(FC + fac::kMkA, lane);
-                awn = ld_afrag(FC + fac::kWA, lane);
-            } else {
-                amk = lda(MK, 0, 0, lane);
-                awn = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
-                             make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
-                             make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
-                             make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
-            }
-            BFrag b0, b1;
-            ldb2_t(BT, 16 * warp, 0, lane, b0, b1);
-            __nv_bfloat16 *kh = hi_of(Bs, B_KB), *kl = lo_of(Bs, B_KB, 32);
-            float ck[2][4], cb2[2][4] = {};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int jc = 16 * warp + 8 * u + 2 * q;
-                const float2 k0 = ld_hl(KT.hi, KT.lo, g, jc), k8 = ld_hl(KT.hi, KT.lo, g + 8, jc);
-                ck[u][0] = k0.x; ck[u][1] = k0.y; ck[u][2] = k8.x; ck[u][3] = k8.y;
-            }
-            const BFrag bq[2] = {b0, b1};
-            mma3n<2>(ck, amk, bq);
-            mma3n<2>(cb2, awn, bq);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + 16 * warp + 8 * u + 2 * q);
-                ck[u][0] *= dc.x; ck[u][1] *= dc.y; ck[u][2] *= dc.x; ck[u][3] *= dc.y;
-                cb2[u][0] *= dc.x; cb2[u][1] *= dc.y; cb2[u][2] *= dc.x; cb2[u][3] *= dc.y;
-            }
-            st_acc16(kh, kl, 0, 16 * warp, ck, lane);   // K' rows (tokens)
-            st_acc16(kh, kl, 16, 16 * warp, cb2, lane); // B' rows
-        }
-        __syncthreads();  // warp 0 has drained the gradient stores: the staging slots are free
+        __syncthreads();  // every b~ / k~ slab is split; warp 0 has drained the gradient stores
         // v split: warp w its own 16 value columns (all tokens), which is all its vA
         // reads; the other readers come after the barrier that follows G2
 #pragma unroll
@@ -562,15 +529,51 @@ __global__ void __launch_bounds__(NT, 2)
             carryB = carp[rB] + carp[64 + rB] + carp[128 + rB] + carp[192 + rB];
         }
 
-        // G2: [DV | DSA] = G [K' | B'] + DY [Q'^T | (W Q_b)^T]
+        // G2: [DV | DSA] = G [K' | B'] + DY [Q'^T | (W Q_b)^T], with K' = d_C o (K~ + M_k' B~) and
+        // B' = d_C o (W B~) never formed: X = (G diag(d_C)) [K~ | B~]^T, then
+        //   G K'^T = X_K + X_B M_k'^T,   G B'^T = X_B W^T   (16 x 16 products on this warp's rows)
         float dvs[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const AFrag gf = a_from_acc(Gh, kk);
+            const float2 d0 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 2 * q);
+            const float2 d1 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 8 + 2 * q);
+            const AFrag gf = make_a(make_float2(Gh[2 * kk][0] * d0.x, Gh[2 * kk][1] * d0.y),
+                                    make_float2(Gh[2 * kk][2] * d0.x, Gh[2 * kk][3] * d0.y),
+                                    make_float2(Gh[2 * kk + 1][0] * d1.x, Gh[2 * kk + 1][1] * d1.y),
+                                    make_float2(Gh[2 * kk + 1][2] * d1.x, Gh[2 * kk + 1][3] * d1.y));
             BFrag b0, b1, b2, b3;
-            ldb2(KB, 0, 16 * kk, lane, b0, b1);
-            ldb2(KB, 16, 16 * kk, lane, b2, b3);
+            ldb2(KT, 0, 16 * kk, lane, b0, b1);
+            ldb2(BT, 0, 16 * kk, lane, b2, b3);
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(dvs, gf, bq); }
+        }
+        {
+            // M_k' (M = token t, K = s) and W as A fragments; an A fragment of a 16 x 16 matrix
+            // holds the B fragments of its transpose: n-tile n is registers n and n + 2
+            AFrag amk, awn;
+            if constexpr (kFac) {
+                amk = ld_afrag(FC + fac::kMkA, lane);
+                awn = ld_afrag(FC + fac::kWA, lane);
+            } else {
+                amk = lda(MK, 0, 0, lane);
+                awn = make_a(make_float2(Wm[g * WS + 2 * q], Wm[g * WS + 2 * q + 1]),
+                             make_float2(Wm[(g + 8) * WS + 2 * q], Wm[(g + 8) * WS + 2 * q + 1]),
+                             make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
+                             make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
+            }
+            auto tb = [](const AFrag &a, int n) {
+                BFrag b;
+                b.hi[0] = a.hi[n]; b.hi[1] = a.hi[n + 2];
+                b.lo[0] = a.lo[n]; b.lo[1] = a.lo[n + 2];
+                return b;
+            };
+            const AFrag xb = a_from_acc(dvs, 1);  // X_B (tiles 2, 3)
+            float dsa[2][4] = {};
+            { const BFrag bm[2] = {tb(amk, 0), tb(amk, 1)}; mma3n<2>(dvs, xb, bm); }
+            { const BFrag bw[2] = {tb(awn, 0), tb(awn, 1)}; mma3n<2>(dsa, xb, bw); }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dvs[2 + u][e] = dsa[u][e];
         }
         const AFrag dyA = lda_t(DYH, 16 * warp, 0, lane);
         {
