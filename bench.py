@@ -419,7 +419,8 @@ def run_ours(args, world, rank, local):
     # --min-timed-s, so that the clock record sampled during it has several samples
     # (every round is K full steps; ms_per_step divides by all timed steps)
     warm_ms = max_over_ranks(w0.elapsed_time(w1) / max(args.warmup, 1), world)
-    rounds = max(1, -(-int(args.min_timed_s * 1e3) // max(int(warm_ms * args.steps), 1)))
+    # (a 15 % margin: warm-up steps can run a little slower than timed ones)
+    rounds = max(1, -(-int(1.15 * args.min_timed_s * 1e3) // max(int(warm_ms * args.steps), 1)))
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
