@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(NT, 2)
                 }
             }
         };
-        // the cumulative decays on warps 2 and 3, clear of warp 0's copies
+        // the cumulative decays on warps 2 and 3 (warps 0 and 1 have just issued the gradient stores)
         const bool exact = __syncthreads_or(prep_decay<kP, E, !kP>(raw, dd, nv, 64));
         if (lost) {  // every thread has passed its wait (the barrier above): leave together
             stuck = c;
