@@ -135,6 +135,10 @@ __global__ void __launch_bounds__(NT, 2)
     float *Gm = reinterpret_cast<float *>(Bs + B_G), *Wm = reinterpret_cast<float *>(Bs + B_W);
     // kP: avec of the chunk, fp32 [C][OS], past the 256 floats the last chunk's dw carry uses
     float *const avs = Gm + 256;
+    // kP: sigmoid(w_pre) of the chunk, fp32 [C][DS], from the decay phase to the dw_pre
+    // factors (the slot takes the masked Gam block M4 only after those are formed)
+    float *const sgs = reinterpret_cast<float *>(Bs + B_M4);
+    static_assert(C * DS * 4 <= HL32, "the sigmoid block fits the M4 slot");
     static_assert(256 * 4 + C * OS * 4 <= C * SP * 4 + 1280, "avec copy fits the Gram and W slots");
     float *S0f = reinterpret_cast<float *>(Bs + B_SX);
     const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, B_BT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, B_AH, 16),
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(NT, 2)
             }
         };
         // the cumulative decays on warps 2 and 3 (warps 0 and 1 have just issued the gradient stores)
-        const bool exact = __syncthreads_or(prep_decay<kP, E, !kP>(raw, dd, nv, 64));
+        const bool exact = __syncthreads_or(prep_decay<kP, E, !kP>(raw, dd, nv, 64, kP ? sgs : nullptr));
         if (lost) {  // every thread has passed its wait (the barrier above): leave together
             stuck = c;
             break;
@@ -604,9 +608,9 @@ __global__ void __launch_bounds__(NT, 2)
         const AFrag dsA = make_a(make_float2(dvs[2][0], dvs[2][1]), make_float2(dvs[2][2], dvs[2][3]),
                                  make_float2(dvs[3][0], dvs[3][1]), make_float2(dvs[3][2], dvs[3][3]));
         // kP: -0.606531 sigmoid (1 - sigmoid) of w_pre at this lane's dw positions (key rows rA / rB,
-        // tokens 2q, 2q + 1, 8 + 2q, 9 + 2q), taken from w_pre itself while the staged rows are
-        // still this chunk's: recovering the sigmoid from the decays (-ln(w) / 0.606531) would lose
-        // its relative precision where it is small (w rounds to 1 in fp32)
+        // tokens 2q, 2q + 1, 8 + 2q, 9 + 2q), from the sigmoid of w_pre itself that the decay
+        // phase kept (before G3 writes M4 over it): recovering the sigmoid from the decays
+        // (-ln(w) / 0.606531) would lose its relative precision where it is small (w rounds to 1)
         float sgf[2][4];
         if constexpr (kP) {
 #pragma unroll
@@ -614,7 +618,7 @@ __global__ void __launch_bounds__(NT, 2)
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int t = 8 * (m >> 1) + 2 * q + (m & 1);
-                    const float sg = sigmoid_f(ld_raw(raw, VW, t, hr ? rB : rA));
+                    const float sg = sgs[t * DS + (hr ? rB : rA)];
                     sgf[hr][m] = -kDecayScale * sg * (1.f - sg);
                 }
         }

@@ -333,8 +333,11 @@ __device__ __forceinline__ float4 rcp4(float4 a) {
 // w_t, which multiplies that sum's absolute rounding (about 1e-5 of the
 // largest r o dr term) by 1 / w_t.
 constexpr float kSmallW = 0.0625f;
+// With kP, sig (if not NULL) receives sigmoid(w_pre) of every staged token,
+// [t][j] with row stride DS, for callers that need it again.
 template <bool kP, typename E, bool kMinW = false>
-__device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0) {
+__device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int first_thread = 0,
+                                           float *sig = nullptr) {
     bool bad = false;
     if constexpr (kP) {
         // the producers' exponentials on all four warps: warp w holds keys
@@ -344,7 +347,11 @@ __device__ __forceinline__ bool prep_decay(const E *raw, float *dd, int nv, int 
         const int lane = threadIdx.x & 31, j = 16 * (threadIdx.x >> 5) + (lane & 15), t0 = 8 * (lane >> 4);
         float wv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) wv[u] = t0 + u < nv ? in_w<true>(raw, t0 + u, j) : 1.f;
+        for (int u = 0; u < 8; ++u) {  // in_w<true>, with the sigmoid kept
+            const float sg = sigmoid_f(ld_raw(raw, VW, t0 + u, j));
+            if (sig) sig[(t0 + u) * DS + j] = sg;
+            wv[u] = t0 + u < nv ? __expf(-kDecayScale * sg) : 1.f;
+        }
         float dl[8], dc = 1.f;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
