@@ -409,10 +409,27 @@ def run_ours(args, world, rank, local):
             e2.record(stream)
             ev_f.append((e0, e1, e2))
 
+    # The step as a user runs it: wkv7_forward_backward, the forward and the
+    # backward as concurrent blocks of batch rows (the library's default split)
+    # on its own streams, forked from and joined back into this stream.  The
+    # workloads with another checkpoint stride run the two calls in a row.
+    use_step = spec.L == 16
+    fbout = {**outs, **gouts}
+    nsplit = 0  # the library's default
+    split = min(2, B) if use_step else 1
+    launches_per_step = 2 * split
+
+    def fb_step():
+        if use_step:
+            wkv7.forward_backward(*(d[n] for n in INPUTS), d["dy"], s0=d["s0"], dsT=d["dsT"], want_factors=use_fac,
+                                  nsplit=nsplit, out=fbout, stream=stream)
+        else:
+            step()
+
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0.record(stream)
     for _ in range(args.warmup):
-        step()
+        fb_step()
     w1.record(stream)
     torch.cuda.synchronize()
     # the timed region repeats whole rounds of K steps until it lasts at least
@@ -428,15 +445,29 @@ def run_ours(args, world, rank, local):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for _ in range(rounds * args.steps):
-            step(record=True)
+            fb_step()
         t_end.record(stream)
         torch.cuda.synchronize()
     wkv7.async_status()  # raises if a kernel's bounded wait on its bulk copies ran out
     barrier(world)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    clocks = clk.summary()
+
+    # each kernel on its own: the same step as wkv7_forward then wkv7_backward on
+    # the whole batch, CUDA events around every launch (the roofline's launch times)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    s0_ev, s1_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0_ev.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    s1_ev.record(stream)
+    torch.cuda.synchronize()
+    wkv7.async_status()
+    seq_step_ms = max_over_ranks(s0_ev.elapsed_time(s1_ev), world) / args.steps
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev_f)
     bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev_f)
-    clocks = clk.summary()
 
     ms_step = total_ms / (rounds * args.steps)
 
@@ -483,6 +514,10 @@ def run_ours(args, world, rank, local):
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
         def run_step(din, o, gq):
+            if use_step:
+                wkv7.forward_backward(*(din.get(n, d[n]) for n in INPUTS), din["dy"], s0=d["s0"], dsT=d["dsT"],
+                                      want_factors=use_fac, nsplit=nsplit, out={**o, **gq}, stream=stream)
+                return
             wkv7.forward(*(din.get(n, d[n]) for n in INPUTS), s0=d["s0"], L=spec.L, want_factors=use_fac, out=o,
                          stream=stream)
             wkv7.backward(*(din.get(n, d[n]) for n in INPUTS), o["ckpt"], din["dy"], dsT=d["dsT"], L=spec.L,
@@ -767,11 +802,15 @@ def run_ours(args, world, rank, local):
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic.get(dom), "algorithmic_bytes": dom_bytes, "launch_ms": dom_ms},
         "hbm_fraction_step": step_gbs / peak,
+        "step": {"entry": "wkv7_forward_backward" if use_step else "wkv7_forward + wkv7_backward",
+                 "blocks_of_batch_rows": split, "launches": launches_per_step,
+                 "sequential_ms_per_step": seq_step_ms,
+                 "sequential": "wkv7_forward then wkv7_backward on the whole batch, one stream"},
         "forward": {"ms": fwd_ms, "tokens_per_s": spec.tokens / (fwd_ms / 1e3),
                     "algorithmic_gbs": fwd_bytes / (fwd_ms / 1e3) / 1e9},
         "backward": {"ms": bwd_ms, "algorithmic_gbs": bwd_bytes / (bwd_ms / 1e3) / 1e9,
                      "kernel": "mma.sync", "tcgen05_variant_ms": bwd_tc_ms},
-        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": 2 * rounds * args.steps, "clocks": clocks,
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches_per_step * rounds * args.steps, "clocks": clocks,
         "fused": fused, "gn_epilogue": gnres, "decode": decode, "timesplit": timesplit,
     }
     print(json.dumps(line), flush=True)

@@ -298,6 +298,41 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
                                   float *ds0, void *stream);
 
 /*
+ * One training step in one call: wkv7_forward (checkpoint stride 16, with
+ * the factor cache when `factors` is given) followed by wkv7_backward on the
+ * same batch.  This entry point is a library convenience; the method's
+ * description has no counterpart to it.  Every head is independent in both
+ * directions, so the batch is cut into `nsplit` contiguous blocks of batch
+ * rows; each block runs its forward and then its backward on a stream of
+ * the library's own, forked from `stream` by an event and joined back into
+ * it.  A block's backward starts as soon as its forward is done, while the
+ * other blocks' forwards finish, which keeps more of the GPU busy than the
+ * two calls in a row.  Results are bit-identical to those two calls.
+ *   r..b, s0, dy, dsT, y, sT, dr..db, ds0   as in wkv7_forward / wkv7_backward
+ *   ckpt      [B][H][ceil(T/16)][N][N], required when T > 0: written by the
+ *             forward half, read by the backward half.
+ *   factors   [B][H][wkv7_factor_floats(T)] or NULL (the backward half then
+ *             rebuilds the per-chunk factors itself).
+ *   nsplit    number of blocks, 0 (the library's default, 2) to 4; more
+ *             blocks than batch rows means one row per block, 1 runs the two
+ *             calls in order on `stream` itself.
+ * Ownership and errors as in wkv7_forward: the caller owns every buffer;
+ * every argument is checked (WKV7_EINVAL, WKV7_EUNSUPPORTED) before anything
+ * is launched; WKV7_ECUDA on a launch or stream error, after which the
+ * library's streams are still joined back into `stream`.  The library keeps
+ * its streams and events (four streams and five events per device) for the
+ * life of the process; concurrent calls from several host threads are
+ * serialised while they enqueue their work.
+ */
+int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype,
+                          const void *r, const void *w, const void *k,
+                          const void *v, const void *a, const void *b,
+                          const float *s0, const float *dy, const float *dsT,
+                          float *y, float *sT, float *ckpt, float *factors,
+                          float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                          float *ds0, int nsplit, void *stream);
+
+/*
  * Status of the kernels' asynchronous copies on the current device.  The
  * kernels stage their inputs with bulk copies whose completion they wait for
  * a bounded time; a wait that runs out (which no correct run should see) sets

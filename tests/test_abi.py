@@ -48,7 +48,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
                      "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused",
-                     "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats"):
+                     "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats",
+                     "wkv7_forward_backward"):
         assert required in names
 
 
@@ -158,6 +159,29 @@ def test_gn_entry_points_reject_bad_arguments(lib):
     bad = list(bwd)
     bad[17] = None  # gn_w
     assert lib.wkv7_backward_gn(*bad) == EINVAL and "gn_w" in wkv7.last_error()
+
+
+def test_forward_backward_rejects_bad_arguments(lib):
+    """The one-call training step: nsplit in 0..4, dy and ckpt required,
+    factors optional but aligned, N = 64; all before any device query."""
+    p = ctypes.c_void_p(4096)
+    args = [1, 4, 1, 64, 0] + [p] * 6 + [None, p, None] + [p, None, p, None] + [p] * 6 + [None, 0, None]
+    for ns in (5, -1):
+        bad = list(args)
+        bad[25] = ns
+        assert lib.wkv7_forward_backward(*bad) == EINVAL and "nsplit" in wkv7.last_error()
+    bad = list(args)
+    bad[12] = None  # dy
+    assert lib.wkv7_forward_backward(*bad) == EINVAL and "dy" in wkv7.last_error()
+    bad = list(args)
+    bad[16] = None  # ckpt
+    assert lib.wkv7_forward_backward(*bad) == EINVAL and "ckpt" in wkv7.last_error()
+    bad = list(args)
+    bad[17] = ctypes.c_void_p(4100)  # factors misaligned
+    assert lib.wkv7_forward_backward(*bad) == EINVAL and "factors" in wkv7.last_error()
+    bad = list(args)
+    bad[3] = 32  # N
+    assert lib.wkv7_forward_backward(*bad) == EINVAL
 
 
 def test_decode_rejects_bad_arguments(lib):
