@@ -513,10 +513,14 @@ def run_ours(args, world, rank, local):
         h2d = sum(pinned[n].numel() * pinned[n].element_size() for n in pinned)
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
+        # The step through wkv7_forward_backward with one block (its two calls in order on
+        # this stream): the copies bound this pipeline, so the split gains nothing here,
+        # and a stream of the library's beside the two copy streams made the overlap
+        # come and go from run to run (22 to 37 ms per step).
         def run_step(din, o, gq):
             if use_step:
                 wkv7.forward_backward(*(din.get(n, d[n]) for n in INPUTS), din["dy"], s0=d["s0"], dsT=d["dsT"],
-                                      want_factors=use_fac, nsplit=nsplit, out={**o, **gq}, stream=stream)
+                                      want_factors=use_fac, nsplit=1, out={**o, **gq}, stream=stream)
                 return
             wkv7.forward(*(din.get(n, d[n]) for n in INPUTS), s0=d["s0"], L=spec.L, want_factors=use_fac, out=o,
                          stream=stream)
@@ -620,7 +624,8 @@ def run_ours(args, world, rank, local):
         link_ms = 1e3 * max(d2h / (d2h_gbs * 1e9), h2d / (h2d_gbs * 1e9), (h2d + d2h) / (both_gbs * 1e9))
         e2e = {"value": world * spec.tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": n_e2e, "pipelined": True,
-               "sequential_ms_per_step": seq_ms,
+               "sequential_ms_per_step": seq_ms, "entry": "wkv7_forward_backward, one block" if use_step else
+               "wkv7_forward + wkv7_backward",
                "link": {"d2h_gbs": d2h_gbs, "h2d_gbs": h2d_gbs, "both_directions_gbs": both_gbs,
                         "link_bound_ms": link_ms, "frac_of_link_bound": link_ms / e2e_ms}}
 

@@ -304,8 +304,8 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
  * description has no counterpart to it.  Every head is independent in both
  * directions, so the batch is cut into `nsplit` contiguous blocks of batch
  * rows; each block runs its forward and then its backward on a stream of
- * the library's own, forked from `stream` by an event and joined back into
- * it.  A block's backward starts as soon as its forward is done, while the
+ * its own: block 0 on `stream` itself, the others on streams of the library,
+ * forked from `stream` by an event and joined back into it.  A block's backward starts as soon as its forward is done, while the
  * other blocks' forwards finish, which keeps more of the GPU busy than the
  * two calls in a row.  Results are bit-identical to those two calls.
  *   r..b, s0, dy, dsT, y, sT, dr..db, ds0   as in wkv7_forward / wkv7_backward
@@ -319,10 +319,11 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
  * Ownership and errors as in wkv7_forward: the caller owns every buffer;
  * every argument is checked (WKV7_EINVAL, WKV7_EUNSUPPORTED) before anything
  * is launched; WKV7_ECUDA on a launch or stream error, after which the
- * library's streams are still joined back into `stream`.  The library keeps
- * its streams and events (four streams and five events per device) for the
- * life of the process; concurrent calls from several host threads are
- * serialised while they enqueue their work.
+ * library's streams are still joined back into `stream`.  The library
+ * creates its streams and events when a call first needs them (at most three
+ * streams and four events per device) and keeps them for the life of the
+ * process; concurrent calls from several host threads are serialised while
+ * they enqueue their work.
  */
 int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype,
                           const void *r, const void *w, const void *k,

@@ -4,9 +4,13 @@
 //
 // Every (b, h) is independent in both directions, so the batch splits into
 // nsplit contiguous row blocks, each running its forward and then its
-// backward on a stream of its own.  The streams are forked from the caller's
-// stream by an event and joined back into it, so the call stays
-// stream-ordered for the caller.  A sub-batch's backward starts as soon as
+// backward on a stream of its own: block 0 on the caller's stream, the others
+// on streams of the library, forked from the caller's stream by an event and
+// joined back into it, so the call stays stream-ordered for the caller.
+// Using the caller's stream for one block keeps the library's own streams to
+// nsplit - 1 (one for the default split): every stream more can share a
+// hardware work queue with the caller's other streams, such as copy streams,
+// and serialise work they meant to overlap.  A sub-batch's backward starts as soon as
 // its own forward is done, while the other sub-batches' forward CTAs are
 // still finishing; with one CTA per head the forward leaves a tail of
 // unevenly loaded SMs and the backward a partly empty second wave, and the
@@ -23,11 +27,12 @@ constexpr int kMaxSplit = 4;
 constexpr int kDefaultSplit = 2;
 constexpr int kMaxDevices = 64;
 
-// Streams and events of one device, created on its first call and kept for
-// the process.  Calls reuse the events, so each call enqueues its work while
+// Streams and events of one device, created when a call first needs them and
+// kept for the process (slot 0 is never used: block 0 runs on the caller's
+// stream).  Calls reuse the events, so each call enqueues its work while
 // holding g_mu (only the enqueueing, not the execution, is serialised).
 struct Pool {
-    bool ready = false;
+    int streams = 1;  // slots 1 .. streams - 1 exist
     cudaStream_t s[kMaxSplit] = {};
     cudaEvent_t fork = nullptr, join[kMaxSplit] = {};
 };
@@ -41,23 +46,24 @@ int cuda_fail(cudaError_t e, const char *what) {
     return wkv7::set_error(WKV7_ECUDA, msg);
 }
 
-// The current device's pool (g_mu held by the caller).
-int pool_of_device(Pool **out) {
+// The current device's pool with streams for blocks 1 .. n - 1 (g_mu held by
+// the caller).
+int pool_of_device(int n, Pool **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return wkv7::set_error(WKV7_EUNSUPPORTED, "device index beyond the stream pool");
     Pool &p = g_pool[dev];
-    if (!p.ready) {
-        for (int i = 0; i < kMaxSplit; ++i) {
-            if ((e = cudaStreamCreateWithFlags(&p.s[i], cudaStreamNonBlocking)) != cudaSuccess)
-                return cuda_fail(e, "stream creation");
-            if ((e = cudaEventCreateWithFlags(&p.join[i], cudaEventDisableTiming)) != cudaSuccess)
-                return cuda_fail(e, "event creation");
-        }
-        if ((e = cudaEventCreateWithFlags(&p.fork, cudaEventDisableTiming)) != cudaSuccess)
+    if (!p.fork && (e = cudaEventCreateWithFlags(&p.fork, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "event creation");
+    for (; p.streams < n; ++p.streams) {
+        const int i = p.streams;
+        if ((e = cudaStreamCreateWithFlags(&p.s[i], cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "stream creation");
+        if ((e = cudaEventCreateWithFlags(&p.join[i], cudaEventDisableTiming)) != cudaSuccess) {
+            cudaStreamDestroy(p.s[i]);
             return cuda_fail(e, "event creation");
-        p.ready = true;
+        }
     }
     *out = &p;
     return WKV7_OK;
@@ -105,20 +111,22 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
 
     std::lock_guard<std::mutex> lock(g_mu);
     Pool *pool = nullptr;
-    int rc = pool_of_device(&pool);
+    int rc = pool_of_device(n, &pool);
     if (rc != WKV7_OK) return rc;
     cudaStream_t caller = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaEventRecord(pool->fork, caller);
     if (e != cudaSuccess) return cuda_fail(e, "fork event");
-    int joined = 0;  // streams given work, joined back into the caller's stream below even after an error
+    int joined = 1;  // library streams given work (1 .. joined - 1), joined back below even after an error
     for (int i = 0; i < n && rc == WKV7_OK; ++i) {
         const int b0 = (int)((long long)i * B / n), b1 = (int)((long long)(i + 1) * B / n), nb = b1 - b0;
-        cudaStream_t s = pool->s[i];
-        if ((e = cudaStreamWaitEvent(s, pool->fork, 0)) != cudaSuccess) {
-            rc = cuda_fail(e, "fork wait");
-            break;
+        cudaStream_t s = i ? pool->s[i] : caller;
+        if (i) {
+            if ((e = cudaStreamWaitEvent(s, pool->fork, 0)) != cudaSuccess) {
+                rc = cuda_fail(e, "fork wait");
+                break;
+            }
+            joined = i + 1;
         }
-        joined = i + 1;
         rc = wkv7_forward(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
                           f32(s0, b0, state), f32(y, b0, seq), f32(sT, b0, state), f32(ckpt, b0, ck),
                           f32(factors, b0, fac), 16, s);
@@ -128,7 +136,7 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
                            f32(dr, b0, seq), f32(dw, b0, seq), f32(dk, b0, seq), f32(dv, b0, seq),
                            f32(da, b0, seq), f32(db, b0, seq), f32(ds0, b0, state), s);
     }
-    for (int i = 0; i < joined; ++i) {
+    for (int i = 1; i < joined; ++i) {
         const cudaError_t j1 = cudaEventRecord(pool->join[i], pool->s[i]);
         const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(caller, pool->join[i], 0) : j1;
         if (j2 != cudaSuccess && rc == WKV7_OK) rc = cuda_fail(j2, "join");
