@@ -672,6 +672,23 @@ def run_ours(args, world, rank, local):
         f_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
         ff = statistics.mean(a.elapsed_time(b) for a, b, _ in fev)
         fb = statistics.mean(b.elapsed_time(c) for _, b, c in fev)
+        # the same step in one call, two blocks of batch rows (wkv7_forward_backward_fused)
+        fbo = {**outs, **fg}
+
+        def fcall():
+            wkv7.forward_backward_fused(*fx, d["dy"], s0=d["s0"], dsT=d["dsT"], nsplit=0, out=fbo, stream=stream)
+
+        for _ in range(args.warmup):
+            fcall()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.steps):
+            fcall()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        wkv7.async_status()
+        fc_ms = max_over_ranks(c0.elapsed_time(c1), world) / args.steps
         # the same step with the producers and epilogues as separate elementwise
         # passes around the plain entry points (torch ops writing w, a, b to HBM
         # and reading the plain gradients back), for comparison
@@ -702,9 +719,10 @@ def run_ours(args, world, rank, local):
         u1.record(stream)
         torch.cuda.synchronize()
         u_ms = max_over_ranks(u0.elapsed_time(u1), world) / n_u
-        fused = {"ms_per_step": f_ms, "tokens_per_s": world * spec.tokens / (f_ms / 1e3), "forward_ms": ff,
+        fused = {"ms_per_step": fc_ms, "tokens_per_s": world * spec.tokens / (fc_ms / 1e3),
+                 "entry": "wkv7_forward_backward_fused, two blocks of batch rows", "launches_per_step": 2 * min(2, B),
+                 "sequential_ms_per_step": f_ms, "forward_ms": ff, "backward_ms": fb,
                  "separate_producers_ms_per_step": u_ms,
-                 "backward_ms": fb, "launches": 2 * args.steps,
                  "roofline": {"bound": "hbm", "kernel": "wkv7 backward (fused producers)",
                               "achieved": bwd_bytes / (fb / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                               "frac": bwd_bytes / (fb / 1e3) / 1e9 / peak, "algorithmic_bytes": bwd_bytes},

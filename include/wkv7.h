@@ -334,6 +334,22 @@ int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype,
                           float *ds0, int nsplit, void *stream);
 
 /*
+ * The same one-call training step through wkv7_forward_fused and
+ * wkv7_backward_fused: (w_pre, kk, avec) in place of (w, a, b) and
+ * (dw_pre, dkk, davec) in place of (dw, da, db), as described there.  The
+ * factor cache is required when T > 0 (WKV7_EINVAL otherwise), since the
+ * fused backward reads it.  Everything else is as in wkv7_forward_backward,
+ * results bit-identical to the two fused calls.
+ */
+int wkv7_forward_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
+                                const void *r, const void *w_pre, const void *k,
+                                const void *v, const void *kk, const void *avec,
+                                const float *s0, const float *dy, const float *dsT,
+                                float *y, float *sT, float *ckpt, float *factors,
+                                float *dr, float *dw_pre, float *dk, float *dv, float *dkk, float *davec,
+                                float *ds0, int nsplit, void *stream);
+
+/*
  * Status of the kernels' asynchronous copies on the current device.  The
  * kernels stage their inputs with bulk copies whose completion they wait for
  * a bounded time; a wait that runs out (which no correct run should see) sets

@@ -69,13 +69,20 @@ int pool_of_device(int n, Pool **out) {
     return WKV7_OK;
 }
 
-}  // namespace
+using ForwardFn = int (*)(int, int, int, int, wkv7_dtype, const void *, const void *, const void *, const void *,
+                         const void *, const void *, const float *, float *, float *, float *, float *, int, void *);
+using BackwardFn = int (*)(int, int, int, int, wkv7_dtype, const void *, const void *, const void *, const void *,
+                          const void *, const void *, const float *, const float *, int, const float *,
+                          const float *, float *, float *, float *, float *, float *, float *, float *, void *);
 
-extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
-                                     const void *k, const void *v, const void *a, const void *b, const float *s0,
-                                     const float *dy, const float *dsT, float *y, float *sT, float *ckpt,
-                                     float *factors, float *dr, float *dw, float *dk, float *dv, float *da,
-                                     float *db, float *ds0, int nsplit, void *stream) {
+// The step through a forward / backward pair of entry points with one
+// signature: the plain ones, or those with the producers fused in (whose w,
+// a, b slots carry w_pre, kk, avec and whose dw, da, db slots receive their
+// gradients).
+int step(ForwardFn fwd, BackwardFn bwd, bool fused, int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
+         const void *k, const void *v, const void *a, const void *b, const float *s0, const float *dy,
+         const float *dsT, float *y, float *sT, float *ckpt, float *factors, float *dr, float *dw, float *dk,
+         float *dv, float *da, float *db, float *ds0, int nsplit, void *stream) {
     if (nsplit < 0 || nsplit > kMaxSplit) {
         char msg[80];
         snprintf(msg, sizeof msg, "nsplit must be 0 (the default) .. %d (got %d)", kMaxSplit, nsplit);
@@ -83,7 +90,10 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
     }
     {   // every argument is checked before the first launch
         const void *req[15] = {r, w, k, v, a, b, dy, y, ckpt, dr, dw, dk, dv, da, db};
-        const char *rn[15] = {"r", "w", "k", "v", "a", "b", "dy", "y", "ckpt", "dr", "dw", "dk", "dv", "da", "db"};
+        const char *rn_plain[15] = {"r", "w", "k", "v", "a", "b", "dy", "y", "ckpt", "dr", "dw", "dk", "dv", "da", "db"};
+        const char *rn_fused[15] = {"r", "w_pre", "k", "v", "kk", "avec", "dy", "y", "ckpt",
+                                    "dr", "dw_pre", "dk", "dv", "dkk", "davec"};
+        const char *const *rn = fused ? rn_fused : rn_plain;
         const void *opt[5] = {s0, dsT, sT, factors, ds0};
         const char *on[5] = {"s0", "dsT", "sT", "factors", "ds0"};
         const int rc = wkv7::check_call(B, T, H, N, dtype, req, rn, 15, opt, on, 5);
@@ -92,10 +102,10 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
     int n = nsplit == 0 ? kDefaultSplit : nsplit;
     if (n > B) n = B;
     if (T == 0 || n == 1) {  // one block: the two calls in order on the caller's stream
-        int rc = wkv7_forward(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, ckpt, factors, 16, stream);
+        int rc = fwd(B, T, H, N, dtype, r, w, k, v, a, b, s0, y, sT, ckpt, factors, 16, stream);
         if (rc != WKV7_OK) return rc;
-        return wkv7_backward(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, 16, dy, dsT, dr, dw, dk, dv, da,
-                             db, ds0, stream);
+        return bwd(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, 16, dy, dsT, dr, dw, dk, dv, da, db, ds0,
+                   stream);
     }
 
     // element offsets of batch row b0 in each layout
@@ -127,14 +137,14 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
             }
             joined = i + 1;
         }
-        rc = wkv7_forward(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
-                          f32(s0, b0, state), f32(y, b0, seq), f32(sT, b0, state), f32(ckpt, b0, ck),
-                          f32(factors, b0, fac), 16, s);
+        rc = fwd(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
+                 f32(s0, b0, state), f32(y, b0, seq), f32(sT, b0, state), f32(ckpt, b0, ck), f32(factors, b0, fac),
+                 16, s);
         if (rc != WKV7_OK) break;
-        rc = wkv7_backward(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
-                           f32(ckpt, b0, ck), f32(factors, b0, fac), 16, f32(dy, b0, seq), f32(dsT, b0, state),
-                           f32(dr, b0, seq), f32(dw, b0, seq), f32(dk, b0, seq), f32(dv, b0, seq),
-                           f32(da, b0, seq), f32(db, b0, seq), f32(ds0, b0, state), s);
+        rc = bwd(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
+                 f32(ckpt, b0, ck), f32(factors, b0, fac), 16, f32(dy, b0, seq), f32(dsT, b0, state),
+                 f32(dr, b0, seq), f32(dw, b0, seq), f32(dk, b0, seq), f32(dv, b0, seq), f32(da, b0, seq),
+                 f32(db, b0, seq), f32(ds0, b0, state), s);
     }
     for (int i = 1; i < joined; ++i) {
         const cudaError_t j1 = cudaEventRecord(pool->join[i], pool->s[i]);
@@ -143,3 +153,27 @@ extern "C" int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtyp
     }
     return rc;
 }
+
+}  // namespace
+
+extern "C" {
+
+int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                          const void *v, const void *a, const void *b, const float *s0, const float *dy,
+                          const float *dsT, float *y, float *sT, float *ckpt, float *factors, float *dr, float *dw,
+                          float *dk, float *dv, float *da, float *db, float *ds0, int nsplit, void *stream) {
+    return step(wkv7_forward, wkv7_backward, false, B, T, H, N, dtype, r, w, k, v, a, b, s0, dy, dsT, y, sT, ckpt, factors,
+                dr, dw, dk, dv, da, db, ds0, nsplit, stream);
+}
+
+int wkv7_forward_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w_pre,
+                                const void *k, const void *v, const void *kk, const void *avec, const float *s0,
+                                const float *dy, const float *dsT, float *y, float *sT, float *ckpt, float *factors,
+                                float *dr, float *dw_pre, float *dk, float *dv, float *dkk, float *davec, float *ds0,
+                                int nsplit, void *stream) {
+    if (T > 0 && !factors) return wkv7::set_error(WKV7_EINVAL, "the fused producers' backward needs the factor cache");
+    return step(wkv7_forward_fused, wkv7_backward_fused, true, B, T, H, N, dtype, r, w_pre, k, v, kk, avec, s0, dy, dsT,
+                y, sT, ckpt, factors, dr, dw_pre, dk, dv, dkk, davec, ds0, nsplit, stream);
+}
+
+}  // extern "C"

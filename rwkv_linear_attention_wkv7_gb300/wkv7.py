@@ -74,6 +74,8 @@ def load(path: str) -> ctypes.CDLL:
     L.wkv7_backward_gn.restype = ci
     L.wkv7_forward_backward.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp] * 3 + [fp] * 4 + [fp] * 7 + [ci, vp]
     L.wkv7_forward_backward.restype = ci
+    L.wkv7_forward_backward_fused.argtypes = L.wkv7_forward_backward.argtypes
+    L.wkv7_forward_backward_fused.restype = ci
     L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
     L.wkv7_decode_step.restype = ci
     L.wkv7_async_status.argtypes = []
@@ -210,12 +212,14 @@ def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool =
 
 
 def forward_backward(r, w, k, v, a, b, dy, s0=None, dsT=None, want_factors: bool = True, nsplit: int = 0,
-                     out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+                     out: Optional[Dict[str, torch.Tensor]] = None, stream=None, _entry: str = "wkv7_forward_backward",
+                     _names=None) -> Dict[str, torch.Tensor]:
     """One training step through wkv7_forward_backward: the forward (checkpoint
     stride 16, and the factor cache with ``want_factors``) and the backward,
     as ``nsplit`` concurrent blocks of batch rows (0: the library's default).
     Returns a dict with 'y', 'sT', 'ckpt', 'factors' (or None) and the
     gradients 'dr' .. 'db', 'ds0'; ``out`` may hold any of them preallocated."""
+    names = _names or GRAD_NAMES
     xs = (r, w, k, v, a, b)
     _check_inputs(xs)
     B, T, H, N = r.shape
@@ -229,10 +233,10 @@ def forward_backward(r, w, k, v, a, b, dy, s0=None, dsT=None, want_factors: bool
 
     res = {"y": get("y", (B, T, H, N)), "sT": get("sT", sshape), "ckpt": get("ckpt", (B, H, ckpt_count(T, 16), N, N)),
            "factors": get("factors", (B, H, factor_floats(T))) if want_factors else None}
-    for n in GRAD_NAMES:
+    for n in names:
         res[n] = get(n, (B, T, H, N))
     res["ds0"] = get("ds0", sshape)
-    for n in ("y",) + GRAD_NAMES:
+    for n in ("y",) + names:
         _f32(res[n], (B, T, H, N), dev, n)
     _f32(res["ckpt"], (B, H, ckpt_count(T, 16), N, N), dev, "ckpt")
     if want_factors:
@@ -240,12 +244,19 @@ def forward_backward(r, w, k, v, a, b, dy, s0=None, dsT=None, want_factors: bool
     for n, t in (("sT", res["sT"]), ("ds0", res["ds0"]), ("s0", s0), ("dsT", dsT)):
         _f32(t, sshape, dev, n)
     _f32(dy, (B, T, H, N), dev, "dy")
-    rc = lib().wkv7_forward_backward(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(dy), _ptr(dsT),
-                                     _ptr(res["y"]), _ptr(res["sT"]), _ptr(res["ckpt"]), _ptr(res["factors"]),
-                                     *(_ptr(res[n]) for n in GRAD_NAMES), _ptr(res["ds0"]), int(nsplit),
-                                     _stream(stream))
-    _check("wkv7_forward_backward", rc)
+    rc = getattr(lib(), _entry)(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(dy), _ptr(dsT),
+                                _ptr(res["y"]), _ptr(res["sT"]), _ptr(res["ckpt"]), _ptr(res["factors"]),
+                                *(_ptr(res[n]) for n in names), _ptr(res["ds0"]), int(nsplit), _stream(stream))
+    _check(_entry, rc)
     return res
+
+
+def forward_backward_fused(r, w_pre, k, v, kk, avec, dy, s0=None, dsT=None, nsplit: int = 0,
+                           out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """forward_backward through wkv7_forward_backward_fused: the producers fused
+    in (inputs w_pre, kk, avec; gradients 'dw_pre', 'dkk', 'davec')."""
+    return forward_backward(r, w_pre, k, v, kk, avec, dy, s0=s0, dsT=dsT, want_factors=True, nsplit=nsplit, out=out,
+                            stream=stream, _entry="wkv7_forward_backward_fused", _names=FUSED_GRAD_NAMES)
 
 
 FUSED_GRAD_NAMES = ("dr", "dw_pre", "dk", "dv", "dkk", "davec")

@@ -49,7 +49,7 @@ def test_header_declares_entry_points():
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
                      "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused",
                      "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats",
-                     "wkv7_forward_backward"):
+                     "wkv7_forward_backward", "wkv7_forward_backward_fused"):
         assert required in names
 
 
@@ -182,6 +182,13 @@ def test_forward_backward_rejects_bad_arguments(lib):
     bad = list(args)
     bad[3] = 32  # N
     assert lib.wkv7_forward_backward(*bad) == EINVAL
+    # the fused form needs the factor cache, and names the fused arguments
+    assert lib.wkv7_forward_backward_fused(*args) == EINVAL and "factor cache" in wkv7.last_error()
+    good = list(args)
+    good[17] = p
+    bad = list(good)
+    bad[6] = None  # w_pre
+    assert lib.wkv7_forward_backward_fused(*bad) == EINVAL and "w_pre" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

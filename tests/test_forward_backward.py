@@ -78,3 +78,18 @@ def test_follows_the_callers_stream():
     st.synchronize()
     wkv7.async_status()
     assert torch.equal(dr, ref["dr"])
+
+
+@pytest.mark.parametrize("B,T,H,dtype,nsplit", [(4, 200, 3, "bf16", 0), (3, 48, 2, "f32", 3), (1, 32, 2, "bf16", 2)])
+def test_fused_bit_identical_to_the_two_fused_calls(B, T, H, dtype, nsplit):
+    """wkv7_forward_backward_fused against wkv7_forward_fused + wkv7_backward_fused."""
+    build()
+    spec = synthetic.WorkloadSpec("fwdbwd_fused", B, T, H, dtype=dtype, s0_std=0.1, with_dsT=True, seed=34)
+    d = synthetic.make_inputs(spec, device="cuda", fused=True)
+    ref = parity.run_gpu(d, L=16, fused=True)
+    got = wkv7.forward_backward_fused(*(d[n] for n in parity.INPUTS_FUSED), d["dy"], s0=d["s0"], dsT=d["dsT"],
+                                      nsplit=nsplit)
+    torch.cuda.synchronize()
+    wkv7.async_status()
+    for n in ("y", "sT", "ckpt") + parity.GRADS_FUSED + ("ds0",):
+        assert torch.equal(got[n], ref[n]), n
