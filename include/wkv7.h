@@ -350,6 +350,28 @@ int wkv7_forward_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype,
                                 float *ds0, int nsplit, void *stream);
 
 /*
+ * The same one-call training step through wkv7_forward_gn and
+ * wkv7_backward_gn (the GroupNorm + bonus output epilogue): do = dL/do in
+ * place of dy, the epilogue's weights gn_w, gn_b, r_k ([H][N]), its output o,
+ * its parameter gradients dgn_w, dgn_b, dr_k ([H][N], summed over every batch
+ * row and token) and the workspace of wkv7_gn_workspace_floats(B, H) floats,
+ * as described there; the factor cache is required when T > 0.  Each block
+ * leaves the per-(b, h) parameter-gradient sums of its rows in the workspace,
+ * and one reduction over all B rows follows on `stream` once the blocks are
+ * joined, in the same order as wkv7_backward_gn's: results bit-identical to
+ * the two calls.  Everything else as in wkv7_forward_backward.
+ */
+int wkv7_forward_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype,
+                             const void *r, const void *w, const void *k,
+                             const void *v, const void *a, const void *b,
+                             const float *s0, const float *do_, const float *dsT,
+                             const float *gn_w, const float *gn_b, const float *r_k,
+                             float *y, float *o, float *sT, float *ckpt, float *factors,
+                             float *dr, float *dw, float *dk, float *dv, float *da, float *db,
+                             float *ds0, float *dgn_w, float *dgn_b, float *dr_k,
+                             float *workspace, int nsplit, void *stream);
+
+/*
  * Status of the kernels' asynchronous copies on the current device.  The
  * kernels stage their inputs with bulk copies whose completion they wait for
  * a bounded time; a wait that runs out (which no correct run should see) sets

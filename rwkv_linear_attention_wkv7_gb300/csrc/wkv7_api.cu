@@ -167,6 +167,7 @@ struct GnArgs {
     float *o = nullptr;                                          // forward
     const float *y = nullptr;                                    // backward: the forward's y
     float *dgn_w = nullptr, *dgn_b = nullptr, *dr_k = nullptr, *ws = nullptr;
+    bool partials_only = false;  // backward: leave the per-(b, h) sums in ws, no reduction over batch rows
 };
 
 // prod = 1: w, a, b carry (w_pre, kk, avec) and the backward writes (dw_pre, dkk, davec)
@@ -229,8 +230,8 @@ int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
         if (need && (L != 16 || !factors))
             return fail(WKV7_EINVAL, "the fused epilogue's backward needs L == 16 and the forward's factor cache");
         TRY(check_ptr(gn.y, "y", need)); TRY(check_ptr(gn.gn_w, "gn_w", true)); TRY(check_ptr(gn.r_k, "r_k", true));
-        TRY(check_ptr(gn.dgn_w, "dgn_w", true)); TRY(check_ptr(gn.dgn_b, "dgn_b", true));
-        TRY(check_ptr(gn.dr_k, "dr_k", true)); TRY(check_ptr(gn.ws, "workspace", true));
+        TRY(check_ptr(gn.dgn_w, "dgn_w", !gn.partials_only)); TRY(check_ptr(gn.dgn_b, "dgn_b", !gn.partials_only));
+        TRY(check_ptr(gn.dr_k, "dr_k", !gn.partials_only)); TRY(check_ptr(gn.ws, "workspace", true));
     }
     TRY(check_device());
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -254,6 +255,7 @@ int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
     if (!(p.err = wkv7::async_error_flag())) return WKV7_ECUDA;
     if (epi) {
         TRY(launch_status(wkv7::launch_backward_chunk(p, st), "wkv7_backward_gn launch"));
+        if (gn.partials_only) return WKV7_OK;
         return launch_status(wkv7::launch_gn_param_reduce(B, H, gn.ws, gn.dgn_w, gn.dgn_b, gn.dr_k, st),
                              "wkv7_backward_gn parameter reduction");
     }
@@ -324,6 +326,30 @@ int wkv7_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype, const void *r
     return backward_impl(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, L, do_, dsT, dr, dw, dk, dv, da, db, ds0,
                          stream, 0, gn);
 }
+
+}  // extern "C"
+
+namespace wkv7 {
+// wkv7_backward_gn without the reduction over batch rows: the per-(b, h)
+// parameter-gradient sums stay in `workspace` (rows [B][H][3][N]) for a
+// caller that runs launch_gn_param_reduce over more rows than this call's.
+int backward_gn_partials(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                         const void *v, const void *a, const void *b, const float *ckpt, const float *factors,
+                         const float *y, const float *do_, const float *dsT, const float *gn_w, const float *r_k,
+                         float *dr, float *dw, float *dk, float *dv, float *da, float *db, float *ds0,
+                         float *workspace, void *stream) {
+    GnArgs gn;
+    gn.gn_w = gn_w; gn.r_k = r_k; gn.y = y; gn.ws = workspace; gn.partials_only = true;
+    if (!gn_w) {
+        g_err[0] = '\0';
+        return fail(WKV7_EINVAL, "gn_w is NULL");
+    }
+    return backward_impl(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, 16, do_, dsT, dr, dw, dk, dv, da, db, ds0,
+                         stream, 0, gn);
+}
+}  // namespace wkv7
+
+extern "C" {
 
 int wkv7_decode_step(int B, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                      const void *v, const void *a, const void *b, float *state, float *y, void *stream) {

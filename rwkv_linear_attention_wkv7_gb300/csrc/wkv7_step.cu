@@ -15,11 +15,22 @@
 // still finishing; with one CTA per head the forward leaves a tail of
 // unevenly loaded SMs and the backward a partly empty second wave, and the
 // sub-batches fill each other's.
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 
 #include "wkv7.h"
 #include "wkv7_internal.cuh"
+
+namespace wkv7 {
+// wkv7_backward_gn without the reduction over batch rows: the per-(b, h)
+// parameter-gradient sums stay in `workspace` (wkv7_api.cu).
+int backward_gn_partials(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
+                         const void *v, const void *a, const void *b, const float *ckpt, const float *factors,
+                         const float *y, const float *do_, const float *dsT, const float *gn_w, const float *r_k,
+                         float *dr, float *dw, float *dk, float *dv, float *da, float *db, float *ds0,
+                         float *workspace, void *stream);
+}  // namespace wkv7
 
 namespace {
 
@@ -69,6 +80,62 @@ int pool_of_device(int n, Pool **out) {
     return WKV7_OK;
 }
 
+// Runs block(b0, nb, stream) for n blocks of batch rows (rows b0 .. b0 + nb - 1):
+// block 0 on the caller's stream, the others on the pool's streams, forked
+// from the caller's stream by an event and joined back into it, also after an
+// error.  g_mu is held while the work is enqueued.
+template <typename Block>
+int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Pool *pool = nullptr;
+    int rc = pool_of_device(n, &pool);
+    if (rc != WKV7_OK) return rc;
+    cudaError_t e = cudaEventRecord(pool->fork, caller);
+    if (e != cudaSuccess) return cuda_fail(e, "fork event");
+    int joined = 1;  // library streams given work (1 .. joined - 1)
+    for (int i = 0; i < n && rc == WKV7_OK; ++i) {
+        const int b0 = (int)((long long)i * B / n), b1 = (int)((long long)(i + 1) * B / n);
+        cudaStream_t s = i ? pool->s[i] : caller;
+        if (i) {
+            if ((e = cudaStreamWaitEvent(s, pool->fork, 0)) != cudaSuccess) {
+                rc = cuda_fail(e, "fork wait");
+                break;
+            }
+            joined = i + 1;
+        }
+        rc = block(b0, b1 - b0, s);
+    }
+    for (int i = 1; i < joined; ++i) {
+        const cudaError_t j1 = cudaEventRecord(pool->join[i], pool->s[i]);
+        const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(caller, pool->join[i], 0) : j1;
+        if (j2 != cudaSuccess && rc == WKV7_OK) rc = cuda_fail(j2, "join");
+    }
+    return rc;
+}
+
+// Element offsets of batch row b0 in the library's layouts.
+struct Rows {
+    size_t esize, seq, state, ck, fac;
+    Rows(int T, int H, wkv7_dtype dtype)
+        : esize(dtype == WKV7_BF16 ? 2 : 4),
+          seq((size_t)T * H * WKV7_HEAD_SIZE),                        // [B][T][H][N]
+          state((size_t)H * WKV7_HEAD_SIZE * WKV7_HEAD_SIZE),         // [B][H][N][N]
+          ck(state * (size_t)wkv7_ckpt_count(T, 16)),                 // [B][H][ceil(T/16)][N][N]
+          fac((size_t)H * (size_t)wkv7_factor_floats(T)) {}           // [B][H][factor floats]
+    const void *in(const void *p, int b0) const {                     // an input row, fp32 or bf16
+        return p ? static_cast<const void *>(static_cast<const char *>(p) + (size_t)b0 * seq * esize) : p;
+    }
+    template <typename P>
+    P *at(P *p, int b0, size_t row) const { return p ? p + (size_t)b0 * row : p; }
+};
+
+int check_nsplit(int nsplit) {
+    if (nsplit >= 0 && nsplit <= kMaxSplit) return WKV7_OK;
+    char msg[80];
+    snprintf(msg, sizeof msg, "nsplit must be 0 (the default) .. %d (got %d)", kMaxSplit, nsplit);
+    return wkv7::set_error(WKV7_EINVAL, msg);
+}
+
 using ForwardFn = int (*)(int, int, int, int, wkv7_dtype, const void *, const void *, const void *, const void *,
                          const void *, const void *, const float *, float *, float *, float *, float *, int, void *);
 using BackwardFn = int (*)(int, int, int, int, wkv7_dtype, const void *, const void *, const void *, const void *,
@@ -83,11 +150,7 @@ int step(ForwardFn fwd, BackwardFn bwd, bool fused, int B, int T, int H, int N, 
          const void *k, const void *v, const void *a, const void *b, const float *s0, const float *dy,
          const float *dsT, float *y, float *sT, float *ckpt, float *factors, float *dr, float *dw, float *dk,
          float *dv, float *da, float *db, float *ds0, int nsplit, void *stream) {
-    if (nsplit < 0 || nsplit > kMaxSplit) {
-        char msg[80];
-        snprintf(msg, sizeof msg, "nsplit must be 0 (the default) .. %d (got %d)", kMaxSplit, nsplit);
-        return wkv7::set_error(WKV7_EINVAL, msg);
-    }
+    if (check_nsplit(nsplit) != WKV7_OK) return WKV7_EINVAL;
     {   // every argument is checked before the first launch
         const void *req[15] = {r, w, k, v, a, b, dy, y, ckpt, dr, dw, dk, dv, da, db};
         const char *rn_plain[15] = {"r", "w", "k", "v", "a", "b", "dy", "y", "ckpt", "dr", "dw", "dk", "dv", "da", "db"};
@@ -108,50 +171,17 @@ int step(ForwardFn fwd, BackwardFn bwd, bool fused, int B, int T, int H, int N, 
                    stream);
     }
 
-    // element offsets of batch row b0 in each layout
-    const size_t esize = dtype == WKV7_BF16 ? 2 : 4;
-    const size_t seq = (size_t)T * H * WKV7_HEAD_SIZE;                              // [B][T][H][N] row
-    const size_t state = (size_t)H * WKV7_HEAD_SIZE * WKV7_HEAD_SIZE;               // [B][H][N][N] row
-    const size_t ck = state * (size_t)wkv7_ckpt_count(T, 16);                       // [B][H][nck][N][N] row
-    const size_t fac = (size_t)H * (size_t)wkv7_factor_floats(T);                   // [B][H][factor floats] row
-    auto in = [&](const void *p, int b0) {
-        return static_cast<const void *>(static_cast<const char *>(p) + (size_t)b0 * seq * esize);
-    };
-    auto f32 = [](auto *p, int b0, size_t row) { return p ? p + (size_t)b0 * row : p; };
-
-    std::lock_guard<std::mutex> lock(g_mu);
-    Pool *pool = nullptr;
-    int rc = pool_of_device(n, &pool);
-    if (rc != WKV7_OK) return rc;
-    cudaStream_t caller = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaEventRecord(pool->fork, caller);
-    if (e != cudaSuccess) return cuda_fail(e, "fork event");
-    int joined = 1;  // library streams given work (1 .. joined - 1), joined back below even after an error
-    for (int i = 0; i < n && rc == WKV7_OK; ++i) {
-        const int b0 = (int)((long long)i * B / n), b1 = (int)((long long)(i + 1) * B / n), nb = b1 - b0;
-        cudaStream_t s = i ? pool->s[i] : caller;
-        if (i) {
-            if ((e = cudaStreamWaitEvent(s, pool->fork, 0)) != cudaSuccess) {
-                rc = cuda_fail(e, "fork wait");
-                break;
-            }
-            joined = i + 1;
-        }
-        rc = fwd(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
-                 f32(s0, b0, state), f32(y, b0, seq), f32(sT, b0, state), f32(ckpt, b0, ck), f32(factors, b0, fac),
-                 16, s);
-        if (rc != WKV7_OK) break;
-        rc = bwd(nb, T, H, N, dtype, in(r, b0), in(w, b0), in(k, b0), in(v, b0), in(a, b0), in(b, b0),
-                 f32(ckpt, b0, ck), f32(factors, b0, fac), 16, f32(dy, b0, seq), f32(dsT, b0, state),
-                 f32(dr, b0, seq), f32(dw, b0, seq), f32(dk, b0, seq), f32(dv, b0, seq), f32(da, b0, seq),
-                 f32(db, b0, seq), f32(ds0, b0, state), s);
-    }
-    for (int i = 1; i < joined; ++i) {
-        const cudaError_t j1 = cudaEventRecord(pool->join[i], pool->s[i]);
-        const cudaError_t j2 = j1 == cudaSuccess ? cudaStreamWaitEvent(caller, pool->join[i], 0) : j1;
-        if (j2 != cudaSuccess && rc == WKV7_OK) rc = cuda_fail(j2, "join");
-    }
-    return rc;
+    const Rows R(T, H, dtype);
+    return run_blocks(B, n, static_cast<cudaStream_t>(stream), [&](int b0, int nb, cudaStream_t s) {
+        int rc = fwd(nb, T, H, N, dtype, R.in(r, b0), R.in(w, b0), R.in(k, b0), R.in(v, b0), R.in(a, b0),
+                     R.in(b, b0), R.at(s0, b0, R.state), R.at(y, b0, R.seq), R.at(sT, b0, R.state),
+                     R.at(ckpt, b0, R.ck), R.at(factors, b0, R.fac), 16, s);
+        if (rc != WKV7_OK) return rc;
+        return bwd(nb, T, H, N, dtype, R.in(r, b0), R.in(w, b0), R.in(k, b0), R.in(v, b0), R.in(a, b0), R.in(b, b0),
+                   R.at(ckpt, b0, R.ck), R.at(factors, b0, R.fac), 16, R.at(dy, b0, R.seq), R.at(dsT, b0, R.state),
+                   R.at(dr, b0, R.seq), R.at(dw, b0, R.seq), R.at(dk, b0, R.seq), R.at(dv, b0, R.seq),
+                   R.at(da, b0, R.seq), R.at(db, b0, R.seq), R.at(ds0, b0, R.state), s);
+    });
 }
 
 }  // namespace
@@ -174,6 +204,68 @@ int wkv7_forward_backward_fused(int B, int T, int H, int N, wkv7_dtype dtype, co
     if (T > 0 && !factors) return wkv7::set_error(WKV7_EINVAL, "the fused producers' backward needs the factor cache");
     return step(wkv7_forward_fused, wkv7_backward_fused, true, B, T, H, N, dtype, r, w_pre, k, v, kk, avec, s0, dy, dsT,
                 y, sT, ckpt, factors, dr, dw_pre, dk, dv, dkk, davec, ds0, nsplit, stream);
+}
+
+int wkv7_forward_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w,
+                             const void *k, const void *v, const void *a, const void *b, const float *s0,
+                             const float *do_, const float *dsT, const float *gn_w, const float *gn_b,
+                             const float *r_k, float *y, float *o, float *sT, float *ckpt, float *factors, float *dr,
+                             float *dw, float *dk, float *dv, float *da, float *db, float *ds0, float *dgn_w,
+                             float *dgn_b, float *dr_k, float *workspace, int nsplit, void *stream) {
+    if (check_nsplit(nsplit) != WKV7_OK) return WKV7_EINVAL;
+    {   // every argument is checked before the first launch
+        const void *req[17] = {r, w, k, v, a, b, do_, y, o, ckpt, factors, dr, dw, dk, dv, da, db};
+        const char *rn[17] = {"r", "w", "k", "v", "a", "b", "do", "y", "o", "ckpt", "factors",
+                              "dr", "dw", "dk", "dv", "da", "db"};
+        // the epilogue's weights, parameter gradients and workspace (any T), then the rest
+        const void *par[7] = {gn_w, gn_b, r_k, dgn_w, dgn_b, dr_k, workspace};
+        const char *pn[7] = {"gn_w", "gn_b", "r_k", "dgn_w", "dgn_b", "dr_k", "workspace"};
+        for (int i = 0; i < 7; ++i) {
+            char msg[80];
+            if (!par[i]) {
+                snprintf(msg, sizeof msg, "%s is NULL", pn[i]);
+                return wkv7::set_error(WKV7_EINVAL, msg);
+            }
+            if (reinterpret_cast<uintptr_t>(par[i]) & 15u) {
+                snprintf(msg, sizeof msg, "%s is not 16-byte aligned", pn[i]);
+                return wkv7::set_error(WKV7_EINVAL, msg);
+            }
+        }
+        const void *opt[4] = {s0, dsT, sT, ds0};
+        const char *on[4] = {"s0", "dsT", "sT", "ds0"};
+        const int rc = wkv7::check_call(B, T, H, N, dtype, req, rn, 17, opt, on, 4);
+        if (rc != WKV7_OK) return rc;
+    }
+    int n = nsplit == 0 ? kDefaultSplit : nsplit;
+    if (n > B) n = B;
+    if (T == 0 || n == 1) {  // one block: the two calls in order on the caller's stream
+        int rc = wkv7_forward_gn(B, T, H, N, dtype, r, w, k, v, a, b, s0, gn_w, gn_b, r_k, y, o, sT, ckpt, factors, 16,
+                                 stream);
+        if (rc != WKV7_OK) return rc;
+        return wkv7_backward_gn(B, T, H, N, dtype, r, w, k, v, a, b, ckpt, factors, 16, y, do_, dsT, gn_w, r_k, dr, dw,
+                                dk, dv, da, db, ds0, dgn_w, dgn_b, dr_k, workspace, stream);
+    }
+    // every block leaves its rows' per-(b, h) parameter-gradient sums in the
+    // workspace; one reduction over all B rows follows once the blocks are joined
+    const Rows R(T, H, dtype);
+    const size_t wsrow = (size_t)H * 3 * WKV7_HEAD_SIZE;
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    int rc = run_blocks(B, n, caller, [&](int b0, int nb, cudaStream_t s) {
+        int e = wkv7_forward_gn(nb, T, H, N, dtype, R.in(r, b0), R.in(w, b0), R.in(k, b0), R.in(v, b0), R.in(a, b0),
+                                R.in(b, b0), R.at(s0, b0, R.state), gn_w, gn_b, r_k, R.at(y, b0, R.seq),
+                                R.at(o, b0, R.seq), R.at(sT, b0, R.state), R.at(ckpt, b0, R.ck),
+                                R.at(factors, b0, R.fac), 16, s);
+        if (e != WKV7_OK) return e;
+        return wkv7::backward_gn_partials(nb, T, H, N, dtype, R.in(r, b0), R.in(w, b0), R.in(k, b0), R.in(v, b0),
+                                          R.in(a, b0), R.in(b, b0), R.at(ckpt, b0, R.ck), R.at(factors, b0, R.fac),
+                                          R.at(y, b0, R.seq), R.at(do_, b0, R.seq), R.at(dsT, b0, R.state), gn_w, r_k,
+                                          R.at(dr, b0, R.seq), R.at(dw, b0, R.seq), R.at(dk, b0, R.seq),
+                                          R.at(dv, b0, R.seq), R.at(da, b0, R.seq), R.at(db, b0, R.seq),
+                                          R.at(ds0, b0, R.state), workspace + (size_t)b0 * wsrow, s);
+    });
+    if (rc != WKV7_OK) return rc;
+    const cudaError_t e = wkv7::launch_gn_param_reduce(B, H, workspace, dgn_w, dgn_b, dr_k, caller);
+    return e == cudaSuccess ? WKV7_OK : cuda_fail(e, "parameter-gradient reduction launch");
 }
 
 }  // extern "C"

@@ -76,6 +76,9 @@ def load(path: str) -> ctypes.CDLL:
     L.wkv7_forward_backward.restype = ci
     L.wkv7_forward_backward_fused.argtypes = L.wkv7_forward_backward.argtypes
     L.wkv7_forward_backward_fused.restype = ci
+    L.wkv7_forward_backward_gn.argtypes = ([ci, ci, ci, ci, ci] + [vp] * 6 + [fp] * 3 + [fp] * 3 + [fp] * 5 + [fp] * 7 +
+                                           [fp] * 3 + [fp, ci, vp])
+    L.wkv7_forward_backward_gn.restype = ci
     L.wkv7_decode_step.argtypes = [ci, ci, ci, ci] + [vp] * 6 + [fp, fp, vp]
     L.wkv7_decode_step.restype = ci
     L.wkv7_async_status.argtypes = []
@@ -332,6 +335,46 @@ def backward_gn(r, w, k, v, a, b, ckpt, factors, y, do, gn_w, r_k, dsT=None, L: 
                                 _stream(stream))
     _check("wkv7_backward_gn", rc)
     return g
+
+
+def forward_backward_gn(r, w, k, v, a, b, do, gn_w, gn_b, r_k, s0=None, dsT=None, nsplit: int = 0, workspace=None,
+                        out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """One training step with the output epilogue through wkv7_forward_backward_gn.
+    Returns 'o', 'y', 'sT', 'ckpt', 'factors', the gradients 'dr' .. 'db', 'ds0'
+    and 'dgn_w', 'dgn_b', 'dr_k'; ``out`` may hold any of them preallocated."""
+    xs = (r, w, k, v, a, b)
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    out = out or {}
+
+    def get(name, shape):
+        t = out.get(name)
+        return t if t is not None else torch.empty(shape, device=dev)
+
+    res = {n: get(n, (B, T, H, N)) for n in ("o", "y") + GRAD_NAMES}
+    res.update(sT=get("sT", (B, H, N, N)), ds0=get("ds0", (B, H, N, N)),
+               ckpt=get("ckpt", (B, H, ckpt_count(T, 16), N, N)), factors=get("factors", (B, H, factor_floats(T))))
+    for n in ("dgn_w", "dgn_b", "dr_k"):
+        res[n] = get(n, (H, N))
+    ws = workspace if workspace is not None else torch.empty(gn_workspace_floats(B, H), device=dev)
+    for n, t in (("gn_w", gn_w), ("gn_b", gn_b), ("r_k", r_k), ("dgn_w", res["dgn_w"]), ("dgn_b", res["dgn_b"]),
+                 ("dr_k", res["dr_k"])):
+        _f32(t, (H, N), dev, n)
+    for n in ("o", "y") + GRAD_NAMES:
+        _f32(res[n], (B, T, H, N), dev, n)
+    _f32(do, (B, T, H, N), dev, "do")
+    for n, t in (("s0", s0), ("dsT", dsT), ("sT", res["sT"]), ("ds0", res["ds0"])):
+        _f32(t, (B, H, N, N), dev, n)
+    _f32(res["ckpt"], (B, H, ckpt_count(T, 16), N, N), dev, "ckpt")
+    _f32(res["factors"], (B, H, factor_floats(T)), dev, "factors")
+    rc = lib().wkv7_forward_backward_gn(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(s0), _ptr(do), _ptr(dsT),
+                                        _ptr(gn_w), _ptr(gn_b), _ptr(r_k), _ptr(res["y"]), _ptr(res["o"]),
+                                        _ptr(res["sT"]), _ptr(res["ckpt"]), _ptr(res["factors"]),
+                                        *(_ptr(res[n]) for n in GRAD_NAMES), _ptr(res["ds0"]), _ptr(res["dgn_w"]),
+                                        _ptr(res["dgn_b"]), _ptr(res["dr_k"]), _ptr(ws), int(nsplit), _stream(stream))
+    _check("wkv7_forward_backward_gn", rc)
+    return res
 
 
 def timesplit_workspace_floats(B: int, T: int, H: int, nseg: int) -> int:

@@ -49,7 +49,7 @@ def test_header_declares_entry_points():
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
                      "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused",
                      "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats",
-                     "wkv7_forward_backward", "wkv7_forward_backward_fused"):
+                     "wkv7_forward_backward", "wkv7_forward_backward_fused", "wkv7_forward_backward_gn"):
         assert required in names
 
 
@@ -189,6 +189,16 @@ def test_forward_backward_rejects_bad_arguments(lib):
     bad = list(good)
     bad[6] = None  # w_pre
     assert lib.wkv7_forward_backward_fused(*bad) == EINVAL and "w_pre" in wkv7.last_error()
+    # the epilogue form: its weights, parameter gradients and workspace are required
+    gn = [1, 4, 1, 64, 0] + [p] * 6 + [None, p, None] + [p, p, p] + [p, p, None, p, p] + [p] * 6 + [None] + \
+         [p, p, p] + [p, 0, None]
+    for i, name in ((15, "gn_b"), (32, "workspace"), (29, "dgn_w")):
+        bad = list(gn)
+        bad[i] = None
+        assert lib.wkv7_forward_backward_gn(*bad) == EINVAL and name in wkv7.last_error()
+    bad = list(gn)
+    bad[33] = 7
+    assert lib.wkv7_forward_backward_gn(*bad) == EINVAL and "nsplit" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

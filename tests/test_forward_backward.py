@@ -93,3 +93,22 @@ def test_fused_bit_identical_to_the_two_fused_calls(B, T, H, dtype, nsplit):
     wkv7.async_status()
     for n in ("y", "sT", "ckpt") + parity.GRADS_FUSED + ("ds0",):
         assert torch.equal(got[n], ref[n]), n
+
+
+@pytest.mark.parametrize("B,T,H,dtype,nsplit", [(4, 200, 3, "bf16", 0), (5, 48, 2, "f32", 4), (2, 0, 2, "f32", 2),
+                                                (1, 32, 2, "bf16", 2)])
+def test_gn_bit_identical_to_the_two_gn_calls(B, T, H, dtype, nsplit):
+    """wkv7_forward_backward_gn against wkv7_forward_gn + wkv7_backward_gn: the blocks
+    leave their rows' parameter-gradient sums, one reduction over all rows follows
+    in the same order, so dgn_w, dgn_b, dr_k are bit-identical too."""
+    build()
+    spec = synthetic.WorkloadSpec("fwdbwd_gn", B, T, H, dtype=dtype, s0_std=0.1, with_dsT=True, seed=35)
+    d = synthetic.make_inputs(spec, device="cuda")
+    gp = {n: t.cuda() for n, t in synthetic.gn_params(H, seed=36).items()}
+    ref = parity.run_gpu_gn(d, gp)
+    got = wkv7.forward_backward_gn(*(d[n] for n in parity.INPUTS), d["dy"], gp["gn_w"], gp["gn_b"], gp["r_k"],
+                                   s0=d["s0"], dsT=d["dsT"], nsplit=nsplit)
+    torch.cuda.synchronize()
+    wkv7.async_status()
+    for n in ("o", "y", "sT", "ckpt") + parity.GRADS + ("ds0", "dgn_w", "dgn_b", "dr_k"):
+        assert torch.equal(got[n], ref[n]), n
