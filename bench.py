@@ -36,7 +36,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_b16_t4096_h32"
 DECODE_WORKLOAD = "decode_b512_h32"
 TIMESPLIT_WORKLOAD = "long_b1_t65536_h8"
-TIMESPLIT_SEGMENTS = 32
+TIMESPLIT_SEGMENTS = 64
 INPUTS = ("r", "w", "k", "v", "a", "b")
 GRADS = ("dr", "dw", "dk", "dv", "da", "db")
 L2_BYTES = 126 * 2**20

@@ -80,12 +80,15 @@ int pool_of_device(int n, Pool **out) {
     return WKV7_OK;
 }
 
-// Runs block(b0, nb, stream) for n blocks of batch rows (rows b0 .. b0 + nb - 1):
-// block 0 on the caller's stream, the others on the pool's streams, forked
-// from the caller's stream by an event and joined back into it, also after an
-// error.  g_mu is held while the work is enqueued.
-template <typename Block>
-int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
+}  // namespace
+
+namespace wkv7 {
+// Runs work(i, stream, ctx) for i = 0 .. n - 1 side by side: piece 0 on the
+// caller's stream, the others on the library's streams, forked from the
+// caller's stream by an event and joined back into it, also after an error.
+// g_mu is held while the work is enqueued.
+int run_side_by_side(int n, cudaStream_t caller, int (*work)(int, cudaStream_t, void *), void *ctx) {
+    if (n < 1 || n > kMaxSplit) return set_error(WKV7_EINVAL, "run_side_by_side: 1 .. 4 pieces");
     std::lock_guard<std::mutex> lock(g_mu);
     Pool *pool = nullptr;
     int rc = pool_of_device(n, &pool);
@@ -94,7 +97,6 @@ int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
     if (e != cudaSuccess) return cuda_fail(e, "fork event");
     int joined = 1;  // library streams given work (1 .. joined - 1)
     for (int i = 0; i < n && rc == WKV7_OK; ++i) {
-        const int b0 = (int)((long long)i * B / n), b1 = (int)((long long)(i + 1) * B / n);
         cudaStream_t s = i ? pool->s[i] : caller;
         if (i) {
             if ((e = cudaStreamWaitEvent(s, pool->fork, 0)) != cudaSuccess) {
@@ -103,7 +105,7 @@ int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
             }
             joined = i + 1;
         }
-        rc = block(b0, b1 - b0, s);
+        rc = work(i, s, ctx);
     }
     for (int i = 1; i < joined; ++i) {
         const cudaError_t j1 = cudaEventRecord(pool->join[i], pool->s[i]);
@@ -111,6 +113,24 @@ int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
         if (j2 != cudaSuccess && rc == WKV7_OK) rc = cuda_fail(j2, "join");
     }
     return rc;
+}
+}  // namespace wkv7
+
+namespace {
+
+// Runs block(b0, nb, stream) for n blocks of batch rows (rows b0 .. b0 + nb - 1)
+// side by side (run_side_by_side).
+template <typename Block>
+int run_blocks(int B, int n, cudaStream_t caller, Block &&block) {
+    struct Ctx {
+        int B, n;
+        Block *block;
+    } ctx{B, n, &block};
+    return wkv7::run_side_by_side(n, caller, [](int i, cudaStream_t s, void *c) -> int {
+        const Ctx &x = *static_cast<const Ctx *>(c);
+        const int b0 = (int)((long long)i * x.B / x.n), b1 = (int)((long long)(i + 1) * x.B / x.n);
+        return (*x.block)(b0, b1 - b0, s);
+    }, &ctx);
 }
 
 // Element offsets of batch row b0 in the library's layouts.

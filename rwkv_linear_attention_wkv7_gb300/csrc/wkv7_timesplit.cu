@@ -25,6 +25,12 @@
 #include "wkv7_internal.cuh"
 #include "wkv7_mma.cuh"
 
+namespace wkv7 {
+// Runs work(i, stream, ctx) for i = 0 .. n - 1 side by side, piece 0 on
+// `caller` and the others on the library's streams (wkv7_step.cu).
+int run_side_by_side(int n, cudaStream_t caller, int (*work)(int, cudaStream_t, void *), void *ctx);
+}  // namespace wkv7
+
 namespace {
 using wkv7::AFrag;
 using wkv7::BFrag;
@@ -280,9 +286,21 @@ int wkv7_forward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const v
     wkv7_identity_kernel<<<(unsigned)((s + 255) / 256), 256, 0, st>>>(ws.ident, nmat);
     if ((rc = cuda_status(cudaGetLastError(), "identity launch")) != WKV7_OK) return rc;
     // (1) M: every segment from I with v = 0 -- the segment pass that reads only w, a, b
-    // and forms no V product and no y; (2) Z: every segment from 0 (end state only, no y)
-    if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, ws.ident, ws.M, 2, st))) return rc;
-    if ((rc = wkv7::forward_state(bs, tseg, H, dtype, w, k, v, a, b, nullptr, ws.Z, 1, st))) return rc;
+    // and forms no V product and no y; (2) Z: every segment from 0 (end state only, no y).
+    // The two are independent and, with B*H small, each fills only part of the GPU:
+    // they run side by side, M on a stream of the library's forked from this one.
+    struct Passes {
+        int bs, tseg, H, dtype;
+        const void *w, *k, *v, *a, *b;
+        const float *ident;
+        float *M, *Z;
+    } ps{bs, tseg, H, dtype, w, k, v, a, b, ws.ident, ws.M, ws.Z};
+    rc = wkv7::run_side_by_side(2, st, [](int i, cudaStream_t s, void *c) -> int {
+        const Passes &x = *static_cast<const Passes *>(c);
+        return i ? wkv7::forward_state(x.bs, x.tseg, x.H, x.dtype, x.w, x.k, x.v, x.a, x.b, x.ident, x.M, 2, s)
+                 : wkv7::forward_state(x.bs, x.tseg, x.H, x.dtype, x.w, x.k, x.v, x.a, x.b, nullptr, x.Z, 1, s);
+    }, &ps);
+    if (rc) return rc;
     // (3) segment start states, and the final state
     wkv7_segment_scan_kernel<false><<<dim3(B * H, kN / kScanRows), kScanThreads, 0, st>>>(H, nseg, ws.M, ws.Z, s0,
                                                                                            ws.starts, sT);
