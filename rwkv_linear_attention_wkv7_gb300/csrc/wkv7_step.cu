@@ -1,20 +1,25 @@
-// wkv7_forward_backward: one training step of the recurrence (the forward
-// with checkpoints at stride 16 and the factor cache, then the backward) as
-// concurrent sub-batches.
+// One training step of the recurrence in one call, as concurrent blocks of
+// batch rows: wkv7_forward_backward (the forward with checkpoints at stride
+// 16 and the factor cache, then the backward), and the same for the fused
+// producers (wkv7_forward_backward_fused) and the output epilogue
+// (wkv7_forward_backward_gn).
 //
 // Every (b, h) is independent in both directions, so the batch splits into
-// nsplit contiguous row blocks, each running its forward and then its
-// backward on a stream of its own: block 0 on the caller's stream, the others
-// on streams of the library, forked from the caller's stream by an event and
-// joined back into it, so the call stays stream-ordered for the caller.
-// Using the caller's stream for one block keeps the library's own streams to
-// nsplit - 1 (one for the default split): every stream more can share a
-// hardware work queue with the caller's other streams, such as copy streams,
-// and serialise work they meant to overlap.  A sub-batch's backward starts as soon as
-// its own forward is done, while the other sub-batches' forward CTAs are
-// still finishing; with one CTA per head the forward leaves a tail of
-// unevenly loaded SMs and the backward a partly empty second wave, and the
-// sub-batches fill each other's.
+// nsplit contiguous blocks of rows, each running its forward and then its
+// backward on a stream of its own.  A block's backward starts as soon as its
+// own forward is done, while the other blocks' forward CTAs are still
+// finishing.  With one CTA per head the forward leaves a tail of unevenly
+// loaded SMs and the backward a partly empty second wave; the blocks fill
+// each other's.
+//
+// Block 0 runs on the caller's stream, the others on streams of the library,
+// forked from the caller's stream by an event and joined back into it, so the
+// call stays stream-ordered for the caller.  Using the caller's stream for
+// one block keeps the library's streams to nsplit - 1 (one for the default
+// split): every extra stream can share a hardware work queue with the
+// caller's other streams, such as copy streams, and serialise work they meant
+// to overlap.  run_side_by_side, the fork / join itself, also runs the time
+// split's two independent segment passes (wkv7_timesplit.cu).
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
