@@ -214,11 +214,13 @@ int wkv7_backward_gn(int B, int T, int H, int N, wkv7_dtype dtype,
  *             Z), a scan S_{k+1} = S_k M_k + Z_k over each head's segments,
  *             then every segment from its start state (y, and checkpoints
  *             and factors kept in the workspace);
- *   backward  every segment with no gradient at its end (gives D_k, what it
- *             sends to its start), a reverse scan G_{k-1} = D_k + G_k M_k^T
- *             from G = dsT, then every segment with G_k at its end.
- * It does about three forwards' and two backwards' work, and pays off when
- * B*H is small next to the GPU's thread-block slots.
+ *   backward  every segment's state gradient alone with no gradient at its
+ *             end (gives D_k, what it sends to its start), a reverse scan
+ *             G_{k-1} = D_k + G_k M_k^T from G = dsT, then every segment with
+ *             G_k at its end.
+ * The state passes are those of wkv7_forward_state / wkv7_backward_state
+ * below.  The split pays off when B*H is small next to the GPU's thread-block
+ * slots.
  *   nseg       segments per sequence; T must be a multiple of 16 * nseg.
  *   workspace  device buffer of wkv7_timesplit_workspace_floats(B, T, H,
  *              nseg) floats, 16-byte aligned, owned by the caller; the
@@ -253,6 +255,35 @@ int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype,
                             const float *dy, const float *dsT,
                             float *dr, float *dw, float *dk, float *dv, float *da, float *db,
                             float *ds0, int nseg, float *workspace, void *stream);
+
+/*
+ * The state passes alone: the summaries a span of a sequence contributes to
+ * the scan above, for spans held in other calls or on other GPUs.  Layouts,
+ * ownership, stream order and errors as in wkv7_forward / wkv7_backward.
+ *
+ * wkv7_forward_state: sT of wkv7_forward for the same w, k, v, a, b and s0,
+ * bit-identical (up to the sign of a zero), without y, checkpoints or
+ * factors.  v == NULL reads v as zero and k not at all: with s0 = I that is
+ * the span's transition product M, with v and s0 = NULL its Z.  sT is
+ * required; r is not an input (y is not formed).
+ *
+ * wkv7_backward_state: ds0 of wkv7_backward for the same r, w, a, b, dy and
+ * dsT with the forward's factor cache, bit-identical, without the per-token
+ * gradients; with dsT = NULL it is the span's D.  The gradient of the state
+ * does not depend on the state itself (nor on k and v), so neither the
+ * checkpoints nor k and v are read.
+ *   factors  [B][H][wkv7_factor_floats(T)] from wkv7_forward (stride 16) on
+ *            the same inputs, required when T > 0;
+ *   ds0      [B][H][N][N], required.
+ */
+int wkv7_forward_state(int B, int T, int H, int N, wkv7_dtype dtype,
+                       const void *w, const void *k, const void *v,
+                       const void *a, const void *b,
+                       const float *s0, float *sT, void *stream);
+int wkv7_backward_state(int B, int T, int H, int N, wkv7_dtype dtype,
+                        const void *r, const void *w, const void *a, const void *b,
+                        const float *factors, const float *dy, const float *dsT,
+                        float *ds0, void *stream);
 
 /* Largest B*H*ceil(T/16) that wkv7_forward_backward_noalloc accepts. */
 #define WKV7_NOALLOC_MAX_CHUNK_HEADS 4096

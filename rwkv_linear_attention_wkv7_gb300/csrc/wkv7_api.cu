@@ -97,6 +97,16 @@ int forward_state(int B, int T, int H, int dtype, const void *w, const void *k, 
     return launch_status(launch_forward_chunk(p, st), "segment pass launch");
 }
 
+int backward_state(int B, int T, int H, int dtype, const void *r, const void *w, const void *a, const void *b,
+                   const float *factors, const float *dy, const float *dsT, float *ds0, cudaStream_t st) {
+    SeqArgs p{};
+    p.B = B; p.T = T; p.H = H; p.L = 16; p.nck = wkv7_ckpt_count(T, 16); p.dtype = dtype;
+    p.r = r; p.w = w; p.k = w; p.v = w; p.a = a; p.b = b;  // k and v are not read: any valid map
+    p.fac_in = factors; p.dy = dy; p.dsT = dsT; p.ds0 = ds0; p.state_only = 1;
+    if (!(p.err = async_error_flag())) return WKV7_ECUDA;
+    return launch_status(launch_backward_state(p, st), "state-gradient pass launch");
+}
+
 int check_call(int B, int T, int H, int N, int dtype, const void *const *req, const char *const *req_names, int nreq,
                const void *const *opt, const char *const *opt_names, int nopt) {
     TRY(check_dims(B, T, H, N, dtype));
@@ -265,6 +275,36 @@ int backward_impl(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, c
 }  // namespace
 
 extern "C" {
+
+int wkv7_forward_state(int B, int T, int H, int N, wkv7_dtype dtype, const void *w, const void *k, const void *v,
+                       const void *a, const void *b, const float *s0, float *sT, void *stream) {
+    g_err[0] = '\0';
+    TRY(check_dims(B, T, H, N, dtype));
+    TRY(check_ptr(sT, "sT", true));
+    TRY(check_ptr(w, "w", T > 0)); TRY(check_ptr(a, "a", T > 0)); TRY(check_ptr(b, "b", T > 0));
+    TRY(check_ptr(k, "k", T > 0 && v)); TRY(check_ptr(v, "v", false)); TRY(check_ptr(s0, "s0", false));
+    TRY(check_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    if (T == 0) return copy_state(s0, sT, B, H, st);
+    return wkv7::forward_state(B, T, H, dtype, w, v ? k : w, v ? v : w, a, b, s0, sT, v ? 1 : 2, st);
+}
+
+int wkv7_backward_state(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *a,
+                        const void *b, const float *factors, const float *dy, const float *dsT, float *ds0,
+                        void *stream) {
+    g_err[0] = '\0';
+    TRY(check_dims(B, T, H, N, dtype));
+    TRY(check_ptr(ds0, "ds0", true));
+    TRY(check_ptr(r, "r", T > 0)); TRY(check_ptr(w, "w", T > 0)); TRY(check_ptr(a, "a", T > 0));
+    TRY(check_ptr(b, "b", T > 0)); TRY(check_ptr(factors, "factors", T > 0)); TRY(check_ptr(dy, "dy", T > 0));
+    TRY(check_ptr(dsT, "dsT", false));
+    TRY(check_device());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    if (T == 0) return copy_state(dsT, ds0, B, H, st);
+    return wkv7::backward_state(B, T, H, dtype, r, w, a, b, factors, dy, dsT, ds0, st);
+}
 
 int wkv7_forward(int B, int T, int H, int N, wkv7_dtype dtype, const void *r, const void *w, const void *k,
                  const void *v, const void *a, const void *b, const float *s0, float *y, float *sT, float *ckpt,

@@ -32,6 +32,10 @@
 
 #include "wkv7_chunk_bwd_exact.cuh"
 
+// The state-gradient instantiation (kSO) ends each chunk after its chain, so
+// the later phases of the chunk loop are unreachable there by design.
+#pragma nv_diag_suppress 128
+
 namespace wkv7 {
 namespace {
 using namespace chunk;
@@ -65,8 +69,15 @@ static_assert(64 * OS * 4 <= HL64, "S_0 staging and the G d_C split share one sl
 static_assert(4 * HL16 >= 64 * SP * 4, "exact-path S_{t-1} fits the four scaled blocks");
 static_assert(5 * 4 * 64 * 4 <= 2 * HL32, "exact-path scratch fits region Y");
 
-template <typename E>
-__host__ __device__ constexpr size_t bwd_smem_bytes() { return raw_bytes<E>() + (size_t)kBytes; }
+// The state-gradient pass (kSO below) keeps only what its chain reads, contiguous: dy, the
+// decays, the b~, a^, r^ and dy splits, and the first half of the factor block.
+constexpr int S_BT = B_DD + C * SP * 4, S_AH = S_BT + HL16, S_RH = S_AH + HL16, S_DYH = S_RH + HL16,
+              S_QQ = S_DYH + HL16;
+constexpr int kStateBytes = S_QQ + fac::kSA * 4;
+static_assert(B_G == S_BT && S_BT % 16 == 0 && S_QQ % 16 == 0, "state-pass layout: aligned, after dy and the decays");
+
+template <typename E, bool kSO = false>
+__host__ __device__ constexpr size_t bwd_smem_bytes() { return raw_bytes<E>() + (size_t)(kSO ? kStateBytes : kBytes); }
 
 __device__ __forceinline__ HL hl(const unsigned char *base, int off, int rows) {
     const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
@@ -78,6 +89,15 @@ __device__ __forceinline__ __nv_bfloat16 *hi_of(unsigned char *base, int off) {
 __device__ __forceinline__ __nv_bfloat16 *lo_of(unsigned char *base, int off, int rows) {
     return reinterpret_cast<__nv_bfloat16 *>(base + off) + rows * MS;
 }
+// An A fragment of a 16 x 16 matrix holds the B fragments of its transpose:
+// n-tile n is registers n and n + 2.
+__device__ __forceinline__ BFrag tb(const AFrag &a, int n) {
+    BFrag b;
+    b.hi[0] = a.hi[n]; b.hi[1] = a.hi[n + 2];
+    b.lo[0] = a.lo[n]; b.lo[1] = a.lo[n + 2];
+    return b;
+}
+
 // A' = W^T-weighted a^ for NS 16-key slabs starting at slab0 (M = token,
 // N = key), the slabs' MMAs issued together; written split to the A' slot.
 template <int NS>
@@ -122,10 +142,17 @@ __device__ __forceinline__ void build_ap(const AFrag &wt, const HL &AH, unsigned
 // accumulate the parameter gradients of their four channels over every token;
 // per-(b,h) partial sums leave at the end (summed over batch rows by
 // wkv7_gn_param_reduce_kernel, no atomics).
-template <typename E, bool kFac, bool kP, bool kGN>
+// kSO (with kFac, without kP or kGN): the state gradient alone, ds0 (what a
+// segment of a sequence sends to its start).  The adjoint does not depend on
+// the state, so only the chain  DSA = X_B W^T + DY (W Q_b)^T,
+// G_prev = Gd + [DY | DSA] [R^ | A^]^T  runs: no start state, no k or v, no SA,
+// Gam or per-token gradient.  Its operations are those of the full kernel, in
+// the same order, so ds0 is bit-identical to it.
+template <typename E, bool kFac, bool kP, bool kGN, bool kSO = false>
 __global__ void __launch_bounds__(NT, 2)
     wkv7_bwd_chunk_kernel(SeqArgs p, const __grid_constant__ InputMaps maps, const __grid_constant__ OutputMaps omaps) {
     static_assert(!kGN || (kFac && !kP), "the epilogue's backward runs on the factor-cache path without producers");
+    static_assert(!kSO || (kFac && !kP && !kGN), "the state-gradient pass runs on the factor cache, plain inputs");
     // bf16 inputs: v is exact in bf16, so products with v as an operand skip its (zero) lo part
     constexpr bool kVLo = !std::is_same<E, __nv_bfloat16>::value;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -141,8 +168,10 @@ __global__ void __launch_bounds__(NT, 2)
     static_assert(C * DS * 4 <= HL32, "the sigmoid block fits the M4 slot");
     static_assert(256 * 4 + C * OS * 4 <= C * SP * 4 + 1280, "avec copy fits the Gram and W slots");
     float *S0f = reinterpret_cast<float *>(Bs + B_SX);
-    const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, B_BT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, B_AH, 16),
-             RH = hl(Bs, B_RH, 16), VM = hl(Bs, B_VV, 16), DYH = hl(Bs, B_DYH, 16), SAH = hl(Bs, B_SAH, 16),
+    constexpr int oBT = kSO ? S_BT : B_BT, oAH = kSO ? S_AH : B_AH, oRH = kSO ? S_RH : B_RH;
+    constexpr int oDYH = kSO ? S_DYH : B_DYH, oQQ = kSO ? S_QQ : B_QQ;
+    const HL SX = hl(Bs, B_SX, 64), BT = hl(Bs, oBT, 16), KT = hl(Bs, B_KT, 16), AH = hl(Bs, oAH, 16),
+             RH = hl(Bs, oRH, 16), VM = hl(Bs, B_VV, 16), DYH = hl(Bs, oDYH, 16), SAH = hl(Bs, B_SAH, 16),
              DSH = hl(Bs, B_DSH, 16), AP = hl(Bs, B_AP, 16), MK = hl(Bs, B_MK, 16),
              QQ = hl(Bs, B_QQ, 32), M3 = hl(Bs, B_M3, 32), M4 = hl(Bs, B_M4, 32);
 
@@ -179,8 +208,10 @@ __global__ void __launch_bounds__(NT, 2)
     // there, and first waited for by the products that read S_0.
     __shared__ __align__(8) uint64_t bar, bar_s;
     __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
-    constexpr unsigned kChunkBytes =
-        (unsigned)(raw_bytes<E>() + C * RS * 4 + (kFac ? fac::kWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
+    // kSO: k and v are not staged, and only the factor block's first half (W, M_k', Q', W Q_b) is
+    constexpr int kFacWords = kSO ? fac::kSA : fac::kWords;
+    constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() - (kSO ? 2 * C * RS * sizeof(E) : 0) + C * RS * 4 +
+                                                (kFac ? kFacWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
     if (tid == 0) {
         mbar_init(&bar, 1);
         mbar_init(&bar_s, 1);
@@ -209,7 +240,7 @@ __global__ void __launch_bounds__(NT, 2)
     // block barrier that precedes every issue) and arrives once.
     const int ccopy = warp >= 1 && lane < 3 ? 3 * (warp - 1) + lane : -1;
     auto stage_in = [&](int c) {  // inputs and dy of chunk c (and y): one tensor copy each
-        if (ccopy >= 0 && ccopy < 7) {
+        if (ccopy >= 0 && ccopy < 7 && !(kSO && (ccopy == VK || ccopy == VV))) {
             void *const dst = ccopy < 6 ? static_cast<void *>(raw + ccopy * C * RS) : static_cast<void *>(dyf);
             tma_rows(dst, &maps.m[ccopy], h, c * C, bi, &bar);
         }
@@ -236,10 +267,10 @@ __global__ void __launch_bounds__(NT, 2)
         return make_a(make_float2(x[0], x[OS]), make_float2(x[8], x[OS + 8]), make_float2(x[8 * OS], x[9 * OS]),
                       make_float2(x[8 * OS + 8], x[9 * OS + 8]));
     };
-    const float *FC = reinterpret_cast<const float *>(Bs + B_QQ);  // factor block of the current chunk
+    const float *FC = reinterpret_cast<const float *>(Bs + oQQ);  // factor block of the current chunk
     auto stage_fac = [&](int c) {
         if constexpr (kFac) {
-            if (ccopy == 7) bulk_g2s(Bs + B_QQ, p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords, fac::kWords * 4, &bar);
+            if (ccopy == 7) bulk_g2s(Bs + oQQ, p.fac_in + ((size_t)bh * nchunks + c) * fac::kWords, kFacWords * 4, &bar);
         }
     };
     stage_in(nchunks - 1);
@@ -322,13 +353,18 @@ __global__ void __launch_bounds__(NT, 2)
             __syncthreads();
         }
         if (exact) {
-            drain_then_load_s0();
-            mbar_wait(&bar_s, ph, p.err, &lost);
-            bwd_chunk_exact<E, kP, OS, kGN>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT),
-                                            reinterpret_cast<float *>(Bs + B_Y), Gh, nv, p, base0, tstride, t0,
-                                            carryA, carryB, Gm, dsv, p.r_k + h * 64);
-            fence_proxy_async();  // the per-token path wrote into slots the copies refill
-            __syncthreads();
+            if constexpr (kSO) {
+                bwd_chunk_exact_state<E, kP>(raw, dyf, Gh, nv);
+                __syncthreads();  // every lane has read the chunk's rows before the copies refill them
+            } else {
+                drain_then_load_s0();
+                mbar_wait(&bar_s, ph, p.err, &lost);
+                bwd_chunk_exact<E, kP, OS, kGN>(raw, dyf, S0f, reinterpret_cast<float *>(Bs + B_BT),
+                                                reinterpret_cast<float *>(Bs + B_Y), Gh, nv, p, base0, tstride, t0,
+                                                carryA, carryB, Gm, dsv, p.r_k + h * 64);
+                fence_proxy_async();  // the per-token path wrote into slots the copies refill
+                __syncthreads();
+            }
             if (c > 0) {
                 stage_in(c - 1);
                 stage_fac(c - 1);
@@ -337,6 +373,32 @@ __global__ void __launch_bounds__(NT, 2)
             continue;
         }
         const float *dC = dd + (C - 1) * DS;
+        // (G diag(d_C)) as the A fragment of key columns 16 kk .. 16 kk + 15 (this warp's value rows)
+        auto gd_a = [&](int kk) {
+            const float2 d0 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 2 * q);
+            const float2 d1 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 8 + 2 * q);
+            return make_a(make_float2(Gh[2 * kk][0] * d0.x, Gh[2 * kk][1] * d0.y),
+                          make_float2(Gh[2 * kk][2] * d0.x, Gh[2 * kk][3] * d0.y),
+                          make_float2(Gh[2 * kk + 1][0] * d1.x, Gh[2 * kk + 1][1] * d1.y),
+                          make_float2(Gh[2 * kk + 1][2] * d1.x, Gh[2 * kk + 1][3] * d1.y));
+        };
+        // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index)
+        auto g5 = [&](const AFrag &dyA, const AFrag &dsA) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                BFrag rr[2], aa[2];
+                ldb2_t(RH, 16 * pp, 0, lane, rr[0], rr[1]);
+                ldb2_t(AH, 16 * pp, 0, lane, aa[0], aa[1]);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int nt = 2 * pp + u;
+                    const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
+                    Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
+                }
+                mma3n<2>(Gh + 2 * pp, dyA, rr);
+                mma3n<2>(Gh + 2 * pp, dsA, aa);
+            }
+        };
 
         // ================= split every operand matrix once (S_0 is split where it is read)
 #pragma unroll
@@ -348,18 +410,18 @@ __global__ void __launch_bounds__(NT, 2)
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
-            st_hl4(hi_of(Bs, B_BT), lo_of(Bs, B_BT, 16), t, j, mul4(in_b4<kP>(raw, t, j), id));
+            st_hl4(hi_of(Bs, oBT), lo_of(Bs, oBT, 16), t, j, mul4(in_b4<kP>(raw, t, j), id));
             if constexpr (kP) *reinterpret_cast<float4 *>(avs + t * OS + j) = ld_raw4(raw, VB, t, j);
-            st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
-            st_hl4(hi_of(Bs, B_AH), lo_of(Bs, B_AH, 16), t, j, mul4(in_a4<kP>(raw, t, j), dp));
-            st_hl4(hi_of(Bs, B_RH), lo_of(Bs, B_RH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
+            if constexpr (!kSO) st_hl4(hi_of(Bs, B_KT), lo_of(Bs, B_KT, 16), t, j, mul4(ld_raw4(raw, VK, t, j), id));
+            st_hl4(hi_of(Bs, oAH), lo_of(Bs, oAH, 16), t, j, mul4(in_a4<kP>(raw, t, j), dp));
+            st_hl4(hi_of(Bs, oRH), lo_of(Bs, oRH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
         }
 #pragma unroll
         for (int m = 0; m < 2; ++m) {  // dy: [t][i] quads
             const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
-            st_hl4(hi_of(Bs, B_DYH), lo_of(Bs, B_DYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
+            st_hl4(hi_of(Bs, oDYH), lo_of(Bs, oDYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
         }
-        drain_then_load_s0();
+        if constexpr (!kSO) drain_then_load_s0();
         if constexpr (kFac)
             __syncwarp();
         else
@@ -456,6 +518,35 @@ __global__ void __launch_bounds__(NT, 2)
         __syncthreads();
         }
         __syncthreads();  // every b~ / k~ slab is split; warp 0 has drained the gradient stores
+        if constexpr (kSO) {  // X_B = (G diag(d_C)) B~^T, DSA = X_B W^T + DY (W Q_b)^T, then G5
+            float xbs[2][4] = {};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const AFrag gf = gd_a(kk);
+                BFrag bq[2];
+                ldb2(BT, 0, 16 * kk, lane, bq[0], bq[1]);
+                mma3n<2>(xbs, gf, bq);
+            }
+            const AFrag awn = ld_afrag(FC + fac::kWA, lane), xb = a_from_acc(xbs, 0);
+            float dsb[2][4] = {};
+            { const BFrag bw[2] = {tb(awn, 0), tb(awn, 1)}; mma3n<2>(dsb, xb, bw); }
+            const AFrag dyA = lda_t(DYH, 16 * warp, 0, lane);
+            {
+                BFrag bq[2];
+                ld_bfrags(FC + fac::kWQbB, lane, bq[0], bq[1]);
+                mma3n<2>(dsb, dyA, bq);
+            }
+            const AFrag dsA = a_from_acc(dsb, 0);
+            __syncthreads();  // the chunk's rows, dy and factors are read
+            if (c > 0) {
+                stage_in(c - 1);
+                stage_fac(c - 1);
+                if (tid == 0) mbar_arrive(&bar);
+            }
+            g5(dyA, dsA);
+            __syncthreads();  // G5 has read d_C, r^ and a^ before the next chunk's decays and splits
+            continue;
+        }
         // v split: warp w its own 16 value columns (all tokens), which is all its vA
         // reads; the other readers come after the barrier that follows G2
 #pragma unroll
@@ -539,20 +630,14 @@ __global__ void __launch_bounds__(NT, 2)
         float dvs[4][4] = {};
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-            const float2 d0 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 2 * q);
-            const float2 d1 = *reinterpret_cast<const float2 *>(dC + 16 * kk + 8 + 2 * q);
-            const AFrag gf = make_a(make_float2(Gh[2 * kk][0] * d0.x, Gh[2 * kk][1] * d0.y),
-                                    make_float2(Gh[2 * kk][2] * d0.x, Gh[2 * kk][3] * d0.y),
-                                    make_float2(Gh[2 * kk + 1][0] * d1.x, Gh[2 * kk + 1][1] * d1.y),
-                                    make_float2(Gh[2 * kk + 1][2] * d1.x, Gh[2 * kk + 1][3] * d1.y));
+            const AFrag gf = gd_a(kk);
             BFrag b0, b1, b2, b3;
             ldb2(KT, 0, 16 * kk, lane, b0, b1);
             ldb2(BT, 0, 16 * kk, lane, b2, b3);
             { const BFrag bq[4] = {b0, b1, b2, b3}; mma3n<4>(dvs, gf, bq); }
         }
         {
-            // M_k' (M = token t, K = s) and W as A fragments; an A fragment of a 16 x 16 matrix
-            // holds the B fragments of its transpose: n-tile n is registers n and n + 2
+            // M_k' (M = token t, K = s) and W as A fragments, their transposes' B fragments by tb
             AFrag amk, awn;
             if constexpr (kFac) {
                 amk = ld_afrag(FC + fac::kMkA, lane);
@@ -564,12 +649,6 @@ __global__ void __launch_bounds__(NT, 2)
                              make_float2(Wm[g * WS + 2 * q + 8], Wm[g * WS + 2 * q + 9]),
                              make_float2(Wm[(g + 8) * WS + 2 * q + 8], Wm[(g + 8) * WS + 2 * q + 9]));
             }
-            auto tb = [](const AFrag &a, int n) {
-                BFrag b;
-                b.hi[0] = a.hi[n]; b.hi[1] = a.hi[n + 2];
-                b.lo[0] = a.lo[n]; b.lo[1] = a.lo[n + 2];
-                return b;
-            };
             const AFrag xb = a_from_acc(dvs, 1);  // X_B (tiles 2, 3)
             float dsa[2][4] = {};
             { const BFrag bm[2] = {tb(amk, 0), tb(amk, 1)}; mma3n<2>(dvs, xb, bm); }
@@ -731,22 +810,8 @@ __global__ void __launch_bounds__(NT, 2)
             mma3n<4>(x4, kk ? ahA : rhA, bq);
         }
 
-        // G5: G_prev = G diag(d_C) + [DY | DSA] [R^ | A^]^T  (rows = value index); issued
-        // before the output code so that its MMAs run under the scalar work
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-            BFrag rr[2], aa[2];
-            ldb2_t(RH, 16 * pp, 0, lane, rr[0], rr[1]);
-            ldb2_t(AH, 16 * pp, 0, lane, aa[0], aa[1]);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int nt = 2 * pp + u;
-                const float2 dc = *reinterpret_cast<const float2 *>(dC + 8 * nt + 2 * q);
-                Gh[nt][0] *= dc.x; Gh[nt][1] *= dc.y; Gh[nt][2] *= dc.x; Gh[nt][3] *= dc.y;
-            }
-            mma3n<2>(Gh + 2 * pp, dyA, rr);
-            mma3n<2>(Gh + 2 * pp, dsA, aa);
-        }
+        // G5, issued before the output code so that its MMAs run under the scalar work
+        g5(dyA, dsA);
         // ================= gradients: staged as [t][key] tiles (stride OS) in the
         // S_0 / G d_C quarters and the v and SA slots, then one tensor store each
         __syncthreads();  // G4 and G5 no longer read those slots
@@ -883,20 +948,21 @@ __global__ void __launch_bounds__(NT, 2)
     }
 }
 
-template <typename E, bool kFac, bool kP, bool kGN = false>
+template <typename E, bool kFac, bool kP, bool kGN = false, bool kSO = false>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
-    const size_t sm = bwd_smem_bytes<E>();
-    InputMaps maps;
-    OutputMaps omaps;
+    const size_t sm = bwd_smem_bytes<E, kSO>();
+    InputMaps maps{};
+    OutputMaps omaps{};
     cudaError_t e = encode_input_maps(&maps, p, p.dy);  // six inputs, dy (or do), and the checkpoints (box OS x 64)
-    if (e == cudaSuccess) e = encode_ckpt_map(&maps.m[7], p.ckpt_in, (long long)p.B * p.H * p.nck * 64, 64);
+    // the state-gradient pass reads no checkpoint and stores no per-token gradient
+    if (e == cudaSuccess && !kSO) e = encode_ckpt_map(&maps.m[7], p.ckpt_in, (long long)p.B * p.H * p.nck * 64, 64);
     if (e == cudaSuccess && kGN) e = encode_rows_map(&maps.m[8], p.y_in, 4, p.B, p.T, p.H);  // the forward's y
-    if (e == cudaSuccess) e = encode_output_maps(&omaps, p);
+    if (e == cudaSuccess && !kSO) e = encode_output_maps(&omaps, p);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac, kP, kGN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(wkv7_bwd_chunk_kernel<E, kFac, kP, kGN, kSO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sm);
     if (e != cudaSuccess) return e;
-    wkv7_bwd_chunk_kernel<E, kFac, kP, kGN><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
+    wkv7_bwd_chunk_kernel<E, kFac, kP, kGN, kSO><<<p.B * p.H, NT, sm, st>>>(p, maps, omaps);
     return cudaGetLastError();
 }
 
@@ -943,6 +1009,12 @@ cudaError_t launch_backward_chunk(const SeqArgs &p, cudaStream_t st) {
     }
     if (p.fac_in) return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false>(p, st) : launch_t<float, true, false>(p, st);
     return p.dtype == 1 ? launch_t<__nv_bfloat16, false, false>(p, st) : launch_t<float, false, false>(p, st);
+}
+
+cudaError_t launch_backward_state(const SeqArgs &p, cudaStream_t st) {
+    if (!p.fac_in || !p.ds0 || p.prod || p.gn_w || p.L != C) return cudaErrorInvalidValue;
+    return p.dtype == 1 ? launch_t<__nv_bfloat16, true, false, false, true>(p, st)
+                        : launch_t<float, true, false, false, true>(p, st);
 }
 
 }  // namespace wkv7

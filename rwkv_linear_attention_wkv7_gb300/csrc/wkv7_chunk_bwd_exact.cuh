@@ -177,5 +177,42 @@ __device__ void bwd_chunk_exact(const E *raw, const float *dys, const float *S0s
     }
 }
 
+// The same chunk for the state gradient alone: G enters as dL/dS_C and
+// leaves as dL/dS_0 through the operations of bwd_chunk_exact, in its order
+// (G += dy_t r_t^T, dsa = G b_t, G <- G diag(w_t) + dsa a_t^T), so the result
+// is bit-identical to it.  dS does not depend on the state: no start state,
+// no k or v, no per-token gradient and no block barrier.
+template <typename E, bool kP>
+__device__ void bwd_chunk_exact_state(const E *raw, const float *dys, float G[8][4], int nv) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, q = lane & 3;
+    const int rA = warp * 16 + g, rB = rA + 8;
+    for (int t = nv - 1; t >= 0; --t) {
+        const float dy0 = dys[t * SP + rA], dy1 = dys[t * SP + rB];
+        float ds0 = 0.f, ds1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = 8 * nt + 2 * q + e;
+                const float rv = ld_raw(raw, VR, t, j), bv = in_b<kP>(raw, t, j);
+                G[nt][e] = __fmaf_rn(dy0, rv, G[nt][e]);
+                G[nt][2 + e] = __fmaf_rn(dy1, rv, G[nt][2 + e]);
+                ds0 = __fmaf_rn(G[nt][e], bv, ds0);
+                ds1 = __fmaf_rn(G[nt][2 + e], bv, ds1);
+            }
+        ds0 = quad_sum(ds0);
+        ds1 = quad_sum(ds1);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int j = 8 * nt + 2 * q + e;
+                const float wv = in_w<kP>(raw, t, j), av = in_a<kP>(raw, t, j);
+                G[nt][e] = __fmaf_rn(G[nt][e], wv, __fmul_rn(ds0, av));
+                G[nt][2 + e] = __fmaf_rn(G[nt][2 + e], wv, __fmul_rn(ds1, av));
+            }
+    }
+}
+
 }  // namespace chunk
 }  // namespace wkv7

@@ -34,9 +34,10 @@ struct SeqArgs {
     float *o;
     const float *y_in;
     float *gn_part;
-    // the time split's segment passes: 0 the whole forward; 1 only the end state sT
-    // (no y); 2 only the end state with v = 0 (the product of the transitions
-    // applied to s0; v and k are not read)
+    // the state passes (the time split's segment summaries): 0 the whole call.
+    // Forward: 1 only the end state sT (no y); 2 only the end state with v = 0
+    // (the product of the transitions applied to s0; v and k are not read).
+    // Backward: 1 only ds0 (r, w, a, b, dy and the factor cache are read).
     int state_only;
 };
 
@@ -61,6 +62,12 @@ int set_error(int code, const char *msg);
 // reads w, a, b (v = 0).  Arguments already checked by the caller.
 int forward_state(int B, int T, int H, int dtype, const void *w, const void *k, const void *v, const void *a,
                   const void *b, const float *s0, float *sT, int state_only, cudaStream_t s);
+// The state-gradient pass: ds0 of the chunked backward of B*T*H inputs (dsT
+// NULL: zeros) from r, w, a, b, dy and the forward's factor cache, without
+// the per-token gradients; bit-identical to the full backward's ds0.
+// Arguments already checked by the caller.
+int backward_state(int B, int T, int H, int dtype, const void *r, const void *w, const void *a, const void *b,
+                   const float *factors, const float *dy, const float *dsT, float *ds0, cudaStream_t s);
 // Host checks shared by every entry point, run before anything is launched:
 // sizes and dtype, the required pointers (non-NULL when T > 0) and the
 // optional ones (NULL allowed), 16-byte alignment of both, and an sm_103a
@@ -78,6 +85,7 @@ cudaError_t launch_forward_chunk(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_backward_plain(const SeqArgs &a, cudaStream_t s);
 bool backward_chunk_supported(const SeqArgs &a);
 cudaError_t launch_backward_chunk(const SeqArgs &a, cudaStream_t s);
+cudaError_t launch_backward_state(const SeqArgs &a, cudaStream_t s);
 bool backward_tc_supported(const SeqArgs &a);
 cudaError_t launch_backward_tc(const SeqArgs &a, cudaStream_t s);
 cudaError_t launch_gn_param_reduce(int B, int H, const float *part, float *dgn_w, float *dgn_b, float *dr_k,

@@ -332,8 +332,8 @@ int wkv7_backward_timesplit(int B, int T, int H, int N, wkv7_dtype dtype, const 
                              ds0, stream);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // (1) no gradient arriving at the segment ends: D = what each segment sends to its start
-    if ((rc = wkv7_backward(bs, tseg, H, N, dtype, r, w, k, v, a, b, ws.ckpt, ws.fac, 16, dy, nullptr, dr, dw, dk, dv,
-                            da, db, ws.D, stream)))
+    // (the state gradient alone, from the factors the forward kept)
+    if ((rc = wkv7::backward_state(bs, tseg, H, dtype, r, w, a, b, ws.fac, dy, nullptr, ws.D, st)))
         return rc;
     // (2) the gradient arriving at every segment's end, and ds0
     wkv7_segment_scan_kernel<true><<<dim3(B * H, kN / kScanRows), kScanThreads, 0, st>>>(H, nseg, ws.M, ws.D, dsT,

@@ -33,9 +33,11 @@ N = wkv7.HEAD_SIZE
 
 
 class CudaSpanSolver:
-    """The span computations on this rank's GPU, through the C ABI.  Within
-    the span, ``nseg`` > 1 cuts every sequence once more into segments that
-    run side by side (the time-split entry points)."""
+    """The span computations on this rank's GPU, through the C ABI.  With
+    ``nseg`` = 1 the summaries M, Z and D come from the state passes alone
+    (wkv7_forward_state, wkv7_backward_state); ``nseg`` > 1 cuts every
+    sequence of the span once more into segments that run side by side (the
+    time-split entry points)."""
 
     def __init__(self, nseg: int = 1):
         self.nseg = nseg
@@ -44,6 +46,10 @@ class CudaSpanSolver:
         r = x["r"]
         B, T, H, _ = r.shape
         eye = torch.eye(N, device=r.device).expand(B, H, N, N).contiguous()
+        if self.nseg == 1:
+            M = wkv7.forward_state(x["w"], x["k"], None, x["a"], x["b"], s0=eye)
+            Z = wkv7.forward_state(x["w"], x["k"], x["v"], x["a"], x["b"])
+            return M, Z
         zero_v = torch.zeros_like(x["v"])
         xs0 = [x[n] if n != "v" else zero_v for n in "rwkvab"]
         _, M, _ = wkv7.forward_timesplit(*xs0, s0=eye, nseg=self.nseg)
@@ -51,10 +57,22 @@ class CudaSpanSolver:
         return M, Z
 
     def forward(self, x, s0):
+        if self.nseg == 1:  # checkpoints and the factor cache for the backward
+            y, sT, ck, fac = wkv7.forward(*(x[n] for n in "rwkvab"), s0=s0, L=16, want_factors=True)
+            return y, sT, (ck, fac)
         y, sT, ws = wkv7.forward_timesplit(*(x[n] for n in "rwkvab"), s0=s0, nseg=self.nseg)
         return y, sT, ws
 
+    def state_grad(self, x, ctx, dy):
+        """D: the gradient the span sends to its start when none arrives at its end."""
+        if self.nseg == 1:
+            return wkv7.backward_state(x["r"], x["w"], x["a"], x["b"], ctx[1], dy)
+        return self.backward(x, ctx, dy, None)["ds0"]
+
     def backward(self, x, ctx, dy, dsT):
+        if self.nseg == 1:
+            ck, fac = ctx
+            return wkv7.backward(*(x[n] for n in "rwkvab"), ck, dy, dsT=dsT, L=16, factors=fac)
         return wkv7.backward_timesplit(*(x[n] for n in "rwkvab"), dy, dsT=dsT, nseg=self.nseg, workspace=ctx)
 
     def scan(self, M, C, init, backward):
@@ -91,7 +109,7 @@ def backward(x: Dict[str, torch.Tensor], ctx, dy: torch.Tensor, dsT: Optional[to
     sequences' ds0 (the same on every rank); ``dsT`` is read on every rank."""
     solver = solver or CudaSpanSolver()
     rank = dist.get_rank(group)
-    D = solver.backward(x, ctx["span"], dy, None)["ds0"]
+    D = solver.state_grad(x, ctx["span"], dy)
     Dg = _all_gather_states(D, group)
     ends, ds0 = solver.scan(ctx["M"], Dg, dsT, True)
     g = solver.backward(x, ctx["span"], dy, ends[:, rank].contiguous())

@@ -62,6 +62,10 @@ def load(path: str) -> ctypes.CDLL:
     L.wkv7_forward_timesplit.restype = ci
     L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
     L.wkv7_backward_timesplit.restype = ci
+    L.wkv7_forward_state.argtypes = [ci, ci, ci, ci, ci] + [vp] * 5 + [fp, fp, vp]
+    L.wkv7_forward_state.restype = ci
+    L.wkv7_backward_state.argtypes = [ci, ci, ci, ci, ci] + [vp] * 4 + [fp] * 4 + [vp]
+    L.wkv7_backward_state.restype = ci
     L.wkv7_forward_fused.argtypes = L.wkv7_forward.argtypes
     L.wkv7_forward_fused.restype = ci
     L.wkv7_backward_fused.argtypes = L.wkv7_backward.argtypes
@@ -421,6 +425,41 @@ def backward_timesplit(r, w, k, v, a, b, dy, dsT=None, nseg: int = 1, workspace=
                                        _stream(stream))
     _check("wkv7_backward_timesplit", rc)
     return g
+
+
+def forward_state(w, k, v, a, b, s0=None, sT=None, stream=None) -> torch.Tensor:
+    """sT of ``forward`` alone (no y, checkpoints or factors).  ``v=None`` reads
+    v as zero (k is then not read): from s0 = I that is the transition product
+    of the inputs' span, see wkv7_forward_state."""
+    xs = [w, k if v is not None else w, v if v is not None else w, a, b]
+    _check_inputs(xs)
+    B, T, H, N = w.shape
+    dev = w.device
+    sT = sT if sT is not None else torch.empty((B, H, N, N), device=dev)
+    _f32(sT, (B, H, N, N), dev, "sT")
+    _f32(s0, (B, H, N, N), dev, "s0")
+    ptrs = [_ptr(w), _ptr(k) if v is not None else None, _ptr(v), _ptr(a), _ptr(b)]
+    rc = lib().wkv7_forward_state(B, T, H, N, _dtype_code(w), *ptrs, _ptr(s0), _ptr(sT), _stream(stream))
+    _check("wkv7_forward_state", rc)
+    return sT
+
+
+def backward_state(r, w, a, b, factors, dy, dsT=None, ds0=None, stream=None) -> torch.Tensor:
+    """ds0 of ``backward`` alone, from the forward's factor cache (no
+    checkpoints; k and v do not enter it), see wkv7_backward_state."""
+    xs = [r, w, a, b]
+    _check_inputs(xs)
+    B, T, H, N = r.shape
+    dev = r.device
+    ds0 = ds0 if ds0 is not None else torch.empty((B, H, N, N), device=dev)
+    _f32(ds0, (B, H, N, N), dev, "ds0")
+    _f32(dy, (B, T, H, N), dev, "dy")
+    _f32(dsT, (B, H, N, N), dev, "dsT")
+    _f32(factors, (B, H, factor_floats(T)), dev, "factors")
+    rc = lib().wkv7_backward_state(B, T, H, N, _dtype_code(r), *map(_ptr, xs), _ptr(factors), _ptr(dy), _ptr(dsT),
+                                   _ptr(ds0), _stream(stream))
+    _check("wkv7_backward_state", rc)
+    return ds0
 
 
 def segment_scan(M, C, init=None, backward: bool = False, out=None, fin=None, stream=None):

@@ -49,7 +49,8 @@ def test_header_declares_entry_points():
     for required in ("wkv7_forward", "wkv7_backward", "wkv7_decode_step", "wkv7_ckpt_count", "wkv7_factor_floats",
                      "wkv7_async_status", "wkv7_last_error", "wkv7_forward_fused", "wkv7_backward_fused",
                      "wkv7_forward_gn", "wkv7_backward_gn", "wkv7_gn_workspace_floats",
-                     "wkv7_forward_backward", "wkv7_forward_backward_fused", "wkv7_forward_backward_gn"):
+                     "wkv7_forward_backward", "wkv7_forward_backward_fused", "wkv7_forward_backward_gn",
+                     "wkv7_forward_state", "wkv7_backward_state"):
         assert required in names
 
 
@@ -199,6 +200,32 @@ def test_forward_backward_rejects_bad_arguments(lib):
     bad = list(gn)
     bad[33] = 7
     assert lib.wkv7_forward_backward_gn(*bad) == EINVAL and "nsplit" in wkv7.last_error()
+
+
+def test_state_passes_reject_bad_arguments(lib):
+    """wkv7_forward_state needs sT (and k when v is given); wkv7_backward_state
+    needs ds0 and the forward's factor cache."""
+    p, odd = ctypes.c_void_p(4096), ctypes.c_void_p(4104)
+    fwd = [1, 4, 1, 64, 0] + [p] * 5 + [None, p, None]
+    bad = list(fwd)
+    bad[11] = None
+    assert lib.wkv7_forward_state(*bad) == EINVAL and "sT" in wkv7.last_error()
+    bad = list(fwd)
+    bad[6] = None  # k missing while v is given
+    assert lib.wkv7_forward_state(*bad) == EINVAL and "k is NULL" in wkv7.last_error()
+    bad = list(fwd)
+    bad[10] = odd
+    assert lib.wkv7_forward_state(*bad) == EINVAL and "aligned" in wkv7.last_error()
+    bwd = [1, 4, 1, 64, 0] + [p] * 4 + [p, p, None, p, None]
+    bad = list(bwd)
+    bad[9] = None
+    assert lib.wkv7_backward_state(*bad) == EINVAL and "factors" in wkv7.last_error()
+    bad = list(bwd)
+    bad[12] = None
+    assert lib.wkv7_backward_state(*bad) == EINVAL and "ds0" in wkv7.last_error()
+    bad = list(bwd)
+    bad[3] = 32
+    assert lib.wkv7_backward_state(*bad) == EINVAL and "N must be 64" in wkv7.last_error()
 
 
 def test_decode_rejects_bad_arguments(lib):

@@ -44,6 +44,9 @@ class OracleSpanSolver:
         g = oracle.backward(*(x[n] for n in "rwkvab"), dy, s0=ctx, dsT=dsT)
         return {k: torch.from_numpy(v) for k, v in g.items()}
 
+    def state_grad(self, x, ctx, dy):
+        return self.backward(x, ctx, dy, None)["ds0"]
+
     def scan(self, M, C, init, backward):
         B, nseg, H = M.shape[:3]
         S = torch.zeros((B, H, N, N), dtype=M.dtype) if init is None else init.to(M.dtype).clone()
@@ -55,7 +58,7 @@ class OracleSpanSolver:
         return out, S
 
 
-def _worker(rank, world, port, use_gpu, out):
+def _worker(rank, world, port, use_gpu, nseg, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     import torch.distributed as dist
     import oracle
@@ -76,7 +79,7 @@ def _worker(rank, world, port, use_gpu, out):
             from rwkv_linear_attention_wkv7_gb300 import build
             build()
             torch.cuda.set_device(0)
-            solver = seqpar.CudaSpanSolver(nseg=2)
+            solver = seqpar.CudaSpanSolver(nseg=nseg)
         else:
             solver = OracleSpanSolver()
         y, sT, ctx = seqpar.forward(x, s0=s0, solver=solver)
@@ -95,12 +98,12 @@ def _worker(rank, world, port, use_gpu, out):
         dist.destroy_process_group()
 
 
-def _run(use_gpu, world=2):
+def _run(use_gpu, world=2, nseg=2):
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, use_gpu, out)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, use_gpu, nseg, out)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
@@ -121,12 +124,13 @@ def test_exchange_oracle_spans(world):
 
 
 @pytest.mark.gpu
-def test_world2_on_one_gpu():
-    """Both ranks on cuda:0 with the library's kernels (two spans of 64 tokens,
-    each cut into 2 segments), against the whole-sequence oracle at the parity
-    bars."""
+@pytest.mark.parametrize("nseg", [1, 2])
+def test_world2_on_one_gpu(nseg):
+    """Both ranks on cuda:0 with the library's kernels (two spans of 64 tokens;
+    nseg 1: the summaries from the state passes, nseg 2: each span cut into 2
+    segments), against the whole-sequence oracle at the parity bars."""
     from tests import parity
-    res = _run(use_gpu=True)
+    res = _run(use_gpu=True, nseg=nseg)
     for rank, errs in res.items():
         assert errs["y"] <= parity.FWD_TOL and errs["sT"] <= parity.FWD_TOL, (rank, errs)
         for k in parity.GRADS + ("ds0",):
