@@ -577,7 +577,7 @@ def run_ours(args, world, rank, local):
         e2e_seq()
         torch.cuda.synchronize()
         barrier(world)
-        n_e2e = 8
+        n_e2e = 24  # steady state: the first inputs in and the last results out are paid once
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(sh)
         for k in range(n_e2e):
