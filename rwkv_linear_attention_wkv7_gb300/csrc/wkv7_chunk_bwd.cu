@@ -98,6 +98,15 @@ __device__ __forceinline__ BFrag tb(const AFrag &a, int n) {
     return b;
 }
 
+// Token of element quad e (0..63) when a warp converts its own 16-key slab
+// (4 quads per token): the 16 lanes of a half-warp take tokens 2 apart and
+// the 8 of a quarter-warp tokens 4 apart, so that their 8-byte accesses to
+// rows of 72 bf16 and their 16-byte accesses to rows of 68 floats fall in
+// distinct banks.
+__device__ __forceinline__ int slab_token(int e) {
+    return 4 * ((e >> 2) & 1) + 2 * ((e >> 3) & 1) + ((e >> 4) & 1) + 8 * (e >> 5);
+}
+
 // A' = W^T-weighted a^ for NS 16-key slabs starting at slab0 (M = token,
 // N = key), the slabs' MMAs issued together; written split to the A' slot.
 template <int NS>
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(NT, 2)
             // with the factor cache, warp w converts its own 16-key slab (all
             // tokens); the block barrier after the splits shows every slab to G2
             const int e = kFac ? lane + 32 * m : tid + NT * m;
-            const int t = kFac ? e >> 2 : e >> 4, j = kFac ? 16 * warp + (e & 3) * 4 : (e & 15) * 4;
+            const int t = kFac ? slab_token(e) : e >> 4, j = kFac ? 16 * warp + (e & 3) * 4 : (e & 15) * 4;
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(NT, 2)
         // reads; the other readers come after the barrier that follows G2
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            const int e = lane + 32 * m, t = e >> 2, i = 16 * warp + (e & 3) * 4;
+            const int e = lane + 32 * m, t = slab_token(e), i = 16 * warp + (e & 3) * 4;
             st_hl4(hi_of(Bs, B_VV), lo_of(Bs, B_VV, 16), t, i, ld_raw4(raw, VV, t, i));
         }
         __syncwarp();
