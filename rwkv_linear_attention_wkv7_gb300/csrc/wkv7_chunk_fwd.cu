@@ -449,10 +449,11 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         fence_proxy_async();  // the staged y tile is read by a tensor store
         __syncthreads();
         if constexpr (kGN) {  // o = GroupNorm(y) + bonus in place over the bonus tile: eight lanes per token,
-                              // eight channels each (the statistics take three shuffle levels)
-            const int t = tid >> 3, j0 = (tid & 7) * 8;
+                              // channels 4l..4l+3 and 32+4l..32+4l+3 each (the eight lanes' 16-byte accesses
+                              // cover 128 contiguous bytes; the statistics take three shuffle levels)
+            const int t = tid >> 3, j0 = (tid & 7) * 4;
             const float4 ya0 = *reinterpret_cast<const float4 *>(ys + t * YS + j0);
-            const float4 ya1 = *reinterpret_cast<const float4 *>(ys + t * YS + j0 + 4);
+            const float4 ya1 = *reinterpret_cast<const float4 *>(ys + t * YS + j0 + 32);
             const float yv[8] = {ya0.x, ya0.y, ya0.z, ya0.w, ya1.x, ya1.y, ya1.z, ya1.w};
             float sum = 0.f;
 #pragma unroll
@@ -473,10 +474,10 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
             const float4 *gb4 = reinterpret_cast<const float4 *>(p.gn_b + h * 64 + j0);
             float4 *ob = reinterpret_cast<float4 *>(bon + t * 64 + j0);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const float4 gw = __ldg(gw4 + hf), gb = __ldg(gb4 + hf), bv = ob[hf];
+            for (int hf = 0; hf < 2; ++hf) {  // channels j0 + 32 hf .. + 3: float4 index 8 hf
+                const float4 gw = __ldg(gw4 + 8 * hf), gb = __ldg(gb4 + 8 * hf), bv = ob[8 * hf];
                 const float *c = cv + 4 * hf;
-                ob[hf] = make_float4(c[0] * rstd * gw.x + gb.x + bv.x, c[1] * rstd * gw.y + gb.y + bv.y,
+                ob[8 * hf] = make_float4(c[0] * rstd * gw.x + gb.x + bv.x, c[1] * rstd * gw.y + gb.y + bv.y,
                                      c[2] * rstd * gw.z + gb.z + bv.z, c[3] * rstd * gw.w + gb.w + bv.w);
             }
             fence_proxy_async();
