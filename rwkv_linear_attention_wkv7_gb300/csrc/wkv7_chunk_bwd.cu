@@ -76,8 +76,14 @@ constexpr int S_BT = B_DD + C * SP * 4, S_AH = S_BT + HL16, S_RH = S_AH + HL16, 
 constexpr int kStateBytes = S_QQ + fac::kSA * 4;
 static_assert(B_G == S_BT && S_BT % 16 == 0 && S_QQ % 16 == 0, "state-pass layout: aligned, after dy and the decays");
 
-template <typename E, bool kSO = false>
-__host__ __device__ constexpr size_t bwd_smem_bytes() { return raw_bytes<E>() + (size_t)(kSO ? kStateBytes : kBytes); }
+// kGN: the head's gn_w and r_k (64 floats each) past the block, read by the do -> dy conversion
+// at every chunk start (shared memory instead of a global load on the chunk's critical path)
+constexpr int kGnParamBytes = 2 * 64 * 4;
+
+template <typename E, bool kSO = false, bool kGN = false>
+__host__ __device__ constexpr size_t bwd_smem_bytes() {
+    return raw_bytes<E>() + (size_t)(kSO ? kStateBytes : kBytes) + (kGN ? kGnParamBytes : 0);
+}
 
 __device__ __forceinline__ HL hl(const unsigned char *base, int off, int rows) {
     const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(base + off);
@@ -236,7 +242,12 @@ __global__ void __launch_bounds__(NT, 2)
     float rkA = 0.f, rkB = 0.f;
     float *const dsv = Wm + 256;
     static_assert(256 * 4 + C * 4 <= 1280, "the dw carry and the per-token sums fit the W slot");
+    float *const gnp = reinterpret_cast<float *>(Bs + kBytes);  // kGN: gn_w [64], r_k [64]
     if constexpr (kGN) {
+        if (tid < 32) {
+            const float *src = tid < 16 ? p.gn_w + h * 64 + 4 * tid : p.r_k + h * 64 + 4 * (tid - 16);
+            *reinterpret_cast<float4 *>(gnp + 4 * tid) = __ldg(reinterpret_cast<const float4 *>(src));
+        }
         rkA = __ldg(p.r_k + h * 64 + rA);
         rkB = __ldg(p.r_k + h * 64 + rB);
     }
@@ -318,10 +329,10 @@ __global__ void __launch_bounds__(NT, 2)
             break;
         }
         if constexpr (kGN) {  // do -> dy through the epilogue: 16 lanes per token (four channels each),
-                              // two tokens per warp at a time; statistics in two shuffle levels
+                              // two tokens per warp at a time; every sum in one round of four shuffle levels
             const int j = 4 * (lane & 15);
-            const float4 gw = __ldg(reinterpret_cast<const float4 *>(p.gn_w + h * 64 + j));
-            const float4 rk = __ldg(reinterpret_cast<const float4 *>(p.r_k + h * 64 + j));
+            const float4 gw = *reinterpret_cast<const float4 *>(gnp + j);
+            const float4 rk = *reinterpret_cast<const float4 *>(gnp + 64 + j);
             auto sum16 = [](float x) {
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -334,18 +345,22 @@ __global__ void __launch_bounds__(NT, 2)
                 const float4 d4 = *reinterpret_cast<const float4 *>(dyf + t * SP + j);
                 const float4 v4 = ld_raw4(raw, VV, t, j), r4 = ld_raw4(raw, VR, t, j), k4 = ld_raw4(raw, VK, t, j);
                 const float dn[4] = {d4.x * gw.x, d4.y * gw.y, d4.z * gw.z, d4.w * gw.w};
-                // sums that need nothing else first: y, dn, the bonus r k r_k, do . v
-                const float sy = sum16(y4.x + y4.y + y4.z + y4.w);
+                // one round of sums, about a shift m0 (the token's first channel) so that the
+                // moments of y - m0 do not cancel: mean = m0 + E[z], var = E[z^2] - E[z]^2,
+                // sum(dn (y - mean)) = sum(dn z) - E[z] sum(dn)
+                const float m0 = __shfl_sync(0xffffffffu, y4.x, lane & 16);
+                const float z[4] = {y4.x - m0, y4.y - m0, y4.z - m0, y4.w - m0};
+                const float sz = sum16(z[0] + z[1] + z[2] + z[3]);
+                const float szz = sum16(z[0] * z[0] + z[1] * z[1] + z[2] * z[2] + z[3] * z[3]);
                 const float sdn = sum16(dn[0] + dn[1] + dn[2] + dn[3]);
+                const float sdz = sum16(dn[0] * z[0] + dn[1] * z[1] + dn[2] * z[2] + dn[3] * z[3]);
                 const float sb = sum16(r4.x * k4.x * rk.x + r4.y * k4.y * rk.y + r4.z * k4.z * rk.z + r4.w * k4.w * rk.w);
                 const float ds = sum16(d4.x * v4.x + d4.y * v4.y + d4.z * v4.z + d4.w * v4.w);
-                const float mean = sy * (1.f / 64.f);
-                const float c[4] = {y4.x - mean, y4.y - mean, y4.z - mean, y4.w - mean};
-                // then the variance and sum(dn xh) = rstd sum(dn (y - mean))
-                const float scc = sum16(c[0] * c[0] + c[1] * c[1] + c[2] * c[2] + c[3] * c[3]);
-                const float sdc = sum16(dn[0] * c[0] + dn[1] * c[1] + dn[2] * c[2] + dn[3] * c[3]);
-                const float rstd = 1.f / sqrtf(scc * (1.f / 64.f) + kGnEps);
-                const float mn = sdn * (1.f / 64.f), mx = rstd * sdc * (1.f / 64.f);
+                const float ez = sz * (1.f / 64.f);
+                const float var = fmaxf(szz * (1.f / 64.f) - ez * ez, 0.f);
+                const float c[4] = {z[0] - ez, z[1] - ez, z[2] - ez, z[3] - ez};
+                const float rstd = rsqrtf(var + kGnEps);
+                const float mn = sdn * (1.f / 64.f), mx = rstd * (sdz - ez * sdn) * (1.f / 64.f);
                 float x[4], dy[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -959,7 +974,7 @@ __global__ void __launch_bounds__(NT, 2)
 
 template <typename E, bool kFac, bool kP, bool kGN = false, bool kSO = false>
 cudaError_t launch_t(const SeqArgs &p, cudaStream_t st) {
-    const size_t sm = bwd_smem_bytes<E, kSO>();
+    const size_t sm = bwd_smem_bytes<E, kSO, kGN>();
     InputMaps maps{};
     OutputMaps omaps{};
     cudaError_t e = encode_input_maps(&maps, p, p.dy);  // six inputs, dy (or do), and the checkpoints (box OS x 64)

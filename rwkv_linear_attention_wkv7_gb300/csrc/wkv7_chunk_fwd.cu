@@ -450,26 +450,32 @@ __global__ void __launch_bounds__(NT, 4) wkv7_fwd_chunk_kernel(SeqArgs p, const 
         __syncthreads();
         if constexpr (kGN) {  // o = GroupNorm(y) + bonus in place over the bonus tile: eight lanes per token,
                               // channels 4l..4l+3 and 32+4l..32+4l+3 each (the eight lanes' 16-byte accesses
-                              // cover 128 contiguous bytes; the statistics take three shuffle levels)
+                              // cover 128 contiguous bytes; the statistics take one round of three
+                              // shuffle levels)
             const int t = tid >> 3, j0 = (tid & 7) * 4;
             const float4 ya0 = *reinterpret_cast<const float4 *>(ys + t * YS + j0);
             const float4 ya1 = *reinterpret_cast<const float4 *>(ys + t * YS + j0 + 32);
             const float yv[8] = {ya0.x, ya0.y, ya0.z, ya0.w, ya1.x, ya1.y, ya1.z, ya1.w};
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum += yv[i];
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float mean = sum * (1.f / 64.f);
-            float cv[8], sq = 0.f;
+            // one round of sums about a shift m0 (the token's first channel), so that the
+            // moments of y - m0 do not cancel: mean = m0 + E[z], var = E[z^2] - E[z]^2
+            const float m0 = __shfl_sync(0xffffffffu, yv[0], lane & ~7);
+            float z[8], sz = 0.f, szz = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                cv[i] = yv[i] - mean;
-                sq += cv[i] * cv[i];
+                z[i] = yv[i] - m0;
+                sz += z[i];
+                szz += z[i] * z[i];
             }
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            const float rstd = 1.f / sqrtf(sq * (1.f / 64.f) + kGnEps);
+            for (int o = 1; o < 8; o <<= 1) {
+                sz += __shfl_xor_sync(0xffffffffu, sz, o);
+                szz += __shfl_xor_sync(0xffffffffu, szz, o);
+            }
+            const float ez = sz * (1.f / 64.f);
+            float cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cv[i] = z[i] - ez;
+            const float rstd = rsqrtf(fmaxf(szz * (1.f / 64.f) - ez * ez, 0.f) + kGnEps);
             const float4 *gw4 = reinterpret_cast<const float4 *>(p.gn_w + h * 64 + j0);
             const float4 *gb4 = reinterpret_cast<const float4 *>(p.gn_b + h * 64 + j0);
             float4 *ob = reinterpret_cast<float4 *>(bon + t * 64 + j0);
