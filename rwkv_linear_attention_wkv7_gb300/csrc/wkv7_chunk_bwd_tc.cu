@@ -196,8 +196,10 @@ __global__ void __launch_bounds__(NT, 2)
 
         // ================= operand matrices (split once, canonical layout)
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // b~, k~, r^, a^ of this warp's 16-key slab, all tokens
-            const int e = lane + 32 * m, t = e >> 2, j = 16 * warp + (e & 3) * 4;
+        for (int m = 0; m < 2; ++m) {  // b~, k~, r^, a^ of this warp's 16-key slab, all tokens: a quarter-warp
+                                       // takes 8 tokens of one quad, a half-warp both quads of one core
+                                       // matrix, so that every access falls in distinct banks
+            const int t = (lane & 7) + 8 * m, j = 16 * warp + 4 * ((lane >> 3) & 1) + 8 * (lane >> 4);
             const float4 d = *reinterpret_cast<const float4 *>(dd + t * DS + j);
             const float4 dp = t ? *reinterpret_cast<const float4 *>(dd + (t - 1) * DS + j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float4 id = rcp4(d);
