@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(NT, 2)
     // there, and first waited for by the products that read S_0.
     __shared__ __align__(8) uint64_t bar, bar_s;
     __shared__ int lost;  // a bounded wait of this CTA ran out (see mbar_wait)
-    // kSO: k and v are not staged, and only the factor block's first half (W, M_k', Q', W Q_b) is
+    // kSO stages neither k nor v, and of the factor block only its first half (W, M_k', Q', W Q_b)
     constexpr int kFacWords = kSO ? fac::kSA : fac::kWords;
     constexpr unsigned kChunkBytes = (unsigned)(raw_bytes<E>() - (kSO ? 2 * C * RS * sizeof(E) : 0) + C * RS * 4 +
                                                 (kFac ? kFacWords * 4 : 0) + (kGN ? C * RS * 4 : 0));
