@@ -219,6 +219,19 @@ def _loss(orc, x, s0, dy, dsT):
     return float(np.sum(y * dy) + np.sum(sT * dsT))
 
 
+def pin_worked_example(orc):
+    """The hand-derived worked example of tests/golden/worked_example_t3.txt
+    (its derivation is in the file): y, sT and every gradient, exactly."""
+    from tests.test_golden import OUT_NAMES, dense, load_fixture
+    inputs, expect = load_fixture()
+    x = {n: inputs[n] for n in ("r", "w", "k", "v", "a", "b")}
+    y, sT, _ = orc.forward(**x, L=16)
+    got = {"y": y, "sT": sT, **orc.backward(**x, dy=inputs["dy"])}
+    for n in OUT_NAMES:
+        want = dense(n, expect[n])
+        assert np.array_equal(np.asarray(got[n]), want), f"worked example {n}: max diff {np.abs(got[n] - want).max():.3e}"
+
+
 def pin_adjoint_identity(orc):
     """y and sT are linear in (s0, v), so for any direction (u0, uv):
     <y(u0, uv), dy> + <sT(u0, uv), dsT> = <u0, ds0> + <uv, dv>."""
@@ -528,5 +541,5 @@ ALL_PINS = [
     pin_projection_erases, pin_rank1_orientation, pin_empty_sequence,
     pin_checkpoints_are_prefix_states, pin_split_sequence, pin_decode_is_streaming,
     pin_linear_in_state_and_values, pin_adjoint_identity, pin_finite_differences,
-    pin_autograd_adjoint,
+    pin_autograd_adjoint, pin_worked_example,
 ] + FUSED_PINS + GN_PINS
