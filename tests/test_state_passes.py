@@ -48,8 +48,8 @@ def test_backward_state_bit_identical(B, T, H, dtype, with_dsT, extreme):
     assert torch.equal(got, ref)
 
 
-def test_backward_state_no_tokens():
-    """T = 0: ds0 = dsT (or zeros)."""
+def test_state_passes_no_tokens():
+    """T = 0: ds0 = dsT and sT = s0 (or zeros)."""
     build()
     B, H = 2, 3
     z = torch.empty((B, 0, H, 64), device="cuda")
@@ -57,6 +57,8 @@ def test_backward_state_no_tokens():
     dsT = torch.randn((B, H, 64, 64), device="cuda")
     assert torch.equal(wkv7.backward_state(z, z, z, z, fac, z, dsT=dsT), dsT)
     assert torch.equal(wkv7.backward_state(z, z, z, z, fac, z), torch.zeros_like(dsT))
+    assert torch.equal(wkv7.forward_state(z, z, z, z, z, s0=dsT), dsT)
+    assert torch.equal(wkv7.forward_state(z, z, None, z, z), torch.zeros_like(dsT))
 
 
 @pytest.mark.parametrize("B,T,H,dtype,extreme", [(2, 96, 3, "bf16", False), (2, 77, 2, "f32", False),
