@@ -322,6 +322,19 @@ __global__ void __launch_bounds__(NT, 2)
                 }
             }
         };
+        // dy split into [t][i] quads; it needs no decay: with plain inputs warps 0 and 1 split it
+        // while warps 2 and 3 form the decays, with the producers (all four warps form the decays)
+        // or the epilogue (dy is the converted do) every warp splits it after the decays
+        auto split_dy = [&](int e) {
+            const int t = e >> 4, j = (e & 15) * 4;
+            st_hl4(hi_of(Bs, oDYH), lo_of(Bs, oDYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
+        };
+        if constexpr (!kP && !kGN) {
+            if (warp < 2) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) split_dy(tid + 64 * m);
+            }
+        }
         // the cumulative decays on warps 2 and 3 (warps 0 and 1 have just issued the gradient stores)
         const bool exact = __syncthreads_or(prep_decay<kP, E, !kP>(raw, dd, nv, 64, kP ? sgs : nullptr));
         if (lost) {  // every thread has passed its wait (the barrier above): leave together
@@ -440,10 +453,9 @@ __global__ void __launch_bounds__(NT, 2)
             st_hl4(hi_of(Bs, oAH), lo_of(Bs, oAH, 16), t, j, mul4(in_a4<kP>(raw, t, j), dp));
             st_hl4(hi_of(Bs, oRH), lo_of(Bs, oRH, 16), t, j, mul4(ld_raw4(raw, VR, t, j), d));
         }
+        if constexpr (kP || kGN) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {  // dy: [t][i] quads
-            const int e = tid + NT * m, t = e >> 4, j = (e & 15) * 4;
-            st_hl4(hi_of(Bs, oDYH), lo_of(Bs, oDYH, 16), t, j, *reinterpret_cast<const float4 *>(dyf + t * SP + j));
+            for (int m = 0; m < 2; ++m) split_dy(tid + NT * m);
         }
         if constexpr (!kSO) drain_then_load_s0();
         if constexpr (kFac)
