@@ -415,8 +415,8 @@ def run_ours(args, world, rank, local):
     # workloads with another checkpoint stride run the two calls in a row.
     use_step = spec.L == 16
     fbout = {**outs, **gouts}
-    nsplit = 0  # the library's default
-    split = min(2, B) if use_step else 1
+    nsplit = args.nsplit  # 0: the library's default
+    split = wkv7.forward_backward_blocks(B, spec.T, spec.H, nsplit) if use_step else 1
     launches_per_step = 2 * split
 
     def fb_step():
@@ -672,8 +672,9 @@ def run_ours(args, world, rank, local):
         f_ms = max_over_ranks(f0.elapsed_time(f1), world) / args.steps
         ff = statistics.mean(a.elapsed_time(b) for a, b, _ in fev)
         fb = statistics.mean(b.elapsed_time(c) for _, b, c in fev)
-        # the same step in one call, two blocks of batch rows (wkv7_forward_backward_fused)
+        # the same step in one call, the library's blocks of batch rows (wkv7_forward_backward_fused)
         fbo = {**outs, **fg}
+        fblocks = wkv7.forward_backward_blocks(B, spec.T, spec.H, 0)
 
         def fcall():
             wkv7.forward_backward_fused(*fx, d["dy"], s0=d["s0"], dsT=d["dsT"], nsplit=0, out=fbo, stream=stream)
@@ -720,7 +721,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         u_ms = max_over_ranks(u0.elapsed_time(u1), world) / n_u
         fused = {"ms_per_step": fc_ms, "tokens_per_s": world * spec.tokens / (fc_ms / 1e3),
-                 "entry": "wkv7_forward_backward_fused, two blocks of batch rows", "launches_per_step": 2 * min(2, B),
+                 "entry": f"wkv7_forward_backward_fused, {fblocks} blocks of batch rows", "launches_per_step": 2 * fblocks,
                  "sequential_ms_per_step": f_ms, "forward_ms": ff, "backward_ms": fb,
                  "separate_producers_ms_per_step": u_ms,
                  "roofline": {"bound": "hbm", "kernel": "wkv7 backward (fused producers)",
@@ -771,8 +772,9 @@ def run_ours(args, world, rank, local):
         g_ms = max_over_ranks(g0.elapsed_time(g1), world) / args.steps
         gf = statistics.mean(a.elapsed_time(b) for a, b, _ in gev)
         gb = statistics.mean(b.elapsed_time(c) for _, b, c in gev)
-        # the same step in one call, two blocks of batch rows (wkv7_forward_backward_gn)
+        # the same step in one call, the library's blocks of batch rows (wkv7_forward_backward_gn)
         gbo = {**go, **gg}
+        gblocks = wkv7.forward_backward_blocks(B, spec.T, spec.H, 0)
 
         def gcall():
             wkv7.forward_backward_gn(*xs, d["dy"], gp["gn_w"], gp["gn_b"], gp["r_k"], s0=d["s0"], dsT=d["dsT"],
@@ -812,8 +814,8 @@ def run_ours(args, world, rank, local):
         sep_ms = max_over_ranks(s0_.elapsed_time(s1_), world) / n_s
         gbytes = bwd_bytes + spec.elems * 4  # + the forward's y, read back by the epilogue's backward
         gnres = {"ms_per_step": gc_ms, "tokens_per_s": world * spec.tokens / (gc_ms / 1e3),
-                 "entry": "wkv7_forward_backward_gn, two blocks of batch rows",
-                 "launches_per_step": 2 * min(2, B) + 1, "sequential_ms_per_step": g_ms, "forward_ms": gf,
+                 "entry": f"wkv7_forward_backward_gn, {gblocks} blocks of batch rows",
+                 "launches_per_step": 2 * gblocks + 1, "sequential_ms_per_step": g_ms, "forward_ms": gf,
                  "backward_ms": gb, "separate_epilogue_ms_per_step": sep_ms,
                  "roofline": {"bound": "hbm", "kernel": "wkv7 backward with the epilogue's backward",
                               "achieved": gbytes / (gb / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
@@ -869,6 +871,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override B of the workload (smaller profiling cases of the same kernels)")
     ap.add_argument("--seq-len", type=int, default=None, help="override T of the workload (profiling cases)")
+    ap.add_argument("--nsplit", type=int, default=0, choices=range(5),
+                    help="blocks of batch rows of the one-call step (0: the library's default)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the batched decode measurement")

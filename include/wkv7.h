@@ -344,9 +344,9 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
  *             forward half, read by the backward half.
  *   factors   [B][H][wkv7_factor_floats(T)] or NULL (the backward half then
  *             rebuilds the per-chunk factors itself).
- *   nsplit    number of blocks, 0 (the library's default, 2) to 4; more
- *             blocks than batch rows means one row per block, 1 runs the two
- *             calls in order on `stream` itself.
+ *   nsplit    number of blocks, 0 (the library's default: 4 when B*H is at
+ *             least 512, else 2) to 4; more blocks than batch rows means one
+ *             row per block, 1 runs the two calls in order on `stream` itself.
  * Ownership and errors as in wkv7_forward: the caller owns every buffer;
  * every argument is checked (WKV7_EINVAL, WKV7_EUNSUPPORTED) before anything
  * is launched; WKV7_ECUDA on a launch or stream error, after which the
@@ -355,7 +355,13 @@ int wkv7_forward_backward_noalloc(int B, int T, int H, int N, wkv7_dtype dtype,
  * streams and four events per device) and keeps them for the life of the
  * process; concurrent calls from several host threads are serialised while
  * they enqueue their work.
+ *
+ * wkv7_forward_backward_blocks: the number of blocks a call of any of the
+ * three one-call forms makes for these B, T, H and nsplit (each block
+ * launches one forward and one backward; the _gn form adds one reduction),
+ * or -1 for B or H < 1, T < 0 or nsplit outside 0 .. 4.  Host only.
  */
+int wkv7_forward_backward_blocks(int B, int T, int H, int nsplit);
 int wkv7_forward_backward(int B, int T, int H, int N, wkv7_dtype dtype,
                           const void *r, const void *w, const void *k,
                           const void *v, const void *a, const void *b,

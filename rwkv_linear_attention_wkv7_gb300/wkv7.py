@@ -62,6 +62,8 @@ def load(path: str) -> ctypes.CDLL:
     L.wkv7_forward_timesplit.restype = ci
     L.wkv7_backward_timesplit.argtypes = [ci, ci, ci, ci, ci] + [vp] * 6 + [fp, fp] + [fp] * 7 + [ci, fp, vp]
     L.wkv7_backward_timesplit.restype = ci
+    L.wkv7_forward_backward_blocks.argtypes = [ci, ci, ci, ci]
+    L.wkv7_forward_backward_blocks.restype = ci
     L.wkv7_forward_state.argtypes = [ci, ci, ci, ci, ci] + [vp] * 5 + [fp, fp, vp]
     L.wkv7_forward_state.restype = ci
     L.wkv7_backward_state.argtypes = [ci, ci, ci, ci, ci] + [vp] * 4 + [fp] * 4 + [vp]
@@ -216,6 +218,15 @@ def backward(r, w, k, v, a, b, ckpt, dy, dsT=None, L: int = 16, want_ds0: bool =
                                 *(_ptr(g[n]) for n in names), _ptr(g["ds0"]), _stream(stream))
     _check(_entry, rc)
     return g
+
+
+def forward_backward_blocks(B: int, T: int, H: int, nsplit: int = 0) -> int:
+    """Blocks of batch rows a one-call step with these sizes and ``nsplit`` runs
+    (each launches one forward and one backward)."""
+    n = lib().wkv7_forward_backward_blocks(B, T, H, nsplit)
+    if n < 1:
+        raise ValueError(f"bad sizes or nsplit (B={B}, T={T}, H={H}, nsplit={nsplit})")
+    return n
 
 
 def forward_backward(r, w, k, v, a, b, dy, s0=None, dsT=None, want_factors: bool = True, nsplit: int = 0,

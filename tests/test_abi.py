@@ -228,6 +228,20 @@ def test_state_passes_reject_bad_arguments(lib):
     assert lib.wkv7_backward_state(*bad) == EINVAL and "N must be 64" in wkv7.last_error()
 
 
+def test_forward_backward_blocks(lib):
+    """The one-call step's block count: four blocks from 512 heads, two below,
+    never more than the batch rows, one without tokens; -1 for bad arguments."""
+    assert lib.wkv7_forward_backward_blocks(16, 4096, 32, 0) == 4
+    assert lib.wkv7_forward_backward_blocks(8, 4096, 32, 0) == 2
+    assert lib.wkv7_forward_backward_blocks(1, 4096, 32, 0) == 1
+    assert lib.wkv7_forward_backward_blocks(3, 64, 2, 4) == 3
+    assert lib.wkv7_forward_backward_blocks(16, 0, 32, 0) == 1
+    assert lib.wkv7_forward_backward_blocks(16, 64, 32, 1) == 1
+    assert lib.wkv7_forward_backward_blocks(0, 64, 32, 0) == -1
+    assert lib.wkv7_forward_backward_blocks(4, 64, 32, 5) == -1
+    assert lib.wkv7_forward_backward_blocks(4, -1, 32, 0) == -1
+
+
 def test_decode_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(4096)
     assert lib.wkv7_decode_step(1, 1, 32, 0, *([p] * 6), p, p, None) == EINVAL
