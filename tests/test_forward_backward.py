@@ -116,11 +116,12 @@ def test_gn_bit_identical_to_the_two_gn_calls(B, T, H, dtype, nsplit):
         assert torch.equal(got[n], ref[n]), n
 
 
-def test_captured_in_a_cuda_graph():
+@pytest.mark.parametrize("nsplit", [0, 4])
+def test_captured_in_a_cuda_graph(nsplit):
     """The one-call step captures into a CUDA graph (its fork onto the library's
     streams and the join back are ordinary cross-stream captures) and the graph
     replays it: new inputs copied into the captured buffers give the same
-    outputs, bit for bit, as the eager call."""
+    outputs, bit for bit, as the eager call (two and four blocks)."""
     build()
     spec = synthetic.WorkloadSpec("fwdbwd_graph", 4, 96, 2, dtype="bf16", s0_std=0.1, with_dsT=True, seed=37)
     d = synthetic.make_inputs(spec, device="cuda")
@@ -128,18 +129,19 @@ def test_captured_in_a_cuda_graph():
     xs = [d[n].clone() for n in parity.INPUTS]
     dy = d["dy"].clone()
     # warm up outside the capture (the library's streams and device tables exist afterwards)
-    out = wkv7.forward_backward(*xs, dy, s0=d["s0"], dsT=d["dsT"])
+    out = wkv7.forward_backward(*xs, dy, s0=d["s0"], dsT=d["dsT"], nsplit=nsplit)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        wkv7.forward_backward(*xs, dy, s0=d["s0"], dsT=d["dsT"], out=out, stream=torch.cuda.current_stream())
+        wkv7.forward_backward(*xs, dy, s0=d["s0"], dsT=d["dsT"], nsplit=nsplit, out=out,
+                              stream=torch.cuda.current_stream())
     for x, n in zip(xs, parity.INPUTS):
         x.copy_(d2[n])
     dy.copy_(d2["dy"])
     graph.replay()
     torch.cuda.synchronize()
     wkv7.async_status()
-    ref = wkv7.forward_backward(*(d2[n] for n in parity.INPUTS), d2["dy"], s0=d["s0"], dsT=d["dsT"])
+    ref = wkv7.forward_backward(*(d2[n] for n in parity.INPUTS), d2["dy"], s0=d["s0"], dsT=d["dsT"], nsplit=1)
     torch.cuda.synchronize()
     for n in OUTS:
         assert torch.equal(out[n], ref[n]), n
